@@ -1,0 +1,325 @@
+"""Benchmark of the verification step on GB300.
+
+Default workload: batched mentored speculative sampling, B=64 requests,
+K=8 drafts, V=152064, bf16 logits (330.9 MB of logits per step, larger than
+the 129 MB L2; two input copies alternate between steps).  One step = one
+``spec_verify_sample`` call over the whole batch.
+
+Prints one JSON line:
+  value      verified requests per second (all ranks), inputs resident in HBM
+  e2e        the same through the C ABI with pinned host buffers: the step's
+             inputs copied host->device and tokens/accepted copied back inside
+             the timed region
+  roofline   the sampling kernel against the measured HBM copy peak
+  cpu_baseline  the CPU oracle on a bounded sample of the same workload
+
+``--impl reference`` times the CPU oracle itself (one bounded sample per
+step) and prints its line with "impl": "reference".
+
+Multi-GPU: one process per GPU under torchrun; requests are independent, so
+each rank verifies its own batch (weak scaling, no data-path collective; a
+barrier and a max-reduce of the elapsed time only).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+KERNEL_SOURCES = ["speculative_decoding_verification_23_gb300/csrc/sample_verify.cu",
+                  "speculative_decoding_verification_23_gb300/csrc/common.cuh",
+                  "speculative_decoding_verification_23_gb300/csrc/spec_internal.h"]
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "sample_verify_batched.json")
+METRIC = "spec-verify rows/s and logits HBM GB/s (% of GB300 peak) at B=64 K=8 V=152064"
+
+
+def kernel_hash() -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except FileNotFoundError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def oracle_baseline(batch, budget_s: float):
+    """Requests/s of the CPU oracle on a bounded sample (whole requests, in order)."""
+    import oracle
+
+    t0 = time.perf_counter()
+    n = 0
+    for b in range(batch.B):
+        oracle.verify_batch(batch, [b])
+        n += 1
+        if time.perf_counter() - t0 > budget_s:
+            break
+    dt = time.perf_counter() - t0
+    return n / dt, n, dt
+
+
+def make_workload(rank: int):
+    from speculative_decoding_verification_23_gb300 import workload as W
+
+    return W.batched(round_=rank)
+
+
+def bench_reference(args, rank, world):
+    batch = make_workload(rank)
+    per_step_budget = max(1.0, 150.0 / max(1, args.steps + args.warmup))
+    for _ in range(args.warmup):
+        oracle_baseline(batch, min(per_step_budget, 2.0))
+    vals = []
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        v, n, dt = oracle_baseline(batch, per_step_budget)
+        vals.append(v)
+    wall = time.perf_counter() - t0
+    value = float(np.mean(vals))
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "requests/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * wall / max(1, args.steps),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": "batched B=64 K=8 V=152064 bf16 logits", "B": 64, "K": 8,
+                                        "V": 152064},
+        "cpu_baseline": {"value": value, "unit": "requests/s", "cores": 1, "kind": "oracle",
+                         "sample": f"whole requests of the B=64 batch, ~{per_step_budget:.1f} s of CPU per step"},
+        "e2e": {"value": value, "unit": "requests/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def bench_gpu(args, rank, world, dist):
+    import torch
+
+    import speculative_decoding_verification_23_gb300 as sv
+    from speculative_decoding_verification_23_gb300.device_batch import to_device
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    sv.load_library()
+    batch = make_workload(rank)
+    copies = [to_device(batch, dev) for _ in range(2)]
+    ws = sv.make_workspace(batch.B, batch.total_drafts, batch.V, dev)
+    outs = [torch.empty(batch.total_drafts + batch.B, dtype=torch.int32, device=dev),
+            torch.empty(batch.B, dtype=torch.int32, device=dev),
+            torch.empty(batch.B, dtype=torch.int32, device=dev)]
+    argv = [c.args() for c in copies]
+    stream = torch.cuda.current_stream(dev)
+
+    def step(k):
+        sv.spec_verify_sample(argv[k % 2], device=dev, workspace=ws, out_tokens=outs[0], out_accepted=outs[1],
+                              out_status=outs[2], stream=stream)
+
+    for k in range(max(3, args.warmup)):
+        step(k)
+    torch.cuda.synchronize()
+    assert int(outs[2].max().item()) == 0, "bench inputs flagged invalid"
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(dev.index) as clk:
+        t_start = torch.cuda.Event(enable_timing=True)
+        t_end = torch.cuda.Event(enable_timing=True)
+        t_start.record(stream)
+        for k in range(args.steps):
+            ev[k][0].record(stream)
+            step(k)
+            ev[k][1].record(stream)
+        t_end.record(stream)
+        torch.cuda.synchronize()
+    elapsed = t_start.elapsed_time(t_end) / 1000.0
+    per_launch = [a.elapsed_time(b) / 1000.0 for a, b in ev]
+    if dist:
+        t = torch.tensor([elapsed], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed = float(t.item())
+        dist.barrier()
+    value = world * batch.B * args.steps / elapsed
+    ms = 1000.0 * elapsed / args.steps
+
+    # ---- end to end: pinned host inputs -> device -> call -> tokens back
+    host = {
+        "target": copies[0].target.cpu().pin_memory(), "draft": copies[0].draft.cpu().pin_memory(),
+        "small": [t.cpu().pin_memory() for t in (copies[0].cu_draft, copies[0].draft_tokens, copies[0].cu_hist,
+                                                 copies[0].hist, copies[0].temperature, copies[0].rep_penalty,
+                                                 copies[0].tv_budget, copies[0].uniforms)],
+    }
+    dstc = copies[1]
+    dsmall = [dstc.cu_draft, dstc.draft_tokens, dstc.cu_hist, dstc.hist, dstc.temperature, dstc.rep_penalty,
+              dstc.tv_budget, dstc.uniforms]
+    out_host = [torch.empty_like(outs[0], device="cpu").pin_memory(),
+                torch.empty_like(outs[1], device="cpu").pin_memory()]
+    h2d = host["target"].numel() * host["target"].element_size() + host["draft"].numel() * host["draft"].element_size()
+    h2d += sum(t.numel() * t.element_size() for t in host["small"])
+    d2h = sum(t.numel() * t.element_size() for t in out_host)
+
+    def e2e_step():
+        dstc.target.copy_(host["target"], non_blocking=True)
+        dstc.draft.copy_(host["draft"], non_blocking=True)
+        for d, h in zip(dsmall, host["small"]):
+            d.copy_(h, non_blocking=True)
+        sv.spec_verify_sample(argv[1], device=dev, workspace=ws, out_tokens=outs[0], out_accepted=outs[1],
+                              out_status=outs[2], stream=stream)
+        out_host[0].copy_(outs[0], non_blocking=True)
+        out_host[1].copy_(outs[1], non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    e_steps = max(3, min(args.steps, 20))
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(e_steps):
+        e2e_step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    e2e_s = a.elapsed_time(b) / 1000.0
+    e2e_value = world * batch.B * e_steps / e2e_s
+    if dist:
+        t = torch.tensor([e2e_s], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_value = world * batch.B * e_steps / float(t.item())
+
+    # ---- roofline of the sampling kernel (one launch per step)
+    peak, peak_kind = measured_peak()
+    alg_bytes = batch.logit_bytes() + 4 * (batch.total_drafts + batch.B) * 2 + 4 * int(batch.hist.size) + 4 * 4 * batch.B
+    launch_s = float(np.mean(per_launch))
+    achieved = alg_bytes / launch_s / 1e9
+    traffic = None
+    if os.path.exists(PROFILE_SUMMARY):
+        with open(PROFILE_SUMMARY) as f:
+            prof = json.load(f)
+        if prof.get("kernel_hash") == kernel_hash():
+            traffic = prof.get("dram_bytes_per_launch")
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "requests/s", "n_gpus": world, "steps": args.steps,
+        "warmup": max(3, args.warmup), "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "batched B=64 K=8 V=152064 bf16 logits", "B": batch.B, "K": 8, "V": batch.V,
+                   "logit_bytes_per_step": batch.logit_bytes(), "parallelism": f"replicas x{world}",
+                   "l2": "inputs 330.9 MB > 129 MB L2; two input copies alternate"},
+        "logit_rows_per_s": value * (2 * 8 + 1),
+        "hbm_gbs": achieved,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": traffic, "peak_kind": peak_kind, "kernel": "sample_verify_kernel",
+                     "algorithmic_bytes_per_launch": alg_bytes, "launch_ms": 1000 * launch_s},
+        "e2e": {"value": e2e_value, "unit": "requests/s", "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
+        "gpu_launches": args.steps,
+        "clocks": clk.summary(),
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        v, n, dt = oracle_baseline(batch, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": v, "unit": "requests/s", "cores": 1, "kind": "oracle",
+                                "sample": f"{n} whole requests of the B=64 batch ({dt:.1f} s, one thread)"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        if rank == 0:
+            bench_reference(args, rank, world)
+        return
+    dist = None
+    if world > 1:
+        import torch.distributed as tdist
+
+        tdist.init_process_group("nccl")
+        dist = tdist
+    try:
+        bench_gpu(args, rank, world, dist)
+    finally:
+        if dist:
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,174 @@
+/*
+ * spec_verify.h — C ABI of the GB300 (sm_103a) speculative-decoding
+ * verification library (libspecverify.so).
+ *
+ * The library runs the step that follows the target model's verify forward:
+ * for every request it turns target logits [K+1, V] and draft logits [K, V]
+ * into the emitted tokens of that round.
+ *
+ *   spec_verify_sample  mentored speculative sampling ("What I Gave Up to
+ *                       Make Speculative Decoding Faster", section "A knob
+ *                       for accepting more draft tokens"): p and q after
+ *                       repetition penalty and temperature (and top-p, as in
+ *                       the "Speculative Decoding" note, section "Warum eine
+ *                       Korrektur noetig ist"); d = TV(p,q) = 1/2 sum|p-q|;
+ *                       theta = min(1, D/d) (1 when d = 0);
+ *                       pi = (1-theta) p + theta q; accept x ~ q with
+ *                       probability min(1, pi(x)/q(x)); keep the prefix up
+ *                       to the first rejection; replace the rejected token
+ *                       by a draw from the normalised residual max(p-q, 0);
+ *                       after a fully accepted draft, a bonus token from p.
+ *                       D = 0 is lossless speculative sampling.
+ *   spec_verify_greedy  greedy longest-prefix verification
+ *                       ("Adaptive-SpecDecode-Lab" README, section "实现"):
+ *                       argmax of each penalised target row, prefix match
+ *                       against the drafts, the target's argmax as the
+ *                       correction on the first mismatch, or as the bonus
+ *                       when every draft matches.
+ *   spec_tv_budget      the per-position quantities alone: d, theta, p(x),
+ *                       q(x).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * Memory: every pointer is caller-owned DEVICE memory (except `args`, which
+ * is a host struct).  The library never allocates or frees memory and never
+ * synchronises the device; all work is enqueued on `stream` and completes
+ * asynchronously.  Inputs are only read; outputs are only written.
+ *
+ * Batch layout (packed ragged rows): request b has K_b = cu_draft[b+1] -
+ * cu_draft[b] drafts (0 <= K_b <= max_k <= 32).  Its draft rows are
+ * cu_draft[b] .. cu_draft[b+1]-1 of draft_logits; its target rows are
+ * off_b .. off_b + K_b of target_logits with off_b = cu_draft[b] + b (row
+ * off_b + i scores the token after [last committed, d_1..d_i]).
+ * cu_draft must be non-decreasing with cu_draft[0] = 0 and
+ * cu_draft[B] = total_drafts.
+ *
+ * Logits: row-major, `ld` elements between rows (ld >= V), fp32 or bf16.
+ * Each buffer must start on a 16-byte boundary, ld * sizeof(dtype) must be a
+ * multiple of 16, and the buffer must hold rows * ld elements (entries
+ * V .. ld-1 of a row are padding and are never used; they may be read).
+ *
+ * Per-request scalars [B] (fp32): temperature T > 0, repetition penalty
+ * alpha > 0 (NULL = 1, no penalty), top_p in (0,1] (NULL = 1, no filter),
+ * TV budget D in [0,1].  Repetition penalty: for every distinct token t of
+ * the request's history plus the drafts preceding the row,
+ * z'_t = z_t/alpha if z_t > 0 else z_t*alpha (fp32, correctly rounded);
+ * then z'' = z'/T.  Top-p keeps every token whose probability is at least
+ * tau, tau being the probability at which the descending cumulative mass
+ * first reaches top_p, and renormalises; it is applied to p and q
+ * separately, before they are compared.
+ *
+ * Uniforms [total_drafts + B] in [0,1): u[off_b + i] (i < K_b) is the
+ * acceptance draw of draft i; u[off_b + K_b] is the final draw (correction
+ * or bonus).  Draws are inverse-CDF in token-id order: the smallest v whose
+ * inclusive prefix mass exceeds u * (total mass).
+ *
+ * Outputs: out_tokens [total_drafts + B], request b writing slots
+ * off_b .. off_b + K_b: the accepted drafts, then the correction or bonus,
+ * then -1.  out_accepted [B] = number of accepted drafts.
+ * out_status [B] (may be NULL) = 0, or an OR of SPEC_STATUS_* for invalid
+ * per-request data; such a request's tokens and accepted count are -1.
+ *
+ * Return value: SPEC_OK (0) once the work is enqueued, or a negative
+ * SPEC_ERR_* from the host-side checks (nothing is enqueued then) or from
+ * the launch.  No entry point ever traps on the device.
+ *
+ * Workspace: spec_workspace_bytes(B, total_drafts, V) bytes of device
+ * memory, at least 256-byte aligned.  Its contents need no initialisation;
+ * each call clears what it needs on `stream`.  Calls that share one
+ * workspace must be ordered (same stream, or synchronised).
+ */
+#ifndef SPEC_VERIFY_H
+#define SPEC_VERIFY_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A CUDA stream handle (cudaStream_t / CUstream); NULL = legacy stream. */
+typedef struct CUstream_st *spec_stream_t;
+
+enum { SPEC_F32 = 0, SPEC_BF16 = 1 };
+
+enum {
+  SPEC_OK = 0,
+  SPEC_ERR_NULL = -1,        /* a required pointer is NULL                 */
+  SPEC_ERR_SHAPE = -2,       /* B, V, total_drafts or ld out of range      */
+  SPEC_ERR_DTYPE = -3,       /* dtype is not SPEC_F32 / SPEC_BF16          */
+  SPEC_ERR_K_TOO_LARGE = -4, /* max_k > SPEC_MAX_K                         */
+  SPEC_ERR_WORKSPACE = -5,   /* workspace NULL, misaligned or too small    */
+  SPEC_ERR_ALIGN = -6,       /* logits not 16-byte aligned / ld*size % 16  */
+  SPEC_ERR_LAUNCH = -7,      /* the CUDA launch failed                     */
+  SPEC_ERR_DEVICE = -8       /* no usable device, or V too large for it    */
+};
+
+/* out_status bits */
+enum {
+  SPEC_STATUS_BAD_TOKEN = 1,  /* a draft or history token outside [0,V)       */
+  SPEC_STATUS_BAD_PARAM = 2,  /* T <= 0, alpha <= 0, top_p not in (0,1],
+                                 D not in [0,1], or NaN                      */
+  SPEC_STATUS_BAD_LOGITS = 4, /* NaN or +inf logit (sampling: or a row whose
+                                 logits are all -inf)                        */
+  SPEC_STATUS_BAD_K = 8,      /* K_b < 0, K_b > max_k, or cu_draft broken     */
+  SPEC_STATUS_TIMEOUT = 16    /* an internal wait ran out (not expected)     */
+};
+
+#define SPEC_MAX_K 32
+/* flags: emit no bonus token after a fully accepted draft (the mentored-
+   decoding engine's behaviour; "Even full acceptance did not buy a
+   speedup").  out_tokens slot off_b + K_b is then -1 in that case. */
+#define SPEC_NO_BONUS 1u
+
+typedef struct {
+  int32_t B;             /* requests, >= 1                                   */
+  int32_t V;             /* vocabulary, >= 1                                 */
+  int32_t total_drafts;  /* sum of K_b = cu_draft[B]                         */
+  int32_t max_k;         /* upper bound on every K_b, <= SPEC_MAX_K          */
+  int32_t dtype;         /* SPEC_F32 or SPEC_BF16 (both logit buffers)        */
+  const int32_t *cu_draft;     /* [B+1]                                      */
+  const void *target_logits;   /* [total_drafts + B, ld_target]              */
+  int64_t ld_target;
+  const void *draft_logits;    /* [total_drafts, ld_draft]; unused by greedy */
+  int64_t ld_draft;
+  const int32_t *draft_tokens; /* [total_drafts]                             */
+  const int32_t *cu_hist;      /* [B+1] or NULL (no history)                 */
+  const int32_t *hist_tokens;  /* [cu_hist[B]] or NULL                       */
+  const float *temperature;    /* [B]; unused by greedy                      */
+  const float *rep_penalty;    /* [B] or NULL                                */
+  const float *top_p;          /* [B] or NULL; unused by greedy              */
+  const float *tv_budget;      /* [B]; unused by greedy                      */
+  const float *uniforms;       /* [total_drafts + B]; sampling only          */
+  uint32_t flags;              /* SPEC_NO_BONUS                              */
+} spec_args;
+
+/* Workspace size in bytes for a batch (covers all three entry points). */
+size_t spec_workspace_bytes(int32_t B, int32_t total_drafts, int32_t V);
+
+/* Mentored speculative sampling (see above).  Needs temperature, tv_budget
+   and uniforms. */
+int spec_verify_sample(const spec_args *args, int32_t *out_tokens, int32_t *out_accepted,
+                       int32_t *out_status, void *workspace, size_t ws_bytes, spec_stream_t stream);
+
+/* Greedy longest-prefix verification (see above).  Reads target_logits,
+   draft_tokens, history and rep_penalty only.  The argmax compares the fp32
+   penalised logits and takes the lowest token id on exact ties. */
+int spec_verify_greedy(const spec_args *args, int32_t *out_tokens, int32_t *out_accepted,
+                       int32_t *out_status, void *workspace, size_t ws_bytes, spec_stream_t stream);
+
+/* Per-position mentored-decoding quantities, [total_drafts] each:
+   out_tv = d = TV(p_i, q_i), out_theta = theta_i, out_p_at_draft = p_i(x_i),
+   out_q_at_draft = q_i(x_i) (the last two may be NULL).  Invalid positions
+   get NaN.  Reads no uniforms. */
+int spec_tv_budget(const spec_args *args, float *out_tv, float *out_theta, float *out_p_at_draft,
+                   float *out_q_at_draft, void *workspace, size_t ws_bytes, spec_stream_t stream);
+
+/* A static description of a return code. */
+const char *spec_status_string(int code);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SPEC_VERIFY_H */

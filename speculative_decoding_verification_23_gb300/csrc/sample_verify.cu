@@ -1,0 +1,920 @@
+// Fused mentored speculative sampling for GB300 (sm_103a).
+//
+// One thread-block cluster of C CTAs handles one work item at a time: a
+// draft position (target row i and draft row i of a request) or a request's
+// bonus row (target row K).  Each CTA owns a contiguous slice of the
+// vocabulary.  Per item:
+//
+//   pass 1  a producer warp streams the CTA's slice of each row from HBM into
+//           a shared-memory ring with 1-D TMA bulk copies; 16 consumer warps
+//           apply the repetition penalty and temperature, and store
+//           e = 2^(z*log2(e)/T - ref) per token in shared memory (fp32), one
+//           exponential per logit, ref being a per-warp running reference.
+//           Every logit is read from HBM exactly once.
+//   sync 1  (max, sum) of both rows: warp -> CTA -> cluster through DSMEM.
+//   top-p   (optional) a mass-weighted radix select on the stored values,
+//           four 8-bit digit passes, each reduced across the cluster.
+//   pass 2  from shared memory: r = max(p - q, 0) summed per 256-token chunk;
+//           TV d = sum r ("What I Gave Up to Make Speculative Decoding
+//           Faster", "A knob for accepting more draft tokens":
+//           d = 1/2 sum|p-q|, which equals sum max(p-q,0) for two
+//           distributions).
+//   sync 2  chunk/CTA prefix sums of r across the cluster.
+//   decide  theta = min(1, D/d); pi(x) = (1-theta) p(x) + theta q(x); accept
+//           iff u q(x) < pi(x); the residual candidate = inverse CDF of r at
+//           u_fin (searched in the CTA, chunk and lane that hold it).
+//           Bonus items do the same inverse CDF on p.
+//   emit    the last CTA to finish a request (an atomic counter) scans the K
+//           acceptance flags with a warp ballot and writes the tokens.
+//
+// Acceptance and correction are evaluated speculatively at every position;
+// the uniforms are assigned per position, so this equals evaluating them in
+// order and stopping at the first rejection.
+#include "common.cuh"
+#include "spec_internal.h"
+
+namespace sv {
+
+namespace {
+
+struct Item {
+  int b, i, K;
+  int tgt_row, dft_row;
+  bool bonus;
+  bool rows_ok;
+};
+
+__device__ __forceinline__ Item decode_item(const SampleParams& P, int item) {
+  Item it;
+  if (item < P.total) {
+    int lo = 0, hi = P.B;
+    while (hi - lo > 1) {
+      int mid = (lo + hi) >> 1;
+      if (__ldg(P.cu_draft + mid) <= item) lo = mid; else hi = mid;
+    }
+    it.b = lo;
+    it.i = item - __ldg(P.cu_draft + lo);
+    it.bonus = false;
+    it.tgt_row = item + lo;
+    it.dft_row = item;
+    it.rows_ok = true;
+  } else {
+    int b = item - P.total;
+    int c0 = __ldg(P.cu_draft + b), c1 = __ldg(P.cu_draft + b + 1);
+    it.b = b;
+    it.i = c1 - c0;
+    it.bonus = true;
+    it.rows_ok = (c0 >= 0 && c0 <= c1 && c1 <= P.total);
+    it.tgt_row = it.rows_ok ? c1 + b : b;
+    it.dft_row = -1;
+  }
+  it.K = __ldg(P.cu_draft + it.b + 1) - __ldg(P.cu_draft + it.b);
+  return it;
+}
+
+struct Shared {
+  unsigned char* ring;
+  float* e;          // [2][slice]
+  uint32_t* bitmap;  // [slice/32]
+  float* refc;       // [2][nch]
+  float* fac;        // [2][nch]
+  float* seg;        // [nch]
+  double* pre;       // [nch]
+  float2* wpart;     // [2][16]
+  double* xchg;      // [2][C][kXchgDoubles]
+  float* hist;       // [2 buf][2 rows][256]
+  float* tot;        // [2 rows][256]
+  int* misc_i;       // small ints
+  double* misc_d;    // small doubles
+  uint64_t* full;
+  uint64_t* empty;
+  uint64_t* csync;   // [2]
+};
+
+__device__ __forceinline__ Shared carve(unsigned char* smem, const SmemLayout& L) {
+  Shared S;
+  S.ring = smem;
+  S.e = reinterpret_cast<float*>(smem + L.off_e);
+  S.bitmap = reinterpret_cast<uint32_t*>(smem + L.off_bitmap);
+  S.refc = reinterpret_cast<float*>(smem + L.off_refc);
+  S.fac = reinterpret_cast<float*>(smem + L.off_fac);
+  S.seg = reinterpret_cast<float*>(smem + L.off_seg);
+  S.pre = reinterpret_cast<double*>(smem + L.off_pre);
+  S.wpart = reinterpret_cast<float2*>(smem + L.off_wpart);
+  S.xchg = reinterpret_cast<double*>(smem + L.off_xchg);
+  S.hist = reinterpret_cast<float*>(smem + L.off_hist);
+  S.tot = reinterpret_cast<float*>(smem + L.off_tot);
+  S.misc_d = reinterpret_cast<double*>(smem + L.off_misc);        // 16 doubles
+  S.misc_i = reinterpret_cast<int*>(smem + L.off_misc + 128);     // 16 ints
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.off_bar);
+  S.full = bars;
+  S.empty = bars + L.nslots;
+  S.csync = bars + 2 * L.nslots;
+  return S;
+}
+
+__device__ __forceinline__ void consumer_sync() { named_sync(1, kConsumerThreads); }
+
+// misc_i slots
+constexpr int kMiFlags = 0;      // OR of status bits found by this CTA for the item
+constexpr int kMiFinalize = 2;
+// misc_i[8 + row]: the selected top-p digit.  misc_d slots: p(x), q(x);
+// misc_d[4..7]: top-p mass above / in the selected bin; misc_d[8]: CTA sum.
+constexpr int kMdPx = 0, kMdQx = 1;
+
+// Cluster-wide reduction point: every CTA publishes kXchgDoubles values
+// (written by consumer thread 0 before calling), all CTAs wait, and the
+// values of all CTAs are then readable in S.xchg[buf][c][*].
+struct ClusterPhase {
+  uint32_t cph = 0;  // number of completed cluster phases of this CTA
+  bool failed = false;
+};
+
+__device__ __forceinline__ double* xchg_slot(const Shared& S, int C, uint32_t buf, int c) {
+  return S.xchg + ((size_t)buf * C + c) * kXchgDoubles;
+}
+
+// Thread 0 pushes `vals` to every CTA's exchange slot [buf][rank] and
+// arrives on every CTA's csync[buf]; then every consumer thread waits.
+__device__ __forceinline__ bool cluster_exchange(const Shared& S, ClusterPhase& ph, int C, uint32_t rank,
+                                                 const double* vals, int nvals) {
+  const uint32_t buf = ph.cph & 1u;
+  const uint32_t parity = (ph.cph >> 1) & 1u;
+  if (threadIdx.x == 0) {
+    double* mine = xchg_slot(S, C, buf, (int)rank);
+    for (int c = 0; c < C; ++c) {
+      uint32_t base = map_rank(mine, (uint32_t)c);
+      for (int j = 0; j < nvals; ++j) st_remote_f64(base + 8u * j, vals[j]);
+    }
+    for (int c = 0; c < C; ++c) mbar_arrive_remote(&S.csync[buf], (uint32_t)c);
+  }
+  bool ok = ph.failed ? false : mbar_wait_cluster(&S.csync[buf], parity);
+  if (!ok) ph.failed = true;  // after one timeout, stop waiting
+  ph.cph++;
+  return ok;
+}
+
+// ------------------------------------------------------------------ pass 1
+// Processes one row of the item: waits for each ring stage, converts,
+// penalises, exponentiates and stores e; returns the warp's (ref, sum).
+template <typename T>
+__device__ __forceinline__ void pass1_row(const Shared& S, const SmemLayout& L, int row, int len,
+                                          uint32_t& seq, bool pen, float alpha, float c, int warp,
+                                          int lane, bool& timeout) {
+  const int nch = (len + kChunk - 1) / kChunk;
+  const int nst = (len + kStage - 1) / kStage;
+  float* e_row = S.e + (size_t)row * L.slice;
+  float* refc_row = S.refc + row * L.nch;
+  float refc = 0.f;
+  bool have_ref = false;
+  float Ssum = 0.f;
+  const float kLim = 18446744073709551616.0f;  // 2^64
+  for (int st = 0; st < nst; ++st) {
+    const uint32_t slot = seq % (uint32_t)L.nslots;
+    const uint32_t par = (seq / (uint32_t)L.nslots) & 1u;
+    ++seq;
+    if (!timeout && !mbar_wait(&S.full[slot], par)) timeout = true;  // after one timeout, stop waiting
+    const int k = st * kConsumerWarps + warp;
+    if (k < nch) {
+      const T* chunk = reinterpret_cast<const T*>(S.ring + (size_t)slot * L.slot_bytes) + warp * kChunk;
+      float z[8];
+      load4(chunk + 4 * lane, z);
+      load4(chunk + 128 + 4 * lane, z + 4);
+      const int ib = k * kChunk;
+      if (ib + kChunk > len) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          int idx = ib + (j < 4 ? 4 * lane + j : 128 + 4 * lane + (j - 4));
+          if (idx >= len) z[j] = -INFINITY;
+        }
+      }
+      if (pen) {
+        const uint32_t wa = S.bitmap[(ib >> 5) + (lane >> 3)];
+        const uint32_t wb = S.bitmap[(ib >> 5) + 4 + (lane >> 3)];
+        const uint32_t sh = 4u * (lane & 7);
+        uint32_t m = ((wa >> sh) & 0xFu) | (((wb >> sh) & 0xFu) << 4);
+        while (m) {
+          const int j = __ffs(m) - 1;
+          m &= m - 1;
+#pragma unroll
+          for (int jj = 0; jj < 8; ++jj)
+            if (jj == j) z[jj] = penalize(z[jj], alpha);
+        }
+      }
+      if (!have_ref) {
+        float mx = z[0];
+#pragma unroll
+        for (int j = 1; j < 8; ++j) mx = fmaxf(mx, z[j]);
+        mx = warp_max(mx);
+        refc = (mx > -INFINITY) ? mx * c : 0.f;
+        have_ref = true;
+      }
+      float e[8];
+      float s;
+      {
+        const float2 c2 = make_float2(c, c);
+        const float2 nr = make_float2(-refc, -refc);
+#pragma unroll
+        for (int j = 0; j < 8; j += 2) {
+          float2 y = __ffma2_rn(make_float2(z[j], z[j + 1]), c2, nr);
+          e[j] = ex2(y.x);
+          e[j + 1] = ex2(y.y);
+        }
+        float2 a = __fadd2_rn(make_float2(e[0], e[1]), make_float2(e[2], e[3]));
+        float2 b2 = __fadd2_rn(make_float2(e[4], e[5]), make_float2(e[6], e[7]));
+        a = __fadd2_rn(a, b2);
+        s = a.x + a.y;
+      }
+      if (__any_sync(0xffffffffu, !(s <= kLim))) {
+        float mx = z[0];
+#pragma unroll
+        for (int j = 1; j < 8; ++j) mx = fmaxf(mx, z[j]);
+        mx = warp_max(mx);
+        const float nref = (mx > -INFINITY) ? mx * c : 0.f;
+        if (nref > refc) {
+          Ssum *= ex2(refc - nref);
+          refc = nref;
+        }
+        const float2 c2 = make_float2(c, c);
+        const float2 nr = make_float2(-refc, -refc);
+#pragma unroll
+        for (int j = 0; j < 8; j += 2) {
+          float2 y = __ffma2_rn(make_float2(z[j], z[j + 1]), c2, nr);
+          e[j] = ex2(y.x);
+          e[j + 1] = ex2(y.y);
+        }
+        float2 a = __fadd2_rn(make_float2(e[0], e[1]), make_float2(e[2], e[3]));
+        float2 b2 = __fadd2_rn(make_float2(e[4], e[5]), make_float2(e[6], e[7]));
+        a = __fadd2_rn(a, b2);
+        s = a.x + a.y;
+      }
+      // row capacity is L.slice (a multiple of 64): groups past it are not stored
+      float* dst = e_row + ib;
+      if (ib + 4 * lane < L.slice) *reinterpret_cast<float4*>(dst + 4 * lane) = make_float4(e[0], e[1], e[2], e[3]);
+      if (ib + 128 + 4 * lane < L.slice)
+        *reinterpret_cast<float4*>(dst + 128 + 4 * lane) = make_float4(e[4], e[5], e[6], e[7]);
+      if (lane == 0) refc_row[k] = refc;
+      Ssum += s;
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&S.empty[slot]);
+  }
+  const float Sw = warp_sum(Ssum);
+  if (lane == 0) S.wpart[row * kConsumerWarps + warp] = make_float2(have_ref ? refc : -INFINITY, Sw);
+}
+
+// Combine the 16 warps' (ref, sum) of one row into (M, S) in double.
+__device__ __forceinline__ void cta_combine(const Shared& S, int row, double& M, double& Ssum) {
+  M = -INFINITY;
+  for (int w = 0; w < kConsumerWarps; ++w) {
+    float2 v = S.wpart[row * kConsumerWarps + w];
+    if (v.x > -INFINITY && (double)v.x > M) M = v.x;
+  }
+  Ssum = 0.0;
+  if (M > -INFINITY) {
+    for (int w = 0; w < kConsumerWarps; ++w) {
+      float2 v = S.wpart[row * kConsumerWarps + w];
+      if (v.x > -INFINITY) Ssum += (double)v.y * exp2((double)v.x - M);
+    }
+  }
+}
+
+// Probability of slice element j of a row with chunk factor f (and top-p).
+// The lane's 8 stored values of chunk k (elements 4l..4l+3 and 128+4l..+3),
+// zero past the CTA's live length.
+__device__ __forceinline__ void load_e8(const float* e_row, int k, int lane, int len, float* v) {
+  const int ib = k * kChunk;
+  if (ib + kChunk <= len) {
+    load4(e_row + ib + 4 * lane, v);
+    load4(e_row + ib + 128 + 4 * lane, v + 4);
+  } else {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int idx = ib + (j < 4 ? 4 * lane + j : 128 + 4 * lane + (j - 4));
+      v[j] = idx < len ? e_row[idx] : 0.f;
+    }
+  }
+}
+
+struct RowProb {
+  float tau;     // keep e*g >= tau
+  float invs;    // 1 / kept mass (top-p), multiplies e*g
+  double kept;   // kept mass in units of e*g
+  bool topp;
+};
+
+__device__ __forceinline__ float prob_of(float e, float f, float g, const RowProb& rp) {
+  if (!rp.topp) return e * f;
+  float ef = e * g;
+  return ef >= rp.tau ? ef * rp.invs : 0.f;
+}
+
+}  // namespace
+
+// -------------------------------------------------------------------- kernel
+template <typename T, bool TOPP>
+__global__ void __launch_bounds__(kThreads, 1) sample_verify_kernel(const __grid_constant__ SampleParams P) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  const SmemLayout& L = P.L;
+  Shared S = carve(smem, L);
+  const int C = P.C;
+  const uint32_t rank = cluster_rank();
+  const int cluster_id = blockIdx.x / C;
+  const int v0 = (int)rank * L.slice;
+  const int len = max(0, min(L.slice, P.V - v0));
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int tid = threadIdx.x;
+
+  if (tid == 0) {
+    for (int s = 0; s < L.nslots; ++s) {
+      mbar_init(&S.full[s], 1);
+      mbar_init(&S.empty[s], kConsumerWarps);
+    }
+    mbar_init(&S.csync[0], C);
+    mbar_init(&S.csync[1], C);
+    fence_mbar_init();
+  }
+  cluster_sync_all();
+
+  if (warp == kConsumerWarps) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0 && len > 0) {
+      const uint64_t policy = l2_policy_evict_first();
+      const int es = (int)sizeof(T);
+      const int nst = (len + kStage - 1) / kStage;
+      uint32_t seq = 0;
+      bool ptimeout = false;
+      for (int item = cluster_id; item < P.n_items; item += P.n_clusters) {
+        Item it = decode_item(P, item);
+        const int nrows = it.bonus ? 1 : 2;
+        for (int r = 0; r < nrows; ++r) {
+          const unsigned char* rowp =
+              r == 0 ? static_cast<const unsigned char*>(P.target) + ((size_t)it.tgt_row * P.ld_t + v0) * es
+                     : static_cast<const unsigned char*>(P.draft) + ((size_t)it.dft_row * P.ld_d + v0) * es;
+          for (int st = 0; st < nst; ++st) {
+            const uint32_t slot = seq % (uint32_t)L.nslots;
+            const uint32_t par = ((seq / (uint32_t)L.nslots) & 1u) ^ 1u;
+            ++seq;
+            if (!ptimeout && !mbar_wait(&S.empty[slot], par)) ptimeout = true;  // consumers see their own
+            const int n = min(kStage, len - st * kStage);
+            const uint32_t bytes = (uint32_t)((n * es + 15) & ~15);
+            mbar_arrive_expect_tx(&S.full[slot], bytes);
+            bulk_g2s(S.ring + (size_t)slot * L.slot_bytes, rowp + (size_t)st * kStage * es, bytes, &S.full[slot],
+                     policy);
+          }
+        }
+      }
+    }
+    __syncwarp();
+  } else {
+    // ----------------------------------------------------------- consumers
+    ClusterPhase ph;
+    uint32_t seq = 0;
+    bool timeout = false;
+    for (int item = cluster_id; item < P.n_items; item += P.n_clusters) {
+      const Item it = decode_item(P, item);
+      const int b = it.b;
+      const int K = it.K;
+      const int d0 = __ldg(P.cu_draft + b);
+      const int off = d0 + b;
+      int flags = 0;
+      if (!it.rows_ok || K < 0 || K > P.max_k || K > kMaxK) flags |= kStatusBadK;
+      const float T_ = P.temperature ? __ldg(P.temperature + b) : 1.f;
+      const float alpha = P.rep_penalty ? __ldg(P.rep_penalty + b) : 1.f;
+      const float tp = P.top_p ? __ldg(P.top_p + b) : 1.f;
+      const float D = P.tv_budget ? __ldg(P.tv_budget + b) : 0.f;
+      if (!(T_ > 0.f) || !(T_ < INFINITY) || !(alpha > 0.f) || !(alpha < INFINITY) || !(tp > 0.f) ||
+          !(tp <= 1.f) || !(D >= 0.f) || !(D <= 1.f))
+        flags |= kStatusBadParam;
+      // invalid scalars are reported as such; the row statistics are then
+      // computed with T = 1 and no penalty so they do not add other flags
+      const bool params_ok = !(flags & kStatusBadParam);
+      const float c = (float)(1.4426950408889634 / (params_ok ? (double)T_ : 1.0));
+      const int x = it.bonus ? -1 : __ldg(P.draft_tokens + item);
+      if (!it.bonus && (x < 0 || x >= P.V)) flags |= kStatusBadToken;
+      const int h0 = P.cu_hist ? __ldg(P.cu_hist + b) : 0;
+      const int h1 = P.cu_hist ? __ldg(P.cu_hist + b + 1) : 0;
+      const int npre = it.bonus ? (it.rows_ok ? K : 0) : it.i;  // drafts before this row
+      const bool pen = params_ok && (alpha != 1.f) && ((h1 > h0) || npre > 0) && len > 0;
+
+      // ---- penalty set of this row within the CTA slice; token validity
+      if (tid == 0) S.misc_i[kMiFlags] = 0;
+      if (pen) {
+        for (int w = tid; w < L.nch * 8; w += kConsumerThreads) S.bitmap[w] = 0u;
+      }
+      consumer_sync();
+      for (int j = h0 + tid; j < h1; j += kConsumerThreads) {
+        const int t = __ldg(P.hist + j);
+        if (t < 0 || t >= P.V) flags |= kStatusBadToken;
+        else if (pen && t >= v0 && t < v0 + len) atomicOr(&S.bitmap[(t - v0) >> 5], 1u << ((t - v0) & 31));
+      }
+      for (int j = tid; j < npre; j += kConsumerThreads) {
+        const int t = __ldg(P.draft_tokens + d0 + j);
+        if (t < 0 || t >= P.V) flags |= kStatusBadToken;
+        else if (pen && t >= v0 && t < v0 + len) atomicOr(&S.bitmap[(t - v0) >> 5], 1u << ((t - v0) & 31));
+      }
+      consumer_sync();
+
+      // ---- pass 1 over the target row, then the draft row
+      pass1_row<T>(S, L, 0, len, seq, pen, alpha, c, warp, lane, timeout);
+      if (!it.bonus) pass1_row<T>(S, L, 1, len, seq, pen, alpha, c, warp, lane, timeout);
+      consumer_sync();
+
+      // ---- sync 1: (M, S) per row across the cluster
+      {
+        double v[kXchgDoubles];
+        if (tid == 0) {
+          cta_combine(S, 0, v[0], v[1]);
+          if (!it.bonus) cta_combine(S, 1, v[2], v[3]); else { v[2] = -INFINITY; v[3] = 0.0; }
+        }
+        if (!cluster_exchange(S, ph, C, rank, v, 4)) timeout = true;
+      }
+      double Mr[2], Sr[2];
+      {
+        const uint32_t buf = (ph.cph - 1) & 1u;
+        for (int r = 0; r < 2; ++r) {
+          double M = -INFINITY;
+          for (int cc = 0; cc < C; ++cc) {
+            double m = xchg_slot(S, C, buf, cc)[2 * r];
+            if (m > M) M = m;
+          }
+          double s = 0.0;
+          if (M > -INFINITY)
+            for (int cc = 0; cc < C; ++cc) {
+              const double* xs = xchg_slot(S, C, buf, cc);
+              if (xs[2 * r] > -INFINITY) s += xs[2 * r + 1] * exp2(xs[2 * r] - M);
+            }
+          Mr[r] = M;
+          Sr[r] = s;
+        }
+      }
+      const int nrows = it.bonus ? 1 : 2;
+      for (int r = 0; r < nrows; ++r)
+        if (!(Sr[r] > 0.0) || !(Sr[r] < INFINITY) || !(Mr[r] < INFINITY)) flags |= kStatusBadLogits;
+      const bool ok_stats = !(flags & kStatusBadLogits);
+
+      // ---- chunk factors: g = 2^(ref_k - M), fac = g / S
+      {
+        const int nch = (len + kChunk - 1) / kChunk;
+        for (int j = tid; j < nrows * nch; j += kConsumerThreads) {
+          const int r = j / nch, k = j % nch;
+          const double g = ok_stats ? exp2((double)S.refc[r * L.nch + k] - Mr[r]) : 0.0;
+          S.fac[r * L.nch + k] = ok_stats ? (float)(g / Sr[r]) : 0.f;
+          // top-p uses g itself; keep it in the seg scratch? store in tot? use refc slot:
+          S.refc[r * L.nch + k] = (float)g;  // refc no longer needed: becomes g
+        }
+      }
+      consumer_sync();
+
+      // ---- optional top-p: tau per row (mass-weighted radix select on e*g)
+      RowProb rp[2];
+      rp[0].topp = rp[1].topp = false;
+      rp[0].tau = rp[1].tau = 0.f;
+      rp[0].invs = rp[1].invs = 0.f;
+      rp[0].kept = rp[1].kept = 1.0;
+      if constexpr (TOPP) {
+        if (params_ok && tp < 1.f && ok_stats) {
+          const int nch = (len + kChunk - 1) / kChunk;
+          uint32_t prefix[2] = {0u, 0u};
+          double above[2] = {0.0, 0.0};
+          double target[2] = {(double)tp * Sr[0], (double)tp * Sr[1]};
+          double kept[2] = {Sr[0], Sr[1]};
+          for (int pass = 0; pass < 4; ++pass) {
+            const int shift = 24 - 8 * pass;
+            const uint32_t hb = ph.cph & 1u;
+            float* hist = S.hist + hb * 512;
+            for (int j = tid; j < 512; j += kConsumerThreads) hist[j] = 0.f;
+            consumer_sync();
+            for (int r = 0; r < nrows; ++r) {
+              const float* er = S.e + (size_t)r * L.slice;
+              for (int k = warp; k < nch; k += kConsumerWarps) {
+                const float g = S.refc[r * L.nch + k];
+                float ev[8];
+                load_e8(er, k, lane, len, ev);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                  const float ef = ev[j] * g;
+                  const uint32_t key = __float_as_uint(ef);
+                  const bool match = pass == 0 || (key >> (shift + 8)) == (prefix[r] >> (shift + 8));
+                  if (match && ef > 0.f) atomicAdd(&hist[r * 256 + ((key >> shift) & 255u)], ef);
+                }
+              }
+            }
+            fence_acq_rel_cluster();
+            consumer_sync();
+            if (!cluster_exchange(S, ph, C, rank, nullptr, 0)) timeout = true;
+            // gather the C histograms: thread -> (row, bin)
+            {
+              const int r = tid >> 8, bin = tid & 255;
+              double s = 0.0;
+              if (r < nrows)
+                for (int cc = 0; cc < C; ++cc) s += (double)ld_remote_f32(map_rank(&hist[r * 256 + bin], (uint32_t)cc));
+              S.tot[r * 256 + bin] = (float)s;
+            }
+            consumer_sync();
+            if (warp < nrows) {
+              const int r = warp;
+              // lane owns bins [8*lane, 8*lane+8); find the largest digit d with
+              // above + sum_{bins >= d} >= target
+              double lsum = 0.0;
+              for (int j = 0; j < 8; ++j) lsum += (double)S.tot[r * 256 + 8 * lane + j];
+              // suffix sums over lanes: exclusive sum of lanes above
+              double incl = lsum;
+              for (int o = 1; o < 32; o <<= 1) {
+                double t = __shfl_down_sync(0xffffffffu, incl, o);
+                if (lane + o < 32) incl += t;
+              }
+              const double excl = incl - lsum;  // mass of bins above this lane's block
+              const double need = target[r] - above[r];
+              const bool hit = (excl < need) && (excl + lsum >= need);
+              unsigned m = __ballot_sync(0xffffffffu, hit);
+              int dsel = 0;
+              double new_above = above[r];
+              double binmass = 0.0;
+              if (m) {
+                const int L0 = 31 - __clz(m);  // highest lane whose block crosses (there is one)
+                double cum = __shfl_sync(0xffffffffu, excl, L0);
+                int dd = 8 * L0;
+                double bm = 0.0;
+                for (int j = 7; j >= 0; --j) {
+                  const double v = (double)S.tot[r * 256 + 8 * L0 + j];
+                  if (cum + v >= need) { dd = 8 * L0 + j; bm = v; break; }
+                  cum += v;
+                }
+                dsel = dd;
+                new_above = above[r] + cum;
+                binmass = bm;
+              } else {
+                // rounding: nothing reaches the target -> keep everything down to the lowest non-empty bin
+                double cum = 0.0;
+                int dd = 0;
+                double bm = 0.0;
+                for (int j = 255; j >= 0; --j) {
+                  const double v = (double)S.tot[r * 256 + j];
+                  if (v > 0.0) { dd = j; bm = v; }
+                }
+                for (int j = 255; j > dd; --j) cum += (double)S.tot[r * 256 + j];
+                dsel = dd;
+                new_above = above[r] + cum;
+                binmass = bm;
+              }
+              if (lane == 0) {
+                S.misc_i[8 + r] = dsel;
+                S.misc_d[4 + 2 * r] = new_above;
+                S.misc_d[5 + 2 * r] = binmass;
+              }
+            }
+            consumer_sync();
+            for (int r = 0; r < nrows; ++r) {
+              prefix[r] |= ((uint32_t)S.misc_i[8 + r]) << shift;
+              above[r] = S.misc_d[4 + 2 * r];
+              kept[r] = above[r] + S.misc_d[5 + 2 * r];
+            }
+            consumer_sync();
+          }
+          for (int r = 0; r < nrows; ++r) {
+            rp[r].topp = true;
+            rp[r].tau = __uint_as_float(prefix[r]);
+            rp[r].invs = (float)(1.0 / kept[r]);
+            rp[r].kept = kept[r];
+          }
+        }
+      }
+
+      // ---- p(x), q(x) by the CTA that holds x
+      if (!it.bonus && tid == 0 && x >= v0 && x < v0 + len) {
+        const int j = x - v0, k = j / kChunk;
+        double pv, qv;
+        if (rp[0].topp) {
+          const float ef = S.e[j] * S.refc[k];
+          pv = ef >= rp[0].tau ? (double)ef / rp[0].kept : 0.0;
+          const float eq = S.e[L.slice + j] * S.refc[L.nch + k];
+          qv = eq >= rp[1].tau ? (double)eq / rp[1].kept : 0.0;
+        } else {
+          pv = (double)S.e[j] * ((double)S.refc[k] / Sr[0]);
+          qv = (double)S.e[L.slice + j] * ((double)S.refc[L.nch + k] / Sr[1]);
+        }
+        S.misc_d[kMdPx] = pv;
+        S.misc_d[kMdQx] = qv;
+      }
+
+      // ---- pass 2: per-chunk sums of r = max(p - q, 0) (positions) or p (bonus)
+      const double u_fin = P.mode == kModeSample ? (double)__ldg(P.uniforms + off + K) : 0.0;
+      bool cdf_of_p = it.bonus;
+      double R = 0.0, Pc = 0.0, Rc = 0.0;
+      double Rcs[kMaxCluster];
+      const int nch = (len + kChunk - 1) / kChunk;
+      for (int attempt = 0; attempt < 2; ++attempt) {
+        for (int k = warp; k < nch; k += kConsumerWarps) {
+          const float fp = S.fac[k], gp = S.refc[k];
+          float e1[8];
+          load_e8(S.e, k, lane, len, e1);
+          float s = 0.f;
+          if (cdf_of_p) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) s += prob_of(e1[j], fp, gp, rp[0]);
+          } else {
+            const float fq = S.fac[L.nch + k], gq = S.refc[L.nch + k];
+            float e2[8];
+            load_e8(S.e + L.slice, k, lane, len, e2);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) s += fmaxf(prob_of(e1[j], fp, gp, rp[0]) - prob_of(e2[j], fq, gq, rp[1]), 0.f);
+          }
+          s = warp_sum(s);
+          if (lane == 0) S.seg[k] = s;
+        }
+        consumer_sync();
+        if (warp == 0) {
+          double run = 0.0;
+          for (int k0 = 0; k0 < nch; k0 += 32) {
+            const int k = k0 + lane;
+            const double v = k < nch ? (double)S.seg[k] : 0.0;
+            const double inc = warp_incl_scan_d(v, lane);
+            if (k < nch) S.pre[k] = run + inc - v;  // exclusive prefix
+            run += __shfl_sync(0xffffffffu, inc, 31);
+          }
+          if (lane == 0) S.misc_d[8] = run;
+        }
+        consumer_sync();
+        {
+          double v[kXchgDoubles];
+          v[0] = S.misc_d[8];
+          if (!cluster_exchange(S, ph, C, rank, v, 1)) timeout = true;
+        }
+        const uint32_t buf = (ph.cph - 1) & 1u;
+        R = 0.0;
+        for (int cc = 0; cc < C; ++cc) {
+          const double rc = xchg_slot(S, C, buf, cc)[0];
+          Rcs[cc] = rc;
+          R += rc;
+        }
+        Pc = 0.0;
+        for (int cc = 0; cc < (int)rank; ++cc) Pc += Rcs[cc];
+        Rc = Rcs[rank];
+        if (!cdf_of_p && !(R > 0.0) && P.mode == kModeSample) {
+          cdf_of_p = true;  // no residual mass: draw from p (never reached when a rejection is possible)
+          Pc = 0.0;
+          continue;
+        }
+        break;
+      }
+
+      // ---- decisions
+      const double tv = (it.bonus || cdf_of_p) ? 0.0 : fmin(R, 1.0);
+      const double theta = (tv <= (double)D) ? 1.0 : (double)D / tv;
+      const bool x_owner = !it.bonus && x >= v0 && x < v0 + len;
+      double pv = 0.0, qv = 0.0;
+      if (x_owner && tid == 0) {
+        pv = S.misc_d[kMdPx];
+        qv = S.misc_d[kMdQx];
+        const double pi = (1.0 - theta) * pv + theta * qv;
+        const double u = P.mode == kModeSample ? (double)__ldg(P.uniforms + off + it.i) : 0.0;
+        if (P.results) {
+          ItemResult* res = P.results + item;
+          res->acc = (u * qv < pi) ? 1 : 0;
+          res->px = (float)pv;
+          res->qx = (float)qv;
+        }
+      }
+      if (!it.bonus && tid == 0 && rank == 0 && P.results) {
+        P.results[item].tv = (float)tv;
+        P.results[item].theta = (float)theta;
+      }
+
+      // ---- candidate: inverse CDF at u_fin within the owning CTA
+      if (P.mode == kModeSample && ok_stats) {
+        const double t = u_fin * R;
+        // owner CTA: first with prefix+mass > t, else the last with mass > 0
+        int owner = -1, last_pos = -1;
+        {
+          double run = 0.0;
+          for (int cc = 0; cc < C; ++cc) {
+            if (Rcs[cc] > 0.0) last_pos = cc;
+            if (owner < 0 && run + Rcs[cc] > t && Rcs[cc] > 0.0) owner = cc;
+            run += Rcs[cc];
+          }
+        }
+        const bool take_last = owner < 0;
+        if (take_last) owner = last_pos;
+        if (owner == (int)rank && warp == 0) {
+          const double tl = t - Pc;
+          int ks = -1, klast = -1;
+          for (int k = 0; k < nch; ++k) {
+            if (S.seg[k] > 0.f) klast = k;
+            if (!take_last && ks < 0 && S.pre[k] + (double)S.seg[k] > tl && S.seg[k] > 0.f) ks = k;
+          }
+          bool tl_last = take_last;
+          if (ks < 0) { ks = klast; tl_last = true; }
+          int found = -1;
+          if (ks >= 0) {
+            const float fp = S.fac[ks], gp = S.refc[ks];
+            float e1[8], w[8];
+            load_e8(S.e, ks, lane, len, e1);
+            if (cdf_of_p) {
+#pragma unroll
+              for (int j = 0; j < 8; ++j) w[j] = prob_of(e1[j], fp, gp, rp[0]);
+            } else {
+              const float fq = S.fac[L.nch + ks], gq = S.refc[L.nch + ks];
+              float e2[8];
+              load_e8(S.e + L.slice, ks, lane, len, e2);
+#pragma unroll
+              for (int j = 0; j < 8; ++j) w[j] = fmaxf(prob_of(e1[j], fp, gp, rp[0]) - prob_of(e2[j], fq, gq, rp[1]), 0.f);
+            }
+            double rem = tl - S.pre[ks];
+            if (!tl_last) {
+              for (int half = 0; half < 2 && found < 0; ++half) {
+                const float* wh = w + 4 * half;
+                const float ls = (wh[0] + wh[1]) + (wh[2] + wh[3]);
+                const float inc = warp_incl_scan(ls, lane);
+                const float exc = inc - ls;
+                const bool hit = ((double)inc > rem) && ((double)exc <= rem) && ls > 0.f;
+                const unsigned m = __ballot_sync(0xffffffffu, hit);
+                if (m) {
+                  const int L0 = __ffs(m) - 1;
+                  int jj = -1;
+                  if (lane == L0) {
+                    double cum = (double)exc;
+                    for (int j = 0; j < 4; ++j) {
+                      cum += (double)wh[j];
+                      if (wh[j] > 0.f && cum > rem) { jj = j; break; }
+                    }
+                    if (jj < 0) {
+                      for (int j = 3; j >= 0; --j) if (wh[j] > 0.f) { jj = j; break; }
+                    }
+                  }
+                  jj = __shfl_sync(0xffffffffu, jj, L0);
+                  found = ks * kChunk + 128 * half + 4 * L0 + jj;
+                } else {
+                  rem -= (double)__shfl_sync(0xffffffffu, inc, 31);
+                }
+              }
+            }
+            if (found < 0) {
+              // the last element with positive mass in the chunk
+              int best = -1;
+              for (int half = 1; half >= 0 && best < 0; --half) {
+                int lj = -1;
+                for (int j = 3; j >= 0; --j) if (w[4 * half + j] > 0.f) { lj = j; break; }
+                const unsigned m = __ballot_sync(0xffffffffu, lj >= 0);
+                if (m) {
+                  const int L0 = 31 - __clz(m);
+                  lj = __shfl_sync(0xffffffffu, lj, L0);
+                  best = ks * kChunk + 128 * half + 4 * L0 + lj;
+                }
+              }
+              found = best;
+            }
+          }
+          if (lane == 0) P.results[item].cand = found >= 0 ? v0 + found : -1;
+        }
+      }
+
+      // ---- status of this CTA's share of the item; arrival count
+      if (timeout) flags |= kStatusTimeout;
+      flags = warp_or(flags);
+      if (lane == 0 && flags) atomicOr(&S.misc_i[kMiFlags], flags);
+      __threadfence();
+      consumer_sync();
+      if (P.mode == kModeTvOnly && tid == 0) {
+        // every CTA checks the same scalars, tokens and row statistics, so its
+        // flags are the request's
+        const bool bad = S.misc_i[kMiFlags] != 0;
+        if (rank == 0) {
+          P.out_tv[item] = bad ? NAN : (float)tv;
+          if (P.out_theta) P.out_theta[item] = bad ? NAN : (float)theta;
+        }
+        if (x_owner) {
+          if (P.out_px) P.out_px[item] = bad ? NAN : (float)pv;
+          if (P.out_qx) P.out_qx[item] = bad ? NAN : (float)qv;
+        } else if (rank == 0 && !(x >= 0 && x < P.V)) {
+          if (P.out_px) P.out_px[item] = NAN;
+          if (P.out_qx) P.out_qx[item] = NAN;
+        }
+      }
+      if (P.mode == kModeSample) {
+        if (tid == 0) {
+          P.inval[(size_t)item * kMaxCluster + rank] = S.misc_i[kMiFlags];
+          __threadfence();
+          const int target = C * (K + 1);
+          const int old = atomicAdd(P.counters + b, 1);
+          S.misc_i[kMiFinalize] = (old == target - 1) && K >= 0 && it.rows_ok;
+        }
+        consumer_sync();
+        if (S.misc_i[kMiFinalize] && warp == 0) {
+          __threadfence();
+          // gather per-position flags and candidates of request b
+          int st = 0;
+          const int nitems_b = K + 1;
+          for (int j = lane; j < nitems_b * C; j += 32) {
+            const int ii = j / C, cc = j % C;
+            const int item_j = ii < K ? d0 + ii : P.total + b;
+            st |= __ldcg(P.inval + (size_t)item_j * kMaxCluster + cc);
+          }
+          st = warp_or(st);
+          int acc = 1;
+          if (lane < K) acc = __ldcg(&P.results[d0 + lane].acc);
+          const unsigned rej = __ballot_sync(0xffffffffu, lane < K && acc == 0);
+          const int jrej = rej ? __ffs(rej) - 1 : K;
+          const bool nobonus = (P.flags & 1u) != 0;
+          int last;
+          if (jrej < K) last = __ldcg(&P.results[d0 + jrej].cand);
+          else last = nobonus ? -1 : __ldcg(&P.results[P.total + b].cand);
+          for (int s = lane; s <= K; s += 32) {
+            int tok;
+            if (st) tok = -1;
+            else if (s < jrej) tok = __ldg(P.draft_tokens + d0 + s);
+            else if (s == jrej) tok = last;
+            else tok = -1;
+            P.out_tokens[off + s] = tok;
+          }
+          if (lane == 0) {
+            P.out_accepted[b] = st ? -1 : jrej;
+            if (P.out_status) P.out_status[b] = st;
+            P.counters[b] = 0;
+          }
+        }
+      }
+      consumer_sync();
+    }
+  }
+  // no CTA may leave while others can still read its shared memory
+  cluster_sync_all();
+}
+
+// Explicit instantiations.
+template __global__ void sample_verify_kernel<float, false>(const __grid_constant__ SampleParams);
+template __global__ void sample_verify_kernel<float, true>(const __grid_constant__ SampleParams);
+template __global__ void sample_verify_kernel<__nv_bfloat16, false>(const __grid_constant__ SampleParams);
+template __global__ void sample_verify_kernel<__nv_bfloat16, true>(const __grid_constant__ SampleParams);
+
+}  // namespace sv
+
+namespace sv {
+
+namespace {
+
+template <typename T, bool TOPP>
+int launch_t(SampleParams& P, cudaStream_t stream) {
+  auto kern = sample_verify_kernel<T, TOPP>;
+  const int smem = P.L.total;
+  // attributes are per function and cheap to set; do it on every call so a
+  // new device or a larger layout is always covered
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) return -8;
+  if (P.C > 8 && cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
+    return -8;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = P.C;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  // clusters that fit on the device at once (cached per configuration)
+  static thread_local int cached_dev = -1, cached_C = 0, cached_smem = 0, cached_n = 0;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev != cached_dev || cached_C != P.C || cached_smem != smem) {
+    cfg.gridDim = dim3(P.C);
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n <= 0) {
+      cudaGetLastError();
+      return -8;
+    }
+    cached_dev = dev; cached_C = P.C; cached_smem = smem; cached_n = n;
+  }
+  P.n_clusters = P.n_items < cached_n ? P.n_items : cached_n;
+  if (P.n_clusters <= 0) return 0;
+  cfg.gridDim = dim3(P.n_clusters * P.C);
+  if (cudaLaunchKernelEx(&cfg, kern, P) != cudaSuccess) {
+    cudaGetLastError();
+    return -7;
+  }
+  return 0;
+}
+
+}  // namespace
+
+// Smallest cluster (1..16) whose per-CTA slice fits in shared memory.
+int choose_sample_layout(int V, int elem_bytes, bool topp, int max_smem, int* C_out, SmemLayout* L_out) {
+  for (int C = 1; C <= kMaxCluster; C *= 2) {
+    SmemLayout L = make_sample_layout(V, C, elem_bytes, topp);
+    if (L.total <= max_smem) {
+      *C_out = C;
+      *L_out = L;
+      return 0;
+    }
+  }
+  return -1;
+}
+
+int launch_sample_verify(SampleParams& P, bool bf16, bool topp, cudaStream_t stream) {
+  if (bf16) return topp ? launch_t<__nv_bfloat16, true>(P, stream) : launch_t<__nv_bfloat16, false>(P, stream);
+  return topp ? launch_t<float, true>(P, stream) : launch_t<float, false>(P, stream);
+}
+
+}  // namespace sv

@@ -1,0 +1,153 @@
+// Internal parameter blocks and workspace layout shared by the entry points
+// (spec_verify.cu) and the kernels.  Host and device code.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+namespace sv {
+
+// ----------------------------------------------------------------- sampling
+constexpr int kChunk = 256;                 // elements per warp-chunk
+constexpr int kConsumerWarps = 16;
+constexpr int kConsumerThreads = kConsumerWarps * 32;
+constexpr int kThreads = kConsumerThreads + 32;  // + one producer warp
+constexpr int kStage = kConsumerWarps * kChunk;  // elements per ring slot
+constexpr int kRingBytes = 64 * 1024;
+constexpr int kXchgDoubles = 8;             // per CTA per exchange buffer
+constexpr int kMaxCluster = 16;
+
+enum SampleMode : int { kModeSample = 0, kModeTvOnly = 1 };
+
+struct ItemResult {       // one per work item (a draft position or a bonus row)
+  int acc;                // acceptance flag (positions)
+  int cand;               // residual candidate (positions) / bonus token
+  float tv, theta, px, qx;
+  int pad[2];
+};
+
+struct SmemLayout {
+  int slice;      // token ids per CTA (multiple of 64)
+  int nch;        // chunks per CTA slice (ceil(slice / 256))
+  int nslots;     // ring slots
+  int slot_bytes;
+  int off_e, off_bitmap, off_refc, off_fac, off_seg, off_pre, off_wpart, off_xchg, off_hist, off_tot,
+      off_misc, off_bar;
+  int total;
+};
+
+inline int align_up_i(int x, int a) { return (x + a - 1) / a * a; }
+
+// Shared-memory layout of the sampling kernel for cluster size C.
+inline SmemLayout make_sample_layout(int V, int C, int elem_bytes, bool topp) {
+  SmemLayout L{};
+  int per = (V + C - 1) / C;
+  L.slice = align_up_i(per, 64);
+  L.nch = (L.slice + kChunk - 1) / kChunk;
+  L.slot_bytes = kStage * elem_bytes;
+  L.nslots = kRingBytes / L.slot_bytes;
+  int off = kRingBytes;
+  L.off_e = off;        off += 2 * L.slice * 4;
+  L.off_bitmap = off;   off += L.nch * 8 * 4;   // 8 words per 256-token chunk
+  L.off_refc = off;     off += align_up_i(2 * L.nch * 4, 16);
+  L.off_fac = off;      off += align_up_i(2 * L.nch * 4, 16);
+  L.off_seg = off;      off += align_up_i(L.nch * 4, 16);
+  L.off_pre = off;      off += align_up_i(L.nch * 8, 16);
+  L.off_wpart = off;    off += 2 * kConsumerWarps * 8;
+  L.off_xchg = off;     off += 2 * C * kXchgDoubles * 8;
+  L.off_hist = off;     off += topp ? 2 * 2 * 256 * 4 : 0;
+  L.off_tot = off;      off += topp ? 2 * 256 * 4 : 0;
+  L.off_misc = off;     off += 256;
+  L.off_bar = off;      off += (2 * L.nslots + 2) * 8;
+  L.total = align_up_i(off, 128);
+  return L;
+}
+
+struct SampleParams {
+  const void* target;
+  long long ld_t;
+  const void* draft;
+  long long ld_d;
+  const int* cu_draft;
+  const int* draft_tokens;
+  const int* cu_hist;
+  const int* hist;
+  const float* temperature;
+  const float* rep_penalty;
+  const float* top_p;
+  const float* tv_budget;
+  const float* uniforms;
+  int B, V, total, max_k;
+  unsigned flags;
+  int mode;
+  // outputs
+  int* out_tokens;
+  int* out_accepted;
+  int* out_status;
+  float* out_tv;
+  float* out_theta;
+  float* out_px;
+  float* out_qx;
+  // workspace
+  int* counters;         // [B]
+  ItemResult* results;   // [total + B]
+  int* inval;            // [(total + B) * kMaxCluster]
+  // geometry
+  int C;
+  int n_items;
+  int n_clusters;
+  SmemLayout L;
+};
+
+// ------------------------------------------------------------------- greedy
+constexpr int kGreedyThreads = 256;
+constexpr int kGreedyChunk = 8192;   // elements per CTA
+
+struct GreedyPartial {
+  float val;
+  int idx;
+  int flags;
+  int pad;
+};
+
+struct GreedyParams {
+  const void* target;
+  long long ld_t;
+  const int* cu_draft;
+  const int* draft_tokens;
+  const int* cu_hist;
+  const int* hist;
+  const float* rep_penalty;
+  int B, V, total, max_k;
+  int nck;               // chunks per row
+  int* out_tokens;
+  int* out_accepted;
+  int* out_status;
+  int* counters;         // [B]
+  GreedyPartial* partials;  // [(total + B) * nck]
+};
+
+// -------------------------------------------------------------- workspace
+struct WorkspaceLayout {
+  size_t off_counters, off_results, off_inval, off_partials, total;
+};
+
+inline size_t align_up_z(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+inline WorkspaceLayout make_workspace_layout(int B, int total, int V) {
+  WorkspaceLayout W{};
+  size_t items = (size_t)total + (size_t)B;
+  size_t nck = ((size_t)V + kGreedyChunk - 1) / kGreedyChunk;
+  W.off_counters = 0;
+  size_t off = align_up_z((size_t)B * 4, 256);
+  W.off_results = off;
+  off = align_up_z(off + items * sizeof(ItemResult), 256);
+  W.off_inval = off;
+  off = align_up_z(off + items * kMaxCluster * 4, 256);
+  W.off_partials = off;
+  off = align_up_z(off + items * nck * sizeof(GreedyPartial), 256);
+  W.total = off;
+  return W;
+}
+
+}  // namespace sv

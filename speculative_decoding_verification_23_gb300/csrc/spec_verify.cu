@@ -1,0 +1,211 @@
+// C ABI of libspecverify.so: host-side validation, workspace layout and
+// launches.  No entry point allocates, frees or synchronises; all device
+// work is enqueued on the caller's stream.
+#include <cstdint>
+#include <cstring>
+
+#include <cuda_runtime.h>
+
+#include "spec_verify.h"
+#include "spec_internal.h"
+
+namespace sv {
+int choose_sample_layout(int V, int elem_bytes, bool topp, int max_smem, int* C_out, SmemLayout* L_out);
+int launch_sample_verify(SampleParams& P, bool bf16, bool topp, cudaStream_t stream);
+int launch_greedy_verify(const GreedyParams& P, bool bf16, cudaStream_t stream);
+}  // namespace sv
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int elem_bytes(int dtype) { return dtype == SPEC_BF16 ? 2 : 4; }
+
+// Checks shared by all entry points.  `need_draft`: draft logits are read.
+int check_common(const spec_args* a, bool need_draft) {
+  if (!a) return SPEC_ERR_NULL;
+  if (a->dtype != SPEC_F32 && a->dtype != SPEC_BF16) return SPEC_ERR_DTYPE;
+  if (a->B < 1 || a->V < 1 || a->total_drafts < 0 || a->max_k < 0) return SPEC_ERR_SHAPE;
+  if (a->max_k > SPEC_MAX_K) return SPEC_ERR_K_TOO_LARGE;
+  if ((long long)a->total_drafts > (long long)a->B * a->max_k) return SPEC_ERR_SHAPE;
+  if (!a->cu_draft || !a->target_logits) return SPEC_ERR_NULL;
+  if (a->total_drafts > 0 && !a->draft_tokens) return SPEC_ERR_NULL;
+  if (a->cu_hist && !a->hist_tokens) return SPEC_ERR_NULL;
+  const int es = elem_bytes(a->dtype);
+  if (a->ld_target < a->V) return SPEC_ERR_SHAPE;
+  if (!aligned16(a->target_logits) || (a->ld_target * es) % 16 != 0) return SPEC_ERR_ALIGN;
+  if (need_draft && a->total_drafts > 0) {
+    if (!a->draft_logits) return SPEC_ERR_NULL;
+    if (a->ld_draft < a->V) return SPEC_ERR_SHAPE;
+    if (!aligned16(a->draft_logits) || (a->ld_draft * es) % 16 != 0) return SPEC_ERR_ALIGN;
+  }
+  return SPEC_OK;
+}
+
+int check_workspace(const spec_args* a, const void* ws, size_t ws_bytes) {
+  if (!ws) return SPEC_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return SPEC_ERR_WORKSPACE;
+  if (ws_bytes < spec_workspace_bytes(a->B, a->total_drafts, a->V)) return SPEC_ERR_WORKSPACE;
+  return SPEC_OK;
+}
+
+int device_max_smem(int* out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) { cudaGetLastError(); return SPEC_ERR_DEVICE; }
+  int v = 0;
+  if (cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess) {
+    cudaGetLastError();
+    return SPEC_ERR_DEVICE;
+  }
+  *out = v;
+  return SPEC_OK;
+}
+
+void fill_sample_inputs(sv::SampleParams& P, const spec_args* a) {
+  std::memset(&P, 0, sizeof(P));
+  P.target = a->target_logits;
+  P.ld_t = a->ld_target;
+  P.draft = a->draft_logits;
+  P.ld_d = a->ld_draft;
+  P.cu_draft = a->cu_draft;
+  P.draft_tokens = a->draft_tokens;
+  P.cu_hist = a->cu_hist;
+  P.hist = a->hist_tokens;
+  P.temperature = a->temperature;
+  P.rep_penalty = a->rep_penalty;
+  P.top_p = a->top_p;
+  P.tv_budget = a->tv_budget;
+  P.uniforms = a->uniforms;
+  P.B = a->B;
+  P.V = a->V;
+  P.total = a->total_drafts;
+  P.max_k = a->max_k;
+  P.flags = a->flags;
+}
+
+int run_sample(sv::SampleParams& P, const spec_args* a, void* ws, cudaStream_t stream) {
+  int max_smem = 0;
+  int rc = device_max_smem(&max_smem);
+  if (rc) return rc;
+  const bool topp = a->top_p != nullptr;
+  int C = 1;
+  sv::SmemLayout L{};
+  if (sv::choose_sample_layout(a->V, elem_bytes(a->dtype), topp, max_smem, &C, &L) != 0) return SPEC_ERR_SHAPE;
+  const sv::WorkspaceLayout W = sv::make_workspace_layout(a->B, a->total_drafts, a->V);
+  unsigned char* w = static_cast<unsigned char*>(ws);
+  P.counters = reinterpret_cast<int*>(w + W.off_counters);
+  P.results = reinterpret_cast<sv::ItemResult*>(w + W.off_results);
+  P.inval = reinterpret_cast<int*>(w + W.off_inval);
+  P.C = C;
+  P.L = L;
+  if (P.mode == sv::kModeSample) {
+    if (cudaMemsetAsync(P.counters, 0, (size_t)a->B * sizeof(int), stream) != cudaSuccess) {
+      cudaGetLastError();
+      return SPEC_ERR_LAUNCH;
+    }
+  }
+  rc = sv::launch_sample_verify(P, a->dtype == SPEC_BF16, topp, stream);
+  return rc;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t spec_workspace_bytes(int32_t B, int32_t total_drafts, int32_t V) {
+  if (B < 0 || total_drafts < 0 || V < 0) return 0;
+  return sv::make_workspace_layout(B, total_drafts, V).total;
+}
+
+int spec_verify_sample(const spec_args* a, int32_t* out_tokens, int32_t* out_accepted, int32_t* out_status,
+                       void* workspace, size_t ws_bytes, spec_stream_t stream) {
+  int rc = check_common(a, true);
+  if (rc) return rc;
+  if (!out_tokens || !out_accepted || !a->temperature || !a->tv_budget || !a->uniforms) return SPEC_ERR_NULL;
+  rc = check_workspace(a, workspace, ws_bytes);
+  if (rc) return rc;
+  sv::SampleParams P;
+  fill_sample_inputs(P, a);
+  P.mode = sv::kModeSample;
+  P.out_tokens = out_tokens;
+  P.out_accepted = out_accepted;
+  P.out_status = out_status;
+  P.n_items = a->total_drafts + a->B;
+  return run_sample(P, a, workspace, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int spec_tv_budget(const spec_args* a, float* out_tv, float* out_theta, float* out_p_at_draft,
+                   float* out_q_at_draft, void* workspace, size_t ws_bytes, spec_stream_t stream) {
+  int rc = check_common(a, true);
+  if (rc) return rc;
+  if (!out_tv || !out_theta || !a->temperature || !a->tv_budget) return SPEC_ERR_NULL;
+  rc = check_workspace(a, workspace, ws_bytes);
+  if (rc) return rc;
+  if (a->total_drafts == 0) return SPEC_OK;
+  sv::SampleParams P;
+  fill_sample_inputs(P, a);
+  P.mode = sv::kModeTvOnly;
+  P.uniforms = nullptr;
+  P.out_tv = out_tv;
+  P.out_theta = out_theta;
+  P.out_px = out_p_at_draft;
+  P.out_qx = out_q_at_draft;
+  P.n_items = a->total_drafts;
+  return run_sample(P, a, workspace, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int spec_verify_greedy(const spec_args* a, int32_t* out_tokens, int32_t* out_accepted, int32_t* out_status,
+                       void* workspace, size_t ws_bytes, spec_stream_t stream) {
+  int rc = check_common(a, false);
+  if (rc) return rc;
+  if (!out_tokens || !out_accepted) return SPEC_ERR_NULL;
+  rc = check_workspace(a, workspace, ws_bytes);
+  if (rc) return rc;
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  int max_smem = 0;
+  rc = device_max_smem(&max_smem);
+  if (rc) return rc;
+  const sv::WorkspaceLayout W = sv::make_workspace_layout(a->B, a->total_drafts, a->V);
+  unsigned char* w = static_cast<unsigned char*>(workspace);
+  sv::GreedyParams P;
+  std::memset(&P, 0, sizeof(P));
+  P.target = a->target_logits;
+  P.ld_t = a->ld_target;
+  P.cu_draft = a->cu_draft;
+  P.draft_tokens = a->draft_tokens;
+  P.cu_hist = a->cu_hist;
+  P.hist = a->hist_tokens;
+  P.rep_penalty = a->rep_penalty;
+  P.B = a->B;
+  P.V = a->V;
+  P.total = a->total_drafts;
+  P.max_k = a->max_k;
+  P.nck = (a->V + sv::kGreedyChunk - 1) / sv::kGreedyChunk;
+  P.out_tokens = out_tokens;
+  P.out_accepted = out_accepted;
+  P.out_status = out_status;
+  P.counters = reinterpret_cast<int*>(w + W.off_counters);
+  P.partials = reinterpret_cast<sv::GreedyPartial*>(w + W.off_partials);
+  if (cudaMemsetAsync(P.counters, 0, (size_t)a->B * sizeof(int), s) != cudaSuccess) {
+    cudaGetLastError();
+    return SPEC_ERR_LAUNCH;
+  }
+  return sv::launch_greedy_verify(P, a->dtype == SPEC_BF16, s) == 0 ? SPEC_OK : SPEC_ERR_LAUNCH;
+}
+
+const char* spec_status_string(int code) {
+  switch (code) {
+    case SPEC_OK: return "ok";
+    case SPEC_ERR_NULL: return "a required pointer is NULL";
+    case SPEC_ERR_SHAPE: return "B, V, total_drafts or ld out of range";
+    case SPEC_ERR_DTYPE: return "unsupported dtype";
+    case SPEC_ERR_K_TOO_LARGE: return "max_k exceeds SPEC_MAX_K (32)";
+    case SPEC_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    case SPEC_ERR_ALIGN: return "logits must be 16-byte aligned with ld*sizeof(dtype) a multiple of 16";
+    case SPEC_ERR_LAUNCH: return "CUDA launch failed";
+    case SPEC_ERR_DEVICE: return "no usable CUDA device (needs sm_103a) or V too large";
+    default: return "unknown status";
+  }
+}
+
+}  // extern "C"

@@ -1,0 +1,199 @@
+"""GPU parity of spec_verify_sample / spec_tv_budget against the oracle.
+
+Tokens, accepted counts and status are compared bit-exactly for every
+request whose decisions all sit further than 1e-6 (in uniform units) from a
+threshold; the near ties are counted.  Probabilities, TV and theta must agree
+within 1e-5 absolute."""
+import numpy as np
+import pytest
+import scipy.special
+import scipy.stats
+
+from speculative_decoding_verification_23_gb300 import workload as W
+from speculative_decoding_verification_23_gb300.device_batch import to_device
+
+import parity as PR
+
+pytestmark = pytest.mark.gpu
+
+
+def _check(batch, requests=None, flags=0, max_near=None):
+    got = PR.run_sample(batch, flags=flags)
+    ref = PR.oracle_sample(batch, requests, bonus=not (flags & 1))
+    bad, near = PR.compare_sample(batch, got, ref, requests)
+    assert not bad, bad[:3]
+    n = batch.B if requests is None else len(list(requests))
+    assert near <= (max_near if max_near is not None else max(1, n // 20)), near
+    return got, ref
+
+
+def test_tiny_rounds():
+    """B=1, K=4, V=1024, fp32, T=0.7, D=0.75: 16 rounds."""
+    for r in range(16):
+        _check(W.tiny(r))
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("V", [3, 5, 257, 4097, 20000, 25000, 50000])
+def test_small_mixed_shapes(dtype, V):
+    """Ragged K (incl. 0), penalties with history, several temperatures and
+    budgets; V spans one chunk, several stages, and 1/2/4-CTA clusters with a
+    ragged tail."""
+    K = [0, 1, 3, 5, 8, 2]
+    batch = W.make_batch(B=6, V=V, K=K, dtype=dtype, seed=1000 + V, rho=[0.3, 0.6, 0.8, 0.9, 0.95, 0.99],
+                         temperature=[0.5, 0.7, 1.0, 1.3, 0.9, 0.6], rep_penalty=[1.0, 1.3, 1.1, 0.8, 1.2, 1.0],
+                         hist_len=min(20, 3 * V), tv_budget=[0.0, 0.2, 0.5, 0.75, 1.0, 0.1])
+    _check(batch)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("V", [5, 3000, 40000])
+def test_top_p(dtype, V):
+    batch = W.make_batch(B=5, V=V, K=[1, 4, 0, 8, 3], dtype=dtype, seed=2000 + V, rho=0.85,
+                         temperature=[0.8, 1.5, 0.8, 1.0, 0.6], rep_penalty=1.0, top_p=[0.9, 0.5, 0.95, 0.3, 1.0],
+                         tv_budget=[0.5, 0.0, 0.5, 0.3, 0.9], draft_topk=4)
+    got, ref = _check(batch)
+    tvg = PR.run_tv(batch)
+    assert PR.compare_tv(batch, tvg, ref) < PR.TOL_PROB
+
+
+@pytest.mark.parametrize("V", [257, 25000, 152064])
+def test_tv_budget_matches_oracle(V):
+    batch = W.make_batch(B=4, V=V, K=[3, 0, 8, 5], dtype="bf16", seed=3000 + V, rho=0.9, temperature=0.7,
+                         rep_penalty=1.1, hist_len=64, tv_budget=[0.0, 0.5, 0.75, 1.0])
+    ref = PR.oracle_sample(batch)
+    got = PR.run_tv(batch)
+    assert PR.compare_tv(batch, got, ref) < PR.TOL_PROB
+
+
+@pytest.mark.parametrize("D", [0.0, 0.5, 0.75, 1.0])
+def test_qwen25_single_d_sweep(D):
+    """B=1, K=8, V=152064 bf16, rho=0.9, T=0.7, penalty 1.1 over 256 history tokens."""
+    batch = W.qwen25_single(D)
+    got, ref = _check(batch, max_near=1)
+    if D == 1.0:
+        assert got[1][0] == 8
+
+
+@pytest.mark.slow
+def test_batched_full_size():
+    """B=64, K=8, V=152064 bf16 (the benchmark workload): 12 requests against
+    the oracle one by one; properties on all 64."""
+    batch = W.batched(0)
+    got = PR.run_sample(batch)
+    sample = list(range(0, 64, 6))
+    ref = PR.oracle_sample(batch, sample)
+    bad, near = PR.compare_sample(batch, got, ref, sample)
+    assert not bad and near <= 1, (bad[:2], near)
+    tok, acc, st = got
+    assert np.all(st == 0)
+    for b in range(64):
+        off = int(batch.cu_draft[b]) + b
+        K = batch.k(b)
+        j = acc[b]
+        assert 0 <= j <= K
+        np.testing.assert_array_equal(tok[off:off + j], batch.draft_tokens[int(batch.cu_draft[b]):][:j])
+        assert 0 <= tok[off + j] < batch.V
+        assert np.all(tok[off + j + 1:off + K + 1] == -1)
+        if float(batch.tv_budget[b]) == 1.0:
+            assert j == K          # D = 1 accepts every draft
+
+
+@pytest.mark.slow
+def test_ragged_top_p_full_size():
+    """B=256, K_b in 1..8, V=152064 fp32, top-p 0.9, D=0.5: 10 requests."""
+    batch = W.ragged_top_p(0)
+    got = PR.run_sample(batch)
+    sample = list(range(0, 256, 26))
+    ref = PR.oracle_sample(batch, sample)
+    bad, near = PR.compare_sample(batch, got, ref, sample)
+    assert not bad and near <= 1, (bad[:2], near)
+    assert np.all(got[2] == 0)
+
+
+def test_equal_distributions_never_reject():
+    batch = W.make_batch(B=3, V=3000, K=[4, 8, 1], dtype="f32", seed=5, rho=0.7, temperature=0.9,
+                         rep_penalty=1.2, hist_len=10, tv_budget=[0.0, 0.3, 1.0])
+    for b in range(batch.B):
+        d0, d1 = int(batch.cu_draft[b]), int(batch.cu_draft[b + 1])
+        off = d0 + b
+        batch.draft[d0:d1] = batch.target[off:off + (d1 - d0)]
+    tok, acc, st = PR.run_sample(batch)
+    assert list(acc) == [4, 8, 1] and np.all(st == 0)
+    tv = PR.run_tv(batch)[0]
+    assert np.max(np.abs(tv)) < 1e-6
+
+
+def test_no_bonus_flag():
+    batch = W.make_batch(B=3, V=2000, K=[2, 3, 0], dtype="bf16", seed=6, tv_budget=1.0)
+    got, ref = _check(batch, flags=1)
+    tok, acc, _ = got
+    assert list(acc) == [2, 3, 0]
+    assert tok[2] == -1 and tok[3 + 1 + 3] == -1 and tok[-1] == -1
+
+
+def test_invalid_inputs_set_status():
+    batch = W.make_batch(B=6, V=500, K=[2, 2, 2, 2, 2, 2], dtype="f32", seed=7, hist_len=4, rep_penalty=1.1)
+    batch.draft_tokens[1] = 500                 # request 0: token out of range
+    batch.temperature[1] = 0.0                  # request 1: T = 0
+    batch.target[2 * 3 + 1, 7] = np.nan         # request 2: NaN logit
+    batch.tv_budget[3] = 1.5                    # request 3: D > 1
+    batch.hist[4 * 4] = -3                      # request 4: bad history token
+    tok, acc, st = PR.run_sample(batch)
+    ref = PR.oracle_sample(batch)
+    assert list(st[:5] != 0) == [True] * 5 and st[5] == 0
+    np.testing.assert_array_equal(st, ref["status"])
+    for b in range(5):
+        assert acc[b] == -1 and np.all(tok[3 * b:3 * b + 3] == -1)
+    bad, _ = PR.compare_sample(batch, (tok, acc, st), ref, [5])
+    assert not bad
+
+
+def test_repeat_calls_are_deterministic():
+    batch = W.make_batch(B=8, V=30000, K=4, dtype="bf16", seed=8, hist_len=32, rep_penalty=1.1, tv_budget=0.4)
+    db = to_device(batch)
+    a = PR.run_sample(batch, db=db)
+    for _ in range(3):
+        b = PR.run_sample(batch, db=db)
+        for x, y in zip(a, b):
+            np.testing.assert_array_equal(x, y)
+
+
+@pytest.mark.parametrize("V,D", [(3, 0.0), (5, 0.25), (8, 0.6)])
+def test_chi_square_first_token_on_gpu(V, D):
+    """The batch is the seed axis: 100000 requests with identical rows, x ~ q
+    drawn by numpy, independent uniforms; the first emitted token follows pi."""
+    rng = np.random.default_rng(40 + V)
+    B, K, T = 100000, 1, 1.0
+    zt = (1.5 * rng.standard_normal((K + 1, V))).astype(np.float32)
+    zd = (1.5 * rng.standard_normal((K, V))).astype(np.float32)
+    ld = 8
+    batch = W.make_batch(B=1, V=V, K=K, dtype="f32", seed=1)   # template for field layout
+    batch.B = B
+    batch.cu_draft = np.arange(B + 1, dtype=np.int32) * K
+    batch.target = np.zeros((B * (K + 1), ld), np.float32)
+    batch.target[:, :V] = np.tile(zt, (B, 1))
+    batch.draft = np.zeros((B * K, ld), np.float32)
+    batch.draft[:, :V] = np.tile(zd, (B, 1))
+    q0 = scipy.special.softmax(zd[0].astype(np.float64) / T)
+    batch.draft_tokens = rng.choice(V, size=B * K, p=q0).astype(np.int32)
+    batch.cu_hist = np.zeros(B + 1, np.int32)
+    batch.hist = np.zeros(0, np.int32)
+    batch.temperature = np.full(B, T, np.float32)
+    batch.rep_penalty = np.ones(B, np.float32)
+    batch.top_p = np.ones(B, np.float32)
+    batch.tv_budget = np.full(B, D, np.float32)
+    batch.uniforms = W.uniforms_from_bits(rng.integers(0, 2 ** 32, size=B * (K + 1), dtype=np.uint64))
+    tok, acc, st = PR.run_sample(batch)
+    first = tok[np.arange(B) * (K + 1)]
+    counts = np.bincount(first, minlength=V)
+    p = scipy.special.softmax(zt[0].astype(np.float64) / T)
+    d = 1 - np.minimum(p, q0).sum()
+    th = 1.0 if d <= D else D / d
+    pi = (1 - th) * p + th * q0
+    _, pval = scipy.stats.chisquare(counts, pi * B)
+    assert pval > 1e-3, (counts, pi * B)
+    # and request by request against the oracle on a slice
+    ref = PR.oracle_sample(batch, range(200))
+    bad, _ = PR.compare_sample(batch, (tok, acc, st), ref, range(200))
+    assert not bad
