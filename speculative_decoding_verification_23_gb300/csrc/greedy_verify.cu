@@ -79,7 +79,7 @@ __global__ void __launch_bounds__(kGreedyThreads) greedy_verify_kernel(const __g
   const int h0 = P.cu_hist ? __ldg(P.cu_hist + b) : 0;
   const int h1 = P.cu_hist ? __ldg(P.cu_hist + b + 1) : 0;
   const int npre = (i >= 0 && i <= K) ? i : 0;
-  const bool pen = alpha != 1.f && (h1 > h0 || npre > 0);
+  const bool pen = !(flags & kStatusBadParam) && alpha != 1.f && (h1 > h0 || npre > 0);
 
   if (tid == 0) s_flags = 0;
   for (int w = tid; w < kGreedyChunk / 32; w += kGreedyThreads) bitmap[w] = 0u;

@@ -86,6 +86,7 @@ struct Shared {
   float* tot;        // [2 rows][256]
   int* misc_i;       // small ints
   double* misc_d;    // small doubles
+  float* misc_f;     // small floats
   uint64_t* full;
   uint64_t* empty;
   uint64_t* csync;   // [2]
@@ -106,6 +107,7 @@ __device__ __forceinline__ Shared carve(unsigned char* smem, const SmemLayout& L
   S.tot = reinterpret_cast<float*>(smem + L.off_tot);
   S.misc_d = reinterpret_cast<double*>(smem + L.off_misc);        // 16 doubles
   S.misc_i = reinterpret_cast<int*>(smem + L.off_misc + 128);     // 16 ints
+  S.misc_f = reinterpret_cast<float*>(smem + L.off_misc + 192);   // 16 floats
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.off_bar);
   S.full = bars;
   S.empty = bars + L.nslots;
@@ -157,7 +159,7 @@ __device__ __forceinline__ bool cluster_exchange(const Shared& S, ClusterPhase& 
 // ------------------------------------------------------------------ pass 1
 // Processes one row of the item: waits for each ring stage, converts,
 // penalises, exponentiates and stores e; returns the warp's (ref, sum).
-template <typename T>
+template <typename T, bool STORE_Z>
 __device__ __forceinline__ void pass1_row(const Shared& S, const SmemLayout& L, int row, int len,
                                           uint32_t& seq, bool pen, float alpha, float c, int warp,
                                           int lane, bool& timeout) {
@@ -248,11 +250,14 @@ __device__ __forceinline__ void pass1_row(const Shared& S, const SmemLayout& L, 
         a = __fadd2_rn(a, b2);
         s = a.x + a.y;
       }
-      // row capacity is L.slice (a multiple of 64): groups past it are not stored
+      // the store holds e, or the penalised logit z' in the top-p variant; row
+      // capacity is L.slice (a multiple of 64): groups past it are not stored
+      const float* sv8 = STORE_Z ? z : e;
       float* dst = e_row + ib;
-      if (ib + 4 * lane < L.slice) *reinterpret_cast<float4*>(dst + 4 * lane) = make_float4(e[0], e[1], e[2], e[3]);
+      if (ib + 4 * lane < L.slice)
+        *reinterpret_cast<float4*>(dst + 4 * lane) = make_float4(sv8[0], sv8[1], sv8[2], sv8[3]);
       if (ib + 128 + 4 * lane < L.slice)
-        *reinterpret_cast<float4*>(dst + 128 + 4 * lane) = make_float4(e[4], e[5], e[6], e[7]);
+        *reinterpret_cast<float4*>(dst + 128 + 4 * lane) = make_float4(sv8[4], sv8[5], sv8[6], sv8[7]);
       if (lane == 0) refc_row[k] = refc;
       Ssum += s;
     }
@@ -263,26 +268,24 @@ __device__ __forceinline__ void pass1_row(const Shared& S, const SmemLayout& L, 
   if (lane == 0) S.wpart[row * kConsumerWarps + warp] = make_float2(have_ref ? refc : -INFINITY, Sw);
 }
 
-// Combine the 16 warps' (ref, sum) of one row into (M, S) in double.
-__device__ __forceinline__ void cta_combine(const Shared& S, int row, double& M, double& Ssum) {
-  M = -INFINITY;
-  for (int w = 0; w < kConsumerWarps; ++w) {
-    float2 v = S.wpart[row * kConsumerWarps + w];
-    if (v.x > -INFINITY && (double)v.x > M) M = v.x;
-  }
-  Ssum = 0.0;
-  if (M > -INFINITY) {
-    for (int w = 0; w < kConsumerWarps; ++w) {
-      float2 v = S.wpart[row * kConsumerWarps + w];
-      if (v.x > -INFINITY) Ssum += (double)v.y * exp2((double)v.x - M);
-    }
-  }
+// Warp-parallel log-sum combine of up to 16 (ref, sum) pairs per row: lane l
+// holds pair (l & 15) of row (l >> 4).  Returns, in every lane of a row's
+// half-warp, M = max ref and S = sum_j S_j 2^(ref_j - M) (accumulated in fp64,
+// scale factors in fp32: one exp2f per lane, no per-thread fp64 math).
+__device__ __forceinline__ void halfwarp_combine(float ref, double s, float& M, double& Ssum) {
+  float m = ref;
+#pragma unroll
+  for (int o = 8; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  double v = (ref > -INFINITY && m > -INFINITY) ? s * (double)exp2f(ref - m) : 0.0;
+#pragma unroll
+  for (int o = 8; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  M = m;
+  Ssum = v;
 }
 
-// Probability of slice element j of a row with chunk factor f (and top-p).
-// The lane's 8 stored values of chunk k (elements 4l..4l+3 and 128+4l..+3),
-// zero past the CTA's live length.
-__device__ __forceinline__ void load_e8(const float* e_row, int k, int lane, int len, float* v) {
+// The lane's 8 stored values of chunk k (elements 4l..4l+3 and 128+4l..+3);
+// `fill` past the CTA's live length (a value of zero probability).
+__device__ __forceinline__ void load_e8(const float* e_row, int k, int lane, int len, float fill, float* v) {
   const int ib = k * kChunk;
   if (ib + kChunk <= len) {
     load4(e_row + ib + 4 * lane, v);
@@ -291,22 +294,36 @@ __device__ __forceinline__ void load_e8(const float* e_row, int k, int lane, int
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       const int idx = ib + (j < 4 ? 4 * lane + j : 128 + 4 * lane + (j - 4));
-      v[j] = idx < len ? e_row[idx] : 0.f;
+      v[j] = idx < len ? e_row[idx] : fill;
     }
   }
 }
 
+// Order-preserving map of an fp32 logit to an unsigned key (ties stay ties).
+__device__ __forceinline__ uint32_t order_key(float z) {
+  const uint32_t u = __float_as_uint(z);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// How a stored value becomes a probability.  Without top-p the store holds
+// e = 2^(z'c - ref_k) and p = e * fac_k with fac_k = 2^(ref_k - M) / S.  The
+// top-p variant stores the penalised logit z' itself, so the nucleus is cut
+// on exact logits (equal logits are kept or dropped together), and
+// p = [key(z') >= tau] 2^(z'c - M) / kept.
 struct RowProb {
-  float tau;     // keep e*g >= tau
-  float invs;    // 1 / kept mass (top-p), multiplies e*g
-  double kept;   // kept mass in units of e*g
-  bool topp;
+  uint32_t tau_key;  // keep key(z') >= tau_key (0 keeps every token)
+  float c, mc;       // log2(e)/T and the row reference M (in units of z'c)
+  float invs;        // 1 / kept mass
+  double kept;       // kept mass, in units of 2^(z'c - M)
 };
 
-__device__ __forceinline__ float prob_of(float e, float f, float g, const RowProb& rp) {
-  if (!rp.topp) return e * f;
-  float ef = e * g;
-  return ef >= rp.tau ? ef * rp.invs : 0.f;
+template <bool TOPP>
+__device__ __forceinline__ float prob_of(float s, float fac, const RowProb& rp) {
+  if constexpr (!TOPP) {
+    return s * fac;
+  } else {
+    return order_key(s) >= rp.tau_key ? ex2(fmaf(s, rp.c, -rp.mc)) * rp.invs : 0.f;
+  }
 }
 
 }  // namespace
@@ -390,7 +407,7 @@ __global__ void __launch_bounds__(kThreads, 1) sample_verify_kernel(const __grid
       // invalid scalars are reported as such; the row statistics are then
       // computed with T = 1 and no penalty so they do not add other flags
       const bool params_ok = !(flags & kStatusBadParam);
-      const float c = (float)(1.4426950408889634 / (params_ok ? (double)T_ : 1.0));
+      const float c = __fdiv_rn(1.44269504088896341f, params_ok ? T_ : 1.f);  // log2(e)/T
       const int x = it.bonus ? -1 : __ldg(P.draft_tokens + item);
       if (!it.bonus && (x < 0 || x >= P.V)) flags |= kStatusBadToken;
       const int h0 = P.cu_hist ? __ldg(P.cu_hist + b) : 0;
@@ -417,68 +434,91 @@ __global__ void __launch_bounds__(kThreads, 1) sample_verify_kernel(const __grid
       consumer_sync();
 
       // ---- pass 1 over the target row, then the draft row
-      pass1_row<T>(S, L, 0, len, seq, pen, alpha, c, warp, lane, timeout);
-      if (!it.bonus) pass1_row<T>(S, L, 1, len, seq, pen, alpha, c, warp, lane, timeout);
+      pass1_row<T, TOPP>(S, L, 0, len, seq, pen, alpha, c, warp, lane, timeout);
+      if (!it.bonus) pass1_row<T, TOPP>(S, L, 1, len, seq, pen, alpha, c, warp, lane, timeout);
       consumer_sync();
 
-      // ---- sync 1: (M, S) per row across the cluster
+      // ---- sync 1: (M, S) per row, warps -> CTA -> cluster
+      if (warp == 0) {
+        const int r = lane >> 4, w = lane & 15;
+        const float2 v = (r == 0 || !it.bonus) ? S.wpart[r * kConsumerWarps + w] : make_float2(-INFINITY, 0.f);
+        float M;
+        double Ssum;
+        halfwarp_combine(v.x, (double)v.y, M, Ssum);
+        if (w == 0) {
+          S.misc_d[10 + 2 * r] = (double)M;
+          S.misc_d[11 + 2 * r] = Ssum;
+        }
+      }
+      consumer_sync();
       {
         double v[kXchgDoubles];
         if (tid == 0) {
-          cta_combine(S, 0, v[0], v[1]);
-          if (!it.bonus) cta_combine(S, 1, v[2], v[3]); else { v[2] = -INFINITY; v[3] = 0.0; }
+          v[0] = S.misc_d[10]; v[1] = S.misc_d[11];
+          v[2] = S.misc_d[12]; v[3] = S.misc_d[13];
         }
         if (!cluster_exchange(S, ph, C, rank, v, 4)) timeout = true;
       }
-      double Mr[2], Sr[2];
-      {
+      if (warp == 0) {
         const uint32_t buf = (ph.cph - 1) & 1u;
-        for (int r = 0; r < 2; ++r) {
-          double M = -INFINITY;
-          for (int cc = 0; cc < C; ++cc) {
-            double m = xchg_slot(S, C, buf, cc)[2 * r];
-            if (m > M) M = m;
-          }
-          double s = 0.0;
-          if (M > -INFINITY)
-            for (int cc = 0; cc < C; ++cc) {
-              const double* xs = xchg_slot(S, C, buf, cc);
-              if (xs[2 * r] > -INFINITY) s += xs[2 * r + 1] * exp2(xs[2 * r] - M);
-            }
-          Mr[r] = M;
-          Sr[r] = s;
+        const int r = lane >> 4, cc = lane & 15;
+        float ref = -INFINITY;
+        double s = 0.0;
+        if (cc < C) {
+          const double* xs = xchg_slot(S, C, buf, cc);
+          ref = (float)xs[2 * r];
+          s = xs[2 * r + 1];
         }
+        float M;
+        double Ssum;
+        halfwarp_combine(ref, s, M, Ssum);
+        if (cc == 0) {
+          S.misc_d[10 + 2 * r] = (double)M;
+          S.misc_d[11 + 2 * r] = Ssum;
+          S.misc_f[2 * r] = (float)(1.0 / Ssum);
+        }
+      }
+      consumer_sync();
+      double Mr[2], Sr[2];
+      float invS[2];
+      for (int r = 0; r < 2; ++r) {
+        Mr[r] = S.misc_d[10 + 2 * r];
+        Sr[r] = S.misc_d[11 + 2 * r];
+        invS[r] = S.misc_f[2 * r];
       }
       const int nrows = it.bonus ? 1 : 2;
       for (int r = 0; r < nrows; ++r)
         if (!(Sr[r] > 0.0) || !(Sr[r] < INFINITY) || !(Mr[r] < INFINITY)) flags |= kStatusBadLogits;
       const bool ok_stats = !(flags & kStatusBadLogits);
 
-      // ---- chunk factors: g = 2^(ref_k - M), fac = g / S
-      {
-        const int nch = (len + kChunk - 1) / kChunk;
+      // ---- chunk factors fac_k = 2^(ref_k - M) / S (stores hold e)
+      const int nch = (len + kChunk - 1) / kChunk;
+      const float zfill = TOPP ? -INFINITY : 0.f;
+      if constexpr (!TOPP) {
         for (int j = tid; j < nrows * nch; j += kConsumerThreads) {
           const int r = j / nch, k = j % nch;
-          const double g = ok_stats ? exp2((double)S.refc[r * L.nch + k] - Mr[r]) : 0.0;
-          S.fac[r * L.nch + k] = ok_stats ? (float)(g / Sr[r]) : 0.f;
-          // top-p uses g itself; keep it in the seg scratch? store in tot? use refc slot:
-          S.refc[r * L.nch + k] = (float)g;  // refc no longer needed: becomes g
+          S.fac[r * L.nch + k] = ok_stats ? exp2f(S.refc[r * L.nch + k] - (float)Mr[r]) * invS[r] : 0.f;
         }
+        consumer_sync();
       }
-      consumer_sync();
 
-      // ---- optional top-p: tau per row (mass-weighted radix select on e*g)
+      // ---- top-p (top-p variant): tau per row by a mass-weighted radix
+      // select over the exact logit keys, four 8-bit digits, MSB first: the
+      // largest key whose upper set {key >= tau} holds at least top_p of the
+      // mass ("Speculative Decoding" note: both p and q include top-p)
       RowProb rp[2];
-      rp[0].topp = rp[1].topp = false;
-      rp[0].tau = rp[1].tau = 0.f;
-      rp[0].invs = rp[1].invs = 0.f;
-      rp[0].kept = rp[1].kept = 1.0;
+      for (int r = 0; r < 2; ++r) {
+        rp[r].tau_key = 0u;
+        rp[r].c = c;
+        rp[r].mc = (float)(ok_stats && Mr[r] > -INFINITY ? Mr[r] : 0.0);
+        rp[r].kept = (ok_stats && r < nrows) ? Sr[r] : 1.0;
+        rp[r].invs = (ok_stats && r < nrows) ? invS[r] : 1.f;
+      }
       if constexpr (TOPP) {
         if (params_ok && tp < 1.f && ok_stats) {
-          const int nch = (len + kChunk - 1) / kChunk;
           uint32_t prefix[2] = {0u, 0u};
           double above[2] = {0.0, 0.0};
-          double target[2] = {(double)tp * Sr[0], (double)tp * Sr[1]};
+          const double target[2] = {(double)tp * Sr[0], (double)tp * Sr[1]};
           double kept[2] = {Sr[0], Sr[1]};
           for (int pass = 0; pass < 4; ++pass) {
             const int shift = 24 - 8 * pass;
@@ -487,25 +527,25 @@ __global__ void __launch_bounds__(kThreads, 1) sample_verify_kernel(const __grid
             for (int j = tid; j < 512; j += kConsumerThreads) hist[j] = 0.f;
             consumer_sync();
             for (int r = 0; r < nrows; ++r) {
-              const float* er = S.e + (size_t)r * L.slice;
+              const float* zr = S.e + (size_t)r * L.slice;
               for (int k = warp; k < nch; k += kConsumerWarps) {
-                const float g = S.refc[r * L.nch + k];
-                float ev[8];
-                load_e8(er, k, lane, len, ev);
+                float zv[8];
+                load_e8(zr, k, lane, len, -INFINITY, zv);
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
-                  const float ef = ev[j] * g;
-                  const uint32_t key = __float_as_uint(ef);
+                  const uint32_t key = order_key(zv[j]);
                   const bool match = pass == 0 || (key >> (shift + 8)) == (prefix[r] >> (shift + 8));
-                  if (match && ef > 0.f) atomicAdd(&hist[r * 256 + ((key >> shift) & 255u)], ef);
+                  if (match) {
+                    const float w = ex2(fmaf(zv[j], c, -rp[r].mc));
+                    if (w > 0.f) atomicAdd(&hist[r * 256 + ((key >> shift) & 255u)], w);
+                  }
                 }
               }
             }
             fence_acq_rel_cluster();
             consumer_sync();
             if (!cluster_exchange(S, ph, C, rank, nullptr, 0)) timeout = true;
-            // gather the C histograms: thread -> (row, bin)
-            {
+            {  // gather the C histograms: thread -> (row, bin)
               const int r = tid >> 8, bin = tid & 255;
               double s = 0.0;
               if (r < nrows)
@@ -514,55 +554,44 @@ __global__ void __launch_bounds__(kThreads, 1) sample_verify_kernel(const __grid
             }
             consumer_sync();
             if (warp < nrows) {
+              // lane owns bins [8*lane, 8*lane+8): find the largest digit d with
+              // above + mass(bins >= d) >= target
               const int r = warp;
-              // lane owns bins [8*lane, 8*lane+8); find the largest digit d with
-              // above + sum_{bins >= d} >= target
               double lsum = 0.0;
               for (int j = 0; j < 8; ++j) lsum += (double)S.tot[r * 256 + 8 * lane + j];
-              // suffix sums over lanes: exclusive sum of lanes above
-              double incl = lsum;
+              double incl = lsum;  // mass of this lane's block and all blocks above it
               for (int o = 1; o < 32; o <<= 1) {
-                double t = __shfl_down_sync(0xffffffffu, incl, o);
+                const double t = __shfl_down_sync(0xffffffffu, incl, o);
                 if (lane + o < 32) incl += t;
               }
-              const double excl = incl - lsum;  // mass of bins above this lane's block
+              const double excl = incl - lsum;
               const double need = target[r] - above[r];
-              const bool hit = (excl < need) && (excl + lsum >= need);
-              unsigned m = __ballot_sync(0xffffffffu, hit);
+              const unsigned m = __ballot_sync(0xffffffffu, (excl < need) && (excl + lsum >= need));
               int dsel = 0;
-              double new_above = above[r];
-              double binmass = 0.0;
+              double cum = 0.0, bm = 0.0;
               if (m) {
-                const int L0 = 31 - __clz(m);  // highest lane whose block crosses (there is one)
-                double cum = __shfl_sync(0xffffffffu, excl, L0);
-                int dd = 8 * L0;
-                double bm = 0.0;
+                const int L0 = 31 - __clz(m);
+                cum = __shfl_sync(0xffffffffu, excl, L0);
+                dsel = 8 * L0;
                 for (int j = 7; j >= 0; --j) {
                   const double v = (double)S.tot[r * 256 + 8 * L0 + j];
-                  if (cum + v >= need) { dd = 8 * L0 + j; bm = v; break; }
+                  if (cum + v >= need) { dsel = 8 * L0 + j; bm = v; break; }
                   cum += v;
                 }
-                dsel = dd;
-                new_above = above[r] + cum;
-                binmass = bm;
               } else {
-                // rounding: nothing reaches the target -> keep everything down to the lowest non-empty bin
-                double cum = 0.0;
-                int dd = 0;
-                double bm = 0.0;
+                // rounding left the target out of reach: keep everything down
+                // to the lowest non-empty bin
                 for (int j = 255; j >= 0; --j) {
                   const double v = (double)S.tot[r * 256 + j];
-                  if (v > 0.0) { dd = j; bm = v; }
+                  if (v > 0.0) { dsel = j; bm = v; }
                 }
-                for (int j = 255; j > dd; --j) cum += (double)S.tot[r * 256 + j];
-                dsel = dd;
-                new_above = above[r] + cum;
-                binmass = bm;
+                cum = 0.0;
+                for (int j = 255; j > dsel; --j) cum += (double)S.tot[r * 256 + j];
               }
               if (lane == 0) {
                 S.misc_i[8 + r] = dsel;
-                S.misc_d[4 + 2 * r] = new_above;
-                S.misc_d[5 + 2 * r] = binmass;
+                S.misc_d[4 + 2 * r] = above[r] + cum;
+                S.misc_d[5 + 2 * r] = bm;
               }
             }
             consumer_sync();
@@ -573,53 +602,44 @@ __global__ void __launch_bounds__(kThreads, 1) sample_verify_kernel(const __grid
             }
             consumer_sync();
           }
+          if (tid == 0)
+            for (int r = 0; r < nrows; ++r) S.misc_f[4 + r] = (float)(1.0 / kept[r]);
+          consumer_sync();
           for (int r = 0; r < nrows; ++r) {
-            rp[r].topp = true;
-            rp[r].tau = __uint_as_float(prefix[r]);
-            rp[r].invs = (float)(1.0 / kept[r]);
+            rp[r].tau_key = prefix[r];
             rp[r].kept = kept[r];
+            rp[r].invs = S.misc_f[4 + r];
           }
         }
       }
 
-      // ---- p(x), q(x) by the CTA that holds x
-      if (!it.bonus && tid == 0 && x >= v0 && x < v0 + len) {
+      // ---- p(x), q(x) by the CTA that holds x (the same formula as pass 2)
+      if (!it.bonus && tid == 0 && x >= v0 && x < v0 + len && ok_stats) {
         const int j = x - v0, k = j / kChunk;
-        double pv, qv;
-        if (rp[0].topp) {
-          const float ef = S.e[j] * S.refc[k];
-          pv = ef >= rp[0].tau ? (double)ef / rp[0].kept : 0.0;
-          const float eq = S.e[L.slice + j] * S.refc[L.nch + k];
-          qv = eq >= rp[1].tau ? (double)eq / rp[1].kept : 0.0;
-        } else {
-          pv = (double)S.e[j] * ((double)S.refc[k] / Sr[0]);
-          qv = (double)S.e[L.slice + j] * ((double)S.refc[L.nch + k] / Sr[1]);
-        }
-        S.misc_d[kMdPx] = pv;
-        S.misc_d[kMdQx] = qv;
+        S.misc_d[kMdPx] = (double)prob_of<TOPP>(S.e[j], TOPP ? 0.f : S.fac[k], rp[0]);
+        S.misc_d[kMdQx] = (double)prob_of<TOPP>(S.e[(size_t)L.slice + j], TOPP ? 0.f : S.fac[L.nch + k], rp[1]);
       }
 
       // ---- pass 2: per-chunk sums of r = max(p - q, 0) (positions) or p (bonus)
       const double u_fin = P.mode == kModeSample ? (double)__ldg(P.uniforms + off + K) : 0.0;
       bool cdf_of_p = it.bonus;
-      double R = 0.0, Pc = 0.0, Rc = 0.0;
+      double R = 0.0, Pc = 0.0;
       double Rcs[kMaxCluster];
-      const int nch = (len + kChunk - 1) / kChunk;
       for (int attempt = 0; attempt < 2; ++attempt) {
         for (int k = warp; k < nch; k += kConsumerWarps) {
-          const float fp = S.fac[k], gp = S.refc[k];
+          const float fp = TOPP ? 0.f : S.fac[k];
           float e1[8];
-          load_e8(S.e, k, lane, len, e1);
+          load_e8(S.e, k, lane, len, zfill, e1);
           float s = 0.f;
           if (cdf_of_p) {
 #pragma unroll
-            for (int j = 0; j < 8; ++j) s += prob_of(e1[j], fp, gp, rp[0]);
+            for (int j = 0; j < 8; ++j) s += prob_of<TOPP>(e1[j], fp, rp[0]);
           } else {
-            const float fq = S.fac[L.nch + k], gq = S.refc[L.nch + k];
+            const float fq = TOPP ? 0.f : S.fac[L.nch + k];
             float e2[8];
-            load_e8(S.e + L.slice, k, lane, len, e2);
+            load_e8(S.e + L.slice, k, lane, len, zfill, e2);
 #pragma unroll
-            for (int j = 0; j < 8; ++j) s += fmaxf(prob_of(e1[j], fp, gp, rp[0]) - prob_of(e2[j], fq, gq, rp[1]), 0.f);
+            for (int j = 0; j < 8; ++j) s += fmaxf(prob_of<TOPP>(e1[j], fp, rp[0]) - prob_of<TOPP>(e2[j], fq, rp[1]), 0.f);
           }
           s = warp_sum(s);
           if (lane == 0) S.seg[k] = s;
@@ -644,17 +664,14 @@ __global__ void __launch_bounds__(kThreads, 1) sample_verify_kernel(const __grid
         }
         const uint32_t buf = (ph.cph - 1) & 1u;
         R = 0.0;
-        for (int cc = 0; cc < C; ++cc) {
-          const double rc = xchg_slot(S, C, buf, cc)[0];
-          Rcs[cc] = rc;
-          R += rc;
-        }
         Pc = 0.0;
-        for (int cc = 0; cc < (int)rank; ++cc) Pc += Rcs[cc];
-        Rc = Rcs[rank];
+        for (int cc = 0; cc < C; ++cc) {
+          Rcs[cc] = xchg_slot(S, C, buf, cc)[0];
+          if (cc < (int)rank) Pc += Rcs[cc];
+          R += Rcs[cc];
+        }
         if (!cdf_of_p && !(R > 0.0) && P.mode == kModeSample) {
-          cdf_of_p = true;  // no residual mass: draw from p (never reached when a rejection is possible)
-          Pc = 0.0;
+          cdf_of_p = true;  // no residual mass: draw from p (only reachable when q(x) = 0)
           continue;
         }
         break;
@@ -662,7 +679,8 @@ __global__ void __launch_bounds__(kThreads, 1) sample_verify_kernel(const __grid
 
       // ---- decisions
       const double tv = (it.bonus || cdf_of_p) ? 0.0 : fmin(R, 1.0);
-      const double theta = (tv <= (double)D) ? 1.0 : (double)D / tv;
+      double theta = 1.0;  // fp64 division by one thread only
+      if (tid == 0) theta = (tv <= (double)D) ? 1.0 : (double)D / tv;
       const bool x_owner = !it.bonus && x >= v0 && x < v0 + len;
       double pv = 0.0, qv = 0.0;
       if (x_owner && tid == 0) {
@@ -708,18 +726,18 @@ __global__ void __launch_bounds__(kThreads, 1) sample_verify_kernel(const __grid
           if (ks < 0) { ks = klast; tl_last = true; }
           int found = -1;
           if (ks >= 0) {
-            const float fp = S.fac[ks], gp = S.refc[ks];
+            const float fp = TOPP ? 0.f : S.fac[ks];
             float e1[8], w[8];
-            load_e8(S.e, ks, lane, len, e1);
+            load_e8(S.e, ks, lane, len, zfill, e1);
             if (cdf_of_p) {
 #pragma unroll
-              for (int j = 0; j < 8; ++j) w[j] = prob_of(e1[j], fp, gp, rp[0]);
+              for (int j = 0; j < 8; ++j) w[j] = prob_of<TOPP>(e1[j], fp, rp[0]);
             } else {
-              const float fq = S.fac[L.nch + ks], gq = S.refc[L.nch + ks];
+              const float fq = TOPP ? 0.f : S.fac[L.nch + ks];
               float e2[8];
-              load_e8(S.e + L.slice, ks, lane, len, e2);
+              load_e8(S.e + L.slice, ks, lane, len, zfill, e2);
 #pragma unroll
-              for (int j = 0; j < 8; ++j) w[j] = fmaxf(prob_of(e1[j], fp, gp, rp[0]) - prob_of(e2[j], fq, gq, rp[1]), 0.f);
+              for (int j = 0; j < 8; ++j) w[j] = fmaxf(prob_of<TOPP>(e1[j], fp, rp[0]) - prob_of<TOPP>(e2[j], fq, rp[1]), 0.f);
             }
             double rem = tl - S.pre[ks];
             if (!tl_last) {
