@@ -1,6 +1,6 @@
 // Device helpers shared by the verification kernels: inline PTX for
 // mbarriers, 1-D TMA bulk copies, cluster (DSMEM) access, and warp
-// reductions.  Every wait here is bounded by wall-clock time (%globaltimer):
+// reductions.  Every wait here is bounded (a cycle-count limit):
 // a wait that runs out returns false and the caller records an error status
 // instead of spinning forever.
 #pragma once
@@ -19,17 +19,9 @@ constexpr int kStatusBadK = 8;
 constexpr int kStatusTimeout = 16;
 
 constexpr int kMaxK = 32;
-// Upper bound on any single wait: far above any legitimate wait (microseconds).
-constexpr unsigned long long kWaitLimitNs = 2000000000ull;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ unsigned long long globaltimer_ns() {
-  unsigned long long t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
 }
 
 // ---------------------------------------------------------------- mbarrier
@@ -79,22 +71,24 @@ __device__ __forceinline__ bool mbar_test_cluster(uint64_t* bar, uint32_t parity
 }
 
 // Bounded waits: true once the phase with `parity` has completed, false if
-// the time limit ran out first.
+// the limit (in SM clock cycles, a few seconds at any clock) ran out first.
+constexpr long long kWaitLimitCycles = 4000000000ll;
+
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
   if (mbar_test(bar, parity)) return true;
-  const unsigned long long t0 = globaltimer_ns();
-  for (uint32_t i = 1;; ++i) {
+  const long long t0 = clock64();
+  for (;;) {
     if (mbar_test(bar, parity)) return true;
-    if ((i & 255u) == 0 && globaltimer_ns() - t0 > kWaitLimitNs) return false;
+    if (clock64() - t0 > kWaitLimitCycles) return false;
   }
 }
 
 __device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity) {
   if (mbar_test_cluster(bar, parity)) return true;
-  const unsigned long long t0 = globaltimer_ns();
-  for (uint32_t i = 1;; ++i) {
+  const long long t0 = clock64();
+  for (;;) {
     if (mbar_test_cluster(bar, parity)) return true;
-    if ((i & 255u) == 0 && globaltimer_ns() - t0 > kWaitLimitNs) return false;
+    if (clock64() - t0 > kWaitLimitCycles) return false;
   }
 }
 

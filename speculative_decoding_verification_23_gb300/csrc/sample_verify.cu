@@ -136,21 +136,26 @@ __device__ __forceinline__ double* xchg_slot(const Shared& S, int C, uint32_t bu
   return S.xchg + ((size_t)buf * C + c) * kXchgDoubles;
 }
 
-// Thread 0 pushes `vals` to every CTA's exchange slot [buf][rank] and
-// arrives on every CTA's csync[buf]; then every consumer thread waits.
+// Warp 0 publishes up to four doubles into exchange slot [buf][rank] of every
+// CTA of the cluster: lane c writes CTA c and then arrives (release, cluster
+// scope) on CTA c's csync[buf], so the C pushes proceed in parallel.  Every
+// consumer thread then waits on its own csync[buf]; afterwards
+// S.xchg[buf][c][*] holds the values of CTA c.  The caller makes any other
+// shared-memory data it wants visible (fence + CTA barrier) beforehand.
 __device__ __forceinline__ bool cluster_exchange(const Shared& S, ClusterPhase& ph, int C, uint32_t rank,
-                                                 const double* vals, int nvals) {
+                                                 int nvals, double a0, double a1, double a2, double a3) {
   const uint32_t buf = ph.cph & 1u;
   const uint32_t parity = (ph.cph >> 1) & 1u;
-  if (threadIdx.x == 0) {
-    double* mine = xchg_slot(S, C, buf, (int)rank);
-    for (int c = 0; c < C; ++c) {
-      uint32_t base = map_rank(mine, (uint32_t)c);
-      for (int j = 0; j < nvals; ++j) st_remote_f64(base + 8u * j, vals[j]);
-    }
-    for (int c = 0; c < C; ++c) mbar_arrive_remote(&S.csync[buf], (uint32_t)c);
+  const int lane = threadIdx.x & 31;
+  if (threadIdx.x < 32 && lane < C) {
+    const uint32_t base = map_rank(xchg_slot(S, C, buf, (int)rank), (uint32_t)lane);
+    if (nvals > 0) st_remote_f64(base, a0);
+    if (nvals > 1) st_remote_f64(base + 8u, a1);
+    if (nvals > 2) st_remote_f64(base + 16u, a2);
+    if (nvals > 3) st_remote_f64(base + 24u, a3);
+    mbar_arrive_remote(&S.csync[buf], (uint32_t)lane);
   }
-  bool ok = ph.failed ? false : mbar_wait_cluster(&S.csync[buf], parity);
+  const bool ok = ph.failed ? false : mbar_wait_cluster(&S.csync[buf], parity);
   if (!ok) ph.failed = true;  // after one timeout, stop waiting
   ph.cph++;
   return ok;
@@ -439,25 +444,20 @@ __global__ void __launch_bounds__(kThreads, 1) sample_verify_kernel(const __grid
       consumer_sync();
 
       // ---- sync 1: (M, S) per row, warps -> CTA -> cluster
-      if (warp == 0) {
-        const int r = lane >> 4, w = lane & 15;
-        const float2 v = (r == 0 || !it.bonus) ? S.wpart[r * kConsumerWarps + w] : make_float2(-INFINITY, 0.f);
-        float M;
-        double Ssum;
-        halfwarp_combine(v.x, (double)v.y, M, Ssum);
-        if (w == 0) {
-          S.misc_d[10 + 2 * r] = (double)M;
-          S.misc_d[11 + 2 * r] = Ssum;
-        }
-      }
-      consumer_sync();
       {
-        double v[kXchgDoubles];
-        if (tid == 0) {
-          v[0] = S.misc_d[10]; v[1] = S.misc_d[11];
-          v[2] = S.misc_d[12]; v[3] = S.misc_d[13];
+        double a0 = 0.0, a1 = 0.0, a2 = 0.0, a3 = 0.0;
+        if (warp == 0) {
+          const int r = lane >> 4, w = lane & 15;
+          const float2 v = (r == 0 || !it.bonus) ? S.wpart[r * kConsumerWarps + w] : make_float2(-INFINITY, 0.f);
+          float M;
+          double Ssum;
+          halfwarp_combine(v.x, (double)v.y, M, Ssum);
+          a0 = __shfl_sync(0xffffffffu, (double)M, 0);
+          a1 = __shfl_sync(0xffffffffu, Ssum, 0);
+          a2 = __shfl_sync(0xffffffffu, (double)M, 16);
+          a3 = __shfl_sync(0xffffffffu, Ssum, 16);
         }
-        if (!cluster_exchange(S, ph, C, rank, v, 4)) timeout = true;
+        if (!cluster_exchange(S, ph, C, rank, 4, a0, a1, a2, a3)) timeout = true;
       }
       if (warp == 0) {
         const uint32_t buf = (ph.cph - 1) & 1u;
@@ -544,7 +544,7 @@ __global__ void __launch_bounds__(kThreads, 1) sample_verify_kernel(const __grid
             }
             fence_acq_rel_cluster();
             consumer_sync();
-            if (!cluster_exchange(S, ph, C, rank, nullptr, 0)) timeout = true;
+            if (!cluster_exchange(S, ph, C, rank, 0, 0.0, 0.0, 0.0, 0.0)) timeout = true;
             {  // gather the C histograms: thread -> (row, bin)
               const int r = tid >> 8, bin = tid & 255;
               double s = 0.0;
@@ -624,7 +624,8 @@ __global__ void __launch_bounds__(kThreads, 1) sample_verify_kernel(const __grid
       const double u_fin = P.mode == kModeSample ? (double)__ldg(P.uniforms + off + K) : 0.0;
       bool cdf_of_p = it.bonus;
       double R = 0.0, Pc = 0.0;
-      double Rcs[kMaxCluster];
+      int owner = -1;
+      bool take_last = false;
       for (int attempt = 0; attempt < 2; ++attempt) {
         for (int k = warp; k < nch; k += kConsumerWarps) {
           const float fp = TOPP ? 0.f : S.fac[k];
@@ -645,31 +646,38 @@ __global__ void __launch_bounds__(kThreads, 1) sample_verify_kernel(const __grid
           if (lane == 0) S.seg[k] = s;
         }
         consumer_sync();
+        double run = 0.0;
         if (warp == 0) {
-          double run = 0.0;
           for (int k0 = 0; k0 < nch; k0 += 32) {
             const int k = k0 + lane;
             const double v = k < nch ? (double)S.seg[k] : 0.0;
             const double inc = warp_incl_scan_d(v, lane);
-            if (k < nch) S.pre[k] = run + inc - v;  // exclusive prefix
+            if (k < nch) S.pre[k] = run + inc - v;  // exclusive prefix within the CTA
             run += __shfl_sync(0xffffffffu, inc, 31);
           }
-          if (lane == 0) S.misc_d[8] = run;
+        }
+        if (!cluster_exchange(S, ph, C, rank, 1, run, 0.0, 0.0, 0.0)) timeout = true;
+        if (warp == 0) {
+          // lane c: mass of CTA c; prefix sums, total, owner of u_fin * R
+          const uint32_t buf = (ph.cph - 1) & 1u;
+          const double rc = lane < C ? xchg_slot(S, C, buf, lane)[0] : 0.0;
+          const double inc = warp_incl_scan_d(rc, lane);
+          const double tot = __shfl_sync(0xffffffffu, inc, 31);
+          const double t = u_fin * tot;
+          const unsigned hit = __ballot_sync(0xffffffffu, lane < C && rc > 0.0 && inc > t);
+          const unsigned pos = __ballot_sync(0xffffffffu, lane < C && rc > 0.0);
+          if (lane == 0) {
+            S.misc_d[14] = tot;
+            S.misc_i[4] = hit ? __ffs(hit) - 1 : (pos ? 31 - __clz(pos) : -1);
+            S.misc_i[5] = hit ? 0 : 1;
+          }
+          if (lane == (int)rank) S.misc_d[15] = inc - rc;
         }
         consumer_sync();
-        {
-          double v[kXchgDoubles];
-          v[0] = S.misc_d[8];
-          if (!cluster_exchange(S, ph, C, rank, v, 1)) timeout = true;
-        }
-        const uint32_t buf = (ph.cph - 1) & 1u;
-        R = 0.0;
-        Pc = 0.0;
-        for (int cc = 0; cc < C; ++cc) {
-          Rcs[cc] = xchg_slot(S, C, buf, cc)[0];
-          if (cc < (int)rank) Pc += Rcs[cc];
-          R += Rcs[cc];
-        }
+        R = S.misc_d[14];
+        Pc = S.misc_d[15];
+        owner = S.misc_i[4];
+        take_last = S.misc_i[5] != 0;
         if (!cdf_of_p && !(R > 0.0) && P.mode == kModeSample) {
           cdf_of_p = true;  // no residual mass: draw from p (only reachable when q(x) = 0)
           continue;
@@ -703,18 +711,6 @@ __global__ void __launch_bounds__(kThreads, 1) sample_verify_kernel(const __grid
       // ---- candidate: inverse CDF at u_fin within the owning CTA
       if (P.mode == kModeSample && ok_stats) {
         const double t = u_fin * R;
-        // owner CTA: first with prefix+mass > t, else the last with mass > 0
-        int owner = -1, last_pos = -1;
-        {
-          double run = 0.0;
-          for (int cc = 0; cc < C; ++cc) {
-            if (Rcs[cc] > 0.0) last_pos = cc;
-            if (owner < 0 && run + Rcs[cc] > t && Rcs[cc] > 0.0) owner = cc;
-            run += Rcs[cc];
-          }
-        }
-        const bool take_last = owner < 0;
-        if (take_last) owner = last_pos;
         if (owner == (int)rank && warp == 0) {
           const double tl = t - Pc;
           int ks = -1, klast = -1;
