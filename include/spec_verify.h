@@ -121,6 +121,15 @@ enum {
    decoding engine's behaviour; "Even full acceptance did not buy a
    speedup").  out_tokens slot off_b + K_b is then -1 in that case. */
 #define SPEC_NO_BONUS 1u
+/* flags, sampling only: kernel strategy hints (results agree with the
+   definition either way; fp32 rounding may differ in the last bits).
+   RESIDENT keeps each CTA's slice of both rows in shared memory and reads
+   every logit once; it suits batches whose work items (sum K_b + B) all fit
+   in one wave of clusters.  STREAMING re-reads each slice from L2 for the
+   second pass and keeps about one item per SM in flight; it suits large
+   batches.  Without a hint the library picks by batch size. */
+#define SPEC_PREFER_RESIDENT 2u
+#define SPEC_PREFER_STREAMING 4u
 
 typedef struct {
   int32_t B;             /* requests, >= 1                                   */
@@ -141,7 +150,7 @@ typedef struct {
   const float *top_p;          /* [B] or NULL; unused by greedy              */
   const float *tv_budget;      /* [B]; unused by greedy                      */
   const float *uniforms;       /* [total_drafts + B]; sampling only          */
-  uint32_t flags;              /* SPEC_NO_BONUS                              */
+  uint32_t flags;              /* SPEC_NO_BONUS | SPEC_PREFER_*              */
 } spec_args;
 
 /* Workspace size in bytes for a batch (covers all three entry points). */

@@ -19,6 +19,8 @@ SPEC_F32 = 0
 SPEC_BF16 = 1
 SPEC_MAX_K = 32
 SPEC_NO_BONUS = 1
+SPEC_PREFER_RESIDENT = 2
+SPEC_PREFER_STREAMING = 4
 
 SPEC_OK = 0
 SPEC_ERR_NULL = -1

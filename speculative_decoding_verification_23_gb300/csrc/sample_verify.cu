@@ -1,35 +1,41 @@
 // Fused mentored speculative sampling for GB300 (sm_103a).
 //
-// One thread-block cluster of C CTAs handles one work item at a time: a
-// draft position (target row i and draft row i of a request) or a request's
-// bonus row (target row K).  Each CTA owns a contiguous slice of the
-// vocabulary.  Per item:
+// A thread-block cluster of C CTAs (C = 1 .. 16) handles one work item at a
+// time: a draft position (target row i and draft row i of a request) or a
+// request's bonus row (target row K).  Each CTA owns a contiguous slice of
+// the vocabulary.  A producer warp streams the CTA's slice of both rows from
+// global memory into a shared-memory ring with 1-D TMA bulk copies (one
+// slot = kStage tokens of the target row followed by the same tokens of the
+// draft row); 16 consumer warps work on the slots.  Per item:
 //
-//   pass 1  a producer warp streams the CTA's slice of each row from HBM into
-//           a shared-memory ring with 1-D TMA bulk copies; 16 consumer warps
-//           apply the repetition penalty and temperature, and store
-//           e = 2^(z*log2(e)/T - ref) per token in shared memory (fp32), one
-//           exponential per logit, ref being a per-warp running reference.
-//           Every logit is read from HBM exactly once.
-//   sync 1  (max, sum) of both rows: warp -> CTA -> cluster through DSMEM.
-//   top-p   (optional) a mass-weighted radix select on the stored values,
-//           four 8-bit digit passes, each reduced across the cluster.
-//   pass 2  from shared memory: r = max(p - q, 0) summed per 256-token chunk;
-//           TV d = sum r ("What I Gave Up to Make Speculative Decoding
-//           Faster", "A knob for accepting more draft tokens":
-//           d = 1/2 sum|p-q|, which equals sum max(p-q,0) for two
+//   pass 1  repetition penalty and temperature; running (reference, sum) of
+//           e = 2^(z'c - ref) per row, c = log2(e)/T: one exponential per
+//           logit.  The resident variant also keeps e (or, with top-p, the
+//           penalised logit z') of every token in shared memory.
+//   sync 1  (max, sum) of both rows: warps -> CTA -> cluster through DSMEM.
+//   top-p   (optional) a mass-weighted radix select over the exact logit
+//           keys, four 8-bit digits, each histogram reduced over the cluster.
+//   pass 2  r = max(p - q, 0) summed per 256-token chunk (bonus rows: p).
+//           The resident variant reads its shared-memory copy; the streaming
+//           variant re-reads the slice (an L2 hit: it was read moments ago)
+//           and recomputes p and q.  TV d = sum r ("What I Gave Up to Make
+//           Speculative Decoding Faster", "A knob for accepting more draft
+//           tokens": d = 1/2 sum|p-q|, equal to sum max(p-q, 0) for two
 //           distributions).
-//   sync 2  chunk/CTA prefix sums of r across the cluster.
+//   sync 2  chunk and CTA prefix sums of r across the cluster.
 //   decide  theta = min(1, D/d); pi(x) = (1-theta) p(x) + theta q(x); accept
 //           iff u q(x) < pi(x); the residual candidate = inverse CDF of r at
-//           u_fin (searched in the CTA, chunk and lane that hold it).
-//           Bonus items do the same inverse CDF on p.
+//           u_fin, found by the CTA, chunk and lane that hold it.  Bonus rows
+//           take the inverse CDF of p.
 //   emit    the last CTA to finish a request (an atomic counter) scans the K
 //           acceptance flags with a warp ballot and writes the tokens.
 //
 // Acceptance and correction are evaluated speculatively at every position;
 // the uniforms are assigned per position, so this equals evaluating them in
-// order and stopping at the first rejection.
+// order and stopping at the first rejection.  The resident variant reads
+// each logit from HBM once and suits small batches (few items, many CTAs
+// each); the streaming variant keeps about one item per SM in flight and
+// suits large batches.
 #include "common.cuh"
 #include "spec_internal.h"
 
@@ -49,7 +55,7 @@ __device__ __forceinline__ Item decode_item(const SampleParams& P, int item) {
   if (item < P.total) {
     int lo = 0, hi = P.B;
     while (hi - lo > 1) {
-      int mid = (lo + hi) >> 1;
+      const int mid = (lo + hi) >> 1;
       if (__ldg(P.cu_draft + mid) <= item) lo = mid; else hi = mid;
     }
     it.b = lo;
@@ -59,8 +65,8 @@ __device__ __forceinline__ Item decode_item(const SampleParams& P, int item) {
     it.dft_row = item;
     it.rows_ok = true;
   } else {
-    int b = item - P.total;
-    int c0 = __ldg(P.cu_draft + b), c1 = __ldg(P.cu_draft + b + 1);
+    const int b = item - P.total;
+    const int c0 = __ldg(P.cu_draft + b), c1 = __ldg(P.cu_draft + b + 1);
     it.b = b;
     it.i = c1 - c0;
     it.bonus = true;
@@ -72,21 +78,41 @@ __device__ __forceinline__ Item decode_item(const SampleParams& P, int item) {
   return it;
 }
 
+// Validity of a request's scalars (read the same way by producer and consumers).
+__device__ __forceinline__ bool item_params_ok(const SampleParams& P, int b) {
+  const float T_ = P.temperature ? __ldg(P.temperature + b) : 1.f;
+  const float alpha = P.rep_penalty ? __ldg(P.rep_penalty + b) : 1.f;
+  const float tp = P.top_p ? __ldg(P.top_p + b) : 1.f;
+  const float D = P.tv_budget ? __ldg(P.tv_budget + b) : 0.f;
+  return (T_ > 0.f) && (T_ < INFINITY) && (alpha > 0.f) && (alpha < INFINITY) && (tp > 0.f) && (tp <= 1.f) &&
+         (D >= 0.f) && (D <= 1.f);
+}
+
+// Top-p radix passes an item makes: 4 when it filters, else 0.
+template <bool TOPP>
+__device__ __forceinline__ int radix_passes(const SampleParams& P, int b) {
+  if constexpr (!TOPP) {
+    return 0;
+  } else {
+    return (item_params_ok(P, b) && __ldg(P.top_p + b) < 1.f) ? 4 : 0;
+  }
+}
+
 struct Shared {
   unsigned char* ring;
-  float* e;          // [2][slice]
-  uint32_t* bitmap;  // [slice/32]
-  float* refc;       // [2][nch]
-  float* fac;        // [2][nch]
+  float* e;          // [2][slice] (resident variant)
+  uint32_t* bitmap;  // [nch * 8]
+  float* refc;       // [2][nch]   (resident variant)
+  float* fac;        // [2][nch]   (resident variant)
   float* seg;        // [nch]
   double* pre;       // [nch]
   float2* wpart;     // [2][16]
   double* xchg;      // [2][C][kXchgDoubles]
   float* hist;       // [2 buf][2 rows][256]
   float* tot;        // [2 rows][256]
-  int* misc_i;       // small ints
-  double* misc_d;    // small doubles
-  float* misc_f;     // small floats
+  double* misc_d;    // 16 doubles
+  int* misc_i;       // 16 ints
+  float* misc_f;     // 16 floats
   uint64_t* full;
   uint64_t* empty;
   uint64_t* csync;   // [2]
@@ -105,9 +131,9 @@ __device__ __forceinline__ Shared carve(unsigned char* smem, const SmemLayout& L
   S.xchg = reinterpret_cast<double*>(smem + L.off_xchg);
   S.hist = reinterpret_cast<float*>(smem + L.off_hist);
   S.tot = reinterpret_cast<float*>(smem + L.off_tot);
-  S.misc_d = reinterpret_cast<double*>(smem + L.off_misc);        // 16 doubles
-  S.misc_i = reinterpret_cast<int*>(smem + L.off_misc + 128);     // 16 ints
-  S.misc_f = reinterpret_cast<float*>(smem + L.off_misc + 192);   // 16 floats
+  S.misc_d = reinterpret_cast<double*>(smem + L.off_misc);
+  S.misc_i = reinterpret_cast<int*>(smem + L.off_misc + 128);
+  S.misc_f = reinterpret_cast<float*>(smem + L.off_misc + 192);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.off_bar);
   S.full = bars;
   S.empty = bars + L.nslots;
@@ -117,18 +143,17 @@ __device__ __forceinline__ Shared carve(unsigned char* smem, const SmemLayout& L
 
 __device__ __forceinline__ void consumer_sync() { named_sync(1, kConsumerThreads); }
 
-// misc_i slots
-constexpr int kMiFlags = 0;      // OR of status bits found by this CTA for the item
-constexpr int kMiFinalize = 2;
-// misc_i[8 + row]: the selected top-p digit.  misc_d slots: p(x), q(x);
-// misc_d[4..7]: top-p mass above / in the selected bin; misc_d[8]: CTA sum.
+// misc_i: [0] status bits of the item found by this CTA, [2] finalize flag,
+// [4] owner CTA of the final draw, [5] owner takes the last positive token,
+// [8 + row] selected top-p digit.
+// misc_d: [0] p(x), [1] q(x), [4..7] top-p mass above / in the selected bin,
+// [10..13] (M, S) of both rows, [14] R, [15] this CTA's prefix of R.
+// misc_f: [0], [2] 1/S per row, [4 + row] 1/kept mass.
+constexpr int kMiFlags = 0, kMiFinalize = 2;
 constexpr int kMdPx = 0, kMdQx = 1;
 
-// Cluster-wide reduction point: every CTA publishes kXchgDoubles values
-// (written by consumer thread 0 before calling), all CTAs wait, and the
-// values of all CTAs are then readable in S.xchg[buf][c][*].
 struct ClusterPhase {
-  uint32_t cph = 0;  // number of completed cluster phases of this CTA
+  uint32_t cph = 0;  // cluster exchanges done by this CTA
   bool failed = false;
 };
 
@@ -142,6 +167,7 @@ __device__ __forceinline__ double* xchg_slot(const Shared& S, int C, uint32_t bu
 // consumer thread then waits on its own csync[buf]; afterwards
 // S.xchg[buf][c][*] holds the values of CTA c.  The caller makes any other
 // shared-memory data it wants visible (fence + CTA barrier) beforehand.
+// Two alternating barriers and buffers keep consecutive exchanges apart.
 __device__ __forceinline__ bool cluster_exchange(const Shared& S, ClusterPhase& ph, int C, uint32_t rank,
                                                  int nvals, double a0, double a1, double a2, double a3) {
   const uint32_t buf = ph.cph & 1u;
@@ -161,122 +187,10 @@ __device__ __forceinline__ bool cluster_exchange(const Shared& S, ClusterPhase& 
   return ok;
 }
 
-// ------------------------------------------------------------------ pass 1
-// Processes one row of the item: waits for each ring stage, converts,
-// penalises, exponentiates and stores e; returns the warp's (ref, sum).
-template <typename T, bool STORE_Z>
-__device__ __forceinline__ void pass1_row(const Shared& S, const SmemLayout& L, int row, int len,
-                                          uint32_t& seq, bool pen, float alpha, float c, int warp,
-                                          int lane, bool& timeout) {
-  const int nch = (len + kChunk - 1) / kChunk;
-  const int nst = (len + kStage - 1) / kStage;
-  float* e_row = S.e + (size_t)row * L.slice;
-  float* refc_row = S.refc + row * L.nch;
-  float refc = 0.f;
-  bool have_ref = false;
-  float Ssum = 0.f;
-  const float kLim = 18446744073709551616.0f;  // 2^64
-  for (int st = 0; st < nst; ++st) {
-    const uint32_t slot = seq % (uint32_t)L.nslots;
-    const uint32_t par = (seq / (uint32_t)L.nslots) & 1u;
-    ++seq;
-    if (!timeout && !mbar_wait(&S.full[slot], par)) timeout = true;  // after one timeout, stop waiting
-    const int k = st * kConsumerWarps + warp;
-    if (k < nch) {
-      const T* chunk = reinterpret_cast<const T*>(S.ring + (size_t)slot * L.slot_bytes) + warp * kChunk;
-      float z[8];
-      load4(chunk + 4 * lane, z);
-      load4(chunk + 128 + 4 * lane, z + 4);
-      const int ib = k * kChunk;
-      if (ib + kChunk > len) {
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          int idx = ib + (j < 4 ? 4 * lane + j : 128 + 4 * lane + (j - 4));
-          if (idx >= len) z[j] = -INFINITY;
-        }
-      }
-      if (pen) {
-        const uint32_t wa = S.bitmap[(ib >> 5) + (lane >> 3)];
-        const uint32_t wb = S.bitmap[(ib >> 5) + 4 + (lane >> 3)];
-        const uint32_t sh = 4u * (lane & 7);
-        uint32_t m = ((wa >> sh) & 0xFu) | (((wb >> sh) & 0xFu) << 4);
-        while (m) {
-          const int j = __ffs(m) - 1;
-          m &= m - 1;
-#pragma unroll
-          for (int jj = 0; jj < 8; ++jj)
-            if (jj == j) z[jj] = penalize(z[jj], alpha);
-        }
-      }
-      if (!have_ref) {
-        float mx = z[0];
-#pragma unroll
-        for (int j = 1; j < 8; ++j) mx = fmaxf(mx, z[j]);
-        mx = warp_max(mx);
-        refc = (mx > -INFINITY) ? mx * c : 0.f;
-        have_ref = true;
-      }
-      float e[8];
-      float s;
-      {
-        const float2 c2 = make_float2(c, c);
-        const float2 nr = make_float2(-refc, -refc);
-#pragma unroll
-        for (int j = 0; j < 8; j += 2) {
-          float2 y = __ffma2_rn(make_float2(z[j], z[j + 1]), c2, nr);
-          e[j] = ex2(y.x);
-          e[j + 1] = ex2(y.y);
-        }
-        float2 a = __fadd2_rn(make_float2(e[0], e[1]), make_float2(e[2], e[3]));
-        float2 b2 = __fadd2_rn(make_float2(e[4], e[5]), make_float2(e[6], e[7]));
-        a = __fadd2_rn(a, b2);
-        s = a.x + a.y;
-      }
-      if (__any_sync(0xffffffffu, !(s <= kLim))) {
-        float mx = z[0];
-#pragma unroll
-        for (int j = 1; j < 8; ++j) mx = fmaxf(mx, z[j]);
-        mx = warp_max(mx);
-        const float nref = (mx > -INFINITY) ? mx * c : 0.f;
-        if (nref > refc) {
-          Ssum *= ex2(refc - nref);
-          refc = nref;
-        }
-        const float2 c2 = make_float2(c, c);
-        const float2 nr = make_float2(-refc, -refc);
-#pragma unroll
-        for (int j = 0; j < 8; j += 2) {
-          float2 y = __ffma2_rn(make_float2(z[j], z[j + 1]), c2, nr);
-          e[j] = ex2(y.x);
-          e[j + 1] = ex2(y.y);
-        }
-        float2 a = __fadd2_rn(make_float2(e[0], e[1]), make_float2(e[2], e[3]));
-        float2 b2 = __fadd2_rn(make_float2(e[4], e[5]), make_float2(e[6], e[7]));
-        a = __fadd2_rn(a, b2);
-        s = a.x + a.y;
-      }
-      // the store holds e, or the penalised logit z' in the top-p variant; row
-      // capacity is L.slice (a multiple of 64): groups past it are not stored
-      const float* sv8 = STORE_Z ? z : e;
-      float* dst = e_row + ib;
-      if (ib + 4 * lane < L.slice)
-        *reinterpret_cast<float4*>(dst + 4 * lane) = make_float4(sv8[0], sv8[1], sv8[2], sv8[3]);
-      if (ib + 128 + 4 * lane < L.slice)
-        *reinterpret_cast<float4*>(dst + 128 + 4 * lane) = make_float4(sv8[4], sv8[5], sv8[6], sv8[7]);
-      if (lane == 0) refc_row[k] = refc;
-      Ssum += s;
-    }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&S.empty[slot]);
-  }
-  const float Sw = warp_sum(Ssum);
-  if (lane == 0) S.wpart[row * kConsumerWarps + warp] = make_float2(have_ref ? refc : -INFINITY, Sw);
-}
-
 // Warp-parallel log-sum combine of up to 16 (ref, sum) pairs per row: lane l
-// holds pair (l & 15) of row (l >> 4).  Returns, in every lane of a row's
-// half-warp, M = max ref and S = sum_j S_j 2^(ref_j - M) (accumulated in fp64,
-// scale factors in fp32: one exp2f per lane, no per-thread fp64 math).
+// holds pair (l & 15) of row (l >> 4).  Every lane of a row's half-warp gets
+// M = max ref and S = sum_j S_j 2^(ref_j - M) (fp64 accumulation, one exp2f
+// per lane).
 __device__ __forceinline__ void halfwarp_combine(float ref, double s, float& M, double& Ssum) {
   float m = ref;
 #pragma unroll
@@ -288,8 +202,51 @@ __device__ __forceinline__ void halfwarp_combine(float ref, double s, float& M, 
   Ssum = v;
 }
 
-// The lane's 8 stored values of chunk k (elements 4l..4l+3 and 128+4l..+3);
-// `fill` past the CTA's live length (a value of zero probability).
+// Element j (0..7) of a lane within a 256-token chunk: 4l+j, then 128+4l+j-4.
+__device__ __forceinline__ int lane_elem(int lane, int j) { return j < 4 ? 4 * lane + j : 128 + 4 * lane + (j - 4); }
+
+// A lane's 8 logits of chunk `ib` (slice offset) of a staged row, in fp32,
+// -inf past the live length, penalised where the bitmap says so.
+template <typename T>
+__device__ __forceinline__ void stage_logits(const T* chunk, int ib, int lane, int len, const uint32_t* bitmap,
+                                             bool pen, float alpha, float* z) {
+  load4(chunk + 4 * lane, z);
+  load4(chunk + 128 + 4 * lane, z + 4);
+  if (ib + kChunk > len) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      if (ib + lane_elem(lane, j) >= len) z[j] = -INFINITY;
+  }
+  if (pen) {
+    const uint32_t wa = bitmap[(ib >> 5) + (lane >> 3)];
+    const uint32_t wb = bitmap[(ib >> 5) + 4 + (lane >> 3)];
+    const uint32_t sh = 4u * (lane & 7);
+    uint32_t m = ((wa >> sh) & 0xFu) | (((wb >> sh) & 0xFu) << 4);
+    while (m) {
+      const int j = __ffs(m) - 1;
+      m &= m - 1;
+#pragma unroll
+      for (int jj = 0; jj < 8; ++jj)
+        if (jj == j) z[jj] = penalize(z[jj], alpha);
+    }
+  }
+}
+
+// The same 8 logits read straight from global memory (used once per item by
+// the streaming variant's candidate search).
+template <typename T>
+__device__ __forceinline__ void global_logits(const T* slice_row, int ib, int lane, int len, const uint32_t* bitmap,
+                                              bool pen, float alpha, float* z) {
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const int idx = ib + lane_elem(lane, j);
+    z[j] = idx < len ? to_f32<T>(slice_row[idx]) : -INFINITY;
+    if (pen && idx < len && ((bitmap[idx >> 5] >> (idx & 31)) & 1u)) z[j] = penalize(z[j], alpha);
+  }
+}
+
+// The lane's 8 stored values of chunk k (resident e-array); `fill` past the
+// live length.
 __device__ __forceinline__ void load_e8(const float* e_row, int k, int lane, int len, float fill, float* v) {
   const int ib = k * kChunk;
   if (ib + kChunk <= len) {
@@ -298,7 +255,7 @@ __device__ __forceinline__ void load_e8(const float* e_row, int k, int lane, int
   } else {
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-      const int idx = ib + (j < 4 ? 4 * lane + j : 128 + 4 * lane + (j - 4));
+      const int idx = ib + lane_elem(lane, j);
       v[j] = idx < len ? e_row[idx] : fill;
     }
   }
@@ -310,31 +267,101 @@ __device__ __forceinline__ uint32_t order_key(float z) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-// How a stored value becomes a probability.  Without top-p the store holds
-// e = 2^(z'c - ref_k) and p = e * fac_k with fac_k = 2^(ref_k - M) / S.  The
-// top-p variant stores the penalised logit z' itself, so the nucleus is cut
-// on exact logits (equal logits are kept or dropped together), and
-// p = [key(z') >= tau] 2^(z'c - M) / kept.
+// How a value becomes a probability.  Resident variant without top-p: the
+// store holds e = 2^(z'c - ref_k) and p = e * fac_k, fac_k = 2^(ref_k - M)/S.
+// Otherwise the value is the penalised logit z' itself (resident top-p
+// store, or any streamed logit) and p = [key(z') >= tau] 2^(z'c - M) / kept;
+// cutting the nucleus on exact logit keys keeps equal logits together.
 struct RowProb {
   uint32_t tau_key;  // keep key(z') >= tau_key (0 keeps every token)
-  float c, mc;       // log2(e)/T and the row reference M (in units of z'c)
+  float c, mc;       // log2(e)/T and the row reference M (units of z'c)
   float invs;        // 1 / kept mass
   double kept;       // kept mass, in units of 2^(z'c - M)
 };
 
-template <bool TOPP>
+template <bool FROM_E>
 __device__ __forceinline__ float prob_of(float s, float fac, const RowProb& rp) {
-  if constexpr (!TOPP) {
+  if constexpr (FROM_E) {
     return s * fac;
   } else {
     return order_key(s) >= rp.tau_key ? ex2(fmaf(s, rp.c, -rp.mc)) * rp.invs : 0.f;
   }
 }
 
+// Pass-1 statistics of one chunk of one row for one warp: running
+// reference `refc` (warp-uniform, units of z'c) and lane sum `Ssum` of
+// 2^(z'c - refc); the reference only moves up, when a chunk would overflow.
+// e receives the chunk's 2^(z'c - refc).
+__device__ __forceinline__ void chunk_stats(const float* z, float c, float& refc, bool& have_ref, float& Ssum,
+                                            float* e) {
+  const float kLim = 18446744073709551616.0f;  // 2^64
+  if (!have_ref) {
+    float mx = z[0];
+#pragma unroll
+    for (int j = 1; j < 8; ++j) mx = fmaxf(mx, z[j]);
+    mx = warp_max(mx);
+    refc = (mx > -INFINITY) ? mx * c : 0.f;
+    have_ref = true;
+  }
+  float s;
+  {
+    const float2 c2 = make_float2(c, c);
+    const float2 nr = make_float2(-refc, -refc);
+#pragma unroll
+    for (int j = 0; j < 8; j += 2) {
+      const float2 y = __ffma2_rn(make_float2(z[j], z[j + 1]), c2, nr);
+      e[j] = ex2(y.x);
+      e[j + 1] = ex2(y.y);
+    }
+    float2 a = __fadd2_rn(make_float2(e[0], e[1]), make_float2(e[2], e[3]));
+    const float2 b2 = __fadd2_rn(make_float2(e[4], e[5]), make_float2(e[6], e[7]));
+    a = __fadd2_rn(a, b2);
+    s = a.x + a.y;
+  }
+  if (__any_sync(0xffffffffu, !(s <= kLim))) {
+    float mx = z[0];
+#pragma unroll
+    for (int j = 1; j < 8; ++j) mx = fmaxf(mx, z[j]);
+    mx = warp_max(mx);
+    const float nref = (mx > -INFINITY) ? mx * c : 0.f;
+    if (nref > refc) {
+      Ssum *= ex2(refc - nref);
+      refc = nref;
+    }
+    const float2 c2 = make_float2(c, c);
+    const float2 nr = make_float2(-refc, -refc);
+#pragma unroll
+    for (int j = 0; j < 8; j += 2) {
+      const float2 y = __ffma2_rn(make_float2(z[j], z[j + 1]), c2, nr);
+      e[j] = ex2(y.x);
+      e[j + 1] = ex2(y.y);
+    }
+    float2 a = __fadd2_rn(make_float2(e[0], e[1]), make_float2(e[2], e[3]));
+    const float2 b2 = __fadd2_rn(make_float2(e[4], e[5]), make_float2(e[6], e[7]));
+    a = __fadd2_rn(a, b2);
+    s = a.x + a.y;
+  }
+  Ssum += s;
+}
+
+// Waits for the next ring slot (consumer side); returns the slot index.
+__device__ __forceinline__ uint32_t next_full(const Shared& S, const SmemLayout& L, uint32_t& seq, bool& timeout) {
+  const uint32_t slot = seq % (uint32_t)L.nslots;
+  const uint32_t par = (seq / (uint32_t)L.nslots) & 1u;
+  ++seq;
+  if (!timeout && !mbar_wait(&S.full[slot], par)) timeout = true;  // after one timeout, stop waiting
+  return slot;
+}
+
+__device__ __forceinline__ void release_slot(const Shared& S, uint32_t slot, int lane) {
+  __syncwarp();
+  if (lane == 0) mbar_arrive(&S.empty[slot]);
+}
+
 }  // namespace
 
 // -------------------------------------------------------------------- kernel
-template <typename T, bool TOPP>
+template <typename T, bool TOPP, bool RESIDENT>
 __global__ void __launch_bounds__(kThreads, 1) sample_verify_kernel(const __grid_constant__ SampleParams P) {
   extern __shared__ __align__(128) unsigned char smem[];
   const SmemLayout& L = P.L;
@@ -344,9 +371,12 @@ __global__ void __launch_bounds__(kThreads, 1) sample_verify_kernel(const __grid
   const int cluster_id = blockIdx.x / C;
   const int v0 = (int)rank * L.slice;
   const int len = max(0, min(L.slice, P.V - v0));
+  const int nst = (len + kStage - 1) / kStage;
+  const int nch = (len + kChunk - 1) / kChunk;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int tid = threadIdx.x;
+  constexpr bool kFromE = RESIDENT && !TOPP;  // stored values are e, not logits
 
   if (tid == 0) {
     for (int s = 0; s < L.nslots; ++s) {
@@ -362,18 +392,21 @@ __global__ void __launch_bounds__(kThreads, 1) sample_verify_kernel(const __grid
   if (warp == kConsumerWarps) {
     // ------------------------------------------------------------ producer
     if (lane == 0 && len > 0) {
-      const uint64_t policy = l2_policy_evict_first();
+      const uint64_t keep_policy = l2_policy_evict_last();
+      const uint64_t drop_policy = l2_policy_evict_first();
       const int es = (int)sizeof(T);
-      const int nst = (len + kStage - 1) / kStage;
       uint32_t seq = 0;
       bool ptimeout = false;
       for (int item = cluster_id; item < P.n_items; item += P.n_clusters) {
-        Item it = decode_item(P, item);
-        const int nrows = it.bonus ? 1 : 2;
-        for (int r = 0; r < nrows; ++r) {
-          const unsigned char* rowp =
-              r == 0 ? static_cast<const unsigned char*>(P.target) + ((size_t)it.tgt_row * P.ld_t + v0) * es
-                     : static_cast<const unsigned char*>(P.draft) + ((size_t)it.dft_row * P.ld_d + v0) * es;
+        const Item it = decode_item(P, item);
+        const unsigned char* rowp =
+            static_cast<const unsigned char*>(P.target) + ((size_t)it.tgt_row * P.ld_t + v0) * es;
+        const unsigned char* rowq =
+            it.bonus ? rowp : static_cast<const unsigned char*>(P.draft) + ((size_t)it.dft_row * P.ld_d + v0) * es;
+        // pass 1; the streaming variant then re-reads for the radix passes and pass 2
+        const int npass = RESIDENT ? 1 : 2 + radix_passes<TOPP>(P, it.b);
+        for (int pass = 0; pass < npass; ++pass) {
+          const uint64_t pol = (RESIDENT || pass == npass - 1) ? drop_policy : keep_policy;
           for (int st = 0; st < nst; ++st) {
             const uint32_t slot = seq % (uint32_t)L.nslots;
             const uint32_t par = ((seq / (uint32_t)L.nslots) & 1u) ^ 1u;
@@ -381,9 +414,11 @@ __global__ void __launch_bounds__(kThreads, 1) sample_verify_kernel(const __grid
             if (!ptimeout && !mbar_wait(&S.empty[slot], par)) ptimeout = true;  // consumers see their own
             const int n = min(kStage, len - st * kStage);
             const uint32_t bytes = (uint32_t)((n * es + 15) & ~15);
-            mbar_arrive_expect_tx(&S.full[slot], bytes);
-            bulk_g2s(S.ring + (size_t)slot * L.slot_bytes, rowp + (size_t)st * kStage * es, bytes, &S.full[slot],
-                     policy);
+            unsigned char* dst = S.ring + (size_t)slot * L.slot_bytes;
+            mbar_arrive_expect_tx(&S.full[slot], it.bonus ? bytes : 2 * bytes);
+            bulk_g2s(dst, rowp + (size_t)st * kStage * es, bytes, &S.full[slot], pol);
+            if (!it.bonus)
+              bulk_g2s(dst + (size_t)kStage * es, rowq + (size_t)st * kStage * es, bytes, &S.full[slot], pol);
           }
         }
       }
@@ -400,18 +435,17 @@ __global__ void __launch_bounds__(kThreads, 1) sample_verify_kernel(const __grid
       const int K = it.K;
       const int d0 = __ldg(P.cu_draft + b);
       const int off = d0 + b;
+      const int nrows = it.bonus ? 1 : 2;
       int flags = 0;
       if (!it.rows_ok || K < 0 || K > P.max_k || K > kMaxK) flags |= kStatusBadK;
       const float T_ = P.temperature ? __ldg(P.temperature + b) : 1.f;
       const float alpha = P.rep_penalty ? __ldg(P.rep_penalty + b) : 1.f;
       const float tp = P.top_p ? __ldg(P.top_p + b) : 1.f;
       const float D = P.tv_budget ? __ldg(P.tv_budget + b) : 0.f;
-      if (!(T_ > 0.f) || !(T_ < INFINITY) || !(alpha > 0.f) || !(alpha < INFINITY) || !(tp > 0.f) ||
-          !(tp <= 1.f) || !(D >= 0.f) || !(D <= 1.f))
-        flags |= kStatusBadParam;
-      // invalid scalars are reported as such; the row statistics are then
-      // computed with T = 1 and no penalty so they do not add other flags
-      const bool params_ok = !(flags & kStatusBadParam);
+      const bool params_ok = item_params_ok(P, b);
+      if (!params_ok) flags |= kStatusBadParam;
+      // invalid scalars are reported as such; the statistics then use T = 1
+      // and no penalty so that they raise no other flag
       const float c = __fdiv_rn(1.44269504088896341f, params_ok ? T_ : 1.f);  // log2(e)/T
       const int x = it.bonus ? -1 : __ldg(P.draft_tokens + item);
       if (!it.bonus && (x < 0 || x >= P.V)) flags |= kStatusBadToken;
@@ -419,12 +453,14 @@ __global__ void __launch_bounds__(kThreads, 1) sample_verify_kernel(const __grid
       const int h1 = P.cu_hist ? __ldg(P.cu_hist + b + 1) : 0;
       const int npre = it.bonus ? (it.rows_ok ? K : 0) : it.i;  // drafts before this row
       const bool pen = params_ok && (alpha != 1.f) && ((h1 > h0) || npre > 0) && len > 0;
+      const int nrad = radix_passes<TOPP>(P, b);
+      const T* gp_row = static_cast<const T*>(P.target) + (size_t)it.tgt_row * P.ld_t + v0;
+      const T* gq_row = it.bonus ? gp_row : static_cast<const T*>(P.draft) + (size_t)it.dft_row * P.ld_d + v0;
 
       // ---- penalty set of this row within the CTA slice; token validity
       if (tid == 0) S.misc_i[kMiFlags] = 0;
-      if (pen) {
+      if (pen)
         for (int w = tid; w < L.nch * 8; w += kConsumerThreads) S.bitmap[w] = 0u;
-      }
       consumer_sync();
       for (int j = h0 + tid; j < h1; j += kConsumerThreads) {
         const int t = __ldg(P.hist + j);
@@ -438,9 +474,40 @@ __global__ void __launch_bounds__(kThreads, 1) sample_verify_kernel(const __grid
       }
       consumer_sync();
 
-      // ---- pass 1 over the target row, then the draft row
-      pass1_row<T, TOPP>(S, L, 0, len, seq, pen, alpha, c, warp, lane, timeout);
-      if (!it.bonus) pass1_row<T, TOPP>(S, L, 1, len, seq, pen, alpha, c, warp, lane, timeout);
+      // ---- pass 1: statistics of both rows (resident: also keep the values)
+      {
+        float refc[2] = {0.f, 0.f}, Ssum[2] = {0.f, 0.f};
+        bool have_ref[2] = {false, false};
+        for (int st = 0; st < nst; ++st) {
+          const uint32_t slot = next_full(S, L, seq, timeout);
+          const int k = st * kConsumerWarps + warp;
+          if (k < nch) {
+            const int ib = k * kChunk;
+            for (int r = 0; r < nrows; ++r) {
+              const T* chunk = reinterpret_cast<const T*>(S.ring + (size_t)slot * L.slot_bytes) + r * kStage +
+                               warp * kChunk;
+              float z[8], e[8];
+              stage_logits<T>(chunk, ib, lane, len, S.bitmap, pen, alpha, z);
+              chunk_stats(z, c, refc[r], have_ref[r], Ssum[r], e);
+              if constexpr (RESIDENT) {
+                // the store holds e, or z' with top-p; row capacity is L.slice
+                float* dst = S.e + (size_t)r * L.slice + ib;
+                const float* sv8 = TOPP ? z : e;
+                if (ib + 4 * lane < L.slice)
+                  *reinterpret_cast<float4*>(dst + 4 * lane) = make_float4(sv8[0], sv8[1], sv8[2], sv8[3]);
+                if (ib + 128 + 4 * lane < L.slice)
+                  *reinterpret_cast<float4*>(dst + 128 + 4 * lane) = make_float4(sv8[4], sv8[5], sv8[6], sv8[7]);
+                if (lane == 0) S.refc[r * L.nch + k] = refc[r];
+              }
+            }
+          }
+          release_slot(S, slot, lane);
+        }
+        for (int r = 0; r < 2; ++r) {
+          const float Sw = warp_sum(Ssum[r]);
+          if (lane == 0) S.wpart[r * kConsumerWarps + warp] = make_float2(have_ref[r] ? refc[r] : -INFINITY, Sw);
+        }
+      }
       consumer_sync();
 
       // ---- sync 1: (M, S) per row, warps -> CTA -> cluster
@@ -448,7 +515,7 @@ __global__ void __launch_bounds__(kThreads, 1) sample_verify_kernel(const __grid
         double a0 = 0.0, a1 = 0.0, a2 = 0.0, a3 = 0.0;
         if (warp == 0) {
           const int r = lane >> 4, w = lane & 15;
-          const float2 v = (r == 0 || !it.bonus) ? S.wpart[r * kConsumerWarps + w] : make_float2(-INFINITY, 0.f);
+          const float2 v = (r < nrows) ? S.wpart[r * kConsumerWarps + w] : make_float2(-INFINITY, 0.f);
           float M;
           double Ssum;
           halfwarp_combine(v.x, (double)v.y, M, Ssum);
@@ -486,15 +553,12 @@ __global__ void __launch_bounds__(kThreads, 1) sample_verify_kernel(const __grid
         Sr[r] = S.misc_d[11 + 2 * r];
         invS[r] = S.misc_f[2 * r];
       }
-      const int nrows = it.bonus ? 1 : 2;
       for (int r = 0; r < nrows; ++r)
         if (!(Sr[r] > 0.0) || !(Sr[r] < INFINITY) || !(Mr[r] < INFINITY)) flags |= kStatusBadLogits;
       const bool ok_stats = !(flags & kStatusBadLogits);
 
-      // ---- chunk factors fac_k = 2^(ref_k - M) / S (stores hold e)
-      const int nch = (len + kChunk - 1) / kChunk;
-      const float zfill = TOPP ? -INFINITY : 0.f;
-      if constexpr (!TOPP) {
+      // ---- chunk factors fac_k = 2^(ref_k - M) / S (resident e store)
+      if constexpr (kFromE) {
         for (int j = tid; j < nrows * nch; j += kConsumerThreads) {
           const int r = j / nch, k = j % nch;
           S.fac[r * L.nch + k] = ok_stats ? exp2f(S.refc[r * L.nch + k] - (float)Mr[r]) * invS[r] : 0.f;
@@ -502,10 +566,6 @@ __global__ void __launch_bounds__(kThreads, 1) sample_verify_kernel(const __grid
         consumer_sync();
       }
 
-      // ---- top-p (top-p variant): tau per row by a mass-weighted radix
-      // select over the exact logit keys, four 8-bit digits, MSB first: the
-      // largest key whose upper set {key >= tau} holds at least top_p of the
-      // mass ("Speculative Decoding" note: both p and q include top-p)
       RowProb rp[2];
       for (int r = 0; r < 2; ++r) {
         rp[r].tau_key = 0u;
@@ -514,8 +574,14 @@ __global__ void __launch_bounds__(kThreads, 1) sample_verify_kernel(const __grid
         rp[r].kept = (ok_stats && r < nrows) ? Sr[r] : 1.0;
         rp[r].invs = (ok_stats && r < nrows) ? invS[r] : 1.f;
       }
+
+      // ---- top-p: tau per row by a mass-weighted radix select over the exact
+      // logit keys, four 8-bit digits, MSB first: the largest key whose upper
+      // set {key >= tau} holds at least top_p of the mass (the "Speculative
+      // Decoding" note: both p and q include top-p)
       if constexpr (TOPP) {
-        if (params_ok && tp < 1.f && ok_stats) {
+        if (nrad > 0) {
+          const bool work = ok_stats;
           uint32_t prefix[2] = {0u, 0u};
           double above[2] = {0.0, 0.0};
           const double target[2] = {(double)tp * Sr[0], (double)tp * Sr[1]};
@@ -526,20 +592,38 @@ __global__ void __launch_bounds__(kThreads, 1) sample_verify_kernel(const __grid
             float* hist = S.hist + hb * 512;
             for (int j = tid; j < 512; j += kConsumerThreads) hist[j] = 0.f;
             consumer_sync();
-            for (int r = 0; r < nrows; ++r) {
-              const float* zr = S.e + (size_t)r * L.slice;
-              for (int k = warp; k < nch; k += kConsumerWarps) {
-                float zv[8];
-                load_e8(zr, k, lane, len, -INFINITY, zv);
+            auto accumulate = [&](const float* zv, int r) {
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                  const uint32_t key = order_key(zv[j]);
-                  const bool match = pass == 0 || (key >> (shift + 8)) == (prefix[r] >> (shift + 8));
-                  if (match) {
-                    const float w = ex2(fmaf(zv[j], c, -rp[r].mc));
-                    if (w > 0.f) atomicAdd(&hist[r * 256 + ((key >> shift) & 255u)], w);
-                  }
+              for (int j = 0; j < 8; ++j) {
+                const uint32_t key = order_key(zv[j]);
+                const bool match = pass == 0 || (key >> (shift + 8)) == (prefix[r] >> (shift + 8));
+                if (match) {
+                  const float w = ex2(fmaf(zv[j], c, -rp[r].mc));
+                  if (w > 0.f) atomicAdd(&hist[r * 256 + ((key >> shift) & 255u)], w);
                 }
+              }
+            };
+            if constexpr (RESIDENT) {
+              if (work)
+                for (int r = 0; r < nrows; ++r)
+                  for (int k = warp; k < nch; k += kConsumerWarps) {
+                    float zv[8];
+                    load_e8(S.e + (size_t)r * L.slice, k, lane, len, -INFINITY, zv);
+                    accumulate(zv, r);
+                  }
+            } else {
+              for (int st = 0; st < nst; ++st) {
+                const uint32_t slot = next_full(S, L, seq, timeout);
+                const int k = st * kConsumerWarps + warp;
+                if (work && k < nch)
+                  for (int r = 0; r < nrows; ++r) {
+                    const T* chunk = reinterpret_cast<const T*>(S.ring + (size_t)slot * L.slot_bytes) +
+                                     r * kStage + warp * kChunk;
+                    float zv[8];
+                    stage_logits<T>(chunk, k * kChunk, lane, len, S.bitmap, pen, alpha, zv);
+                    accumulate(zv, r);
+                  }
+                release_slot(S, slot, lane);
               }
             }
             fence_acq_rel_cluster();
@@ -549,17 +633,18 @@ __global__ void __launch_bounds__(kThreads, 1) sample_verify_kernel(const __grid
               const int r = tid >> 8, bin = tid & 255;
               double s = 0.0;
               if (r < nrows)
-                for (int cc = 0; cc < C; ++cc) s += (double)ld_remote_f32(map_rank(&hist[r * 256 + bin], (uint32_t)cc));
+                for (int cc = 0; cc < C; ++cc)
+                  s += (double)ld_remote_f32(map_rank(&hist[r * 256 + bin], (uint32_t)cc));
               S.tot[r * 256 + bin] = (float)s;
             }
             consumer_sync();
             if (warp < nrows) {
-              // lane owns bins [8*lane, 8*lane+8): find the largest digit d with
+              // lane owns bins [8*lane, 8*lane+8): the largest digit d with
               // above + mass(bins >= d) >= target
               const int r = warp;
               double lsum = 0.0;
               for (int j = 0; j < 8; ++j) lsum += (double)S.tot[r * 256 + 8 * lane + j];
-              double incl = lsum;  // mass of this lane's block and all blocks above it
+              double incl = lsum;  // mass of this lane's block and every block above it
               for (int o = 1; o < 32; o <<= 1) {
                 const double t = __shfl_down_sync(0xffffffffu, incl, o);
                 if (lane + o < 32) incl += t;
@@ -600,52 +685,100 @@ __global__ void __launch_bounds__(kThreads, 1) sample_verify_kernel(const __grid
               above[r] = S.misc_d[4 + 2 * r];
               kept[r] = above[r] + S.misc_d[5 + 2 * r];
             }
+            if (tid == 0)
+              for (int r = 0; r < nrows; ++r) S.misc_f[4 + r] = (float)(1.0 / kept[r]);
             consumer_sync();
           }
-          if (tid == 0)
-            for (int r = 0; r < nrows; ++r) S.misc_f[4 + r] = (float)(1.0 / kept[r]);
-          consumer_sync();
-          for (int r = 0; r < nrows; ++r) {
-            rp[r].tau_key = prefix[r];
-            rp[r].kept = kept[r];
-            rp[r].invs = S.misc_f[4 + r];
-          }
+          if (work)
+            for (int r = 0; r < nrows; ++r) {
+              rp[r].tau_key = prefix[r];
+              rp[r].kept = kept[r];
+              rp[r].invs = S.misc_f[4 + r];
+            }
         }
       }
 
-      // ---- p(x), q(x) by the CTA that holds x (the same formula as pass 2)
-      if (!it.bonus && tid == 0 && x >= v0 && x < v0 + len && ok_stats) {
+      // ---- resident: p(x), q(x) from the stored values (the pass-2 formula)
+      if (RESIDENT && !it.bonus && tid == 0 && x >= v0 && x < v0 + len && ok_stats) {
         const int j = x - v0, k = j / kChunk;
-        S.misc_d[kMdPx] = (double)prob_of<TOPP>(S.e[j], TOPP ? 0.f : S.fac[k], rp[0]);
-        S.misc_d[kMdQx] = (double)prob_of<TOPP>(S.e[(size_t)L.slice + j], TOPP ? 0.f : S.fac[L.nch + k], rp[1]);
+        S.misc_d[kMdPx] = (double)prob_of<kFromE>(S.e[j], kFromE ? S.fac[k] : 0.f, rp[0]);
+        S.misc_d[kMdQx] = (double)prob_of<kFromE>(S.e[(size_t)L.slice + j], kFromE ? S.fac[L.nch + k] : 0.f, rp[1]);
       }
 
       // ---- pass 2: per-chunk sums of r = max(p - q, 0) (positions) or p (bonus)
       const double u_fin = P.mode == kModeSample ? (double)__ldg(P.uniforms + off + K) : 0.0;
       bool cdf_of_p = it.bonus;
-      double R = 0.0, Pc = 0.0;
-      int owner = -1;
-      bool take_last = false;
-      for (int attempt = 0; attempt < 2; ++attempt) {
+      if constexpr (RESIDENT) {
         for (int k = warp; k < nch; k += kConsumerWarps) {
-          const float fp = TOPP ? 0.f : S.fac[k];
+          const float fp = kFromE ? S.fac[k] : 0.f;
           float e1[8];
-          load_e8(S.e, k, lane, len, zfill, e1);
+          load_e8(S.e, k, lane, len, kFromE ? 0.f : -INFINITY, e1);
           float s = 0.f;
-          if (cdf_of_p) {
+          if (it.bonus) {
 #pragma unroll
-            for (int j = 0; j < 8; ++j) s += prob_of<TOPP>(e1[j], fp, rp[0]);
+            for (int j = 0; j < 8; ++j) s += prob_of<kFromE>(e1[j], fp, rp[0]);
           } else {
-            const float fq = TOPP ? 0.f : S.fac[L.nch + k];
+            const float fq = kFromE ? S.fac[L.nch + k] : 0.f;
             float e2[8];
-            load_e8(S.e + L.slice, k, lane, len, zfill, e2);
+            load_e8(S.e + L.slice, k, lane, len, kFromE ? 0.f : -INFINITY, e2);
 #pragma unroll
-            for (int j = 0; j < 8; ++j) s += fmaxf(prob_of<TOPP>(e1[j], fp, rp[0]) - prob_of<TOPP>(e2[j], fq, rp[1]), 0.f);
+            for (int j = 0; j < 8; ++j)
+              s += fmaxf(prob_of<kFromE>(e1[j], fp, rp[0]) - prob_of<kFromE>(e2[j], fq, rp[1]), 0.f);
           }
           s = warp_sum(s);
           if (lane == 0) S.seg[k] = s;
         }
-        consumer_sync();
+      } else {
+        for (int st = 0; st < nst; ++st) {
+          const uint32_t slot = next_full(S, L, seq, timeout);
+          const int k = st * kConsumerWarps + warp;
+          if (k < nch) {
+            const int ib = k * kChunk;
+            const T* base = reinterpret_cast<const T*>(S.ring + (size_t)slot * L.slot_bytes) + warp * kChunk;
+            float zp[8], pv8[8];
+            stage_logits<T>(base, ib, lane, len, S.bitmap, pen, alpha, zp);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) pv8[j] = prob_of<false>(zp[j], 0.f, rp[0]);
+            float s = 0.f;
+            if (it.bonus) {
+#pragma unroll
+              for (int j = 0; j < 8; ++j) s += pv8[j];
+            } else {
+              float zq[8], qv8[8];
+              stage_logits<T>(base + kStage, ib, lane, len, S.bitmap, pen, alpha, zq);
+#pragma unroll
+              for (int j = 0; j < 8; ++j) {
+                qv8[j] = prob_of<false>(zq[j], 0.f, rp[1]);
+                s += fmaxf(pv8[j] - qv8[j], 0.f);
+              }
+              // the lane holding x records p(x), q(x)
+              const int jx = x - v0 - ib;
+              if (ok_stats && jx >= 0 && jx < kChunk) {
+                const int owner_lane = jx < 128 ? (jx >> 2) : ((jx - 128) >> 2);
+                const int jj = jx < 128 ? (jx & 3) : 4 + ((jx - 128) & 3);
+                if (lane == owner_lane) {
+                  float px = 0.f, qx = 0.f;
+#pragma unroll
+                  for (int j = 0; j < 8; ++j)
+                    if (j == jj) { px = pv8[j]; qx = qv8[j]; }
+                  S.misc_d[kMdPx] = (double)px;
+                  S.misc_d[kMdQx] = (double)qx;
+                }
+              }
+            }
+            s = warp_sum(s);
+            if (lane == 0) S.seg[k] = s;
+          }
+          release_slot(S, slot, lane);
+        }
+      }
+      consumer_sync();
+
+      // ---- sync 2: CTA prefix sums, cluster totals, owner of the final draw
+      double R = 0.0, Pc = 0.0;
+      int owner = -1;
+      bool take_last = false;
+      for (int attempt = 0; attempt < 2; ++attempt) {
         double run = 0.0;
         if (warp == 0) {
           for (int k0 = 0; k0 < nch; k0 += 32) {
@@ -678,8 +811,30 @@ __global__ void __launch_bounds__(kThreads, 1) sample_verify_kernel(const __grid
         Pc = S.misc_d[15];
         owner = S.misc_i[4];
         take_last = S.misc_i[5] != 0;
-        if (!cdf_of_p && !(R > 0.0) && P.mode == kModeSample) {
-          cdf_of_p = true;  // no residual mass: draw from p (only reachable when q(x) = 0)
+        if (attempt == 0 && !cdf_of_p && !(R > 0.0) && P.mode == kModeSample && ok_stats) {
+          // no residual mass (only reachable when q(x) = 0): draw from p; the
+          // chunk sums of p come from the resident store or from global memory
+          cdf_of_p = true;
+          for (int k = warp; k < nch; k += kConsumerWarps) {
+            float w[8];
+            if constexpr (RESIDENT) {
+              float e1[8];
+              load_e8(S.e, k, lane, len, kFromE ? 0.f : -INFINITY, e1);
+#pragma unroll
+              for (int j = 0; j < 8; ++j) w[j] = prob_of<kFromE>(e1[j], kFromE ? S.fac[k] : 0.f, rp[0]);
+            } else {
+              float zp[8];
+              global_logits<T>(gp_row, k * kChunk, lane, len, S.bitmap, pen, alpha, zp);
+#pragma unroll
+              for (int j = 0; j < 8; ++j) w[j] = prob_of<false>(zp[j], 0.f, rp[0]);
+            }
+            float s = 0.f;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) s += w[j];
+            s = warp_sum(s);
+            if (lane == 0) S.seg[k] = s;
+          }
+          consumer_sync();
           continue;
         }
         break;
@@ -709,79 +864,99 @@ __global__ void __launch_bounds__(kThreads, 1) sample_verify_kernel(const __grid
       }
 
       // ---- candidate: inverse CDF at u_fin within the owning CTA
-      if (P.mode == kModeSample && ok_stats) {
-        const double t = u_fin * R;
-        if (owner == (int)rank && warp == 0) {
-          const double tl = t - Pc;
-          int ks = -1, klast = -1;
-          for (int k = 0; k < nch; ++k) {
-            if (S.seg[k] > 0.f) klast = k;
-            if (!take_last && ks < 0 && S.pre[k] + (double)S.seg[k] > tl && S.seg[k] > 0.f) ks = k;
-          }
-          bool tl_last = take_last;
-          if (ks < 0) { ks = klast; tl_last = true; }
-          int found = -1;
-          if (ks >= 0) {
-            const float fp = TOPP ? 0.f : S.fac[ks];
-            float e1[8], w[8];
-            load_e8(S.e, ks, lane, len, zfill, e1);
+      if (P.mode == kModeSample && ok_stats && owner == (int)rank && warp == 0) {
+        const double tl = u_fin * R - Pc;
+        int ks = -1, klast = -1;
+        for (int k0 = 0; k0 < nch; k0 += 32) {
+          const int k = k0 + lane;
+          const float sg = k < nch ? S.seg[k] : 0.f;
+          const bool pos = sg > 0.f;
+          const bool hit = pos && !take_last && (k < nch ? S.pre[k] : 0.0) + (double)sg > tl;
+          const unsigned mh = __ballot_sync(0xffffffffu, hit);
+          const unsigned mp = __ballot_sync(0xffffffffu, pos);
+          if (mp) klast = k0 + 31 - __clz(mp);
+          if (ks < 0 && mh) ks = k0 + __ffs(mh) - 1;
+        }
+        bool tl_last = take_last;
+        if (ks < 0) { ks = klast; tl_last = true; }
+        int found = -1;
+        if (ks >= 0) {
+          float w[8];
+          const int ib = ks * kChunk;
+          if constexpr (RESIDENT) {
+            float e1[8];
+            load_e8(S.e, ks, lane, len, kFromE ? 0.f : -INFINITY, e1);
+            const float fp = kFromE ? S.fac[ks] : 0.f;
             if (cdf_of_p) {
 #pragma unroll
-              for (int j = 0; j < 8; ++j) w[j] = prob_of<TOPP>(e1[j], fp, rp[0]);
+              for (int j = 0; j < 8; ++j) w[j] = prob_of<kFromE>(e1[j], fp, rp[0]);
             } else {
-              const float fq = TOPP ? 0.f : S.fac[L.nch + ks];
               float e2[8];
-              load_e8(S.e + L.slice, ks, lane, len, zfill, e2);
+              load_e8(S.e + L.slice, ks, lane, len, kFromE ? 0.f : -INFINITY, e2);
+              const float fq = kFromE ? S.fac[L.nch + ks] : 0.f;
 #pragma unroll
-              for (int j = 0; j < 8; ++j) w[j] = fmaxf(prob_of<TOPP>(e1[j], fp, rp[0]) - prob_of<TOPP>(e2[j], fq, rp[1]), 0.f);
+              for (int j = 0; j < 8; ++j)
+                w[j] = fmaxf(prob_of<kFromE>(e1[j], fp, rp[0]) - prob_of<kFromE>(e2[j], fq, rp[1]), 0.f);
             }
-            double rem = tl - S.pre[ks];
-            if (!tl_last) {
-              for (int half = 0; half < 2 && found < 0; ++half) {
-                const float* wh = w + 4 * half;
-                const float ls = (wh[0] + wh[1]) + (wh[2] + wh[3]);
-                const float inc = warp_incl_scan(ls, lane);
-                const float exc = inc - ls;
-                const bool hit = ((double)inc > rem) && ((double)exc <= rem) && ls > 0.f;
-                const unsigned m = __ballot_sync(0xffffffffu, hit);
-                if (m) {
-                  const int L0 = __ffs(m) - 1;
-                  int jj = -1;
-                  if (lane == L0) {
-                    double cum = (double)exc;
-                    for (int j = 0; j < 4; ++j) {
-                      cum += (double)wh[j];
-                      if (wh[j] > 0.f && cum > rem) { jj = j; break; }
-                    }
-                    if (jj < 0) {
-                      for (int j = 3; j >= 0; --j) if (wh[j] > 0.f) { jj = j; break; }
-                    }
-                  }
-                  jj = __shfl_sync(0xffffffffu, jj, L0);
-                  found = ks * kChunk + 128 * half + 4 * L0 + jj;
-                } else {
-                  rem -= (double)__shfl_sync(0xffffffffu, inc, 31);
-                }
-              }
-            }
-            if (found < 0) {
-              // the last element with positive mass in the chunk
-              int best = -1;
-              for (int half = 1; half >= 0 && best < 0; --half) {
-                int lj = -1;
-                for (int j = 3; j >= 0; --j) if (w[4 * half + j] > 0.f) { lj = j; break; }
-                const unsigned m = __ballot_sync(0xffffffffu, lj >= 0);
-                if (m) {
-                  const int L0 = 31 - __clz(m);
-                  lj = __shfl_sync(0xffffffffu, lj, L0);
-                  best = ks * kChunk + 128 * half + 4 * L0 + lj;
-                }
-              }
-              found = best;
+          } else {
+            float zp[8];
+            global_logits<T>(gp_row, ib, lane, len, S.bitmap, pen, alpha, zp);
+            if (cdf_of_p) {
+#pragma unroll
+              for (int j = 0; j < 8; ++j) w[j] = prob_of<false>(zp[j], 0.f, rp[0]);
+            } else {
+              float zq[8];
+              global_logits<T>(gq_row, ib, lane, len, S.bitmap, pen, alpha, zq);
+#pragma unroll
+              for (int j = 0; j < 8; ++j)
+                w[j] = fmaxf(prob_of<false>(zp[j], 0.f, rp[0]) - prob_of<false>(zq[j], 0.f, rp[1]), 0.f);
             }
           }
-          if (lane == 0) P.results[item].cand = found >= 0 ? v0 + found : -1;
+          double rem = tl - S.pre[ks];
+          if (!tl_last) {
+            for (int half = 0; half < 2 && found < 0; ++half) {
+              const float* wh = w + 4 * half;
+              const float ls = (wh[0] + wh[1]) + (wh[2] + wh[3]);
+              const float inc = warp_incl_scan(ls, lane);
+              const float exc = inc - ls;
+              const bool hit = ((double)inc > rem) && ((double)exc <= rem) && ls > 0.f;
+              const unsigned m = __ballot_sync(0xffffffffu, hit);
+              if (m) {
+                const int L0 = __ffs(m) - 1;
+                int jj = -1;
+                if (lane == L0) {
+                  double cum = (double)exc;
+                  for (int j = 0; j < 4; ++j) {
+                    cum += (double)wh[j];
+                    if (wh[j] > 0.f && cum > rem) { jj = j; break; }
+                  }
+                  if (jj < 0)
+                    for (int j = 3; j >= 0; --j)
+                      if (wh[j] > 0.f) { jj = j; break; }
+                }
+                jj = __shfl_sync(0xffffffffu, jj, L0);
+                found = ib + 128 * half + 4 * L0 + jj;
+              } else {
+                rem -= (double)__shfl_sync(0xffffffffu, inc, 31);
+              }
+            }
+          }
+          if (found < 0) {
+            // the last element with positive mass in the chunk
+            for (int half = 1; half >= 0 && found < 0; --half) {
+              int lj = -1;
+              for (int j = 3; j >= 0; --j)
+                if (w[4 * half + j] > 0.f) { lj = j; break; }
+              const unsigned m = __ballot_sync(0xffffffffu, lj >= 0);
+              if (m) {
+                const int L0 = 31 - __clz(m);
+                lj = __shfl_sync(0xffffffffu, lj, L0);
+                found = ib + 128 * half + 4 * L0 + lj;
+              }
+            }
+          }
         }
+        if (lane == 0) P.results[item].cand = found >= 0 ? v0 + found : -1;
       }
 
       // ---- status of this CTA's share of the item; arrival count
@@ -817,10 +992,8 @@ __global__ void __launch_bounds__(kThreads, 1) sample_verify_kernel(const __grid
         consumer_sync();
         if (S.misc_i[kMiFinalize] && warp == 0) {
           __threadfence();
-          // gather per-position flags and candidates of request b
           int st = 0;
-          const int nitems_b = K + 1;
-          for (int j = lane; j < nitems_b * C; j += 32) {
+          for (int j = lane; j < (K + 1) * C; j += 32) {
             const int ii = j / C, cc = j % C;
             const int item_j = ii < K ? d0 + ii : P.total + b;
             st |= __ldcg(P.inval + (size_t)item_j * kMaxCluster + cc);
@@ -845,7 +1018,6 @@ __global__ void __launch_bounds__(kThreads, 1) sample_verify_kernel(const __grid
           if (lane == 0) {
             P.out_accepted[b] = st ? -1 : jrej;
             if (P.out_status) P.out_status[b] = st;
-            P.counters[b] = 0;
           }
         }
       }
@@ -856,27 +1028,20 @@ __global__ void __launch_bounds__(kThreads, 1) sample_verify_kernel(const __grid
   cluster_sync_all();
 }
 
-// Explicit instantiations.
-template __global__ void sample_verify_kernel<float, false>(const __grid_constant__ SampleParams);
-template __global__ void sample_verify_kernel<float, true>(const __grid_constant__ SampleParams);
-template __global__ void sample_verify_kernel<__nv_bfloat16, false>(const __grid_constant__ SampleParams);
-template __global__ void sample_verify_kernel<__nv_bfloat16, true>(const __grid_constant__ SampleParams);
-
-}  // namespace sv
-
-namespace sv {
-
 namespace {
 
-template <typename T, bool TOPP>
+template <typename T, bool TOPP, bool RESIDENT>
 int launch_t(SampleParams& P, cudaStream_t stream) {
-  auto kern = sample_verify_kernel<T, TOPP>;
+  auto kern = sample_verify_kernel<T, TOPP, RESIDENT>;
   const int smem = P.L.total;
-  // attributes are per function and cheap to set; do it on every call so a
-  // new device or a larger layout is always covered
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) return -8;
-  if (P.C > 8 && cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) {
+    cudaGetLastError();
     return -8;
+  }
+  if (P.C > 8 && cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess) {
+    cudaGetLastError();
+    return -8;
+  }
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -888,7 +1053,7 @@ int launch_t(SampleParams& P, cudaStream_t stream) {
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  // clusters that fit on the device at once (cached per configuration)
+  // clusters resident at once (cached per device and configuration)
   static thread_local int cached_dev = -1, cached_C = 0, cached_smem = 0, cached_n = 0;
   int dev = 0;
   cudaGetDevice(&dev);
@@ -913,10 +1078,10 @@ int launch_t(SampleParams& P, cudaStream_t stream) {
 
 }  // namespace
 
-// Smallest cluster (1..16) whose per-CTA slice fits in shared memory.
-int choose_sample_layout(int V, int elem_bytes, bool topp, int max_smem, int* C_out, SmemLayout* L_out) {
+// Resident layout: the smallest cluster (1..16) whose slice fits.
+int choose_resident_layout(int V, int elem_bytes, bool topp, int max_smem, int* C_out, SmemLayout* L_out) {
   for (int C = 1; C <= kMaxCluster; C *= 2) {
-    SmemLayout L = make_sample_layout(V, C, elem_bytes, topp);
+    const SmemLayout L = make_resident_layout(V, C, elem_bytes, topp);
     if (L.total <= max_smem) {
       *C_out = C;
       *L_out = L;
@@ -926,9 +1091,22 @@ int choose_sample_layout(int V, int elem_bytes, bool topp, int max_smem, int* C_
   return -1;
 }
 
+// Streaming layout for cluster size C (-1 if it does not fit).
+int choose_stream_layout(int V, int C, int elem_bytes, bool topp, int max_smem, SmemLayout* L_out) {
+  const SmemLayout L = make_stream_layout(V, C, elem_bytes, topp, max_smem);
+  if (L.total <= 0) return -1;
+  *L_out = L;
+  return 0;
+}
+
 int launch_sample_verify(SampleParams& P, bool bf16, bool topp, cudaStream_t stream) {
-  if (bf16) return topp ? launch_t<__nv_bfloat16, true>(P, stream) : launch_t<__nv_bfloat16, false>(P, stream);
-  return topp ? launch_t<float, true>(P, stream) : launch_t<float, false>(P, stream);
+  const bool res = P.L.resident != 0;
+  if (bf16) {
+    if (topp) return res ? launch_t<__nv_bfloat16, true, true>(P, stream) : launch_t<__nv_bfloat16, true, false>(P, stream);
+    return res ? launch_t<__nv_bfloat16, false, true>(P, stream) : launch_t<__nv_bfloat16, false, false>(P, stream);
+  }
+  if (topp) return res ? launch_t<float, true, true>(P, stream) : launch_t<float, true, false>(P, stream);
+  return res ? launch_t<float, false, true>(P, stream) : launch_t<float, false, false>(P, stream);
 }
 
 }  // namespace sv

@@ -12,8 +12,9 @@ constexpr int kChunk = 256;                 // elements per warp-chunk
 constexpr int kConsumerWarps = 16;
 constexpr int kConsumerThreads = kConsumerWarps * 32;
 constexpr int kThreads = kConsumerThreads + 32;  // + one producer warp
-constexpr int kStage = kConsumerWarps * kChunk;  // elements per ring slot
-constexpr int kRingBytes = 64 * 1024;
+constexpr int kStage = kConsumerWarps * kChunk;  // elements of each row per ring slot
+constexpr int kResidentRingBytes = 64 * 1024;
+constexpr int kStreamRingMaxBytes = 192 * 1024;
 constexpr int kXchgDoubles = 8;             // per CTA per exchange buffer
 constexpr int kMaxCluster = 16;
 
@@ -26,11 +27,17 @@ struct ItemResult {       // one per work item (a draft position or a bonus row)
   int pad[2];
 };
 
+// Shared memory of the sampling kernel.  A ring slot holds one stage: the
+// CTA's next kStage tokens of the target row followed by the same tokens of
+// the draft row.  The resident variant also keeps one fp32 value per token
+// of its slice of both rows (the e-array); the streaming variant re-reads
+// the rows through the ring instead and spends the space on a deeper ring.
 struct SmemLayout {
   int slice;      // token ids per CTA (multiple of 64)
   int nch;        // chunks per CTA slice (ceil(slice / 256))
   int nslots;     // ring slots
   int slot_bytes;
+  int resident;
   int off_e, off_bitmap, off_refc, off_fac, off_seg, off_pre, off_wpart, off_xchg, off_hist, off_tot,
       off_misc, off_bar;
   int total;
@@ -38,19 +45,11 @@ struct SmemLayout {
 
 inline int align_up_i(int x, int a) { return (x + a - 1) / a * a; }
 
-// Shared-memory layout of the sampling kernel for cluster size C.
-inline SmemLayout make_sample_layout(int V, int C, int elem_bytes, bool topp) {
-  SmemLayout L{};
-  int per = (V + C - 1) / C;
-  L.slice = align_up_i(per, 64);
-  L.nch = (L.slice + kChunk - 1) / kChunk;
-  L.slot_bytes = kStage * elem_bytes;
-  L.nslots = kRingBytes / L.slot_bytes;
-  int off = kRingBytes;
-  L.off_e = off;        off += 2 * L.slice * 4;
+// Everything but the ring and the e-array, from `off` on.
+inline int layout_tail(SmemLayout& L, int off, int C, bool topp) {
   L.off_bitmap = off;   off += L.nch * 8 * 4;   // 8 words per 256-token chunk
-  L.off_refc = off;     off += align_up_i(2 * L.nch * 4, 16);
-  L.off_fac = off;      off += align_up_i(2 * L.nch * 4, 16);
+  L.off_refc = off;     off += L.resident ? align_up_i(2 * L.nch * 4, 16) : 0;
+  L.off_fac = off;      off += L.resident ? align_up_i(2 * L.nch * 4, 16) : 0;
   L.off_seg = off;      off += align_up_i(L.nch * 4, 16);
   L.off_pre = off;      off += align_up_i(L.nch * 8, 16);
   L.off_wpart = off;    off += 2 * kConsumerWarps * 8;
@@ -59,7 +58,37 @@ inline SmemLayout make_sample_layout(int V, int C, int elem_bytes, bool topp) {
   L.off_tot = off;      off += topp ? 2 * 256 * 4 : 0;
   L.off_misc = off;     off += 256;
   L.off_bar = off;      off += (2 * L.nslots + 2) * 8;
-  L.total = align_up_i(off, 128);
+  return align_up_i(off, 128);
+}
+
+// Resident variant for cluster size C: 64 KB ring + the e-array.
+inline SmemLayout make_resident_layout(int V, int C, int elem_bytes, bool topp) {
+  SmemLayout L{};
+  L.resident = 1;
+  L.slice = align_up_i((V + C - 1) / C, 64);
+  L.nch = (L.slice + kChunk - 1) / kChunk;
+  L.slot_bytes = 2 * kStage * elem_bytes;
+  L.nslots = kResidentRingBytes / L.slot_bytes;
+  L.off_e = kResidentRingBytes;
+  L.total = layout_tail(L, L.off_e + 2 * L.slice * 4, C, topp);
+  return L;
+}
+
+// Streaming variant: the deepest ring (whole slots, at most 192 KB, at
+// least 2 slots) that fits in `max_smem`; total = 0 if none does.
+inline SmemLayout make_stream_layout(int V, int C, int elem_bytes, bool topp, int max_smem) {
+  SmemLayout L{};
+  L.resident = 0;
+  L.slice = align_up_i((V + C - 1) / C, 64);
+  L.nch = (L.slice + kChunk - 1) / kChunk;
+  L.slot_bytes = 2 * kStage * elem_bytes;
+  for (int ns = kStreamRingMaxBytes / L.slot_bytes; ns >= 2; --ns) {
+    L.nslots = ns;
+    L.off_e = ns * L.slot_bytes;
+    L.total = layout_tail(L, L.off_e, C, topp);
+    if (L.total <= max_smem) return L;
+  }
+  L.total = 0;
   return L;
 }
 

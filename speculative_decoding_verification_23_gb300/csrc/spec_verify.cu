@@ -10,7 +10,8 @@
 #include "spec_internal.h"
 
 namespace sv {
-int choose_sample_layout(int V, int elem_bytes, bool topp, int max_smem, int* C_out, SmemLayout* L_out);
+int choose_resident_layout(int V, int elem_bytes, bool topp, int max_smem, int* C_out, SmemLayout* L_out);
+int choose_stream_layout(int V, int C, int elem_bytes, bool topp, int max_smem, SmemLayout* L_out);
 int launch_sample_verify(SampleParams& P, bool bf16, bool topp, cudaStream_t stream);
 int launch_greedy_verify(const GreedyParams& P, bool bf16, cudaStream_t stream);
 }  // namespace sv
@@ -49,15 +50,14 @@ int check_workspace(const spec_args* a, const void* ws, size_t ws_bytes) {
   return SPEC_OK;
 }
 
-int device_max_smem(int* out) {
+int device_props(int* max_smem, int* num_sms) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) { cudaGetLastError(); return SPEC_ERR_DEVICE; }
-  int v = 0;
-  if (cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess) {
+  if (cudaDeviceGetAttribute(max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
     cudaGetLastError();
     return SPEC_ERR_DEVICE;
   }
-  *out = v;
   return SPEC_OK;
 }
 
@@ -83,29 +83,41 @@ void fill_sample_inputs(sv::SampleParams& P, const spec_args* a) {
   P.flags = a->flags;
 }
 
+// Picks the kernel variant.  Resident (each logit read once, values kept in
+// the shared memory of a C-CTA cluster) when every work item gets its own
+// cluster in one wave; streaming (slices re-read from L2, about one item per
+// SM in flight) otherwise.  SPEC_PREFER_* flags override the choice.
 int run_sample(sv::SampleParams& P, const spec_args* a, void* ws, cudaStream_t stream) {
-  int max_smem = 0;
-  int rc = device_max_smem(&max_smem);
+  int max_smem = 0, num_sms = 0;
+  int rc = device_props(&max_smem, &num_sms);
   if (rc) return rc;
   const bool topp = a->top_p != nullptr;
-  int C = 1;
-  sv::SmemLayout L{};
-  if (sv::choose_sample_layout(a->V, elem_bytes(a->dtype), topp, max_smem, &C, &L) != 0) return SPEC_ERR_SHAPE;
+  const int es = elem_bytes(a->dtype);
+  int C_res = 0;
+  sv::SmemLayout L_res{}, L_str{};
+  const bool res_ok = sv::choose_resident_layout(a->V, es, topp, max_smem, &C_res, &L_res) == 0;
+  int C_str = 1;
+  while (C_str <= sv::kMaxCluster && sv::choose_stream_layout(a->V, C_str, es, topp, max_smem, &L_str) != 0) C_str *= 2;
+  const bool str_ok = C_str <= sv::kMaxCluster;
+  bool resident;
+  if ((a->flags & SPEC_PREFER_RESIDENT) && res_ok) resident = true;
+  else if ((a->flags & SPEC_PREFER_STREAMING) && str_ok) resident = false;
+  else resident = res_ok && (!str_ok || (long long)P.n_items * C_res <= num_sms);
+  if (!resident && !str_ok) return SPEC_ERR_SHAPE;
   const sv::WorkspaceLayout W = sv::make_workspace_layout(a->B, a->total_drafts, a->V);
   unsigned char* w = static_cast<unsigned char*>(ws);
   P.counters = reinterpret_cast<int*>(w + W.off_counters);
   P.results = reinterpret_cast<sv::ItemResult*>(w + W.off_results);
   P.inval = reinterpret_cast<int*>(w + W.off_inval);
-  P.C = C;
-  P.L = L;
+  P.C = resident ? C_res : C_str;
+  P.L = resident ? L_res : L_str;
   if (P.mode == sv::kModeSample) {
     if (cudaMemsetAsync(P.counters, 0, (size_t)a->B * sizeof(int), stream) != cudaSuccess) {
       cudaGetLastError();
       return SPEC_ERR_LAUNCH;
     }
   }
-  rc = sv::launch_sample_verify(P, a->dtype == SPEC_BF16, topp, stream);
-  return rc;
+  return sv::launch_sample_verify(P, a->dtype == SPEC_BF16, topp, stream);
 }
 
 }  // namespace
@@ -162,8 +174,8 @@ int spec_verify_greedy(const spec_args* a, int32_t* out_tokens, int32_t* out_acc
   rc = check_workspace(a, workspace, ws_bytes);
   if (rc) return rc;
   const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  int max_smem = 0;
-  rc = device_max_smem(&max_smem);
+  int max_smem = 0, num_sms = 0;
+  rc = device_props(&max_smem, &num_sms);
   if (rc) return rc;
   const sv::WorkspaceLayout W = sv::make_workspace_layout(a->B, a->total_drafts, a->V);
   unsigned char* w = static_cast<unsigned char*>(workspace);

@@ -19,14 +19,14 @@ def run_sample(batch, *, flags=0, device="cuda", db=None):
     return tok.cpu().numpy().astype(np.int64), acc.cpu().numpy().astype(np.int64), st.cpu().numpy().astype(np.int64)
 
 
-def run_tv(batch, *, device="cuda", db=None):
+def run_tv(batch, *, flags=0, device="cuda", db=None):
     import torch
 
     import speculative_decoding_verification_23_gb300 as sv
     from speculative_decoding_verification_23_gb300.device_batch import to_device
 
     db = db or to_device(batch, device)
-    tv, th, px, qx = sv.spec_tv_budget(db.args(), device=torch.device(device))
+    tv, th, px, qx = sv.spec_tv_budget(db.args(flags=flags), device=torch.device(device))
     torch.cuda.synchronize()
     return [t.cpu().numpy().astype(np.float64) for t in (tv, th, px, qx)]
 

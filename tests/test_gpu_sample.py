@@ -16,8 +16,12 @@ import parity as PR
 
 pytestmark = pytest.mark.gpu
 
+RESIDENT, STREAMING = 2, 4       # SPEC_PREFER_* strategy hints
+VARIANTS = pytest.mark.parametrize("variant", [RESIDENT, STREAMING], ids=["resident", "streaming"])
+
 
 def _check(batch, requests=None, flags=0, max_near=None):
+    """Run the GPU path (with strategy `flags`) and the oracle; compare."""
     got = PR.run_sample(batch, flags=flags)
     ref = PR.oracle_sample(batch, requests, bonus=not (flags & 1))
     bad, near = PR.compare_sample(batch, got, ref, requests)
@@ -27,15 +31,17 @@ def _check(batch, requests=None, flags=0, max_near=None):
     return got, ref
 
 
-def test_tiny_rounds():
+@VARIANTS
+def test_tiny_rounds(variant):
     """B=1, K=4, V=1024, fp32, T=0.7, D=0.75: 16 rounds."""
     for r in range(16):
-        _check(W.tiny(r))
+        _check(W.tiny(r), flags=variant)
 
 
+@VARIANTS
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 @pytest.mark.parametrize("V", [3, 5, 257, 4097, 20000, 25000, 50000])
-def test_small_mixed_shapes(dtype, V):
+def test_small_mixed_shapes(dtype, V, variant):
     """Ragged K (incl. 0), penalties with history, several temperatures and
     budgets; V spans one chunk, several stages, and 1/2/4-CTA clusters with a
     ragged tail."""
@@ -43,44 +49,53 @@ def test_small_mixed_shapes(dtype, V):
     batch = W.make_batch(B=6, V=V, K=K, dtype=dtype, seed=1000 + V, rho=[0.3, 0.6, 0.8, 0.9, 0.95, 0.99],
                          temperature=[0.5, 0.7, 1.0, 1.3, 0.9, 0.6], rep_penalty=[1.0, 1.3, 1.1, 0.8, 1.2, 1.0],
                          hist_len=min(20, 3 * V), tv_budget=[0.0, 0.2, 0.5, 0.75, 1.0, 0.1])
-    _check(batch)
+    _check(batch, flags=variant)
 
 
+@VARIANTS
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 @pytest.mark.parametrize("V", [5, 3000, 40000])
-def test_top_p(dtype, V):
+def test_top_p(dtype, V, variant):
     batch = W.make_batch(B=5, V=V, K=[1, 4, 0, 8, 3], dtype=dtype, seed=2000 + V, rho=0.85,
                          temperature=[0.8, 1.5, 0.8, 1.0, 0.6], rep_penalty=1.0, top_p=[0.9, 0.5, 0.95, 0.3, 1.0],
                          tv_budget=[0.5, 0.0, 0.5, 0.3, 0.9], draft_topk=4)
-    got, ref = _check(batch)
-    tvg = PR.run_tv(batch)
+    got, ref = _check(batch, flags=variant)
+    tvg = PR.run_tv(batch, flags=variant)
     assert PR.compare_tv(batch, tvg, ref) < PR.TOL_PROB
 
 
+@VARIANTS
 @pytest.mark.parametrize("V", [257, 25000, 152064])
-def test_tv_budget_matches_oracle(V):
+def test_tv_budget_matches_oracle(V, variant):
     batch = W.make_batch(B=4, V=V, K=[3, 0, 8, 5], dtype="bf16", seed=3000 + V, rho=0.9, temperature=0.7,
                          rep_penalty=1.1, hist_len=64, tv_budget=[0.0, 0.5, 0.75, 1.0])
     ref = PR.oracle_sample(batch)
-    got = PR.run_tv(batch)
+    got = PR.run_tv(batch, flags=variant)
     assert PR.compare_tv(batch, got, ref) < PR.TOL_PROB
 
 
+@VARIANTS
 @pytest.mark.parametrize("D", [0.0, 0.5, 0.75, 1.0])
-def test_qwen25_single_d_sweep(D):
+def test_qwen25_single_d_sweep(D, variant):
     """B=1, K=8, V=152064 bf16, rho=0.9, T=0.7, penalty 1.1 over 256 history tokens."""
     batch = W.qwen25_single(D)
-    got, ref = _check(batch, max_near=1)
+    got, ref = _check(batch, flags=variant, max_near=1)
     if D == 1.0:
         assert got[1][0] == 8
 
 
+@pytest.fixture(scope="module")
+def batched_batch():
+    return W.batched(0)
+
+
 @pytest.mark.slow
-def test_batched_full_size():
+@VARIANTS
+def test_batched_full_size(batched_batch, variant):
     """B=64, K=8, V=152064 bf16 (the benchmark workload): 12 requests against
     the oracle one by one; properties on all 64."""
-    batch = W.batched(0)
-    got = PR.run_sample(batch)
+    batch = batched_batch
+    got = PR.run_sample(batch, flags=variant)
     sample = list(range(0, 64, 6))
     ref = PR.oracle_sample(batch, sample)
     bad, near = PR.compare_sample(batch, got, ref, sample)
@@ -99,11 +114,17 @@ def test_batched_full_size():
             assert j == K          # D = 1 accepts every draft
 
 
+@pytest.fixture(scope="module")
+def ragged_batch():
+    return W.ragged_top_p(0)
+
+
 @pytest.mark.slow
-def test_ragged_top_p_full_size():
+@VARIANTS
+def test_ragged_top_p_full_size(ragged_batch, variant):
     """B=256, K_b in 1..8, V=152064 fp32, top-p 0.9, D=0.5: 10 requests."""
-    batch = W.ragged_top_p(0)
-    got = PR.run_sample(batch)
+    batch = ragged_batch
+    got = PR.run_sample(batch, flags=variant)
     sample = list(range(0, 256, 26))
     ref = PR.oracle_sample(batch, sample)
     bad, near = PR.compare_sample(batch, got, ref, sample)
@@ -111,35 +132,38 @@ def test_ragged_top_p_full_size():
     assert np.all(got[2] == 0)
 
 
-def test_equal_distributions_never_reject():
+@VARIANTS
+def test_equal_distributions_never_reject(variant):
     batch = W.make_batch(B=3, V=3000, K=[4, 8, 1], dtype="f32", seed=5, rho=0.7, temperature=0.9,
                          rep_penalty=1.2, hist_len=10, tv_budget=[0.0, 0.3, 1.0])
     for b in range(batch.B):
         d0, d1 = int(batch.cu_draft[b]), int(batch.cu_draft[b + 1])
         off = d0 + b
         batch.draft[d0:d1] = batch.target[off:off + (d1 - d0)]
-    tok, acc, st = PR.run_sample(batch)
+    tok, acc, st = PR.run_sample(batch, flags=variant)
     assert list(acc) == [4, 8, 1] and np.all(st == 0)
-    tv = PR.run_tv(batch)[0]
+    tv = PR.run_tv(batch, flags=variant)[0]
     assert np.max(np.abs(tv)) < 1e-6
 
 
-def test_no_bonus_flag():
+@VARIANTS
+def test_no_bonus_flag(variant):
     batch = W.make_batch(B=3, V=2000, K=[2, 3, 0], dtype="bf16", seed=6, tv_budget=1.0)
-    got, ref = _check(batch, flags=1)
+    got, ref = _check(batch, flags=1 | variant)
     tok, acc, _ = got
     assert list(acc) == [2, 3, 0]
     assert tok[2] == -1 and tok[3 + 1 + 3] == -1 and tok[-1] == -1
 
 
-def test_invalid_inputs_set_status():
+@VARIANTS
+def test_invalid_inputs_set_status(variant):
     batch = W.make_batch(B=6, V=500, K=[2, 2, 2, 2, 2, 2], dtype="f32", seed=7, hist_len=4, rep_penalty=1.1)
     batch.draft_tokens[1] = 500                 # request 0: token out of range
     batch.temperature[1] = 0.0                  # request 1: T = 0
     batch.target[2 * 3 + 1, 7] = np.nan         # request 2: NaN logit
     batch.tv_budget[3] = 1.5                    # request 3: D > 1
     batch.hist[4 * 4] = -3                      # request 4: bad history token
-    tok, acc, st = PR.run_sample(batch)
+    tok, acc, st = PR.run_sample(batch, flags=variant)
     ref = PR.oracle_sample(batch)
     assert list(st[:5] != 0) == [True] * 5 and st[5] == 0
     np.testing.assert_array_equal(st, ref["status"])
@@ -149,18 +173,20 @@ def test_invalid_inputs_set_status():
     assert not bad
 
 
-def test_repeat_calls_are_deterministic():
+@VARIANTS
+def test_repeat_calls_are_deterministic(variant):
     batch = W.make_batch(B=8, V=30000, K=4, dtype="bf16", seed=8, hist_len=32, rep_penalty=1.1, tv_budget=0.4)
     db = to_device(batch)
-    a = PR.run_sample(batch, db=db)
+    a = PR.run_sample(batch, db=db, flags=variant)
     for _ in range(3):
-        b = PR.run_sample(batch, db=db)
+        b = PR.run_sample(batch, db=db, flags=variant)
         for x, y in zip(a, b):
             np.testing.assert_array_equal(x, y)
 
 
+@VARIANTS
 @pytest.mark.parametrize("V,D", [(3, 0.0), (5, 0.25), (8, 0.6)])
-def test_chi_square_first_token_on_gpu(V, D):
+def test_chi_square_first_token_on_gpu(V, D, variant):
     """The batch is the seed axis: 100000 requests with identical rows, x ~ q
     drawn by numpy, independent uniforms; the first emitted token follows pi."""
     rng = np.random.default_rng(40 + V)
@@ -184,7 +210,7 @@ def test_chi_square_first_token_on_gpu(V, D):
     batch.top_p = np.ones(B, np.float32)
     batch.tv_budget = np.full(B, D, np.float32)
     batch.uniforms = W.uniforms_from_bits(rng.integers(0, 2 ** 32, size=B * (K + 1), dtype=np.uint64))
-    tok, acc, st = PR.run_sample(batch)
+    tok, acc, st = PR.run_sample(batch, flags=variant)
     first = tok[np.arange(B) * (K + 1)]
     counts = np.bincount(first, minlength=V)
     p = scipy.special.softmax(zt[0].astype(np.float64) / T)
