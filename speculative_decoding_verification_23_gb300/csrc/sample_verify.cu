@@ -279,69 +279,146 @@ struct RowProb {
   double kept;       // kept mass, in units of 2^(z'c - M)
 };
 
-template <bool FROM_E>
-__device__ __forceinline__ float prob_of(float s, float fac, const RowProb& rp) {
-  if constexpr (FROM_E) {
+// Probability modes: kPE = stored e times its chunk factor (resident, no
+// top-p); kPZ = logit, no top-p; kPZT = logit with the top-p cut.
+enum { kPE = 0, kPZ = 1, kPZT = 2 };
+
+template <int MODE>
+__device__ __forceinline__ float prob1(float s, float fac, const RowProb& rp) {
+  if constexpr (MODE == kPE) {
     return s * fac;
+  } else if constexpr (MODE == kPZ) {
+    return ex2(fmaf(s, rp.c, -rp.mc)) * rp.invs;
   } else {
     return order_key(s) >= rp.tau_key ? ex2(fmaf(s, rp.c, -rp.mc)) * rp.invs : 0.f;
   }
 }
 
-// Pass-1 statistics of one chunk of one row for one warp: running
-// reference `refc` (warp-uniform, units of z'c) and lane sum `Ssum` of
-// 2^(z'c - refc); the reference only moves up, when a chunk would overflow.
-// e receives the chunk's 2^(z'c - refc).
-__device__ __forceinline__ void chunk_stats(const float* z, float c, float& refc, bool& have_ref, float& Ssum,
-                                            float* e) {
+// The same for a lane's 8 values, in packed fp32x2 arithmetic (bit-identical
+// to prob1 element by element).
+template <int MODE>
+__device__ __forceinline__ void probs8(const float* s, float fac, const RowProb& rp, float* p) {
+  if constexpr (MODE == kPE) {
+    const float2 f2 = make_float2(fac, fac);
+#pragma unroll
+    for (int j = 0; j < 8; j += 2) {
+      const float2 r = __fmul2_rn(make_float2(s[j], s[j + 1]), f2);
+      p[j] = r.x;
+      p[j + 1] = r.y;
+    }
+  } else {
+    const float2 c2 = make_float2(rp.c, rp.c), m2 = make_float2(-rp.mc, -rp.mc);
+    const float2 i2 = make_float2(rp.invs, rp.invs);
+#pragma unroll
+    for (int j = 0; j < 8; j += 2) {
+      const float2 y = __ffma2_rn(make_float2(s[j], s[j + 1]), c2, m2);
+      const float2 r = __fmul2_rn(make_float2(ex2(y.x), ex2(y.y)), i2);
+      p[j] = r.x;
+      p[j + 1] = r.y;
+    }
+    if constexpr (MODE == kPZT) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        if (order_key(s[j]) < rp.tau_key) p[j] = 0.f;
+    }
+  }
+}
+
+// r = max(p - q, 0) for 8 values; returns their sum.
+__device__ __forceinline__ float resid8(const float* p, const float* q, float* r) {
+  const float2 m1 = make_float2(-1.f, -1.f);
+  float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+  for (int j = 0; j < 8; j += 2) {
+    const float2 d = __ffma2_rn(make_float2(q[j], q[j + 1]), m1, make_float2(p[j], p[j + 1]));
+    r[j] = fmaxf(d.x, 0.f);
+    r[j + 1] = fmaxf(d.y, 0.f);
+    acc = __fadd2_rn(acc, make_float2(r[j], r[j + 1]));
+  }
+  return acc.x + acc.y;
+}
+
+__device__ __forceinline__ float sum8(const float* v) {
+  float2 a = __fadd2_rn(make_float2(v[0], v[1]), make_float2(v[2], v[3]));
+  const float2 b = __fadd2_rn(make_float2(v[4], v[5]), make_float2(v[6], v[7]));
+  a = __fadd2_rn(a, b);
+  return a.x + a.y;
+}
+
+// Warp 0 of every CTA: the chunk sums seg[0..nch) summed in fp64 over lane
+// blocks of consecutive chunks, then scanned across lanes.  Every use (the
+// CTA total exchanged over the cluster and the owner's search) takes this
+// one order of summation.
+__device__ __forceinline__ double seg_block_scan(const float* seg, int nch, int lane, int& k0, int& k1,
+                                                 double& block, double& incl) {
+  const int bl = (nch + 31) / 32;
+  k0 = min(nch, lane * bl);
+  k1 = min(nch, k0 + bl);
+  double s = 0.0;
+  for (int k = k0; k < k1; ++k) s += (double)seg[k];
+  block = s;
+  incl = warp_incl_scan_d(s, lane);
+  return __shfl_sync(0xffffffffu, incl, 31);
+}
+
+__device__ __forceinline__ void exps8(const float* z, float c, float refc, float* e) {
+  const float2 c2 = make_float2(c, c), nr = make_float2(-refc, -refc);
+#pragma unroll
+  for (int j = 0; j < 8; j += 2) {
+    const float2 y = __ffma2_rn(make_float2(z[j], z[j + 1]), c2, nr);
+    e[j] = ex2(y.x);
+    e[j + 1] = ex2(y.y);
+  }
+}
+
+__device__ __forceinline__ float max8(const float* z) {
+  float m = fmaxf(fmaxf(z[0], z[1]), fmaxf(z[2], z[3]));
+  return fmaxf(m, fmaxf(fmaxf(z[4], z[5]), fmaxf(z[6], z[7])));
+}
+
+// Pass-1 statistics of one chunk of NR rows (1 or 2) for one warp: per row a
+// running reference refc (warp-uniform, units of z'c) and a lane sum Ssum of
+// 2^(z'c - refc).  A reference starts at the row's first chunk maximum and
+// only moves up, when a chunk would overflow (sum above 2^64).  e receives
+// the chunk's 2^(z'c - refc).
+template <int NR>
+__device__ __forceinline__ void chunk_stats_n(float (&z)[2][8], float c, float* refc, bool& have_ref, float* Ssum,
+                                              float (&e)[2][8]) {
   const float kLim = 18446744073709551616.0f;  // 2^64
   if (!have_ref) {
-    float mx = z[0];
 #pragma unroll
-    for (int j = 1; j < 8; ++j) mx = fmaxf(mx, z[j]);
-    mx = warp_max(mx);
-    refc = (mx > -INFINITY) ? mx * c : 0.f;
+    for (int r = 0; r < NR; ++r) {
+      const float mx = warp_max(max8(z[r]));
+      refc[r] = (mx > -INFINITY) ? mx * c : 0.f;
+    }
     have_ref = true;
   }
-  float s;
-  {
-    const float2 c2 = make_float2(c, c);
-    const float2 nr = make_float2(-refc, -refc);
+  float s[NR];
 #pragma unroll
-    for (int j = 0; j < 8; j += 2) {
-      const float2 y = __ffma2_rn(make_float2(z[j], z[j + 1]), c2, nr);
-      e[j] = ex2(y.x);
-      e[j + 1] = ex2(y.y);
-    }
-    float2 a = __fadd2_rn(make_float2(e[0], e[1]), make_float2(e[2], e[3]));
-    const float2 b2 = __fadd2_rn(make_float2(e[4], e[5]), make_float2(e[6], e[7]));
-    a = __fadd2_rn(a, b2);
-    s = a.x + a.y;
+  for (int r = 0; r < NR; ++r) {
+    exps8(z[r], c, refc[r], e[r]);
+    s[r] = sum8(e[r]);
   }
-  if (__any_sync(0xffffffffu, !(s <= kLim))) {
-    float mx = z[0];
+  bool bad = false;
 #pragma unroll
-    for (int j = 1; j < 8; ++j) mx = fmaxf(mx, z[j]);
-    mx = warp_max(mx);
-    const float nref = (mx > -INFINITY) ? mx * c : 0.f;
-    if (nref > refc) {
-      Ssum *= ex2(refc - nref);
-      refc = nref;
-    }
-    const float2 c2 = make_float2(c, c);
-    const float2 nr = make_float2(-refc, -refc);
+  for (int r = 0; r < NR; ++r) bad |= !(s[r] <= kLim);
+  if (__any_sync(0xffffffffu, bad)) {
 #pragma unroll
-    for (int j = 0; j < 8; j += 2) {
-      const float2 y = __ffma2_rn(make_float2(z[j], z[j + 1]), c2, nr);
-      e[j] = ex2(y.x);
-      e[j + 1] = ex2(y.y);
+    for (int r = 0; r < NR; ++r) {
+      if (__any_sync(0xffffffffu, !(s[r] <= kLim))) {
+        const float mx = warp_max(max8(z[r]));
+        const float nref = (mx > -INFINITY) ? mx * c : 0.f;
+        if (nref > refc[r]) {
+          Ssum[r] *= ex2(refc[r] - nref);
+          refc[r] = nref;
+        }
+        exps8(z[r], c, refc[r], e[r]);
+        s[r] = sum8(e[r]);
+      }
     }
-    float2 a = __fadd2_rn(make_float2(e[0], e[1]), make_float2(e[2], e[3]));
-    const float2 b2 = __fadd2_rn(make_float2(e[4], e[5]), make_float2(e[6], e[7]));
-    a = __fadd2_rn(a, b2);
-    s = a.x + a.y;
   }
-  Ssum += s;
+#pragma unroll
+  for (int r = 0; r < NR; ++r) Ssum[r] += s[r];
 }
 
 // Waits for the next ring slot (consumer side); returns the slot index.
@@ -477,22 +554,26 @@ __global__ void __launch_bounds__(kThreads, 1) sample_verify_kernel(const __grid
       // ---- pass 1: statistics of both rows (resident: also keep the values)
       {
         float refc[2] = {0.f, 0.f}, Ssum[2] = {0.f, 0.f};
-        bool have_ref[2] = {false, false};
+        bool have_ref = false;
         for (int st = 0; st < nst; ++st) {
           const uint32_t slot = next_full(S, L, seq, timeout);
           const int k = st * kConsumerWarps + warp;
           if (k < nch) {
             const int ib = k * kChunk;
-            for (int r = 0; r < nrows; ++r) {
-              const T* chunk = reinterpret_cast<const T*>(S.ring + (size_t)slot * L.slot_bytes) + r * kStage +
-                               warp * kChunk;
-              float z[8], e[8];
-              stage_logits<T>(chunk, ib, lane, len, S.bitmap, pen, alpha, z);
-              chunk_stats(z, c, refc[r], have_ref[r], Ssum[r], e);
-              if constexpr (RESIDENT) {
-                // the store holds e, or z' with top-p; row capacity is L.slice
+            const T* base = reinterpret_cast<const T*>(S.ring + (size_t)slot * L.slot_bytes) + warp * kChunk;
+            float z[2][8], e[2][8];
+            stage_logits<T>(base, ib, lane, len, S.bitmap, pen, alpha, z[0]);
+            if (nrows == 2) {
+              stage_logits<T>(base + kStage, ib, lane, len, S.bitmap, pen, alpha, z[1]);
+              chunk_stats_n<2>(z, c, refc, have_ref, Ssum, e);
+            } else {
+              chunk_stats_n<1>(z, c, refc, have_ref, Ssum, e);
+            }
+            if constexpr (RESIDENT) {
+              // the store holds e, or z' with top-p; row capacity is L.slice
+              for (int r = 0; r < nrows; ++r) {
                 float* dst = S.e + (size_t)r * L.slice + ib;
-                const float* sv8 = TOPP ? z : e;
+                const float* sv8 = TOPP ? z[r] : e[r];
                 if (ib + 4 * lane < L.slice)
                   *reinterpret_cast<float4*>(dst + 4 * lane) = make_float4(sv8[0], sv8[1], sv8[2], sv8[3]);
                 if (ib + 128 + 4 * lane < L.slice)
@@ -505,7 +586,7 @@ __global__ void __launch_bounds__(kThreads, 1) sample_verify_kernel(const __grid
         }
         for (int r = 0; r < 2; ++r) {
           const float Sw = warp_sum(Ssum[r]);
-          if (lane == 0) S.wpart[r * kConsumerWarps + warp] = make_float2(have_ref[r] ? refc[r] : -INFINITY, Sw);
+          if (lane == 0) S.wpart[r * kConsumerWarps + warp] = make_float2(have_ref && r < nrows ? refc[r] : -INFINITY, Sw);
         }
       }
       consumer_sync();
@@ -699,10 +780,12 @@ __global__ void __launch_bounds__(kThreads, 1) sample_verify_kernel(const __grid
       }
 
       // ---- resident: p(x), q(x) from the stored values (the pass-2 formula)
+      constexpr int kMode = TOPP ? kPZT : (RESIDENT ? kPE : kPZ);
+      const float efill = kMode == kPE ? 0.f : -INFINITY;  // a stored value of zero probability
       if (RESIDENT && !it.bonus && tid == 0 && x >= v0 && x < v0 + len && ok_stats) {
         const int j = x - v0, k = j / kChunk;
-        S.misc_d[kMdPx] = (double)prob_of<kFromE>(S.e[j], kFromE ? S.fac[k] : 0.f, rp[0]);
-        S.misc_d[kMdQx] = (double)prob_of<kFromE>(S.e[(size_t)L.slice + j], kFromE ? S.fac[L.nch + k] : 0.f, rp[1]);
+        S.misc_d[kMdPx] = (double)prob1<kMode>(S.e[j], kFromE ? S.fac[k] : 0.f, rp[0]);
+        S.misc_d[kMdQx] = (double)prob1<kMode>(S.e[(size_t)L.slice + j], kFromE ? S.fac[L.nch + k] : 0.f, rp[1]);
       }
 
       // ---- pass 2: per-chunk sums of r = max(p - q, 0) (positions) or p (bonus)
@@ -710,20 +793,17 @@ __global__ void __launch_bounds__(kThreads, 1) sample_verify_kernel(const __grid
       bool cdf_of_p = it.bonus;
       if constexpr (RESIDENT) {
         for (int k = warp; k < nch; k += kConsumerWarps) {
-          const float fp = kFromE ? S.fac[k] : 0.f;
-          float e1[8];
-          load_e8(S.e, k, lane, len, kFromE ? 0.f : -INFINITY, e1);
-          float s = 0.f;
+          float ep[8], pp[8];
+          load_e8(S.e, k, lane, len, efill, ep);
+          probs8<kMode>(ep, kFromE ? S.fac[k] : 0.f, rp[0], pp);
+          float s;
           if (it.bonus) {
-#pragma unroll
-            for (int j = 0; j < 8; ++j) s += prob_of<kFromE>(e1[j], fp, rp[0]);
+            s = sum8(pp);
           } else {
-            const float fq = kFromE ? S.fac[L.nch + k] : 0.f;
-            float e2[8];
-            load_e8(S.e + L.slice, k, lane, len, kFromE ? 0.f : -INFINITY, e2);
-#pragma unroll
-            for (int j = 0; j < 8; ++j)
-              s += fmaxf(prob_of<kFromE>(e1[j], fp, rp[0]) - prob_of<kFromE>(e2[j], fq, rp[1]), 0.f);
+            float eq[8], qq[8], rr[8];
+            load_e8(S.e + L.slice, k, lane, len, efill, eq);
+            probs8<kMode>(eq, kFromE ? S.fac[L.nch + k] : 0.f, rp[1], qq);
+            s = resid8(pp, qq, rr);
           }
           s = warp_sum(s);
           if (lane == 0) S.seg[k] = s;
@@ -735,22 +815,18 @@ __global__ void __launch_bounds__(kThreads, 1) sample_verify_kernel(const __grid
           if (k < nch) {
             const int ib = k * kChunk;
             const T* base = reinterpret_cast<const T*>(S.ring + (size_t)slot * L.slot_bytes) + warp * kChunk;
-            float zp[8], pv8[8];
+            float zp[8], pp[8];
             stage_logits<T>(base, ib, lane, len, S.bitmap, pen, alpha, zp);
-#pragma unroll
-            for (int j = 0; j < 8; ++j) pv8[j] = prob_of<false>(zp[j], 0.f, rp[0]);
-            float s = 0.f;
+            float s;
             if (it.bonus) {
-#pragma unroll
-              for (int j = 0; j < 8; ++j) s += pv8[j];
+              probs8<kMode>(zp, 0.f, rp[0], pp);
+              s = sum8(pp);
             } else {
-              float zq[8], qv8[8];
+              float zq[8], qq[8], rr[8];
               stage_logits<T>(base + kStage, ib, lane, len, S.bitmap, pen, alpha, zq);
-#pragma unroll
-              for (int j = 0; j < 8; ++j) {
-                qv8[j] = prob_of<false>(zq[j], 0.f, rp[1]);
-                s += fmaxf(pv8[j] - qv8[j], 0.f);
-              }
+              probs8<kMode>(zp, 0.f, rp[0], pp);
+              probs8<kMode>(zq, 0.f, rp[1], qq);
+              s = resid8(pp, qq, rr);
               // the lane holding x records p(x), q(x)
               const int jx = x - v0 - ib;
               if (ok_stats && jx >= 0 && jx < kChunk) {
@@ -760,7 +836,7 @@ __global__ void __launch_bounds__(kThreads, 1) sample_verify_kernel(const __grid
                   float px = 0.f, qx = 0.f;
 #pragma unroll
                   for (int j = 0; j < 8; ++j)
-                    if (j == jj) { px = pv8[j]; qx = qv8[j]; }
+                    if (j == jj) { px = pp[j]; qx = qq[j]; }
                   S.misc_d[kMdPx] = (double)px;
                   S.misc_d[kMdQx] = (double)qx;
                 }
@@ -774,22 +850,18 @@ __global__ void __launch_bounds__(kThreads, 1) sample_verify_kernel(const __grid
       }
       consumer_sync();
 
-      // ---- sync 2: CTA prefix sums, cluster totals, owner of the final draw
+      // ---- sync 2: CTA totals, cluster prefix, owner of the final draw
       double R = 0.0, Pc = 0.0;
       int owner = -1;
       bool take_last = false;
       for (int attempt = 0; attempt < 2; ++attempt) {
-        double run = 0.0;
+        double Rc = 0.0;
         if (warp == 0) {
-          for (int k0 = 0; k0 < nch; k0 += 32) {
-            const int k = k0 + lane;
-            const double v = k < nch ? (double)S.seg[k] : 0.0;
-            const double inc = warp_incl_scan_d(v, lane);
-            if (k < nch) S.pre[k] = run + inc - v;  // exclusive prefix within the CTA
-            run += __shfl_sync(0xffffffffu, inc, 31);
-          }
+          int k0, k1;
+          double blk, inc;
+          Rc = seg_block_scan(S.seg, nch, lane, k0, k1, blk, inc);
         }
-        if (!cluster_exchange(S, ph, C, rank, 1, run, 0.0, 0.0, 0.0)) timeout = true;
+        if (!cluster_exchange(S, ph, C, rank, 1, Rc, 0.0, 0.0, 0.0)) timeout = true;
         if (warp == 0) {
           // lane c: mass of CTA c; prefix sums, total, owner of u_fin * R
           const uint32_t buf = (ph.cph - 1) & 1u;
@@ -816,22 +888,14 @@ __global__ void __launch_bounds__(kThreads, 1) sample_verify_kernel(const __grid
           // chunk sums of p come from the resident store or from global memory
           cdf_of_p = true;
           for (int k = warp; k < nch; k += kConsumerWarps) {
-            float w[8];
+            float v[8], pp[8];
             if constexpr (RESIDENT) {
-              float e1[8];
-              load_e8(S.e, k, lane, len, kFromE ? 0.f : -INFINITY, e1);
-#pragma unroll
-              for (int j = 0; j < 8; ++j) w[j] = prob_of<kFromE>(e1[j], kFromE ? S.fac[k] : 0.f, rp[0]);
+              load_e8(S.e, k, lane, len, efill, v);
             } else {
-              float zp[8];
-              global_logits<T>(gp_row, k * kChunk, lane, len, S.bitmap, pen, alpha, zp);
-#pragma unroll
-              for (int j = 0; j < 8; ++j) w[j] = prob_of<false>(zp[j], 0.f, rp[0]);
+              global_logits<T>(gp_row, k * kChunk, lane, len, S.bitmap, pen, alpha, v);
             }
-            float s = 0.f;
-#pragma unroll
-            for (int j = 0; j < 8; ++j) s += w[j];
-            s = warp_sum(s);
+            probs8<kMode>(v, kFromE ? S.fac[k] : 0.f, rp[0], pp);
+            const float s = warp_sum(sum8(pp));
             if (lane == 0) S.seg[k] = s;
           }
           consumer_sync();
@@ -863,69 +927,84 @@ __global__ void __launch_bounds__(kThreads, 1) sample_verify_kernel(const __grid
         P.results[item].theta = (float)theta;
       }
 
-      // ---- candidate: inverse CDF at u_fin within the owning CTA
+      // ---- candidate: inverse CDF at u_fin within the owning CTA: the lane
+      // block, then the chunk, then the lane and element that hold it
       if (P.mode == kModeSample && ok_stats && owner == (int)rank && warp == 0) {
         const double tl = u_fin * R - Pc;
-        int ks = -1, klast = -1;
-        for (int k0 = 0; k0 < nch; k0 += 32) {
-          const int k = k0 + lane;
-          const float sg = k < nch ? S.seg[k] : 0.f;
-          const bool pos = sg > 0.f;
-          const bool hit = pos && !take_last && (k < nch ? S.pre[k] : 0.0) + (double)sg > tl;
-          const unsigned mh = __ballot_sync(0xffffffffu, hit);
-          const unsigned mp = __ballot_sync(0xffffffffu, pos);
-          if (mp) klast = k0 + 31 - __clz(mp);
-          if (ks < 0 && mh) ks = k0 + __ffs(mh) - 1;
-        }
+        int k0, k1;
+        double blk, inc;
+        seg_block_scan(S.seg, nch, lane, k0, k1, blk, inc);
+        const double exc = inc - blk;
+        int ks = -1;
+        double rem = 0.0;
         bool tl_last = take_last;
-        if (ks < 0) { ks = klast; tl_last = true; }
+        const unsigned mh = __ballot_sync(0xffffffffu, !take_last && blk > 0.0 && inc > tl);
+        if (mh) {
+          const int L0 = __ffs(mh) - 1;
+          if (lane == L0) {
+            double cum = exc;
+            int klast = -1;
+            for (int k = k0; k < k1; ++k) {
+              const double sg = (double)S.seg[k];
+              if (sg > 0.0) {
+                if (cum + sg > tl) { ks = k; rem = tl - cum; break; }
+                klast = k;
+              }
+              cum += sg;
+            }
+            if (ks < 0) ks = klast;  // rounding: the block's last chunk with mass
+          }
+          ks = __shfl_sync(0xffffffffu, ks, L0);
+          rem = __shfl_sync(0xffffffffu, rem, L0);
+          tl_last = false;
+          if (ks >= 0 && rem <= 0.0 && (double)S.seg[ks] <= 0.0) tl_last = true;
+        }
+        if (ks < 0) {
+          // the last chunk with mass
+          const unsigned mp = __ballot_sync(0xffffffffu, blk > 0.0);
+          if (mp) {
+            const int L1 = 31 - __clz(mp);
+            int kl = -1;
+            if (lane == L1)
+              for (int k = k1 - 1; k >= k0; --k)
+                if (S.seg[k] > 0.f) { kl = k; break; }
+            ks = __shfl_sync(0xffffffffu, kl, L1);
+          }
+          tl_last = true;
+        }
         int found = -1;
         if (ks >= 0) {
           float w[8];
           const int ib = ks * kChunk;
-          if constexpr (RESIDENT) {
-            float e1[8];
-            load_e8(S.e, ks, lane, len, kFromE ? 0.f : -INFINITY, e1);
-            const float fp = kFromE ? S.fac[ks] : 0.f;
+          {
+            float vp[8], pp[8];
+            if constexpr (RESIDENT) load_e8(S.e, ks, lane, len, efill, vp);
+            else global_logits<T>(gp_row, ib, lane, len, S.bitmap, pen, alpha, vp);
+            probs8<kMode>(vp, kFromE ? S.fac[ks] : 0.f, rp[0], pp);
             if (cdf_of_p) {
 #pragma unroll
-              for (int j = 0; j < 8; ++j) w[j] = prob_of<kFromE>(e1[j], fp, rp[0]);
+              for (int j = 0; j < 8; ++j) w[j] = pp[j];
             } else {
-              float e2[8];
-              load_e8(S.e + L.slice, ks, lane, len, kFromE ? 0.f : -INFINITY, e2);
-              const float fq = kFromE ? S.fac[L.nch + ks] : 0.f;
-#pragma unroll
-              for (int j = 0; j < 8; ++j)
-                w[j] = fmaxf(prob_of<kFromE>(e1[j], fp, rp[0]) - prob_of<kFromE>(e2[j], fq, rp[1]), 0.f);
-            }
-          } else {
-            float zp[8];
-            global_logits<T>(gp_row, ib, lane, len, S.bitmap, pen, alpha, zp);
-            if (cdf_of_p) {
-#pragma unroll
-              for (int j = 0; j < 8; ++j) w[j] = prob_of<false>(zp[j], 0.f, rp[0]);
-            } else {
-              float zq[8];
-              global_logits<T>(gq_row, ib, lane, len, S.bitmap, pen, alpha, zq);
-#pragma unroll
-              for (int j = 0; j < 8; ++j)
-                w[j] = fmaxf(prob_of<false>(zp[j], 0.f, rp[0]) - prob_of<false>(zq[j], 0.f, rp[1]), 0.f);
+              float vq[8], qq[8];
+              if constexpr (RESIDENT) load_e8(S.e + L.slice, ks, lane, len, efill, vq);
+              else global_logits<T>(gq_row, ib, lane, len, S.bitmap, pen, alpha, vq);
+              probs8<kMode>(vq, kFromE ? S.fac[L.nch + ks] : 0.f, rp[1], qq);
+              resid8(pp, qq, w);
             }
           }
-          double rem = tl - S.pre[ks];
           if (!tl_last) {
             for (int half = 0; half < 2 && found < 0; ++half) {
               const float* wh = w + 4 * half;
               const float ls = (wh[0] + wh[1]) + (wh[2] + wh[3]);
-              const float inc = warp_incl_scan(ls, lane);
-              const float exc = inc - ls;
-              const bool hit = ((double)inc > rem) && ((double)exc <= rem) && ls > 0.f;
+              const float incl = warp_incl_scan(ls, lane);
+              const float excl = incl - ls;
+              const bool hit = ((double)incl > rem) && ((double)excl <= rem) && ls > 0.f;
               const unsigned m = __ballot_sync(0xffffffffu, hit);
               if (m) {
                 const int L0 = __ffs(m) - 1;
                 int jj = -1;
                 if (lane == L0) {
-                  double cum = (double)exc;
+                  double cum = (double)excl;
                   for (int j = 0; j < 4; ++j) {
                     cum += (double)wh[j];
                     if (wh[j] > 0.f && cum > rem) { jj = j; break; }
@@ -937,7 +1016,7 @@ __global__ void __launch_bounds__(kThreads, 1) sample_verify_kernel(const __grid
                 jj = __shfl_sync(0xffffffffu, jj, L0);
                 found = ib + 128 * half + 4 * L0 + jj;
               } else {
-                rem -= (double)__shfl_sync(0xffffffffu, inc, 31);
+                rem -= (double)__shfl_sync(0xffffffffu, incl, 31);
               }
             }
           }
