@@ -5,8 +5,8 @@
 // request's bonus row (target row K).  Each CTA owns a contiguous slice of
 // the vocabulary.  A producer warp streams the CTA's slice of both rows from
 // global memory into a shared-memory ring with 1-D TMA bulk copies (one
-// slot = kStage tokens of the target row followed by the same tokens of the
-// draft row); 16 consumer warps work on the slots.  Per item:
+// slot = one stage: the CTA's next 256 tokens per consumer warp of the target
+// row followed by the same tokens of the draft row); 16 consumer warps work on the slots.  Per item:
 //
 //   pass 1  repetition penalty and temperature; running (reference, sum) of
 //           e = 2^(z'c - ref) per row, c = log2(e)/T: one exponential per
@@ -105,7 +105,6 @@ struct Shared {
   float* refc;       // [2][nch]   (resident variant)
   float* fac;        // [2][nch]   (resident variant)
   float* seg;        // [nch]
-  double* pre;       // [nch]
   float2* wpart;     // [2][16]
   double* xchg;      // [2][C][kXchgDoubles]
   float* hist;       // [2 buf][2 rows][256]
@@ -126,7 +125,6 @@ __device__ __forceinline__ Shared carve(unsigned char* smem, const SmemLayout& L
   S.refc = reinterpret_cast<float*>(smem + L.off_refc);
   S.fac = reinterpret_cast<float*>(smem + L.off_fac);
   S.seg = reinterpret_cast<float*>(smem + L.off_seg);
-  S.pre = reinterpret_cast<double*>(smem + L.off_pre);
   S.wpart = reinterpret_cast<float2*>(smem + L.off_wpart);
   S.xchg = reinterpret_cast<double*>(smem + L.off_xchg);
   S.hist = reinterpret_cast<float*>(smem + L.off_hist);
@@ -141,7 +139,9 @@ __device__ __forceinline__ Shared carve(unsigned char* smem, const SmemLayout& L
   return S;
 }
 
-__device__ __forceinline__ void consumer_sync() { named_sync(1, kConsumerThreads); }
+// Barrier over the consumer warps only (the producer warp keeps streaming).
+template <int NCT>
+__device__ __forceinline__ void consumer_sync() { named_sync(1, NCT); }
 
 // misc_i: [0] status bits of the item found by this CTA, [2] finalize flag,
 // [4] owner CTA of the final draw, [5] owner takes the last positive token,
@@ -217,7 +217,7 @@ __device__ __forceinline__ void stage_logits(const T* chunk, int ib, int lane, i
     for (int j = 0; j < 8; ++j)
       if (ib + lane_elem(lane, j) >= len) z[j] = -INFINITY;
   }
-  if (pen) {
+  if (pen && __any_sync(0xffffffffu, bitmap[(ib >> 5) + (lane & 7)] != 0u)) {
     const uint32_t wa = bitmap[(ib >> 5) + (lane >> 3)];
     const uint32_t wb = bitmap[(ib >> 5) + 4 + (lane >> 3)];
     const uint32_t sh = 4u * (lane & 7);
@@ -225,24 +225,117 @@ __device__ __forceinline__ void stage_logits(const T* chunk, int ib, int lane, i
     while (m) {
       const int j = __ffs(m) - 1;
       m &= m - 1;
+      float v = z[0];
+#pragma unroll
+      for (int jj = 1; jj < 8; ++jj)
+        if (jj == j) v = z[jj];
+      v = penalize(v, alpha);
 #pragma unroll
       for (int jj = 0; jj < 8; ++jj)
-        if (jj == j) z[jj] = penalize(z[jj], alpha);
+        if (jj == j) z[jj] = v;
+    }
+  }
+}
+
+// A lane's 8 raw values of a staged chunk, as loaded (converted later).
+template <typename T>
+struct Raw8;
+template <>
+struct Raw8<__nv_bfloat16> {
+  uint2 a, b;
+};
+template <>
+struct Raw8<float> {
+  float4 a, b;
+};
+
+__device__ __forceinline__ void load_raw8(const __nv_bfloat16* chunk, int lane, Raw8<__nv_bfloat16>& r) {
+  r.a = *reinterpret_cast<const uint2*>(chunk + 4 * lane);
+  r.b = *reinterpret_cast<const uint2*>(chunk + 128 + 4 * lane);
+}
+__device__ __forceinline__ void load_raw8(const float* chunk, int lane, Raw8<float>& r) {
+  r.a = *reinterpret_cast<const float4*>(chunk + 4 * lane);
+  r.b = *reinterpret_cast<const float4*>(chunk + 128 + 4 * lane);
+}
+__device__ __forceinline__ void cvt_raw8(const Raw8<__nv_bfloat16>& r, float* z) {
+  z[0] = __uint_as_float(r.a.x << 16); z[1] = __uint_as_float(r.a.x & 0xffff0000u);
+  z[2] = __uint_as_float(r.a.y << 16); z[3] = __uint_as_float(r.a.y & 0xffff0000u);
+  z[4] = __uint_as_float(r.b.x << 16); z[5] = __uint_as_float(r.b.x & 0xffff0000u);
+  z[6] = __uint_as_float(r.b.y << 16); z[7] = __uint_as_float(r.b.y & 0xffff0000u);
+}
+__device__ __forceinline__ void cvt_raw8(const Raw8<float>& r, float* z) {
+  z[0] = r.a.x; z[1] = r.a.y; z[2] = r.a.z; z[3] = r.a.w;
+  z[4] = r.b.x; z[5] = r.b.y; z[6] = r.b.z; z[7] = r.b.w;
+}
+
+// Both rows of a staged chunk (row 1 at +row_stride elements; only row 0
+// when nrows == 1): every shared-memory load is issued first, then the
+// conversion; the tail mask and the repetition penalty are rare,
+// warp-uniform branches.
+template <typename T>
+__device__ __forceinline__ void stage_chunk2(const T* chunk, int row_stride, int nrows, int ib, int lane, int len,
+                                             const uint32_t* bitmap, bool pen, float alpha, float (&z)[2][8]) {
+  Raw8<T> r0, r1;
+  load_raw8(chunk, lane, r0);
+  if (nrows == 2) load_raw8(chunk + row_stride, lane, r1);
+  const uint32_t pw = pen ? bitmap[(ib >> 5) + (lane & 7)] : 0u;
+  cvt_raw8(r0, z[0]);
+  if (nrows == 2) cvt_raw8(r1, z[1]);
+  if (ib + kChunk > len) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      if (ib + lane_elem(lane, j) >= len) z[0][j] = z[1][j] = -INFINITY;
+  }
+  if (pen && __any_sync(0xffffffffu, pw != 0u)) {
+    const uint32_t wa = bitmap[(ib >> 5) + (lane >> 3)];
+    const uint32_t wb = bitmap[(ib >> 5) + 4 + (lane >> 3)];
+    const uint32_t sh = 4u * (lane & 7);
+    uint32_t m = ((wa >> sh) & 0xFu) | (((wb >> sh) & 0xFu) << 4);
+    while (m) {
+      const int j = __ffs(m) - 1;
+      m &= m - 1;
+      float v0 = z[0][0], v1 = z[1][0];
+#pragma unroll
+      for (int jj = 1; jj < 8; ++jj)
+        if (jj == j) { v0 = z[0][jj]; v1 = z[1][jj]; }
+      v0 = penalize(v0, alpha);
+      v1 = penalize(v1, alpha);
+#pragma unroll
+      for (int jj = 0; jj < 8; ++jj)
+        if (jj == j) { z[0][jj] = v0; z[1][jj] = v1; }
     }
   }
 }
 
 // The same 8 logits read straight from global memory (used once per item by
-// the streaming variant's candidate search).
+// the streaming variant's candidate search).  Loads first, then conversion,
+// so that callers can issue the loads of several rows back to back.
 template <typename T>
-__device__ __forceinline__ void global_logits(const T* slice_row, int ib, int lane, int len, const uint32_t* bitmap,
-                                              bool pen, float alpha, float* z) {
+__device__ __forceinline__ void global_raw(const T* slice_row, int ib, int lane, int len, T* raw) {
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
     const int idx = ib + lane_elem(lane, j);
-    z[j] = idx < len ? to_f32<T>(slice_row[idx]) : -INFINITY;
+    raw[j] = slice_row[idx < len ? idx : 0];
+  }
+}
+
+template <typename T>
+__device__ __forceinline__ void convert_raw(const T* raw, int ib, int lane, int len, const uint32_t* bitmap, bool pen,
+                                            float alpha, float* z) {
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const int idx = ib + lane_elem(lane, j);
+    z[j] = idx < len ? to_f32<T>(raw[j]) : -INFINITY;
     if (pen && idx < len && ((bitmap[idx >> 5] >> (idx & 31)) & 1u)) z[j] = penalize(z[j], alpha);
   }
+}
+
+template <typename T>
+__device__ __forceinline__ void global_logits(const T* slice_row, int ib, int lane, int len, const uint32_t* bitmap,
+                                              bool pen, float alpha, float* z) {
+  T raw[8];
+  global_raw<T>(slice_row, ib, lane, len, raw);
+  convert_raw<T>(raw, ib, lane, len, bitmap, pen, alpha, z);
 }
 
 // The lane's 8 stored values of chunk k (resident e-array); `fill` past the
@@ -421,12 +514,56 @@ __device__ __forceinline__ void chunk_stats_n(float (&z)[2][8], float c, float* 
   for (int r = 0; r < NR; ++r) Ssum[r] += s[r];
 }
 
+// Position in the ring: slot index and the parity of its current use.
+struct RingCursor {
+  uint32_t slot = 0, phase = 0;
+  __device__ __forceinline__ void advance(int nslots) {
+    if (++slot == (uint32_t)nslots) {
+      slot = 0;
+      phase ^= 1u;
+    }
+  }
+};
+
+// Streaming pass-1 statistics of one chunk of NR rows with a per-lane running
+// reference (no warp-wide step in the hot loop): each lane keeps refc, the
+// running maximum of z'c it has seen when a chunk would overflow (sum above
+// 2^64; first set from the lane's first chunk), and Ssum of 2^(z'c - refc).
+template <int NR>
+__device__ __forceinline__ void chunk_stats_lane(float (&z)[2][8], float c, float* refc, bool& have_ref, float* Ssum) {
+  const float kLim = 18446744073709551616.0f;  // 2^64
+  if (!have_ref) {
+#pragma unroll
+    for (int r = 0; r < NR; ++r) {
+      const float mx = max8(z[r]);
+      refc[r] = (mx > -INFINITY) ? mx * c : 0.f;
+    }
+    have_ref = true;
+  }
+#pragma unroll
+  for (int r = 0; r < NR; ++r) {
+    float e[8];
+    exps8(z[r], c, refc[r], e);
+    float s = sum8(e);
+    if (!(s <= kLim)) {  // rare and lane-local
+      const float mx = max8(z[r]);
+      const float nref = (mx > -INFINITY) ? mx * c : 0.f;
+      if (nref > refc[r]) {
+        Ssum[r] *= ex2(refc[r] - nref);
+        refc[r] = nref;
+      }
+      exps8(z[r], c, refc[r], e);
+      s = sum8(e);
+    }
+    Ssum[r] += s;
+  }
+}
+
 // Waits for the next ring slot (consumer side); returns the slot index.
-__device__ __forceinline__ uint32_t next_full(const Shared& S, const SmemLayout& L, uint32_t& seq, bool& timeout) {
-  const uint32_t slot = seq % (uint32_t)L.nslots;
-  const uint32_t par = (seq / (uint32_t)L.nslots) & 1u;
-  ++seq;
-  if (!timeout && !mbar_wait(&S.full[slot], par)) timeout = true;  // after one timeout, stop waiting
+__device__ __forceinline__ uint32_t next_full(const Shared& S, const SmemLayout& L, RingCursor& rc, bool& timeout) {
+  const uint32_t slot = rc.slot;
+  if (!timeout && !mbar_wait(&S.full[slot], rc.phase)) timeout = true;  // after one timeout, stop waiting
+  rc.advance(L.nslots);
   return slot;
 }
 
@@ -439,7 +576,11 @@ __device__ __forceinline__ void release_slot(const Shared& S, uint32_t slot, int
 
 // -------------------------------------------------------------------- kernel
 template <typename T, bool TOPP, bool RESIDENT>
-__global__ void __launch_bounds__(kThreads, 1) sample_verify_kernel(const __grid_constant__ SampleParams P) {
+__global__ void __launch_bounds__(((RESIDENT ? kResidentWarps : kStreamWarps) + 1) * 32, RESIDENT ? 1 : kStreamCtasPerSm)
+    sample_verify_kernel(const __grid_constant__ SampleParams P) {
+  constexpr int NW = RESIDENT ? kResidentWarps : kStreamWarps;  // consumer warps
+  constexpr int NCT = NW * 32;                                    // consumer threads
+  constexpr int STAGE = NW * kChunk;                              // tokens of each row per slot
   extern __shared__ __align__(128) unsigned char smem[];
   const SmemLayout& L = P.L;
   Shared S = carve(smem, L);
@@ -448,7 +589,7 @@ __global__ void __launch_bounds__(kThreads, 1) sample_verify_kernel(const __grid
   const int cluster_id = blockIdx.x / C;
   const int v0 = (int)rank * L.slice;
   const int len = max(0, min(L.slice, P.V - v0));
-  const int nst = (len + kStage - 1) / kStage;
+  const int nst = (len + STAGE - 1) / STAGE;
   const int nch = (len + kChunk - 1) / kChunk;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -458,7 +599,7 @@ __global__ void __launch_bounds__(kThreads, 1) sample_verify_kernel(const __grid
   if (tid == 0) {
     for (int s = 0; s < L.nslots; ++s) {
       mbar_init(&S.full[s], 1);
-      mbar_init(&S.empty[s], kConsumerWarps);
+      mbar_init(&S.empty[s], NW);
     }
     mbar_init(&S.csync[0], C);
     mbar_init(&S.csync[1], C);
@@ -466,13 +607,13 @@ __global__ void __launch_bounds__(kThreads, 1) sample_verify_kernel(const __grid
   }
   cluster_sync_all();
 
-  if (warp == kConsumerWarps) {
+  if (warp == NW) {
     // ------------------------------------------------------------ producer
     if (lane == 0 && len > 0) {
       const uint64_t keep_policy = l2_policy_evict_last();
       const uint64_t drop_policy = l2_policy_evict_first();
       const int es = (int)sizeof(T);
-      uint32_t seq = 0;
+      RingCursor rc;
       bool ptimeout = false;
       for (int item = cluster_id; item < P.n_items; item += P.n_clusters) {
         const Item it = decode_item(P, item);
@@ -485,17 +626,17 @@ __global__ void __launch_bounds__(kThreads, 1) sample_verify_kernel(const __grid
         for (int pass = 0; pass < npass; ++pass) {
           const uint64_t pol = (RESIDENT || pass == npass - 1) ? drop_policy : keep_policy;
           for (int st = 0; st < nst; ++st) {
-            const uint32_t slot = seq % (uint32_t)L.nslots;
-            const uint32_t par = ((seq / (uint32_t)L.nslots) & 1u) ^ 1u;
-            ++seq;
-            if (!ptimeout && !mbar_wait(&S.empty[slot], par)) ptimeout = true;  // consumers see their own
-            const int n = min(kStage, len - st * kStage);
+            const uint32_t slot = rc.slot;
+            // first use of a slot: the phase "before" its first completes at once
+            if (!ptimeout && !mbar_wait(&S.empty[slot], rc.phase ^ 1u)) ptimeout = true;  // consumers see their own
+            rc.advance(L.nslots);
+            const int n = min(STAGE, len - st * STAGE);
             const uint32_t bytes = (uint32_t)((n * es + 15) & ~15);
             unsigned char* dst = S.ring + (size_t)slot * L.slot_bytes;
             mbar_arrive_expect_tx(&S.full[slot], it.bonus ? bytes : 2 * bytes);
-            bulk_g2s(dst, rowp + (size_t)st * kStage * es, bytes, &S.full[slot], pol);
+            bulk_g2s(dst, rowp + (size_t)st * STAGE * es, bytes, &S.full[slot], pol);
             if (!it.bonus)
-              bulk_g2s(dst + (size_t)kStage * es, rowq + (size_t)st * kStage * es, bytes, &S.full[slot], pol);
+              bulk_g2s(dst + (size_t)STAGE * es, rowq + (size_t)st * STAGE * es, bytes, &S.full[slot], pol);
           }
         }
       }
@@ -504,7 +645,7 @@ __global__ void __launch_bounds__(kThreads, 1) sample_verify_kernel(const __grid
   } else {
     // ----------------------------------------------------------- consumers
     ClusterPhase ph;
-    uint32_t seq = 0;
+    RingCursor seq;
     bool timeout = false;
     for (int item = cluster_id; item < P.n_items; item += P.n_clusters) {
       const Item it = decode_item(P, item);
@@ -535,21 +676,22 @@ __global__ void __launch_bounds__(kThreads, 1) sample_verify_kernel(const __grid
       const T* gq_row = it.bonus ? gp_row : static_cast<const T*>(P.draft) + (size_t)it.dft_row * P.ld_d + v0;
 
       // ---- penalty set of this row within the CTA slice; token validity
+      const bool cpen = pen;
       if (tid == 0) S.misc_i[kMiFlags] = 0;
-      if (pen)
-        for (int w = tid; w < L.nch * 8; w += kConsumerThreads) S.bitmap[w] = 0u;
-      consumer_sync();
-      for (int j = h0 + tid; j < h1; j += kConsumerThreads) {
+      if (cpen)
+        for (int w = tid; w < L.nch * 8; w += NCT) S.bitmap[w] = 0u;
+      consumer_sync<NCT>();
+      for (int j = h0 + tid; j < h1; j += NCT) {
         const int t = __ldg(P.hist + j);
         if (t < 0 || t >= P.V) flags |= kStatusBadToken;
-        else if (pen && t >= v0 && t < v0 + len) atomicOr(&S.bitmap[(t - v0) >> 5], 1u << ((t - v0) & 31));
+        else if (cpen && t >= v0 && t < v0 + len) atomicOr(&S.bitmap[(t - v0) >> 5], 1u << ((t - v0) & 31));
       }
-      for (int j = tid; j < npre; j += kConsumerThreads) {
+      for (int j = tid; j < npre; j += NCT) {
         const int t = __ldg(P.draft_tokens + d0 + j);
         if (t < 0 || t >= P.V) flags |= kStatusBadToken;
-        else if (pen && t >= v0 && t < v0 + len) atomicOr(&S.bitmap[(t - v0) >> 5], 1u << ((t - v0) & 31));
+        else if (cpen && t >= v0 && t < v0 + len) atomicOr(&S.bitmap[(t - v0) >> 5], 1u << ((t - v0) & 31));
       }
-      consumer_sync();
+      consumer_sync<NCT>();
 
       // ---- pass 1: statistics of both rows (resident: also keep the values)
       {
@@ -557,19 +699,16 @@ __global__ void __launch_bounds__(kThreads, 1) sample_verify_kernel(const __grid
         bool have_ref = false;
         for (int st = 0; st < nst; ++st) {
           const uint32_t slot = next_full(S, L, seq, timeout);
-          const int k = st * kConsumerWarps + warp;
+          const int k = st * NW + warp;
           if (k < nch) {
             const int ib = k * kChunk;
             const T* base = reinterpret_cast<const T*>(S.ring + (size_t)slot * L.slot_bytes) + warp * kChunk;
-            float z[2][8], e[2][8];
-            stage_logits<T>(base, ib, lane, len, S.bitmap, pen, alpha, z[0]);
-            if (nrows == 2) {
-              stage_logits<T>(base + kStage, ib, lane, len, S.bitmap, pen, alpha, z[1]);
-              chunk_stats_n<2>(z, c, refc, have_ref, Ssum, e);
-            } else {
-              chunk_stats_n<1>(z, c, refc, have_ref, Ssum, e);
-            }
+            float z[2][8];
+            stage_chunk2<T>(base, STAGE, nrows, ib, lane, len, S.bitmap, cpen, alpha, z);
             if constexpr (RESIDENT) {
+              float e[2][8];
+              if (nrows == 2) chunk_stats_n<2>(z, c, refc, have_ref, Ssum, e);
+              else chunk_stats_n<1>(z, c, refc, have_ref, Ssum, e);
               // the store holds e, or z' with top-p; row capacity is L.slice
               for (int r = 0; r < nrows; ++r) {
                 float* dst = S.e + (size_t)r * L.slice + ib;
@@ -580,23 +719,36 @@ __global__ void __launch_bounds__(kThreads, 1) sample_verify_kernel(const __grid
                   *reinterpret_cast<float4*>(dst + 128 + 4 * lane) = make_float4(sv8[4], sv8[5], sv8[6], sv8[7]);
                 if (lane == 0) S.refc[r * L.nch + k] = refc[r];
               }
+            } else {
+              if (nrows == 2) chunk_stats_lane<2>(z, c, refc, have_ref, Ssum);
+              else chunk_stats_lane<1>(z, c, refc, have_ref, Ssum);
             }
           }
           release_slot(S, slot, lane);
         }
         for (int r = 0; r < 2; ++r) {
-          const float Sw = warp_sum(Ssum[r]);
-          if (lane == 0) S.wpart[r * kConsumerWarps + warp] = make_float2(have_ref && r < nrows ? refc[r] : -INFINITY, Sw);
+          if constexpr (RESIDENT) {
+            const float Sw = warp_sum(Ssum[r]);
+            if (lane == 0)
+              S.wpart[r * kMaxConsumerWarps + warp] = make_float2(have_ref && r < nrows ? refc[r] : -INFINITY, Sw);
+          } else {
+            // combine the lanes' (reference, sum) pairs
+            const float ref = have_ref && r < nrows ? refc[r] : -INFINITY;
+            const float Mw = warp_max(ref);
+            const double v = (ref > -INFINITY && Mw > -INFINITY) ? (double)Ssum[r] * (double)exp2f(ref - Mw) : 0.0;
+            const double Sw = warp_sum_d(v);
+            if (lane == 0) S.wpart[r * kMaxConsumerWarps + warp] = make_float2(Mw, (float)Sw);
+          }
         }
       }
-      consumer_sync();
+      consumer_sync<NCT>();
 
       // ---- sync 1: (M, S) per row, warps -> CTA -> cluster
       {
         double a0 = 0.0, a1 = 0.0, a2 = 0.0, a3 = 0.0;
         if (warp == 0) {
           const int r = lane >> 4, w = lane & 15;
-          const float2 v = (r < nrows) ? S.wpart[r * kConsumerWarps + w] : make_float2(-INFINITY, 0.f);
+          const float2 v = (r < nrows && w < NW) ? S.wpart[r * kMaxConsumerWarps + w] : make_float2(-INFINITY, 0.f);
           float M;
           double Ssum;
           halfwarp_combine(v.x, (double)v.y, M, Ssum);
@@ -626,7 +778,7 @@ __global__ void __launch_bounds__(kThreads, 1) sample_verify_kernel(const __grid
           S.misc_f[2 * r] = (float)(1.0 / Ssum);
         }
       }
-      consumer_sync();
+      consumer_sync<NCT>();
       double Mr[2], Sr[2];
       float invS[2];
       for (int r = 0; r < 2; ++r) {
@@ -640,11 +792,11 @@ __global__ void __launch_bounds__(kThreads, 1) sample_verify_kernel(const __grid
 
       // ---- chunk factors fac_k = 2^(ref_k - M) / S (resident e store)
       if constexpr (kFromE) {
-        for (int j = tid; j < nrows * nch; j += kConsumerThreads) {
+        for (int j = tid; j < nrows * nch; j += NCT) {
           const int r = j / nch, k = j % nch;
           S.fac[r * L.nch + k] = ok_stats ? exp2f(S.refc[r * L.nch + k] - (float)Mr[r]) * invS[r] : 0.f;
         }
-        consumer_sync();
+        consumer_sync<NCT>();
       }
 
       RowProb rp[2];
@@ -671,8 +823,8 @@ __global__ void __launch_bounds__(kThreads, 1) sample_verify_kernel(const __grid
             const int shift = 24 - 8 * pass;
             const uint32_t hb = ph.cph & 1u;
             float* hist = S.hist + hb * 512;
-            for (int j = tid; j < 512; j += kConsumerThreads) hist[j] = 0.f;
-            consumer_sync();
+            for (int j = tid; j < 512; j += NCT) hist[j] = 0.f;
+            consumer_sync<NCT>();
             auto accumulate = [&](const float* zv, int r) {
 #pragma unroll
               for (int j = 0; j < 8; ++j) {
@@ -687,7 +839,7 @@ __global__ void __launch_bounds__(kThreads, 1) sample_verify_kernel(const __grid
             if constexpr (RESIDENT) {
               if (work)
                 for (int r = 0; r < nrows; ++r)
-                  for (int k = warp; k < nch; k += kConsumerWarps) {
+                  for (int k = warp; k < nch; k += NW) {
                     float zv[8];
                     load_e8(S.e + (size_t)r * L.slice, k, lane, len, -INFINITY, zv);
                     accumulate(zv, r);
@@ -695,30 +847,30 @@ __global__ void __launch_bounds__(kThreads, 1) sample_verify_kernel(const __grid
             } else {
               for (int st = 0; st < nst; ++st) {
                 const uint32_t slot = next_full(S, L, seq, timeout);
-                const int k = st * kConsumerWarps + warp;
+                const int k = st * NW + warp;
                 if (work && k < nch)
                   for (int r = 0; r < nrows; ++r) {
                     const T* chunk = reinterpret_cast<const T*>(S.ring + (size_t)slot * L.slot_bytes) +
-                                     r * kStage + warp * kChunk;
+                                     r * STAGE + warp * kChunk;
                     float zv[8];
-                    stage_logits<T>(chunk, k * kChunk, lane, len, S.bitmap, pen, alpha, zv);
+                    stage_logits<T>(chunk, k * kChunk, lane, len, S.bitmap, cpen, alpha, zv);
                     accumulate(zv, r);
                   }
                 release_slot(S, slot, lane);
               }
             }
             fence_acq_rel_cluster();
-            consumer_sync();
+            consumer_sync<NCT>();
             if (!cluster_exchange(S, ph, C, rank, 0, 0.0, 0.0, 0.0, 0.0)) timeout = true;
-            {  // gather the C histograms: thread -> (row, bin)
-              const int r = tid >> 8, bin = tid & 255;
+            for (int j = tid; j < 512; j += NCT) {  // gather the C histograms: (row, bin)
+              const int r = j >> 8, bin = j & 255;
               double s = 0.0;
               if (r < nrows)
                 for (int cc = 0; cc < C; ++cc)
                   s += (double)ld_remote_f32(map_rank(&hist[r * 256 + bin], (uint32_t)cc));
               S.tot[r * 256 + bin] = (float)s;
             }
-            consumer_sync();
+            consumer_sync<NCT>();
             if (warp < nrows) {
               // lane owns bins [8*lane, 8*lane+8): the largest digit d with
               // above + mass(bins >= d) >= target
@@ -760,7 +912,7 @@ __global__ void __launch_bounds__(kThreads, 1) sample_verify_kernel(const __grid
                 S.misc_d[5 + 2 * r] = bm;
               }
             }
-            consumer_sync();
+            consumer_sync<NCT>();
             for (int r = 0; r < nrows; ++r) {
               prefix[r] |= ((uint32_t)S.misc_i[8 + r]) << shift;
               above[r] = S.misc_d[4 + 2 * r];
@@ -768,7 +920,7 @@ __global__ void __launch_bounds__(kThreads, 1) sample_verify_kernel(const __grid
             }
             if (tid == 0)
               for (int r = 0; r < nrows; ++r) S.misc_f[4 + r] = (float)(1.0 / kept[r]);
-            consumer_sync();
+            consumer_sync<NCT>();
           }
           if (work)
             for (int r = 0; r < nrows; ++r) {
@@ -792,7 +944,7 @@ __global__ void __launch_bounds__(kThreads, 1) sample_verify_kernel(const __grid
       const double u_fin = P.mode == kModeSample ? (double)__ldg(P.uniforms + off + K) : 0.0;
       bool cdf_of_p = it.bonus;
       if constexpr (RESIDENT) {
-        for (int k = warp; k < nch; k += kConsumerWarps) {
+        for (int k = warp; k < nch; k += NW) {
           float ep[8], pp[8];
           load_e8(S.e, k, lane, len, efill, ep);
           probs8<kMode>(ep, kFromE ? S.fac[k] : 0.f, rp[0], pp);
@@ -811,19 +963,20 @@ __global__ void __launch_bounds__(kThreads, 1) sample_verify_kernel(const __grid
       } else {
         for (int st = 0; st < nst; ++st) {
           const uint32_t slot = next_full(S, L, seq, timeout);
-          const int k = st * kConsumerWarps + warp;
+          const int k = st * NW + warp;
           if (k < nch) {
             const int ib = k * kChunk;
             const T* base = reinterpret_cast<const T*>(S.ring + (size_t)slot * L.slot_bytes) + warp * kChunk;
-            float zp[8], pp[8];
-            stage_logits<T>(base, ib, lane, len, S.bitmap, pen, alpha, zp);
+            float zz[2][8], pp[8];
+            stage_chunk2<T>(base, STAGE, nrows, ib, lane, len, S.bitmap, cpen, alpha, zz);
+            const float* zp = zz[0];
             float s;
             if (it.bonus) {
               probs8<kMode>(zp, 0.f, rp[0], pp);
               s = sum8(pp);
             } else {
-              float zq[8], qq[8], rr[8];
-              stage_logits<T>(base + kStage, ib, lane, len, S.bitmap, pen, alpha, zq);
+              const float* zq = zz[1];
+              float qq[8], rr[8];
               probs8<kMode>(zp, 0.f, rp[0], pp);
               probs8<kMode>(zq, 0.f, rp[1], qq);
               s = resid8(pp, qq, rr);
@@ -848,7 +1001,7 @@ __global__ void __launch_bounds__(kThreads, 1) sample_verify_kernel(const __grid
           release_slot(S, slot, lane);
         }
       }
-      consumer_sync();
+      consumer_sync<NCT>();
 
       // ---- sync 2: CTA totals, cluster prefix, owner of the final draw
       double R = 0.0, Pc = 0.0;
@@ -878,7 +1031,7 @@ __global__ void __launch_bounds__(kThreads, 1) sample_verify_kernel(const __grid
           }
           if (lane == (int)rank) S.misc_d[15] = inc - rc;
         }
-        consumer_sync();
+        consumer_sync<NCT>();
         R = S.misc_d[14];
         Pc = S.misc_d[15];
         owner = S.misc_i[4];
@@ -887,18 +1040,18 @@ __global__ void __launch_bounds__(kThreads, 1) sample_verify_kernel(const __grid
           // no residual mass (only reachable when q(x) = 0): draw from p; the
           // chunk sums of p come from the resident store or from global memory
           cdf_of_p = true;
-          for (int k = warp; k < nch; k += kConsumerWarps) {
+          for (int k = warp; k < nch; k += NW) {
             float v[8], pp[8];
             if constexpr (RESIDENT) {
               load_e8(S.e, k, lane, len, efill, v);
             } else {
-              global_logits<T>(gp_row, k * kChunk, lane, len, S.bitmap, pen, alpha, v);
+              global_logits<T>(gp_row, k * kChunk, lane, len, S.bitmap, cpen, alpha, v);
             }
             probs8<kMode>(v, kFromE ? S.fac[k] : 0.f, rp[0], pp);
             const float s = warp_sum(sum8(pp));
             if (lane == 0) S.seg[k] = s;
           }
-          consumer_sync();
+          consumer_sync<NCT>();
           continue;
         }
         break;
@@ -977,17 +1130,23 @@ __global__ void __launch_bounds__(kThreads, 1) sample_verify_kernel(const __grid
           float w[8];
           const int ib = ks * kChunk;
           {
-            float vp[8], pp[8];
-            if constexpr (RESIDENT) load_e8(S.e, ks, lane, len, efill, vp);
-            else global_logits<T>(gp_row, ib, lane, len, S.bitmap, pen, alpha, vp);
+            float vp[8], pp[8], vq[8];
+            if constexpr (RESIDENT) {
+              load_e8(S.e, ks, lane, len, efill, vp);
+              if (!cdf_of_p) load_e8(S.e + L.slice, ks, lane, len, efill, vq);
+            } else {
+              T rawp[8], rawq[8];
+              global_raw<T>(gp_row, ib, lane, len, rawp);
+              if (!cdf_of_p) global_raw<T>(gq_row, ib, lane, len, rawq);
+              convert_raw<T>(rawp, ib, lane, len, S.bitmap, cpen, alpha, vp);
+              if (!cdf_of_p) convert_raw<T>(rawq, ib, lane, len, S.bitmap, cpen, alpha, vq);
+            }
             probs8<kMode>(vp, kFromE ? S.fac[ks] : 0.f, rp[0], pp);
             if (cdf_of_p) {
 #pragma unroll
               for (int j = 0; j < 8; ++j) w[j] = pp[j];
             } else {
-              float vq[8], qq[8];
-              if constexpr (RESIDENT) load_e8(S.e + L.slice, ks, lane, len, efill, vq);
-              else global_logits<T>(gq_row, ib, lane, len, S.bitmap, pen, alpha, vq);
+              float qq[8];
               probs8<kMode>(vq, kFromE ? S.fac[L.nch + ks] : 0.f, rp[1], qq);
               resid8(pp, qq, w);
             }
@@ -1043,7 +1202,7 @@ __global__ void __launch_bounds__(kThreads, 1) sample_verify_kernel(const __grid
       flags = warp_or(flags);
       if (lane == 0 && flags) atomicOr(&S.misc_i[kMiFlags], flags);
       __threadfence();
-      consumer_sync();
+      consumer_sync<NCT>();
       if (P.mode == kModeTvOnly && tid == 0) {
         // every CTA checks the same scalars, tokens and row statistics, so its
         // flags are the request's
@@ -1068,7 +1227,7 @@ __global__ void __launch_bounds__(kThreads, 1) sample_verify_kernel(const __grid
           const int old = atomicAdd(P.counters + b, 1);
           S.misc_i[kMiFinalize] = (old == target - 1) && K >= 0 && it.rows_ok;
         }
-        consumer_sync();
+        consumer_sync<NCT>();
         if (S.misc_i[kMiFinalize] && warp == 0) {
           __threadfence();
           int st = 0;
@@ -1100,7 +1259,7 @@ __global__ void __launch_bounds__(kThreads, 1) sample_verify_kernel(const __grid
           }
         }
       }
-      consumer_sync();
+      consumer_sync<NCT>();
     }
   }
   // no CTA may leave while others can still read its shared memory
@@ -1127,7 +1286,7 @@ int launch_t(SampleParams& P, cudaStream_t stream) {
   attr[0].val.clusterDim.x = P.C;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(((RESIDENT ? kResidentWarps : kStreamWarps) + 1) * 32);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cfg.attrs = attr;
@@ -1171,8 +1330,9 @@ int choose_resident_layout(int V, int elem_bytes, bool topp, int max_smem, int* 
 }
 
 // Streaming layout for cluster size C (-1 if it does not fit).
-int choose_stream_layout(int V, int C, int elem_bytes, bool topp, int max_smem, SmemLayout* L_out) {
-  const SmemLayout L = make_stream_layout(V, C, elem_bytes, topp, max_smem);
+int choose_stream_layout(int V, int C, int elem_bytes, bool topp, int max_smem, int smem_per_sm,
+                         SmemLayout* L_out) {
+  const SmemLayout L = make_stream_layout(V, C, elem_bytes, topp, max_smem, smem_per_sm);
   if (L.total <= 0) return -1;
   *L_out = L;
   return 0;

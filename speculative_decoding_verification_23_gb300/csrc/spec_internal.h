@@ -8,13 +8,18 @@
 namespace sv {
 
 // ----------------------------------------------------------------- sampling
-constexpr int kChunk = 256;                 // elements per warp-chunk
-constexpr int kConsumerWarps = 16;
-constexpr int kConsumerThreads = kConsumerWarps * 32;
-constexpr int kThreads = kConsumerThreads + 32;  // + one producer warp
-constexpr int kStage = kConsumerWarps * kChunk;  // elements of each row per ring slot
+constexpr int kChunk = 256;                 // tokens per warp-chunk (8 per lane)
+// Consumer warps per CTA: the resident variant runs one 16-warp CTA per SM;
+// the streaming variant runs two 8-warp CTAs per SM, so that one CTA's
+// per-item synchronisation overlaps the other's streaming.  Each CTA also
+// has one producer warp.  A ring slot carries kChunk tokens per consumer warp
+// of each row.
+constexpr int kResidentWarps = 16;
+constexpr int kStreamWarps = 16;
+constexpr int kMaxConsumerWarps = 16;
 constexpr int kResidentRingBytes = 64 * 1024;
 constexpr int kStreamRingMaxBytes = 192 * 1024;
+constexpr int kStreamCtasPerSm = 1;
 constexpr int kXchgDoubles = 8;             // per CTA per exchange buffer
 constexpr int kMaxCluster = 16;
 
@@ -28,22 +33,23 @@ struct ItemResult {       // one per work item (a draft position or a bonus row)
 };
 
 // Shared memory of the sampling kernel.  A ring slot holds one stage: the
-// CTA's next kStage tokens of the target row followed by the same tokens of
+// CTA's next `stage` tokens of the target row followed by the same tokens of
 // the draft row.  The resident variant also keeps one fp32 value per token
 // of its slice of both rows (the e-array); the streaming variant re-reads
-// the rows through the ring instead and spends the space on a deeper ring.
+// the rows through the ring instead.
 struct SmemLayout {
   int slice;      // token ids per CTA (multiple of 64)
   int nch;        // chunks per CTA slice (ceil(slice / 256))
+  int nw;         // consumer warps
+  int stage;      // tokens of each row per slot (nw * 256)
   int nslots;     // ring slots
   int slot_bytes;
   int resident;
-  int off_e, off_bitmap, off_refc, off_fac, off_seg, off_pre, off_wpart, off_xchg, off_hist, off_tot,
-      off_misc, off_bar;
+  int off_e, off_bitmap, off_refc, off_fac, off_seg, off_wpart, off_xchg, off_hist, off_tot, off_misc, off_bar;
   int total;
 };
 
-inline int align_up_i(int x, int a) { return (x + a - 1) / a * a; }
+__host__ __device__ inline int align_up_i(int x, int a) { return (x + a - 1) / a * a; }
 
 // Everything but the ring and the e-array, from `off` on.
 inline int layout_tail(SmemLayout& L, int off, int C, bool topp) {
@@ -51,13 +57,12 @@ inline int layout_tail(SmemLayout& L, int off, int C, bool topp) {
   L.off_refc = off;     off += L.resident ? align_up_i(2 * L.nch * 4, 16) : 0;
   L.off_fac = off;      off += L.resident ? align_up_i(2 * L.nch * 4, 16) : 0;
   L.off_seg = off;      off += align_up_i(L.nch * 4, 16);
-  L.off_pre = off;      off += align_up_i(L.nch * 8, 16);
-  L.off_wpart = off;    off += 2 * kConsumerWarps * 8;
+  L.off_wpart = off;    off += 2 * kMaxConsumerWarps * 8;
   L.off_xchg = off;     off += 2 * C * kXchgDoubles * 8;
   L.off_hist = off;     off += topp ? 2 * 2 * 256 * 4 : 0;
   L.off_tot = off;      off += topp ? 2 * 256 * 4 : 0;
   L.off_misc = off;     off += 256;
-  L.off_bar = off;      off += (2 * L.nslots + 2) * 8;
+  L.off_bar = off;      off += (2 * L.nslots + 2) * 8;  // full, empty, csync[2]
   return align_up_i(off, 128);
 }
 
@@ -65,28 +70,34 @@ inline int layout_tail(SmemLayout& L, int off, int C, bool topp) {
 inline SmemLayout make_resident_layout(int V, int C, int elem_bytes, bool topp) {
   SmemLayout L{};
   L.resident = 1;
+  L.nw = kResidentWarps;
+  L.stage = L.nw * kChunk;
   L.slice = align_up_i((V + C - 1) / C, 64);
   L.nch = (L.slice + kChunk - 1) / kChunk;
-  L.slot_bytes = 2 * kStage * elem_bytes;
+  L.slot_bytes = 2 * L.stage * elem_bytes;
   L.nslots = kResidentRingBytes / L.slot_bytes;
   L.off_e = kResidentRingBytes;
   L.total = layout_tail(L, L.off_e + 2 * L.slice * 4, C, topp);
   return L;
 }
 
-// Streaming variant: the deepest ring (whole slots, at most 192 KB, at
-// least 2 slots) that fits in `max_smem`; total = 0 if none does.
-inline SmemLayout make_stream_layout(int V, int C, int elem_bytes, bool topp, int max_smem) {
+// Streaming variant: the deepest ring (whole slots, at most 96 KB, at least
+// 2 slots) such that two CTAs fit in one SM's `smem_per_sm` and one in
+// `max_smem`; total = 0 if none does.
+inline SmemLayout make_stream_layout(int V, int C, int elem_bytes, bool topp, int max_smem, int smem_per_sm) {
   SmemLayout L{};
   L.resident = 0;
+  L.nw = kStreamWarps;
+  L.stage = L.nw * kChunk;
   L.slice = align_up_i((V + C - 1) / C, 64);
   L.nch = (L.slice + kChunk - 1) / kChunk;
-  L.slot_bytes = 2 * kStage * elem_bytes;
+  L.slot_bytes = 2 * L.stage * elem_bytes;
+  const int budget = smem_per_sm / kStreamCtasPerSm - 1024;  // the driver reserves ~1 KB per CTA
   for (int ns = kStreamRingMaxBytes / L.slot_bytes; ns >= 2; --ns) {
     L.nslots = ns;
     L.off_e = ns * L.slot_bytes;
     L.total = layout_tail(L, L.off_e, C, topp);
-    if (L.total <= max_smem) return L;
+    if (L.total <= max_smem && L.total <= budget) return L;
   }
   L.total = 0;
   return L;

@@ -11,7 +11,8 @@
 
 namespace sv {
 int choose_resident_layout(int V, int elem_bytes, bool topp, int max_smem, int* C_out, SmemLayout* L_out);
-int choose_stream_layout(int V, int C, int elem_bytes, bool topp, int max_smem, SmemLayout* L_out);
+int choose_stream_layout(int V, int C, int elem_bytes, bool topp, int max_smem, int smem_per_sm,
+                         SmemLayout* L_out);
 int launch_sample_verify(SampleParams& P, bool bf16, bool topp, cudaStream_t stream);
 int launch_greedy_verify(const GreedyParams& P, bool bf16, cudaStream_t stream);
 }  // namespace sv
@@ -50,14 +51,17 @@ int check_workspace(const spec_args* a, const void* ws, size_t ws_bytes) {
   return SPEC_OK;
 }
 
-int device_props(int* max_smem, int* num_sms) {
+int device_props(int* max_smem, int* num_sms, int* smem_per_sm = nullptr) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) { cudaGetLastError(); return SPEC_ERR_DEVICE; }
+  int per_sm = 0;
   if (cudaDeviceGetAttribute(max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+      cudaDeviceGetAttribute(num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess) {
     cudaGetLastError();
     return SPEC_ERR_DEVICE;
   }
+  if (smem_per_sm) *smem_per_sm = per_sm;
   return SPEC_OK;
 }
 
@@ -88,8 +92,8 @@ void fill_sample_inputs(sv::SampleParams& P, const spec_args* a) {
 // cluster in one wave; streaming (slices re-read from L2, about one item per
 // SM in flight) otherwise.  SPEC_PREFER_* flags override the choice.
 int run_sample(sv::SampleParams& P, const spec_args* a, void* ws, cudaStream_t stream) {
-  int max_smem = 0, num_sms = 0;
-  int rc = device_props(&max_smem, &num_sms);
+  int max_smem = 0, num_sms = 0, smem_per_sm = 0;
+  int rc = device_props(&max_smem, &num_sms, &smem_per_sm);
   if (rc) return rc;
   const bool topp = a->top_p != nullptr;
   const int es = elem_bytes(a->dtype);
@@ -97,7 +101,9 @@ int run_sample(sv::SampleParams& P, const spec_args* a, void* ws, cudaStream_t s
   sv::SmemLayout L_res{}, L_str{};
   const bool res_ok = sv::choose_resident_layout(a->V, es, topp, max_smem, &C_res, &L_res) == 0;
   int C_str = 1;
-  while (C_str <= sv::kMaxCluster && sv::choose_stream_layout(a->V, C_str, es, topp, max_smem, &L_str) != 0) C_str *= 2;
+  while (C_str <= sv::kMaxCluster &&
+         sv::choose_stream_layout(a->V, C_str, es, topp, max_smem, smem_per_sm, &L_str) != 0)
+    C_str *= 2;
   const bool str_ok = C_str <= sv::kMaxCluster;
   bool resident;
   if ((a->flags & SPEC_PREFER_RESIDENT) && res_ok) resident = true;
