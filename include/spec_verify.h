@@ -102,7 +102,9 @@ enum {
   SPEC_ERR_WORKSPACE = -5,   /* workspace NULL, misaligned or too small    */
   SPEC_ERR_ALIGN = -6,       /* logits not 16-byte aligned / ld*size % 16  */
   SPEC_ERR_LAUNCH = -7,      /* the CUDA launch failed                     */
-  SPEC_ERR_DEVICE = -8       /* no usable device, or V too large for it    */
+  SPEC_ERR_DEVICE = -8,      /* no usable device, or V too large for it    */
+  SPEC_ERR_STATIC_SCRATCH = -9 /* spec_verify_sample_static: the batch needs
+                                  more than SPEC_STATIC_SCRATCH_BYTES        */
 };
 
 /* out_status bits */
@@ -173,6 +175,40 @@ int spec_verify_greedy(const spec_args *args, int32_t *out_tokens, int32_t *out_
    get NaN.  Reads no uniforms. */
 int spec_tv_budget(const spec_args *args, float *out_tv, float *out_theta, float *out_p_at_draft,
                    float *out_q_at_draft, void *workspace, size_t ws_bytes, spec_stream_t stream);
+
+/* Fixed-scratch variant of spec_verify_sample: no workspace argument.
+ *
+ * The method has no counterpart to this call.  It serves callers that cannot
+ * hand the library a workspace: a serving loop that planned all of its
+ * device memory up front and has nothing left to give out per call, or a
+ * caller for which a cudaMalloc at the point of the call (it may synchronise
+ * the device) is not acceptable.
+ *
+ * Arguments, checks, kernels and results are those of spec_verify_sample;
+ * the workspace is replaced by one buffer per device that the library holds
+ * as a file-scope __device__ array of SPEC_STATIC_SCRATCH_BYTES (1 MiB).  The
+ * call allocates and frees nothing.
+ *
+ * Size limit: with n = total_drafts + B the batch needs
+ * align256(4 B) + align256(32 n) + align256(64 n) bytes; every batch with
+ * n <= 10000 fits.  A batch that does not fit returns SPEC_ERR_STATIC_SCRATCH
+ * and enqueues nothing.
+ *
+ * Zeroing: only the B per-request arrival counters at the start of the
+ * buffer must be zero when the kernel starts; each call clears them on
+ * `stream` (cudaMemsetAsync) before its launch.  Everything else in the
+ * buffer is written before it is read.
+ *
+ * First call on a device: it looks the buffer's address up with
+ * cudaGetSymbolAddress (that device current) and caches it; make this first
+ * call outside any stream capture.  A failed lookup returns SPEC_ERR_DEVICE.
+ *
+ * Races: all calls on one device share the buffer.  They must be ordered
+ * (one stream, or synchronised); two calls in flight at once, on two streams
+ * or from two host threads, race and corrupt each other's results. */
+#define SPEC_STATIC_SCRATCH_BYTES (1u << 20)
+int spec_verify_sample_static(const spec_args *args, int32_t *out_tokens, int32_t *out_accepted,
+                              int32_t *out_status, spec_stream_t stream);
 
 /* A static description of a return code. */
 const char *spec_status_string(int code);

@@ -31,6 +31,8 @@ SPEC_ERR_WORKSPACE = -5
 SPEC_ERR_ALIGN = -6
 SPEC_ERR_LAUNCH = -7
 SPEC_ERR_DEVICE = -8
+SPEC_ERR_STATIC_SCRATCH = -9
+SPEC_STATIC_SCRATCH_BYTES = 1 << 20
 
 SPEC_STATUS_BAD_TOKEN = 1
 SPEC_STATUS_BAD_PARAM = 2
@@ -39,7 +41,7 @@ SPEC_STATUS_BAD_K = 8
 SPEC_STATUS_TIMEOUT = 16
 
 EXPORTED = ("spec_workspace_bytes", "spec_verify_sample", "spec_verify_greedy", "spec_tv_budget",
-            "spec_status_string")
+            "spec_verify_sample_static", "spec_status_string")
 
 
 class SpecArgs(ctypes.Structure):
@@ -96,6 +98,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.spec_tv_budget.restype = ctypes.c_int
     lib.spec_tv_budget.argtypes = [ctypes.POINTER(SpecArgs), ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                    ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]
+    lib.spec_verify_sample_static.restype = ctypes.c_int
+    lib.spec_verify_sample_static.argtypes = [ctypes.POINTER(SpecArgs), ctypes.c_void_p, ctypes.c_void_p,
+                                              ctypes.c_void_p, ctypes.c_void_p]
     lib.spec_status_string.restype = ctypes.c_char_p
     lib.spec_status_string.argtypes = [ctypes.c_int]
     _lib = lib
@@ -242,6 +247,25 @@ def spec_verify_greedy(args: SpecArgs, *, device=None, workspace=None, out_token
                                 _ptr(workspace), workspace.numel(), _stream_handle(stream))
     if rc != SPEC_OK:
         raise SpecError(rc, "spec_verify_greedy")
+    return out_tokens, out_accepted, out_status
+
+
+def spec_verify_sample_static(args: SpecArgs, *, device=None, out_tokens=None, out_accepted=None, out_status=None,
+                              stream=None):
+    """``spec_verify_sample`` without a workspace, through
+    ``spec_verify_sample_static``: the library's fixed per-device scratch
+    (SPEC_STATIC_SCRATCH_BYTES) serves every call, so calls on one device
+    must be ordered.  Pass preallocated outputs to allocate nothing here
+    either."""
+    import torch
+
+    lib = load_library()
+    device = device or torch.device("cuda", torch.cuda.current_device())
+    out_tokens, out_accepted, out_status = _outputs(args, device, out_tokens, out_accepted, out_status)
+    rc = lib.spec_verify_sample_static(ctypes.byref(args), _ptr(out_tokens), _ptr(out_accepted), _ptr(out_status),
+                                       _stream_handle(stream))
+    if rc != SPEC_OK:
+        raise SpecError(rc, "spec_verify_sample_static")
     return out_tokens, out_accepted, out_status
 
 

@@ -3,6 +3,7 @@
 // work is enqueued on the caller's stream.
 #include <cstdint>
 #include <cstring>
+#include <mutex>
 
 #include <cuda_runtime.h>
 
@@ -126,6 +127,32 @@ int run_sample(sv::SampleParams& P, const spec_args* a, void* ws, cudaStream_t s
   return sv::launch_sample_verify(P, a->dtype == SPEC_BF16, topp, stream);
 }
 
+// ---- fixed device scratch of spec_verify_sample_static
+// One buffer per device, placed by the CUDA runtime when this module loads;
+// no call of this library allocates it.  Its address is looked up once per
+// device (cudaGetSymbolAddress with that device current) and cached.
+static __device__ __align__(256) unsigned char g_static_scratch[SPEC_STATIC_SCRATCH_BYTES];
+
+constexpr int kScratchCacheDevices = 64;
+std::mutex g_scratch_mu;
+void* g_scratch_addr[kScratchCacheDevices] = {};
+
+int static_scratch_address(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) { cudaGetLastError(); return SPEC_ERR_DEVICE; }
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  void* p = (dev >= 0 && dev < kScratchCacheDevices) ? g_scratch_addr[dev] : nullptr;
+  if (!p) {
+    if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || !p) {
+      cudaGetLastError();
+      return SPEC_ERR_DEVICE;
+    }
+    if (dev >= 0 && dev < kScratchCacheDevices) g_scratch_addr[dev] = p;
+  }
+  *out = p;
+  return SPEC_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -150,6 +177,27 @@ int spec_verify_sample(const spec_args* a, int32_t* out_tokens, int32_t* out_acc
   P.out_status = out_status;
   P.n_items = a->total_drafts + a->B;
   return run_sample(P, a, workspace, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int spec_verify_sample_static(const spec_args* a, int32_t* out_tokens, int32_t* out_accepted, int32_t* out_status,
+                              spec_stream_t stream) {
+  int rc = check_common(a, true);
+  if (rc) return rc;
+  if (!out_tokens || !out_accepted || !a->temperature || !a->tv_budget || !a->uniforms) return SPEC_ERR_NULL;
+  // the sampling kernel uses the counters, results and flags regions only
+  if (sv::make_workspace_layout(a->B, a->total_drafts, a->V).off_partials > SPEC_STATIC_SCRATCH_BYTES)
+    return SPEC_ERR_STATIC_SCRATCH;
+  void* scratch = nullptr;
+  rc = static_scratch_address(&scratch);
+  if (rc) return rc;
+  sv::SampleParams P;
+  fill_sample_inputs(P, a);
+  P.mode = sv::kModeSample;
+  P.out_tokens = out_tokens;
+  P.out_accepted = out_accepted;
+  P.out_status = out_status;
+  P.n_items = a->total_drafts + a->B;
+  return run_sample(P, a, scratch, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int spec_tv_budget(const spec_args* a, float* out_tv, float* out_theta, float* out_p_at_draft,
@@ -222,6 +270,8 @@ const char* spec_status_string(int code) {
     case SPEC_ERR_ALIGN: return "logits must be 16-byte aligned with ld*sizeof(dtype) a multiple of 16";
     case SPEC_ERR_LAUNCH: return "CUDA launch failed";
     case SPEC_ERR_DEVICE: return "no usable CUDA device (needs sm_103a) or V too large";
+    case SPEC_ERR_STATIC_SCRATCH:
+      return "batch needs more than the fixed scratch of spec_verify_sample_static (SPEC_STATIC_SCRATCH_BYTES)";
     default: return "unknown status";
   }
 }
