@@ -62,58 +62,107 @@ def measured_peak():
 
 
 class ClockSampler:
-    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+    """SM clock and clock-event (throttle) reasons sampled during the timed
+    region.  Reads NVML through ctypes every millisecond (read-only queries;
+    nothing is set), so that even a timed region of a few milliseconds gets
+    samples; falls back to ``nvidia-smi -lms 100`` when NVML cannot load."""
 
-    def __init__(self, index: int):
-        self.index = index
+    # nvmlClocksEventReasons bits (nvml.h)
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, device):
+        self.device = device
+        self.samples = []           # (sm_mhz, max_mhz, reasons_mask)
+        self.stop = threading.Event()
         self.proc = None
-        self.lines = []
+        self.thread = None
+        self.source = None
+
+    def _nvml_handle(self):
+        import ctypes
+
+        nvml = ctypes.CDLL("libnvidia-ml.so.1")
+        if nvml.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        import torch
+
+        pr = torch.cuda.get_device_properties(self.device)
+        bus = f"{pr.pci_domain_id:08x}:{pr.pci_bus_id:02x}:{pr.pci_device_id:02x}.0".encode()
+        h = ctypes.c_void_p()
+        if nvml.nvmlDeviceGetHandleByPciBusId_v2(ctypes.c_char_p(bus), ctypes.byref(h)) != 0:
+            raise OSError("no NVML handle for " + bus.decode())
+        reasons = getattr(nvml, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            nvml.nvmlDeviceGetCurrentClocksThrottleReasons
+        return nvml, h, reasons
+
+    def _poll_nvml(self, nvml, h, reasons):
+        import ctypes
+
+        clk, mx, rs = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+        nvml.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx))          # NVML_CLOCK_SM = 1
+        while True:
+            if nvml.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(clk)) == 0 and reasons(h, ctypes.byref(rs)) == 0:
+                self.samples.append((float(clk.value), float(mx.value), int(rs.value)))
+            if self.stop.wait(0.001):
+                break
+
+    def _read_smi(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm, mx = float(parts[1]), float(parts[2])
+            except ValueError:
+                continue
+            mask = 0
+            for bit, v in zip((0x8, 0x40, 0x20, 0x4), parts[5:9]):
+                if v.lower().startswith("active"):
+                    mask |= bit
+            self.samples.append((sm, mx, mask))
 
     def __enter__(self):
-        q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
         try:
-            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={q}",
-                                          "--format=csv,noheader,nounits", "-lms", "100"],
-                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-            self.t = threading.Thread(target=self._read, daemon=True)
-            self.t.start()
-        except FileNotFoundError:
-            self.proc = None
+            nvml, h, reasons = self._nvml_handle()
+            self.thread = threading.Thread(target=self._poll_nvml, args=(nvml, h, reasons), daemon=True)
+            self.source = "nvml 1 ms"
+        except (OSError, AttributeError):
+            q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                 "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                 "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+            try:
+                self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.device.index}", f"--query-gpu={q}",
+                                              "--format=csv,noheader,nounits", "-lms", "100"],
+                                             stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                self.thread = threading.Thread(target=self._read_smi, daemon=True)
+                self.source = "nvidia-smi 100 ms"
+            except FileNotFoundError:
+                return self
+        self.thread.start()
         return self
 
-    def _read(self):
-        for line in self.proc.stdout:
-            self.lines.append(line.strip())
-
     def __exit__(self, *exc):
+        self.stop.set()
         if self.proc:
             self.proc.terminate()
             try:
                 self.proc.wait(timeout=5)
             except subprocess.TimeoutExpired:
                 self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=5)
 
     def summary(self):
-        sm, mx, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in self.lines:
-            parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 9:
-                continue
-            try:
-                sm.append(float(parts[1]))
-                mx.append(float(parts[2]))
-            except ValueError:
-                continue
-            for n, v in zip(names, parts[5:9]):
-                if v.lower().startswith("active"):
-                    reasons.add(n)
-        if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
-                "samples": len(sm)}
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0, "source": self.source}
+        mask = 0
+        for _, _, m in self.samples:
+            mask |= m
+        return {"sm_mhz": statistics.median(s[0] for s in self.samples),
+                "sm_max_mhz": max(s[1] for s in self.samples),
+                "reasons": sorted(n for b, n in self.REASONS.items() if mask & b),
+                "samples": len(self.samples), "source": self.source}
 
 
 def oracle_baseline(batch, budget_s: float):
@@ -194,7 +243,7 @@ def bench_gpu(args, rank, world, dist):
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
-    with ClockSampler(dev.index) as clk:
+    with ClockSampler(dev) as clk:
         t_start = torch.cuda.Event(enable_timing=True)
         t_end = torch.cuda.Event(enable_timing=True)
         t_start.record(stream)
