@@ -166,13 +166,14 @@ class ClockSampler:
 
 
 def oracle_baseline(batch, budget_s: float):
-    """Requests/s of the CPU oracle on a bounded sample (whole requests, in order)."""
+    """Requests/s of the CPU oracle on a bounded sample: whole requests of the
+    batch in order, cycling through the batch until `budget_s` has passed."""
     import oracle
 
     t0 = time.perf_counter()
     n = 0
-    for b in range(batch.B):
-        oracle.verify_batch(batch, [b])
+    while True:
+        oracle.verify_batch(batch, [n % batch.B])
         n += 1
         if time.perf_counter() - t0 > budget_s:
             break
@@ -337,7 +338,7 @@ def bench_gpu(args, rank, world, dist):
     if rank == 0 and not args.no_cpu_baseline:
         v, n, dt = oracle_baseline(batch, args.cpu_seconds)
         line["cpu_baseline"] = {"value": v, "unit": "requests/s", "cores": 1, "kind": "oracle",
-                                "sample": f"{n} whole requests of the B=64 batch ({dt:.1f} s, one thread)"}
+                                "sample": f"{n} whole requests cycled through the B=64 batch ({dt:.1f} s, one thread)"}
     if rank == 0:
         print(json.dumps(line), flush=True)
 
