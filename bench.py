@@ -38,7 +38,8 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
-KERNEL_SOURCES = ["speculative_decoding_verification_23_gb300/csrc/sample_verify.cu",
+KERNEL_SOURCES = ["speculative_decoding_verification_23_gb300/csrc/pipe_verify.cu",
+                  "speculative_decoding_verification_23_gb300/csrc/verify_common.cuh",
                   "speculative_decoding_verification_23_gb300/csrc/common.cuh",
                   "speculative_decoding_verification_23_gb300/csrc/spec_internal.h"]
 PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "sample_verify_batched.json")
@@ -329,7 +330,7 @@ def bench_gpu(args, rank, world, dist):
         "logit_rows_per_s": value * (2 * 8 + 1),
         "hbm_gbs": achieved,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "traffic": traffic, "peak_kind": peak_kind, "kernel": "sample_verify_kernel",
+                     "traffic": traffic, "peak_kind": peak_kind, "kernel": "pipe_verify_kernel",
                      "algorithmic_bytes_per_launch": alg_bytes, "launch_ms": 1000 * launch_s},
         "e2e": {"value": e2e_value, "unit": "requests/s", "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
         "gpu_launches": args.steps,

@@ -1,0 +1,1262 @@
+// Pipelined streaming kernel of mentored speculative sampling without top-p
+// ("What I Gave Up to Make Speculative Decoding Faster", section "A knob for
+// accepting more draft tokens"), for batches with more work items than SMs.
+//
+// A work item is one draft position (target row + draft row) or one bonus
+// row, as in the cluster kernel.  One CTA per SM loops over its items; the
+// warps have four roles:
+//   group A (kPipeWarpsA warps): item k+1's penalty set, then its pass-1
+//       statistics (per lane a running reference and the sum of
+//       2^(z'c - ref), z' the penalised logit, c = log2(e)/T) from a TMA ring
+//       fed from HBM with L2 policy evict_last;
+//   group B (kPipeWarpsB warps): item k's softmax combine, pass 2 (per
+//       segment the sum of the residual max(p-q, 0), or of p for a bonus
+//       row) from a second TMA ring that re-reads the rows (L2 hits,
+//       evict_first), the prefix over segments (TV d = total residual mass),
+//       the decisions (theta, pi(x), acceptance), the inverse-CDF candidate
+//       and the request's finalisation;
+//   two producer warps (lane 0 issues the bulk copies of one ring each).
+// Only group A's ring reads HBM, so HBM keeps streaming while group B runs
+// the per-item serial steps.
+//
+// Repetition penalty: group A turns the item's penalty set (history plus the
+// drafts before the row) into a sorted token list with per-segment offsets.
+// Before a warp reads its segment of a ring slot, its lanes overwrite the
+// penalised positions with -inf (group A first copies their raw logits into
+// the list), so the hot loops never test the penalty; group B adds the
+// penalised tokens' exact terms from the list: to the softmax sums and to
+// each segment's residual mass.
+//
+// Rare items leave the pipeline and are recomputed at the end by all
+// compute warps with direct global loads ("deferred"): an item with more
+// than kPipeListCap distinct penalised tokens, and a rejected position whose
+// residual mass is zero (its correction is then drawn from p).
+#include "common.cuh"
+#include "spec_internal.h"
+#include "verify_common.cuh"
+
+namespace sv {
+
+namespace {
+
+constexpr int kNA = kPipeWarpsA;
+constexpr int kNB = kPipeWarpsB;
+constexpr int kNC = kNA + kNB;                 // compute warps
+constexpr int kThreadsA = kNA * 32;
+constexpr int kThreadsB = kNB * 32;
+constexpr int kThreadsC = kNC * 32;
+constexpr int kPipeThreads = kThreadsC + 64;   // + producer warps A and B
+constexpr int kBarA = 1, kBarB = 2, kBarC = 3;  // named barriers of the groups
+constexpr float kLim = 18446744073709551616.0f;  // 2^64
+
+struct PSmem {
+  unsigned char* ring_a;
+  unsigned char* ring_b;
+  uint32_t* bm;       // [bm_words] penalty bitmap: group A's scratch, then the slow path's
+  float* part;        // [nseg][32] pass-2 lane sums (slow path: 256-token chunk sums)
+  float* segt;        // [nseg] segment residual mass
+  float* segc;        // [nseg] penalised tokens' share of it
+  int* ltok[2];       // [cap] sorted penalised tokens of the item in buffer k & 1
+  float* lzp[2];      // [cap] their raw target logits; later their residual terms
+  float* lzq[2];      // [cap] their raw draft logits
+  int* segst[2];      // [nseg + 1] list offset of each segment
+  PipeStats* stats;   // [2]
+  float2* bred;       // [kNB][2] group B warp partials of the penalised terms
+  float2* cwp;        // [kNC][2] slow path warp partials
+  int* scan;          // [kNC] scan scratch
+  double* md;         // [16]
+  int* mi;            // [16]: [0] group B status bits, [2] B finalize flag, [3] slow finalize flag,
+                      //       [4] slow: draw from p
+  float* mf;          // [16]
+  uint32_t* cmask;    // [32] candidate segment penalty mask
+  uint32_t* defer;    // [kPipeMaxIters / 32] deferred items of this CTA
+  uint64_t* full_a;
+  uint64_t* empty_a;
+  uint64_t* full_b;
+  uint64_t* empty_b;
+  uint64_t* stats_full;   // [2] A -> B: item statistics ready
+  uint64_t* stats_empty;  // [2] B and producer B -> A: buffer free again
+};
+
+__device__ __forceinline__ PSmem carve(unsigned char* smem, const PipeLayout& L) {
+  PSmem S;
+  S.ring_a = smem + L.off_ring_a;
+  S.ring_b = smem + L.off_ring_b;
+  S.bm = reinterpret_cast<uint32_t*>(smem + L.off_bm);
+  S.part = reinterpret_cast<float*>(smem + L.off_part);
+  S.segt = reinterpret_cast<float*>(smem + L.off_segt);
+  S.segc = reinterpret_cast<float*>(smem + L.off_segc);
+  for (int i = 0; i < 2; ++i) {
+    unsigned char* lb = smem + L.off_list + i * kPipeListCap * 12;
+    S.ltok[i] = reinterpret_cast<int*>(lb);
+    S.lzp[i] = reinterpret_cast<float*>(lb + kPipeListCap * 4);
+    S.lzq[i] = reinterpret_cast<float*>(lb + kPipeListCap * 8);
+    S.segst[i] = reinterpret_cast<int*>(smem + L.off_segst + i * align_up_i((L.nseg + 1) * 4, 16));
+  }
+  S.stats = reinterpret_cast<PipeStats*>(smem + L.off_stats);
+  unsigned char* m = smem + L.off_misc;
+  S.bred = reinterpret_cast<float2*>(m);
+  S.cwp = reinterpret_cast<float2*>(m + 128);
+  S.scan = reinterpret_cast<int*>(m + 384);
+  S.md = reinterpret_cast<double*>(m + 448);
+  S.mi = reinterpret_cast<int*>(m + 576);
+  S.mf = reinterpret_cast<float*>(m + 640);
+  S.cmask = reinterpret_cast<uint32_t*>(m + 704);
+  S.defer = reinterpret_cast<uint32_t*>(smem + L.off_defer);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.off_bar);
+  S.full_a = bars;
+  S.empty_a = bars + L.slots_a;
+  S.full_b = bars + 2 * L.slots_a;
+  S.empty_b = bars + 2 * L.slots_a + L.slots_b;
+  S.stats_full = bars + 2 * L.slots_a + 2 * L.slots_b;
+  S.stats_empty = S.stats_full + 2;
+  return S;
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ int warp_incl_scan_i(int v, int lane) {
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int t = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += t;
+  }
+  return v;
+}
+
+// 16 bytes of a staged row as fp32: 8 bf16 or 4 fp32 values, in token order.
+__device__ __forceinline__ void cvt16(const uint4& v, float (&z)[8]) {
+  z[0] = __uint_as_float(v.x << 16);
+  z[1] = __uint_as_float(v.x & 0xffff0000u);
+  z[2] = __uint_as_float(v.y << 16);
+  z[3] = __uint_as_float(v.y & 0xffff0000u);
+  z[4] = __uint_as_float(v.z << 16);
+  z[5] = __uint_as_float(v.z & 0xffff0000u);
+  z[6] = __uint_as_float(v.w << 16);
+  z[7] = __uint_as_float(v.w & 0xffff0000u);
+}
+__device__ __forceinline__ void cvt16(const uint4& v, float (&z)[4]) {
+  z[0] = __uint_as_float(v.x);
+  z[1] = __uint_as_float(v.y);
+  z[2] = __uint_as_float(v.z);
+  z[3] = __uint_as_float(v.w);
+}
+
+template <typename T>
+struct Vec {
+  static constexpr int N = 16 / (int)sizeof(T);  // values per 16-byte vector
+};
+
+template <typename T>
+__device__ __forceinline__ T neg_inf();
+template <>
+__device__ __forceinline__ float neg_inf<float>() { return -INFINITY; }
+template <>
+__device__ __forceinline__ __nv_bfloat16 neg_inf<__nv_bfloat16>() { return __ushort_as_bfloat16((unsigned short)0xFF80u); }
+
+// A warp segment is kPipeSegBytes of one row: lane l holds the 16-byte
+// vectors j*32 + l (j = 0..3), i.e. tokens (j*32 + l)*N + e of the segment.
+__device__ __forceinline__ void lds_seg(const unsigned char* seg, int lane, uint4 (&v)[4]) {
+#pragma unroll
+  for (int j = 0; j < 4; ++j) v[j] = *reinterpret_cast<const uint4*>(seg + (j * 32 + lane) * 16);
+}
+
+template <int N>
+__device__ __forceinline__ void mask_tail(float (&z)[4][N], int lane, int nvalid) {
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+#pragma unroll
+    for (int e = 0; e < N; ++e)
+      if ((j * 32 + lane) * N + e >= nvalid) z[j][e] = -INFINITY;
+}
+
+// Overwrites the penalised positions [e0, e1) of the list that fall in this
+// warp's segment with -inf, in both staged rows; with CAPTURE their raw
+// values are first copied to the list.  The writes are ordered before the
+// slot goes back to the TMA producer (proxy fence) and before the warp reads
+// the segment (__syncwarp).
+template <typename T, bool CAPTURE>
+__device__ __forceinline__ void patch_segment(unsigned char* rowp, unsigned char* rowq, bool two_rows, const int* ltok,
+                                              float* lzp, float* lzq, int e0, int e1, int base, int lane) {
+  bool wrote = false;
+  for (int e = e0 + lane; e < e1; e += 32) {
+    const int o = ltok[e] - base;
+    T* p = reinterpret_cast<T*>(rowp) + o;
+    T* q = reinterpret_cast<T*>(rowq) + o;
+    if constexpr (CAPTURE) {
+      lzp[e] = to_f32<T>(*p);
+      lzq[e] = two_rows ? to_f32<T>(*q) : 0.f;
+    }
+    *p = neg_inf<T>();
+    if (two_rows) *q = neg_inf<T>();
+    wrote = true;
+  }
+  if (wrote) fence_proxy_async_smem();
+  __syncwarp();
+}
+
+// Pass-1 statistics of one row segment for one lane: the running reference
+// `ref` (units of z'c) only moves up, when a segment's sum of 2^(z'c - ref)
+// would exceed 2^64 (and on the first segment with a finite value); `run`
+// accumulates the sums.  NaN or +inf logits make `run` NaN, which the
+// combine reports as invalid logits.
+template <int N>
+__device__ __forceinline__ void stats_row(const float (&z)[4][N], float c, float& ref, float& run) {
+  const float2 c2 = make_float2(c, c);
+  float2 nr = make_float2(-ref, -ref);
+  float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+#pragma unroll
+    for (int e = 0; e < N; e += 2) {
+      const float2 y = __ffma2_rn(make_float2(z[j][e], z[j][e + 1]), c2, nr);
+      acc = __fadd2_rn(acc, make_float2(ex2(y.x), ex2(y.y)));
+    }
+  float s = acc.x + acc.y;
+  if (!(s <= kLim)) {
+    float mx = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+#pragma unroll
+      for (int e = 0; e < N; ++e) mx = fmaxf(mx, z[j][e]);
+    if (mx > -INFINITY) {
+      const float nref = mx * c;
+      if (nref > ref) {
+        run *= ex2(ref - nref);
+        ref = nref;
+      }
+      nr = make_float2(-ref, -ref);
+      acc = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+#pragma unroll
+        for (int e = 0; e < N; e += 2) {
+          const float2 y = __ffma2_rn(make_float2(z[j][e], z[j][e + 1]), c2, nr);
+          acc = __fadd2_rn(acc, make_float2(ex2(y.x), ex2(y.y)));
+        }
+      s = acc.x + acc.y;
+    } else if (mx == -INFINITY) {
+      s = 0.f;  // nothing finite in this segment while the reference is unset
+    }
+  }
+  run += s;
+}
+
+// Group A: statistics of NR rows of one warp segment of a ring slot.
+template <typename T, int NR>
+__device__ __forceinline__ void seg_stats(const unsigned char* seg, int row_bytes, int lane, int nvalid, float c,
+                                          float (&ref)[2], float (&run)[2]) {
+  constexpr int N = Vec<T>::N;
+  uint4 v[NR][4];
+#pragma unroll
+  for (int r = 0; r < NR; ++r) lds_seg(seg + r * row_bytes, lane, v[r]);
+#pragma unroll
+  for (int r = 0; r < NR; ++r) {
+    float z[4][N];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) cvt16(v[r][j], z[j]);
+    if (nvalid < 128 * N) mask_tail<N>(z, lane, nvalid);
+    stats_row<N>(z, c, ref[r], run[r]);
+  }
+}
+
+// Group B: this lane's share of one segment's residual mass sum max(p-q, 0)
+// (BONUS: of p), p = 2^(z'c - Mp) / Sp and q = 2^(z'c - Mq) / Sq.
+template <typename T, bool BONUS>
+__device__ __forceinline__ float seg_resid(const unsigned char* seg, int row_bytes, int lane, int nvalid, float c,
+                                           float Mp, float Mq, float ip, float iq) {
+  constexpr int N = Vec<T>::N;
+  uint4 vp[4], vq[4];
+  lds_seg(seg, lane, vp);
+  if (!BONUS) lds_seg(seg + row_bytes, lane, vq);
+  float zp[4][N], zq[4][N];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    cvt16(vp[j], zp[j]);
+    if (!BONUS) cvt16(vq[j], zq[j]);
+  }
+  if (nvalid < 128 * N) {
+    mask_tail<N>(zp, lane, nvalid);
+    if (!BONUS) mask_tail<N>(zq, lane, nvalid);
+  }
+  const float2 c2 = make_float2(c, c), np2 = make_float2(-Mp, -Mp), nq2 = make_float2(-Mq, -Mq);
+  const float2 ip2 = make_float2(ip, ip), iq2 = make_float2(iq, iq), m1 = make_float2(-1.f, -1.f);
+  float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+#pragma unroll
+    for (int e = 0; e < N; e += 2) {
+      const float2 yp = __ffma2_rn(make_float2(zp[j][e], zp[j][e + 1]), c2, np2);
+      const float2 p = __fmul2_rn(make_float2(ex2(yp.x), ex2(yp.y)), ip2);
+      if (BONUS) {
+        acc = __fadd2_rn(acc, p);
+      } else {
+        const float2 yq = __ffma2_rn(make_float2(zq[j][e], zq[j][e + 1]), c2, nq2);
+        const float2 q = __fmul2_rn(make_float2(ex2(yq.x), ex2(yq.y)), iq2);
+        const float2 d = __ffma2_rn(q, m1, p);
+        acc = __fadd2_rn(acc, make_float2(fmaxf(d.x, 0.f), fmaxf(d.y, 0.f)));
+      }
+    }
+  return acc.x + acc.y;
+}
+
+// The same probability and residual for one token (bit-identical to the
+// packed arithmetic above, component by component).
+__device__ __forceinline__ float prob_of(float z, float c, float M, float inv) {
+  return __fmul_rn(ex2(fmaf(z, c, -M)), inv);
+}
+__device__ __forceinline__ float resid_of(float p, float q) { return fmaxf(fmaf(q, -1.f, p), 0.f); }
+
+// (reference, sum) of a warp from its lanes'.
+__device__ __forceinline__ float2 warp_combine(float ref, float s) {
+  const float M = warp_max(ref);
+  const float t = (ref > -INFINITY) ? s * ex2(ref - M) : s;
+  return make_float2(M, warp_sum(t));
+}
+
+__device__ __forceinline__ void combine_into(float2 v, float& M, float& S) {
+  // S is kept relative to M; v = (ref, sum)
+  if (v.x > M) {
+    S = (M > -INFINITY ? S * ex2(M - v.x) : S) + v.y;
+    M = v.x;
+  } else {
+    S += (v.x > -INFINITY) ? v.y * ex2(v.x - M) : v.y;
+  }
+}
+
+// Online (reference, sum) update with one value v (units of z'c).
+__device__ __forceinline__ void online_add(float v, float& ref, float& s) {
+  if (v > -INFINITY) {
+    if (v > ref) {
+      s = (ref > -INFINITY ? s * ex2(ref - v) : 0.f) + 1.f;
+      ref = v;
+    } else {
+      s += ex2(v - ref);
+    }
+  }
+}
+
+// Records one item's status; the last item of its request to finish writes
+// the request's tokens (first rejected position's candidate, or the bonus).
+// `tg` is the thread's index in the calling group of `nthr` threads (named
+// barrier `bar`); the group's warp 0 writes.
+__device__ __forceinline__ void finish_item(const SampleParams& P, const Item& it, int item, int flags, int tg, int bar,
+                                            int nthr, int* shflag) {
+  const int b = it.b, K = it.K;
+  if (tg == 0) {
+    P.inval[(size_t)item * kMaxCluster] = flags;
+    __threadfence();
+    const int old = atomicAdd(P.counters + b, 1);
+    *shflag = (old == K) && K >= 0 && it.rows_ok;
+  }
+  named_sync(bar, nthr);
+  if (*shflag && tg < 32) {
+    const int lane = tg;
+    __threadfence();
+    const int d0 = __ldg(P.cu_draft + b), off = d0 + b;
+    int st = 0;
+    for (int j = lane; j < K + 1; j += 32) {
+      const int item_j = j < K ? d0 + j : P.total + b;
+      st |= __ldcg(P.inval + (size_t)item_j * kMaxCluster);
+    }
+    st = warp_or(st);
+    int acc = 1;
+    if (lane < K) acc = __ldcg(&P.results[d0 + lane].acc);
+    const unsigned rej = __ballot_sync(0xffffffffu, lane < K && acc == 0);
+    const int jrej = rej ? __ffs(rej) - 1 : K;
+    const bool nobonus = (P.flags & 1u) != 0;
+    int last;
+    if (jrej < K) last = __ldcg(&P.results[d0 + jrej].cand);
+    else last = nobonus ? -1 : __ldcg(&P.results[P.total + b].cand);
+    for (int s = lane; s <= K; s += 32) {
+      int tok;
+      if (st) tok = -1;
+      else if (s < jrej) tok = __ldg(P.draft_tokens + d0 + s);
+      else if (s == jrej) tok = last;
+      else tok = -1;
+      P.out_tokens[off + s] = tok;
+    }
+    if (lane == 0) {
+      P.out_accepted[b] = st ? -1 : jrej;
+      if (P.out_status) P.out_status[b] = st;
+    }
+  }
+}
+
+// Per-request scalars and the status bits that follow from them.
+struct Scalars {
+  int b, K, d0, off, nrows, x, flags;
+  float alpha, c, D;
+  bool params_ok, pen, uniforms_ok;
+  int h0, h1, npre;
+};
+
+__device__ __forceinline__ Scalars item_scalars(const SampleParams& P, const Item& it, int item) {
+  Scalars s;
+  s.b = it.b;
+  s.K = it.K;
+  s.d0 = __ldg(P.cu_draft + it.b);
+  s.off = s.d0 + it.b;
+  s.nrows = it.bonus ? 1 : 2;
+  s.flags = 0;
+  if (!it.rows_ok || s.K < 0 || s.K > P.max_k || s.K > kMaxK) s.flags |= kStatusBadK;
+  const float T_ = P.temperature ? __ldg(P.temperature + s.b) : 1.f;
+  s.alpha = P.rep_penalty ? __ldg(P.rep_penalty + s.b) : 1.f;
+  s.D = P.tv_budget ? __ldg(P.tv_budget + s.b) : 0.f;
+  s.params_ok = item_params_ok(P, s.b);
+  if (!s.params_ok) s.flags |= kStatusBadParam;
+  // invalid scalars are reported; the statistics then use T = 1, no penalty
+  s.c = __fdiv_rn(1.44269504088896341f, s.params_ok ? T_ : 1.f);
+  s.x = it.bonus ? -1 : __ldg(P.draft_tokens + item);
+  if (!it.bonus && (s.x < 0 || s.x >= P.V)) s.flags |= kStatusBadToken;
+  s.h0 = P.cu_hist ? __ldg(P.cu_hist + s.b) : 0;
+  s.h1 = P.cu_hist ? __ldg(P.cu_hist + s.b + 1) : 0;
+  s.npre = it.bonus ? (it.rows_ok ? s.K : 0) : it.i;
+  s.pen = s.params_ok && s.alpha != 1.f && (s.h1 > s.h0 || s.npre > 0);
+  s.uniforms_ok = !(s.flags & kStatusBadK);
+  return s;
+}
+
+// Marks the penalty set of a request row in `bm` (if pen) and reports
+// out-of-range tokens; threads t of nt.
+__device__ __forceinline__ int mark_penalty_set(const SampleParams& P, const Scalars& s, uint32_t* bm, int t, int nt) {
+  int flags = 0;
+  for (int j = s.h0 + t; j < s.h1; j += nt) {
+    const int tok = __ldg(P.hist + j);
+    if (tok < 0 || tok >= P.V) flags |= kStatusBadToken;
+    else if (s.pen) atomicOr(&bm[tok >> 5], 1u << (tok & 31));
+  }
+  for (int j = t; j < s.npre; j += nt) {
+    const int tok = __ldg(P.draft_tokens + s.d0 + j);
+    if (tok < 0 || tok >= P.V) flags |= kStatusBadToken;
+    else if (s.pen) atomicOr(&bm[tok >> 5], 1u << (tok & 31));
+  }
+  return flags;
+}
+
+// ------------------------------------------------------------ producers
+template <typename T, bool IS_A>
+__device__ void producer(const SampleParams& P, const PipeLayout& L, const PSmem& S) {
+  const uint64_t pol = IS_A ? l2_policy_evict_last() : l2_policy_evict_first();
+  constexpr int es = (int)sizeof(T);
+  const int stage = (IS_A ? kNA : kNB) * L.seg;
+  const int nst = IS_A ? L.nst_a : L.nst_b;
+  const int nslots = IS_A ? L.slots_a : L.slots_b;
+  const int slot_bytes = IS_A ? L.slot_a : L.slot_b;
+  unsigned char* ring = IS_A ? S.ring_a : S.ring_b;
+  uint64_t* full = IS_A ? S.full_a : S.full_b;
+  uint64_t* empty = IS_A ? S.empty_a : S.empty_b;
+  RingCursor rc;
+  bool to = false;
+  int k = 0;
+  for (int item = blockIdx.x; item < P.n_items; item += gridDim.x, ++k) {
+    const Item it = decode_item(P, item);
+    if (!IS_A) {
+      // pass 2 of item k starts once group A has finished its pass 1 (the
+      // rows are then in L2); a deferred item is not streamed again
+      const int kb = k & 1;
+      if (!to && !mbar_wait(&S.stats_full[kb], (uint32_t)(k >> 1) & 1u)) to = true;
+      const int cnt = S.stats[kb].count;
+      mbar_arrive(&S.stats_empty[kb]);
+      if (cnt < 0) continue;
+    }
+    const unsigned char* rowp = static_cast<const unsigned char*>(P.target) + (size_t)it.tgt_row * P.ld_t * es;
+    const unsigned char* rowq =
+        it.bonus ? rowp : static_cast<const unsigned char*>(P.draft) + (size_t)it.dft_row * P.ld_d * es;
+    for (int st = 0; st < nst; ++st) {
+      const uint32_t slot = rc.slot;
+      // first use of a slot: the phase "before" its first completes at once
+      if (!to && !mbar_wait(&empty[slot], rc.phase ^ 1u)) to = true;
+      rc.advance(nslots);
+      const int n = min(stage, P.V - st * stage);
+      const uint32_t bytes = (uint32_t)((n * es + 15) & ~15);
+      unsigned char* dst = ring + (size_t)slot * slot_bytes;
+      mbar_arrive_expect_tx(&full[slot], it.bonus ? bytes : 2 * bytes);
+      bulk_g2s(dst, rowp + (size_t)st * stage * es, bytes, &full[slot], pol);
+      if (!it.bonus) bulk_g2s(dst + (size_t)stage * es, rowq + (size_t)st * stage * es, bytes, &full[slot], pol);
+    }
+  }
+}
+
+// ------------------------------------------------------------- group A
+template <typename T>
+__device__ void group_a(const SampleParams& P, const PipeLayout& L, const PSmem& S, int wa, int lane) {
+  const int ta = wa * 32 + lane;
+  const int SEG = L.seg;
+  const int wps = SEG / 32;  // bitmap words per segment
+  const int row_bytes = kNA * kPipeSegBytes;
+  RingCursor rc;
+  bool timeout = false;
+  int k = 0;
+  for (int item = blockIdx.x; item < P.n_items; item += gridDim.x, ++k) {
+    const int kb = k & 1;
+    PipeStats& st = S.stats[kb];
+    // buffer kb is free once group B and producer B are done with item k-2
+    if (!timeout && !mbar_wait(&S.stats_empty[kb], ((uint32_t)(k >> 1) & 1u) ^ 1u)) timeout = true;
+    const Item it = decode_item(P, item);
+    const Scalars sc = item_scalars(P, it, item);
+    int flags = mark_penalty_set(P, sc, S.bm, ta, kThreadsA);
+
+    // ---- sorted penalty list with per-segment offsets; clears the bitmap
+    int count = 0;
+    if (sc.pen) {
+      named_sync(kBarA, kThreadsA);
+      const int wpt = (L.bm_words + kThreadsA - 1) / kThreadsA;
+      const int w0 = min(L.bm_words, ta * wpt), w1 = min(L.bm_words, w0 + wpt);
+      int cnt = 0;
+      for (int w = w0; w < w1; ++w) cnt += __popc(S.bm[w]);
+      const int incl = warp_incl_scan_i(cnt, lane);
+      if (lane == 31) S.scan[wa] = incl;
+      named_sync(kBarA, kThreadsA);
+      int base = incl - cnt, total = 0;
+      for (int w2 = 0; w2 < kNA; ++w2) {
+        const int v = S.scan[w2];
+        if (w2 < wa) base += v;
+        total += v;
+      }
+      if (total <= kPipeListCap) {
+        count = total;
+        int* segst = S.segst[kb];
+        int* ltok = S.ltok[kb];
+        int pos = base;
+        for (int w = w0; w < w1; ++w) {
+          if (w % wps == 0) segst[w / wps] = pos;
+          uint32_t word = S.bm[w];
+          if (word) {
+            S.bm[w] = 0u;
+            while (word) {
+              const int bit = __ffs(word) - 1;
+              word &= word - 1;
+              ltok[pos++] = 32 * w + bit;
+            }
+          }
+        }
+        if (ta == 0) segst[L.nseg] = total;
+      } else {
+        count = -1;  // too many for the list: the item is recomputed by the slow path
+        for (int w = w0; w < w1; ++w) S.bm[w] = 0u;
+      }
+      named_sync(kBarA, kThreadsA);
+    }
+
+    // ---- pass 1
+    const bool skip = count < 0;
+    float ref[2] = {-INFINITY, -INFINITY}, run[2] = {0.f, 0.f};
+    for (int stn = 0; stn < L.nst_a; ++stn) {
+      const uint32_t slot = rc.slot;
+      if (!timeout && !mbar_wait(&S.full_a[slot], rc.phase)) timeout = true;
+      rc.advance(L.slots_a);
+      const int s_id = stn * kNA + wa;
+      if (!skip && s_id < L.nseg) {
+        unsigned char* seg = S.ring_a + (size_t)slot * L.slot_a + wa * kPipeSegBytes;
+        const int base = s_id * SEG;
+        if (count > 0) {
+          const int e0 = S.segst[kb][s_id], e1 = S.segst[kb][s_id + 1];
+          if (e1 > e0)
+            patch_segment<T, true>(seg, seg + row_bytes, sc.nrows == 2, S.ltok[kb], S.lzp[kb], S.lzq[kb], e0, e1,
+                                   base, lane);
+        }
+        const int nvalid = min(SEG, P.V - base);
+        if (sc.nrows == 2) seg_stats<T, 2>(seg, row_bytes, lane, nvalid, sc.c, ref, run);
+        else seg_stats<T, 1>(seg, row_bytes, lane, nvalid, sc.c, ref, run);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&S.empty_a[slot]);
+    }
+
+    // ---- hand-off to group B
+    if (timeout) flags |= kStatusTimeout;
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      const float2 wv = warp_combine(ref[r], run[r]);
+      if (lane == 0) st.wp[wa][r] = wv;
+    }
+    flags = warp_or(flags);
+    if (lane == 0) st.wflags[wa] = flags;
+    if (ta == 0) st.count = count;
+    named_sync(kBarA, kThreadsA);
+    if (ta == 0) mbar_arrive(&S.stats_full[kb]);
+  }
+}
+
+// Inverse CDF within segment s (warp-wide): the first token whose inclusive
+// prefix of w exceeds rem, w = max(p-q, 0) or p (ponly); `take_last` or no
+// such token: the segment's last token with w > 0.  Returns -1 if none.
+template <typename T>
+__device__ int search_segment(const SampleParams& P, const PipeLayout& L, const PSmem& S, int kb, int count,
+                              const T* gp, const T* gq, bool ponly, int s, double rem, bool take_last, float c,
+                              float alpha, const float* M, const float* inv, int lane) {
+  constexpr int N = Vec<T>::N;
+  constexpr int LT = 4 * N;  // tokens per lane, contiguous
+  const int sbase = s * L.seg;
+  const int base = sbase + lane * LT;
+  uint32_t pm = 0;
+  if (count > 0) {
+    S.cmask[lane] = 0u;
+    __syncwarp();
+    for (int e = S.segst[kb][s] + lane; e < S.segst[kb][s + 1]; e += 32) {
+      const int o = S.ltok[kb][e] - sbase;
+      atomicOr(&S.cmask[o / LT], 1u << (o % LT));
+    }
+    __syncwarp();
+    pm = S.cmask[lane];
+  }
+  uint4 vp[4], vq[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const bool in = base + j * N < P.V;
+    vp[j] = in ? __ldg(reinterpret_cast<const uint4*>(gp + base + j * N)) : make_uint4(0u, 0u, 0u, 0u);
+    vq[j] = (in && !ponly) ? __ldg(reinterpret_cast<const uint4*>(gq + base + j * N)) : make_uint4(0u, 0u, 0u, 0u);
+  }
+  float w[LT];
+  float ls = 0.f;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    float zp[N], zq[N];
+    cvt16(vp[j], zp);
+    cvt16(vq[j], zq);
+#pragma unroll
+    for (int e = 0; e < N; ++e) {
+      const int i = j * N + e;
+      float a = zp[e], bq = zq[e];
+      if ((pm >> i) & 1u) {
+        a = penalize(a, alpha);
+        bq = penalize(bq, alpha);
+      }
+      float v = 0.f;
+      if (base + i < P.V) {
+        const float p = prob_of(a, c, M[0], inv[0]);
+        v = ponly ? p : resid_of(p, prob_of(bq, c, M[1], inv[1]));
+      }
+      w[i] = v;
+      ls += v;
+    }
+  }
+  const float incl = warp_incl_scan(ls, lane);
+  const float excl = incl - ls;
+  int found = -1;
+  if (!take_last) {
+    const unsigned m = __ballot_sync(0xffffffffu, ((double)incl > rem) && ((double)excl <= rem) && ls > 0.f);
+    if (m) {
+      const int L0 = __ffs(m) - 1;
+      int jj = -1;
+      if (lane == L0) {
+        double cum = (double)excl;
+        int lastpos = -1;
+#pragma unroll
+        for (int i = 0; i < LT; ++i) {
+          if (jj < 0) {
+            cum += (double)w[i];
+            if (w[i] > 0.f) {
+              lastpos = i;
+              if (cum > rem) jj = i;
+            }
+          }
+        }
+        if (jj < 0) jj = lastpos;
+      }
+      jj = __shfl_sync(0xffffffffu, jj, L0);
+      if (jj >= 0) found = sbase + L0 * LT + jj;
+    }
+  }
+  if (found < 0) {
+    const unsigned mp = __ballot_sync(0xffffffffu, ls > 0.f);
+    if (mp) {
+      const int L1 = 31 - __clz(mp);
+      int jj = -1;
+      if (lane == L1) {
+#pragma unroll
+        for (int i = 0; i < LT; ++i)
+          if (w[i] > 0.f) jj = i;
+      }
+      jj = __shfl_sync(0xffffffffu, jj, L1);
+      found = sbase + L1 * LT + jj;
+    }
+  }
+  return found;
+}
+
+// Warp-wide owner search over per-unit masses seg[0..n) (fp64 blocks of
+// consecutive units per lane, then a lane scan): the first unit with mass
+// whose inclusive prefix exceeds t, and t minus the prefix before it; if
+// rounding leaves t out of reach, the last unit with mass (take_last).
+// Returns the total mass.
+__device__ __forceinline__ double owner_search(const float* seg, int n, double u, int lane, int& ks, double& rem,
+                                               bool& take_last) {
+  int k0, k1;
+  double blk, inc;
+  const double R = seg_block_scan(seg, n, lane, k0, k1, blk, inc);
+  const double t = u * R;
+  ks = -1;
+  rem = 0.0;
+  take_last = false;
+  const unsigned mh = __ballot_sync(0xffffffffu, blk > 0.0 && inc > t);
+  if (mh) {
+    const int L0 = __ffs(mh) - 1;
+    int kk = -1;
+    double rr = 0.0;
+    bool tl = false;
+    if (lane == L0) {
+      double cum = inc - blk;
+      int klast = -1;
+      for (int k = k0; k < k1; ++k) {
+        const double sg = (double)seg[k];
+        if (sg > 0.0) {
+          if (cum + sg > t) {
+            kk = k;
+            rr = t - cum;
+            break;
+          }
+          klast = k;
+        }
+        cum += sg;
+      }
+      if (kk < 0) {
+        kk = klast;
+        tl = true;
+      }
+    }
+    ks = __shfl_sync(0xffffffffu, kk, L0);
+    rem = __shfl_sync(0xffffffffu, rr, L0);
+    take_last = __shfl_sync(0xffffffffu, (int)tl, L0) != 0;
+  }
+  if (ks < 0) {
+    const unsigned mp = __ballot_sync(0xffffffffu, blk > 0.0);
+    if (mp) {
+      const int L1 = 31 - __clz(mp);
+      int kl = -1;
+      if (lane == L1)
+        for (int k = k1 - 1; k >= k0; --k)
+          if (seg[k] > 0.f) {
+            kl = k;
+            break;
+          }
+      ks = __shfl_sync(0xffffffffu, kl, L1);
+    }
+    take_last = true;
+  }
+  return R;
+}
+
+// ------------------------------------------------------------- group B
+template <typename T>
+__device__ void group_b(const SampleParams& P, const PipeLayout& L, const PSmem& S, int wb, int lane) {
+  const int tb = wb * 32 + lane;
+  const int SEG = L.seg;
+  const int row_bytes = kNB * kPipeSegBytes;
+  RingCursor rc;
+  bool timeout = false;
+  int k = 0;
+  for (int item = blockIdx.x; item < P.n_items; item += gridDim.x, ++k) {
+    const int kb = k & 1;
+    const PipeStats& st = S.stats[kb];
+    const Item it = decode_item(P, item);
+    const Scalars sc = item_scalars(P, it, item);
+    int flags = sc.flags;
+    const T* gp = static_cast<const T*>(P.target) + (size_t)it.tgt_row * P.ld_t;
+    const T* gq = it.bonus ? gp : static_cast<const T*>(P.draft) + (size_t)it.dft_row * P.ld_d;
+    // loads the decisions need, issued early
+    float xzp = 0.f, xzq = 0.f, u_acc = 0.f, u_fin = 0.f;
+    if (tb == 0) {
+      if (sc.x >= 0 && sc.x < P.V) {
+        xzp = to_f32<T>(gp[sc.x]);
+        xzq = to_f32<T>(gq[sc.x]);
+      }
+      if (P.mode == kModeSample && sc.uniforms_ok) {
+        u_fin = __ldg(P.uniforms + sc.off + sc.K);
+        if (!it.bonus) u_acc = __ldg(P.uniforms + sc.off + it.i);
+      }
+    }
+    if (!timeout && !mbar_wait(&S.stats_full[kb], (uint32_t)(k >> 1) & 1u)) timeout = true;
+    const int count = st.count;
+    for (int w = 0; w < kNA; ++w) flags |= st.wflags[w];
+    if (count < 0) {
+      if (tb == 0) S.defer[k >> 5] |= 1u << (k & 31);
+      named_sync(kBarB, kThreadsB);
+      if (tb == 0) mbar_arrive(&S.stats_empty[kb]);
+      continue;
+    }
+
+    // ---- sync 1: penalised tokens' softmax terms, then (M, S) per row
+    float pref[2] = {-INFINITY, -INFINITY}, psum[2] = {0.f, 0.f};
+    int lflags = 0;
+    for (int e = tb; e < count; e += kThreadsB) {
+      const float zp = S.lzp[kb][e], zq = S.lzq[kb][e];
+      if (is_bad_logit(zp) || (sc.nrows == 2 && is_bad_logit(zq))) lflags |= kStatusBadLogits;
+      online_add(penalize(zp, sc.alpha) * sc.c, pref[0], psum[0]);
+      if (sc.nrows == 2) online_add(penalize(zq, sc.alpha) * sc.c, pref[1], psum[1]);
+    }
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      const float2 wv = warp_combine(pref[r], psum[r]);
+      if (lane == 0) S.bred[wb * 2 + r] = wv;
+    }
+    lflags = warp_or(lflags);
+    if (lane == 0 && lflags) atomicOr(&S.mi[0], lflags);
+    named_sync(kBarB, kThreadsB);
+    flags |= S.mi[0];
+    float M[2], Ssum[2], inv[2];
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      M[r] = -INFINITY;
+      Ssum[r] = 0.f;
+      for (int w = 0; w < kNA; ++w) combine_into(st.wp[w][r], M[r], Ssum[r]);
+      for (int w = 0; w < kNB; ++w) combine_into(S.bred[w * 2 + r], M[r], Ssum[r]);
+    }
+    for (int r = 0; r < sc.nrows; ++r)
+      if (!(Ssum[r] > 0.f) || !(Ssum[r] < INFINITY) || !(M[r] < INFINITY)) flags |= kStatusBadLogits;
+    const bool ok_stats = !(flags & kStatusBadLogits);
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      const bool use = ok_stats && r < sc.nrows;
+      inv[r] = use ? __fdiv_rn(1.f, Ssum[r]) : 1.f;
+      if (!use) M[r] = 0.f;
+    }
+
+    // p(x), q(x) (one thread; x may be penalised itself)
+    float px = 0.f, qx = 0.f;
+    if (tb == 0 && !it.bonus && sc.x >= 0 && sc.x < P.V && ok_stats) {
+      bool xpen = false;
+      if (count > 0) {
+        const int sx = sc.x / SEG;
+        for (int e = S.segst[kb][sx]; e < S.segst[kb][sx + 1]; ++e) xpen |= S.ltok[kb][e] == sc.x;
+      }
+      const float zp = xpen ? penalize(xzp, sc.alpha) : xzp;
+      const float zq = xpen ? penalize(xzq, sc.alpha) : xzq;
+      px = prob_of(zp, sc.c, M[0], inv[0]);
+      qx = prob_of(zq, sc.c, M[1], inv[1]);
+    }
+
+    // residual terms of the penalised tokens, summed per segment in list order
+    if (count > 0) {
+      for (int e = tb; e < count; e += kThreadsB) {
+        float r = prob_of(penalize(S.lzp[kb][e], sc.alpha), sc.c, M[0], inv[0]);
+        if (sc.nrows == 2) r = resid_of(r, prob_of(penalize(S.lzq[kb][e], sc.alpha), sc.c, M[1], inv[1]));
+        S.lzp[kb][e] = r;
+      }
+      named_sync(kBarB, kThreadsB);
+    }
+    for (int s = tb; s < L.nseg; s += kThreadsB) {
+      float a = 0.f;
+      if (count > 0)
+        for (int e = S.segst[kb][s]; e < S.segst[kb][s + 1]; ++e) a += S.lzp[kb][e];
+      S.segc[s] = a;
+    }
+
+    // ---- pass 2
+    for (int stn = 0; stn < L.nst_b; ++stn) {
+      const uint32_t slot = rc.slot;
+      if (!timeout && !mbar_wait(&S.full_b[slot], rc.phase)) timeout = true;
+      rc.advance(L.slots_b);
+      const int s_id = stn * kNB + wb;
+      if (s_id < L.nseg) {
+        unsigned char* seg = S.ring_b + (size_t)slot * L.slot_b + wb * kPipeSegBytes;
+        const int base = s_id * SEG;
+        if (count > 0) {
+          const int e0 = S.segst[kb][s_id], e1 = S.segst[kb][s_id + 1];
+          if (e1 > e0)
+            patch_segment<T, false>(seg, seg + row_bytes, sc.nrows == 2, S.ltok[kb], nullptr, nullptr, e0, e1, base,
+                                    lane);
+        }
+        const int nvalid = min(SEG, P.V - base);
+        const float v = it.bonus ? seg_resid<T, true>(seg, row_bytes, lane, nvalid, sc.c, M[0], M[1], inv[0], inv[1])
+                                 : seg_resid<T, false>(seg, row_bytes, lane, nvalid, sc.c, M[0], M[1], inv[0], inv[1]);
+        S.part[s_id * 32 + lane] = v;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&S.empty_b[slot]);
+    }
+    if (timeout) flags |= kStatusTimeout;
+    {
+      const int f = warp_or(flags);
+      if (lane == 0 && f) atomicOr(&S.mi[0], f);
+    }
+    named_sync(kBarB, kThreadsB);
+    for (int s = wb; s < L.nseg; s += kNB) {
+      const float v = warp_sum(S.part[s * 32 + lane]);
+      if (lane == 0) S.segt[s] = v + S.segc[s];
+    }
+    named_sync(kBarB, kThreadsB);
+    flags = S.mi[0];
+
+    // ---- sync 2, decisions, candidate (warp 0 of the group)
+    bool deferred = false;
+    if (wb == 0) {
+      int ks;
+      double rem;
+      bool take_last;
+      const double R = owner_search(S.segt, L.nseg, (double)__shfl_sync(0xffffffffu, u_fin, 0), lane, ks, rem,
+                                    take_last);
+      const double tv = it.bonus ? 0.0 : fmin(R, 1.0);
+      double theta = 1.0;
+      int acc = 1;
+      if (lane == 0) {
+        if (tv > (double)sc.D) theta = (double)sc.D / tv;
+        if (!it.bonus) {
+          const double pi = (1.0 - theta) * (double)px + theta * (double)qx;
+          acc = ((double)u_acc * (double)qx < pi) ? 1 : 0;
+        }
+      }
+      acc = __shfl_sync(0xffffffffu, acc, 0);
+      const bool sample = P.mode == kModeSample;
+      const bool need_cand = sample && flags == 0 && (it.bonus ? !(P.flags & 1u) : acc == 0);
+      int cand = -1;
+      if (need_cand) {
+        if (!it.bonus && !(R > 0.0)) {
+          deferred = true;  // correction from p: recomputed by the slow path
+        } else if (ks >= 0) {
+          cand = search_segment<T>(P, L, S, kb, count, gp, gq, it.bonus, ks, rem, take_last, sc.c, sc.alpha, M, inv,
+                                   lane);
+        }
+      }
+      if (lane == 0) {
+        if (deferred) {
+          S.defer[k >> 5] |= 1u << (k & 31);
+        } else if (sample) {
+          ItemResult* res = P.results + item;
+          res->acc = acc;
+          res->cand = cand;
+          res->tv = (float)tv;
+          res->theta = (float)theta;
+          res->px = px;
+          res->qx = qx;
+        } else {
+          const bool bad = flags != 0;
+          P.out_tv[item] = bad ? NAN : (float)tv;
+          if (P.out_theta) P.out_theta[item] = bad ? NAN : (float)theta;
+          if (P.out_px) P.out_px[item] = bad ? NAN : px;
+          if (P.out_qx) P.out_qx[item] = bad ? NAN : qx;
+        }
+        S.mi[1] = deferred ? 1 : 0;
+      }
+    }
+    named_sync(kBarB, kThreadsB);
+    deferred = S.mi[1] != 0;
+    if (tb == 0) S.mi[0] = 0;  // every B thread has read it; the next item's bits come after the barriers below
+    if (P.mode == kModeSample && !deferred) finish_item(P, it, item, flags, tb, kBarB, kThreadsB, &S.mi[2]);
+    named_sync(kBarB, kThreadsB);
+    if (tb == 0) mbar_arrive(&S.stats_empty[kb]);
+  }
+}
+
+// ------------------------------------------------------------- slow path
+// One deferred item with all compute warps and direct global loads: the
+// same method in 256-token chunks (penalty from a bitmap).
+template <typename T>
+__device__ void slow_item(const SampleParams& P, const PipeLayout& L, const PSmem& S, int item, int warp, int lane) {
+  constexpr int NW = kNC, NT = kThreadsC;
+  const int tid = warp * 32 + lane;
+  const Item it = decode_item(P, item);
+  const Scalars sc = item_scalars(P, it, item);
+  const int V = P.V;
+  const int nch = (V + kChunk - 1) / kChunk;
+  const T* gp = static_cast<const T*>(P.target) + (size_t)it.tgt_row * P.ld_t;
+  const T* gq = it.bonus ? gp : static_cast<const T*>(P.draft) + (size_t)it.dft_row * P.ld_d;
+  if (tid == 0) S.mi[0] = 0;
+  int flags = sc.flags | mark_penalty_set(P, sc, S.bm, tid, NT);
+  named_sync(kBarC, NT);
+
+  // pass 1
+  float refc[2] = {0.f, 0.f}, Ssum[2] = {0.f, 0.f};
+  bool have_ref = false;
+  for (int kk = warp; kk < nch; kk += NW) {
+    float z[2][8];
+    global_logits<T>(gp, kk * kChunk, lane, V, S.bm, sc.pen, sc.alpha, z[0]);
+    if (sc.nrows == 2) {
+      global_logits<T>(gq, kk * kChunk, lane, V, S.bm, sc.pen, sc.alpha, z[1]);
+      chunk_stats_lane<2>(z, sc.c, refc, have_ref, Ssum);
+    } else {
+      chunk_stats_lane<1>(z, sc.c, refc, have_ref, Ssum);
+    }
+  }
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    const float ref = have_ref && r < sc.nrows ? refc[r] : -INFINITY;
+    const float2 wv = warp_combine(ref, ref > -INFINITY ? Ssum[r] : 0.f);
+    if (lane == 0) S.cwp[warp * 2 + r] = wv;
+  }
+  named_sync(kBarC, NT);
+  float M[2], Sr[2], inv[2];
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    M[r] = -INFINITY;
+    Sr[r] = 0.f;
+    for (int w = 0; w < NW; ++w) combine_into(S.cwp[w * 2 + r], M[r], Sr[r]);
+  }
+  for (int r = 0; r < sc.nrows; ++r)
+    if (!(Sr[r] > 0.f) || !(Sr[r] < INFINITY) || !(M[r] < INFINITY)) flags |= kStatusBadLogits;
+  const bool ok_stats = !(flags & kStatusBadLogits);
+  RowProb rp[2];
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    const bool use = ok_stats && r < sc.nrows;
+    inv[r] = use ? __fdiv_rn(1.f, Sr[r]) : 1.f;
+    if (!use) M[r] = 0.f;
+    rp[r].tau_key = 0u;
+    rp[r].c = sc.c;
+    rp[r].mc = M[r];
+    rp[r].invs = inv[r];
+    rp[r].kept = 1.0;
+  }
+
+  // pass 2 (ponly: chunk sums of p instead of the residual)
+  float* seg = S.part;
+  bool ponly = it.bonus;
+  double R = 0.0;
+  int ks = -1;
+  double rem = 0.0;
+  bool take_last = false;
+  float px = 0.f, qx = 0.f;
+  double tv = 0.0, theta = 1.0;
+  int acc = 1;
+  for (int attempt = 0; attempt < 2; ++attempt) {
+    for (int kk = warp; kk < nch; kk += NW) {
+      float z[8], pp[8];
+      global_logits<T>(gp, kk * kChunk, lane, V, S.bm, sc.pen, sc.alpha, z);
+      probs8<kPZ>(z, 0.f, rp[0], pp);
+      float s;
+      if (ponly) {
+        s = sum8(pp);
+      } else {
+        float zq[8], qq[8], rr[8];
+        global_logits<T>(gq, kk * kChunk, lane, V, S.bm, sc.pen, sc.alpha, zq);
+        probs8<kPZ>(zq, 0.f, rp[1], qq);
+        s = resid8(pp, qq, rr);
+      }
+      s = warp_sum(s);
+      if (lane == 0) seg[kk] = s;
+    }
+    named_sync(kBarC, NT);
+    if (warp == 0) {
+      const float uf = (P.mode == kModeSample && sc.uniforms_ok) ? __ldg(P.uniforms + sc.off + sc.K) : 0.f;
+      R = owner_search(seg, nch, (double)uf, lane, ks, rem, take_last);
+      if (attempt == 0 && lane == 0) {
+        if (!it.bonus && sc.x >= 0 && sc.x < V && ok_stats) {
+          float zp = to_f32<T>(gp[sc.x]), zq = to_f32<T>(gq[sc.x]);
+          if (sc.pen && ((S.bm[sc.x >> 5] >> (sc.x & 31)) & 1u)) {
+            zp = penalize(zp, sc.alpha);
+            zq = penalize(zq, sc.alpha);
+          }
+          px = prob_of(zp, sc.c, M[0], inv[0]);
+          qx = prob_of(zq, sc.c, M[1], inv[1]);
+        }
+        tv = it.bonus ? 0.0 : fmin(R, 1.0);
+        if (tv > (double)sc.D) theta = (double)sc.D / tv;
+        if (!it.bonus) {
+          const float ua = (P.mode == kModeSample && sc.uniforms_ok) ? __ldg(P.uniforms + sc.off + it.i) : 0.f;
+          const double pi = (1.0 - theta) * (double)px + theta * (double)qx;
+          acc = ((double)ua * (double)qx < pi) ? 1 : 0;
+        }
+        S.mi[4] = (P.mode == kModeSample && !it.bonus && acc == 0 && !(R > 0.0) && ok_stats) ? 1 : 0;
+      }
+    }
+    named_sync(kBarC, NT);
+    if (attempt == 0 && S.mi[4]) {
+      ponly = true;  // no residual mass: the correction is drawn from p
+      continue;
+    }
+    break;
+  }
+
+  // candidate (warp 0): the owning chunk, then the lane and element
+  if (warp == 0) acc = __shfl_sync(0xffffffffu, acc, 0);
+  const bool need_cand =
+      P.mode == kModeSample && flags == 0 && ok_stats && (it.bonus ? !(P.flags & 1u) : acc == 0);
+  if (warp == 0) {
+    int found = -1;
+    if (need_cand && ks >= 0) {
+      const int ib = ks * kChunk;
+      float w[8];
+      {
+        float zp[8], pp[8];
+        global_logits<T>(gp, ib, lane, V, S.bm, sc.pen, sc.alpha, zp);
+        probs8<kPZ>(zp, 0.f, rp[0], pp);
+        if (ponly) {
+#pragma unroll
+          for (int j = 0; j < 8; ++j) w[j] = pp[j];
+        } else {
+          float zq[8], qq[8];
+          global_logits<T>(gq, ib, lane, V, S.bm, sc.pen, sc.alpha, zq);
+          probs8<kPZ>(zq, 0.f, rp[1], qq);
+          resid8(pp, qq, w);
+        }
+      }
+      if (!take_last) {
+        for (int half = 0; half < 2 && found < 0; ++half) {
+          const float* wh = w + 4 * half;
+          const float ls = (wh[0] + wh[1]) + (wh[2] + wh[3]);
+          const float incl = warp_incl_scan(ls, lane);
+          const float excl = incl - ls;
+          const bool hit = ((double)incl > rem) && ((double)excl <= rem) && ls > 0.f;
+          const unsigned m = __ballot_sync(0xffffffffu, hit);
+          if (m) {
+            const int L0 = __ffs(m) - 1;
+            int jj = -1;
+            if (lane == L0) {
+              double cum = (double)excl;
+              for (int j = 0; j < 4; ++j) {
+                cum += (double)wh[j];
+                if (wh[j] > 0.f && cum > rem) {
+                  jj = j;
+                  break;
+                }
+              }
+              if (jj < 0)
+                for (int j = 3; j >= 0; --j)
+                  if (wh[j] > 0.f) {
+                    jj = j;
+                    break;
+                  }
+            }
+            jj = __shfl_sync(0xffffffffu, jj, L0);
+            found = ib + 128 * half + 4 * L0 + jj;
+          } else {
+            rem -= (double)__shfl_sync(0xffffffffu, incl, 31);
+          }
+        }
+      }
+      if (found < 0) {
+        for (int half = 1; half >= 0 && found < 0; --half) {
+          int lj = -1;
+          for (int j = 3; j >= 0; --j)
+            if (w[4 * half + j] > 0.f) {
+              lj = j;
+              break;
+            }
+          const unsigned m = __ballot_sync(0xffffffffu, lj >= 0);
+          if (m) {
+            const int L0 = 31 - __clz(m);
+            lj = __shfl_sync(0xffffffffu, lj, L0);
+            found = ib + 128 * half + 4 * L0 + lj;
+          }
+        }
+      }
+    }
+    if (lane == 0) {
+      if (P.mode == kModeSample) {
+        ItemResult* res = P.results + item;
+        res->acc = acc;
+        res->cand = found;
+        res->tv = (float)tv;
+        res->theta = (float)theta;
+        res->px = px;
+        res->qx = qx;
+      } else {
+        const bool bad = flags != 0;
+        P.out_tv[item] = bad ? NAN : (float)tv;
+        if (P.out_theta) P.out_theta[item] = bad ? NAN : (float)theta;
+        if (P.out_px) P.out_px[item] = bad ? NAN : px;
+        if (P.out_qx) P.out_qx[item] = bad ? NAN : qx;
+      }
+    }
+  }
+  {
+    const int f = warp_or(flags);
+    if (lane == 0 && f) atomicOr(&S.mi[0], f);
+  }
+  named_sync(kBarC, NT);
+  flags = S.mi[0];
+  if (P.mode == kModeSample) finish_item(P, it, item, flags, tid, kBarC, NT, &S.mi[3]);
+  // clear the bitmap for the next deferred item
+  if (sc.pen) {
+    for (int j = sc.h0 + tid; j < sc.h1; j += NT) {
+      const int t = __ldg(P.hist + j);
+      if (t >= 0 && t < V) S.bm[t >> 5] = 0u;
+    }
+    for (int j = tid; j < sc.npre; j += NT) {
+      const int t = __ldg(P.draft_tokens + sc.d0 + j);
+      if (t >= 0 && t < V) S.bm[t >> 5] = 0u;
+    }
+  }
+  named_sync(kBarC, NT);
+}
+
+// ---------------------------------------------------------------- kernel
+template <typename T>
+__global__ void __launch_bounds__(kPipeThreads, 1) pipe_verify_kernel(const __grid_constant__ SampleParams P) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  const PipeLayout& L = P.PL;
+  const PSmem S = carve(smem, L);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int tid = threadIdx.x;
+  if (tid == 0) {
+    for (int s = 0; s < L.slots_a; ++s) {
+      mbar_init(&S.full_a[s], 1);
+      mbar_init(&S.empty_a[s], kNA);
+    }
+    for (int s = 0; s < L.slots_b; ++s) {
+      mbar_init(&S.full_b[s], 1);
+      mbar_init(&S.empty_b[s], kNB);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&S.stats_full[i], 1);
+      mbar_init(&S.stats_empty[i], 2);
+    }
+    fence_mbar_init();
+  }
+  for (int w = tid; w < L.bm_words; w += kPipeThreads) S.bm[w] = 0u;
+  for (int w = tid; w < kPipeMaxIters / 32; w += kPipeThreads) S.defer[w] = 0u;
+  if (tid < 16) S.mi[tid] = 0;
+  __syncthreads();
+
+  if (warp < kNA) {
+    group_a<T>(P, L, S, warp, lane);
+  } else if (warp < kNC) {
+    group_b<T>(P, L, S, warp - kNA, lane);
+  } else {
+    if (lane == 0) {
+      if (warp == kNC) producer<T, true>(P, L, S);
+      else producer<T, false>(P, L, S);
+    }
+    return;
+  }
+  // deferred items of this CTA, after the pipeline has drained
+  named_sync(kBarC, kThreadsC);
+  int k = 0;
+  for (int item = blockIdx.x; item < P.n_items; item += gridDim.x, ++k)
+    if ((S.defer[k >> 5] >> (k & 31)) & 1u) slow_item<T>(P, L, S, item, warp, lane);
+}
+
+}  // namespace
+
+// Layout for the pipelined kernel (-1 if it does not fit `max_smem`).
+int choose_pipe_layout(int V, int elem_bytes, int max_smem, PipeLayout* out) {
+  for (int slots_a = 3; slots_a >= 2; --slots_a) {
+    const PipeLayout L = make_pipe_layout(V, elem_bytes, slots_a, 2);
+    if (L.total <= max_smem) {
+      *out = L;
+      return 0;
+    }
+  }
+  return -1;
+}
+
+int launch_pipe_verify(SampleParams& P, bool bf16, int num_sms, cudaStream_t stream) {
+  const int smem = P.PL.total;
+  const int grid = P.n_items < num_sms ? P.n_items : num_sms;
+  if (grid <= 0) return 0;
+  P.C = 1;
+  P.n_clusters = grid;
+  if (bf16) {
+    auto kern = pipe_verify_kernel<__nv_bfloat16>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) {
+      cudaGetLastError();
+      return -8;
+    }
+    kern<<<grid, kPipeThreads, smem, stream>>>(P);
+  } else {
+    auto kern = pipe_verify_kernel<float>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) {
+      cudaGetLastError();
+      return -8;
+    }
+    kern<<<grid, kPipeThreads, smem, stream>>>(P);
+  }
+  if (cudaGetLastError() != cudaSuccess) return -7;
+  return 0;
+}
+
+}  // namespace sv

@@ -5,6 +5,8 @@
 #include <cstddef>
 #include <cstdint>
 
+#include <vector_types.h>
+
 namespace sv {
 
 // ----------------------------------------------------------------- sampling
@@ -103,6 +105,65 @@ inline SmemLayout make_stream_layout(int V, int C, int elem_bytes, bool topp, in
   return L;
 }
 
+// ------------------------------------------- pipelined streaming sampling
+// One CTA per SM, persistent over its items.  Warp group A computes the
+// pass-1 statistics of item k+1 from HBM while warp group B runs pass 2 (an
+// L2 re-read), the decisions and the candidate search of item k; each group
+// has its own TMA producer warp and shared-memory ring.
+constexpr int kPipeWarpsA = 8;
+constexpr int kPipeWarpsB = 8;
+constexpr int kPipeSegBytes = 2048;   // one row's bytes per warp per stage (64 per lane)
+constexpr int kPipeListCap = 1024;    // distinct penalised tokens per item the pipeline handles
+constexpr int kPipeMaxIters = 8192;   // items per CTA (deferred-item bits)
+
+// Pass-1 result of one item, handed from group A to group B.
+struct PipeStats {
+  float2 wp[kPipeWarpsA][2];  // per A warp and row: (reference, sum)
+  int wflags[kPipeWarpsA];    // status bits found by each A warp
+  int count;                  // penalised-token list length; -1 = too many (item deferred)
+  int pad[3];
+};
+
+struct PipeLayout {
+  int seg;              // tokens of a row per warp segment (kPipeSegBytes / elem bytes)
+  int nseg;             // segments per row
+  int nst_a, nst_b;     // stages per row (group A / group B)
+  int slots_a, slots_b;
+  int slot_a, slot_b;   // bytes per ring slot
+  int bm_words;         // bitmap words (nseg * seg / 32)
+  int off_ring_a, off_ring_b, off_bm, off_part, off_segt, off_segc, off_list, off_segst, off_stats, off_misc,
+      off_defer, off_bar;
+  int total;
+};
+
+inline PipeLayout make_pipe_layout(int V, int elem_bytes, int slots_a, int slots_b) {
+  PipeLayout L{};
+  L.seg = kPipeSegBytes / elem_bytes;
+  L.nseg = (V + L.seg - 1) / L.seg;
+  L.nst_a = (L.nseg + kPipeWarpsA - 1) / kPipeWarpsA;
+  L.nst_b = (L.nseg + kPipeWarpsB - 1) / kPipeWarpsB;
+  L.slots_a = slots_a;
+  L.slots_b = slots_b;
+  L.slot_a = 2 * kPipeWarpsA * kPipeSegBytes;
+  L.slot_b = 2 * kPipeWarpsB * kPipeSegBytes;
+  L.bm_words = L.nseg * L.seg / 32;
+  int off = 0;
+  L.off_ring_a = off;  off += slots_a * L.slot_a;
+  L.off_ring_b = off;  off += slots_b * L.slot_b;
+  L.off_bm = off;      off += align_up_i(L.bm_words * 4, 16);
+  L.off_part = off;    off += L.nseg * 32 * 4;
+  L.off_segt = off;    off += align_up_i(L.nseg * 4, 16);
+  L.off_segc = off;    off += align_up_i(L.nseg * 4, 16);
+  L.off_list = off;    off += 2 * kPipeListCap * 12;
+  L.off_segst = off;   off += 2 * align_up_i((L.nseg + 1) * 4, 16);
+  L.off_stats = off;   off += 2 * (int)sizeof(PipeStats);
+  L.off_misc = off;    off += 1024;
+  L.off_defer = off;   off += kPipeMaxIters / 8;
+  L.off_bar = off;     off += (2 * slots_a + 2 * slots_b + 4) * 8;
+  L.total = align_up_i(off, 128);
+  return L;
+}
+
 struct SampleParams {
   const void* target;
   long long ld_t;
@@ -137,6 +198,7 @@ struct SampleParams {
   int n_items;
   int n_clusters;
   SmemLayout L;
+  PipeLayout PL;   // pipelined streaming kernel only
 };
 
 // ------------------------------------------------------------------- greedy

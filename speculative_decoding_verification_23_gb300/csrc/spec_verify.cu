@@ -16,6 +16,8 @@ int choose_stream_layout(int V, int C, int elem_bytes, bool topp, int max_smem, 
                          SmemLayout* L_out);
 int launch_sample_verify(SampleParams& P, bool bf16, bool topp, cudaStream_t stream);
 int launch_greedy_verify(const GreedyParams& P, bool bf16, cudaStream_t stream);
+int choose_pipe_layout(int V, int elem_bytes, int max_smem, PipeLayout* out);
+int launch_pipe_verify(SampleParams& P, bool bf16, int num_sms, cudaStream_t stream);
 }  // namespace sv
 
 namespace {
@@ -90,8 +92,10 @@ void fill_sample_inputs(sv::SampleParams& P, const spec_args* a) {
 
 // Picks the kernel variant.  Resident (each logit read once, values kept in
 // the shared memory of a C-CTA cluster) when every work item gets its own
-// cluster in one wave; streaming (slices re-read from L2, about one item per
-// SM in flight) otherwise.  SPEC_PREFER_* flags override the choice.
+// cluster in one wave; streaming otherwise: the pipelined kernel (one CTA
+// per SM, pass 1 of the next item overlapping pass 2 of the current one)
+// without top-p, the cluster kernel's streaming variant with top-p.
+// SPEC_PREFER_* flags override the choice between resident and streaming.
 int run_sample(sv::SampleParams& P, const spec_args* a, void* ws, cudaStream_t stream) {
   int max_smem = 0, num_sms = 0, smem_per_sm = 0;
   int rc = device_props(&max_smem, &num_sms, &smem_per_sm);
@@ -110,12 +114,24 @@ int run_sample(sv::SampleParams& P, const spec_args* a, void* ws, cudaStream_t s
   if ((a->flags & SPEC_PREFER_RESIDENT) && res_ok) resident = true;
   else if ((a->flags & SPEC_PREFER_STREAMING) && str_ok) resident = false;
   else resident = res_ok && (!str_ok || (long long)P.n_items * C_res <= num_sms);
-  if (!resident && !str_ok) return SPEC_ERR_SHAPE;
+  sv::PipeLayout L_pipe{};
+  const bool pipe_ok = !topp && sv::choose_pipe_layout(a->V, es, max_smem, &L_pipe) == 0 &&
+                       (long long)P.n_items <= (long long)num_sms * sv::kPipeMaxIters;
+  if (!resident && !str_ok && !pipe_ok) return SPEC_ERR_SHAPE;
   const sv::WorkspaceLayout W = sv::make_workspace_layout(a->B, a->total_drafts, a->V);
   unsigned char* w = static_cast<unsigned char*>(ws);
   P.counters = reinterpret_cast<int*>(w + W.off_counters);
   P.results = reinterpret_cast<sv::ItemResult*>(w + W.off_results);
   P.inval = reinterpret_cast<int*>(w + W.off_inval);
+  if (!resident && pipe_ok) {
+    P.PL = L_pipe;
+    if (P.mode == sv::kModeSample &&
+        cudaMemsetAsync(P.counters, 0, (size_t)a->B * sizeof(int), stream) != cudaSuccess) {
+      cudaGetLastError();
+      return SPEC_ERR_LAUNCH;
+    }
+    return sv::launch_pipe_verify(P, a->dtype == SPEC_BF16, num_sms, stream);
+  }
   P.C = resident ? C_res : C_str;
   P.L = resident ? L_res : L_str;
   if (P.mode == sv::kModeSample) {
