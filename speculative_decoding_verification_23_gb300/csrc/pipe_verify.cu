@@ -49,69 +49,59 @@ constexpr int kPipeThreads = kThreadsC + 64;   // + producer warps A and B
 constexpr int kBarA = 1, kBarB = 2, kBarC = 3;  // named barriers of the groups
 constexpr float kLim = 18446744073709551616.0f;  // 2^64
 
-struct PSmem {
-  unsigned char* ring_a;
-  unsigned char* ring_b;
-  uint32_t* bm;       // [bm_words] penalty bitmap: group A's scratch, then the slow path's
-  float* part;        // [nseg][32] pass-2 lane sums (slow path: 256-token chunk sums)
-  float* segt;        // [nseg] segment residual mass
-  float* segc;        // [nseg] penalised tokens' share of it
-  int* ltok[2];       // [cap] sorted penalised tokens of the item in buffer k & 1
-  float* lzp[2];      // [cap] their raw target logits; later their residual terms
-  float* lzq[2];      // [cap] their raw draft logits
-  int* segst[2];      // [nseg + 1] list offset of each segment
-  PipeStats* stats;   // [2]
-  float2* bred;       // [kNB][2] group B warp partials of the penalised terms
-  float2* cwp;        // [kNC][2] slow path warp partials
-  int* scan;          // [kNC] scan scratch
-  double* md;         // [16]
-  int* mi;            // [16]: [0] group B status bits, [2] B finalize flag, [3] slow finalize flag,
-                      //       [4] slow: draw from p
-  float* mf;          // [16]
-  uint32_t* cmask;    // [32] candidate segment penalty mask
-  uint32_t* defer;    // [kPipeMaxIters / 32] deferred items of this CTA
-  uint64_t* full_a;
-  uint64_t* empty_a;
-  uint64_t* full_b;
-  uint64_t* empty_b;
-  uint64_t* stats_full;   // [2] A -> B: item statistics ready
-  uint64_t* stats_empty;  // [2] B and producer B -> A: buffer free again
-};
+extern __shared__ __align__(128) unsigned char pipe_smem[];
 
-__device__ __forceinline__ PSmem carve(unsigned char* smem, const PipeLayout& L) {
-  PSmem S;
-  S.ring_a = smem + L.off_ring_a;
-  S.ring_b = smem + L.off_ring_b;
-  S.bm = reinterpret_cast<uint32_t*>(smem + L.off_bm);
-  S.part = reinterpret_cast<float*>(smem + L.off_part);
-  S.segt = reinterpret_cast<float*>(smem + L.off_segt);
-  S.segc = reinterpret_cast<float*>(smem + L.off_segc);
-  for (int i = 0; i < 2; ++i) {
-    unsigned char* lb = smem + L.off_list + i * kPipeListCap * 12;
-    S.ltok[i] = reinterpret_cast<int*>(lb);
-    S.lzp[i] = reinterpret_cast<float*>(lb + kPipeListCap * 4);
-    S.lzq[i] = reinterpret_cast<float*>(lb + kPipeListCap * 8);
-    S.segst[i] = reinterpret_cast<int*>(smem + L.off_segst + i * align_up_i((L.nseg + 1) * 4, 16));
+// Shared-memory regions, addressed from the layout in parameter space (no
+// table of pointers that would have to live in local memory).
+struct PSmem {
+  const PipeLayout& L;
+  __device__ __forceinline__ explicit PSmem(const PipeLayout& l) : L(l) {}
+  __device__ __forceinline__ unsigned char* at(int off) const { return pipe_smem + off; }
+  __device__ __forceinline__ unsigned char* ring_a() const { return at(L.off_ring_a); }
+  __device__ __forceinline__ unsigned char* ring_b() const { return at(L.off_ring_b); }
+  // penalty bitmap: group A's scratch, then the slow path's
+  __device__ __forceinline__ uint32_t* bm() const { return reinterpret_cast<uint32_t*>(at(L.off_bm)); }
+  // [nseg][32] pass-2 lane sums (slow path: 256-token chunk sums)
+  __device__ __forceinline__ float* part() const { return reinterpret_cast<float*>(at(L.off_part)); }
+  // [nseg] segment residual mass and the penalised tokens' share of it
+  __device__ __forceinline__ float* segt() const { return reinterpret_cast<float*>(at(L.off_segt)); }
+  __device__ __forceinline__ float* segc() const { return reinterpret_cast<float*>(at(L.off_segc)); }
+  // item buffer kb: sorted penalised tokens, their raw target logits (later
+  // their residual terms), their raw draft logits, and segment offsets
+  __device__ __forceinline__ int* ltok(int kb) const {
+    return reinterpret_cast<int*>(at(L.off_list + kb * kPipeListCap * 12));
   }
-  S.stats = reinterpret_cast<PipeStats*>(smem + L.off_stats);
-  unsigned char* m = smem + L.off_misc;
-  S.bred = reinterpret_cast<float2*>(m);
-  S.cwp = reinterpret_cast<float2*>(m + 128);
-  S.scan = reinterpret_cast<int*>(m + 384);
-  S.md = reinterpret_cast<double*>(m + 448);
-  S.mi = reinterpret_cast<int*>(m + 576);
-  S.mf = reinterpret_cast<float*>(m + 640);
-  S.cmask = reinterpret_cast<uint32_t*>(m + 704);
-  S.defer = reinterpret_cast<uint32_t*>(smem + L.off_defer);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.off_bar);
-  S.full_a = bars;
-  S.empty_a = bars + L.slots_a;
-  S.full_b = bars + 2 * L.slots_a;
-  S.empty_b = bars + 2 * L.slots_a + L.slots_b;
-  S.stats_full = bars + 2 * L.slots_a + 2 * L.slots_b;
-  S.stats_empty = S.stats_full + 2;
-  return S;
-}
+  __device__ __forceinline__ float* lzp(int kb) const {
+    return reinterpret_cast<float*>(at(L.off_list + kb * kPipeListCap * 12 + kPipeListCap * 4));
+  }
+  __device__ __forceinline__ float* lzq(int kb) const {
+    return reinterpret_cast<float*>(at(L.off_list + kb * kPipeListCap * 12 + kPipeListCap * 8));
+  }
+  __device__ __forceinline__ int* segst(int kb) const {
+    return reinterpret_cast<int*>(at(L.off_segst + kb * align_up_i((L.nseg + 1) * 4, 16)));
+  }
+  __device__ __forceinline__ PipeStats* stats(int kb) const {
+    return reinterpret_cast<PipeStats*>(at(L.off_stats)) + kb;
+  }
+  // misc: [kNB][2] group B warp partials, [kNC][2] slow-path warp partials,
+  // scan scratch, scalars, the candidate segment's penalty mask
+  __device__ __forceinline__ float2* bred() const { return reinterpret_cast<float2*>(at(L.off_misc)); }
+  __device__ __forceinline__ float2* cwp() const { return reinterpret_cast<float2*>(at(L.off_misc + 128)); }
+  __device__ __forceinline__ int* scan() const { return reinterpret_cast<int*>(at(L.off_misc + 384)); }
+  // mi: [0] group B status bits, [1] B deferral, [2] B finalize flag,
+  //     [3] slow finalize flag, [4] slow: draw from p
+  __device__ __forceinline__ int* mi() const { return reinterpret_cast<int*>(at(L.off_misc + 576)); }
+  __device__ __forceinline__ uint32_t* cmask() const { return reinterpret_cast<uint32_t*>(at(L.off_misc + 704)); }
+  __device__ __forceinline__ uint32_t* defer() const { return reinterpret_cast<uint32_t*>(at(L.off_defer)); }
+  __device__ __forceinline__ uint64_t* bars() const { return reinterpret_cast<uint64_t*>(at(L.off_bar)); }
+  __device__ __forceinline__ uint64_t* full_a() const { return bars(); }
+  __device__ __forceinline__ uint64_t* empty_a() const { return bars() + L.slots_a; }
+  __device__ __forceinline__ uint64_t* full_b() const { return bars() + 2 * L.slots_a; }
+  __device__ __forceinline__ uint64_t* empty_b() const { return bars() + 2 * L.slots_a + L.slots_b; }
+  // [2] A -> B: item statistics ready; B and producer B -> A: buffer free
+  __device__ __forceinline__ uint64_t* stats_full() const { return bars() + 2 * L.slots_a + 2 * L.slots_b; }
+  __device__ __forceinline__ uint64_t* stats_empty() const { return stats_full() + 2; }
+};
 
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -438,16 +428,16 @@ __device__ __forceinline__ int mark_penalty_set(const SampleParams& P, const Sca
 
 // ------------------------------------------------------------ producers
 template <typename T, bool IS_A>
-__device__ void producer(const SampleParams& P, const PipeLayout& L, const PSmem& S) {
+__device__ __forceinline__ void producer(const SampleParams& P, const PipeLayout& L, const PSmem& S) {
   const uint64_t pol = IS_A ? l2_policy_evict_last() : l2_policy_evict_first();
   constexpr int es = (int)sizeof(T);
   const int stage = (IS_A ? kNA : kNB) * L.seg;
   const int nst = IS_A ? L.nst_a : L.nst_b;
   const int nslots = IS_A ? L.slots_a : L.slots_b;
   const int slot_bytes = IS_A ? L.slot_a : L.slot_b;
-  unsigned char* ring = IS_A ? S.ring_a : S.ring_b;
-  uint64_t* full = IS_A ? S.full_a : S.full_b;
-  uint64_t* empty = IS_A ? S.empty_a : S.empty_b;
+  unsigned char* ring = IS_A ? S.ring_a() : S.ring_b();
+  uint64_t* full = IS_A ? S.full_a() : S.full_b();
+  uint64_t* empty = IS_A ? S.empty_a() : S.empty_b();
   RingCursor rc;
   bool to = false;
   int k = 0;
@@ -457,9 +447,9 @@ __device__ void producer(const SampleParams& P, const PipeLayout& L, const PSmem
       // pass 2 of item k starts once group A has finished its pass 1 (the
       // rows are then in L2); a deferred item is not streamed again
       const int kb = k & 1;
-      if (!to && !mbar_wait(&S.stats_full[kb], (uint32_t)(k >> 1) & 1u)) to = true;
-      const int cnt = S.stats[kb].count;
-      mbar_arrive(&S.stats_empty[kb]);
+      if (!to && !mbar_wait(&S.stats_full()[kb], (uint32_t)(k >> 1) & 1u)) to = true;
+      const int cnt = S.stats(kb)->count;
+      mbar_arrive(&S.stats_empty()[kb]);
       if (cnt < 0) continue;
     }
     const unsigned char* rowp = static_cast<const unsigned char*>(P.target) + (size_t)it.tgt_row * P.ld_t * es;
@@ -482,7 +472,7 @@ __device__ void producer(const SampleParams& P, const PipeLayout& L, const PSmem
 
 // ------------------------------------------------------------- group A
 template <typename T>
-__device__ void group_a(const SampleParams& P, const PipeLayout& L, const PSmem& S, int wa, int lane) {
+__device__ __forceinline__ void group_a(const SampleParams& P, const PipeLayout& L, const PSmem& S, int wa, int lane) {
   const int ta = wa * 32 + lane;
   const int SEG = L.seg;
   const int wps = SEG / 32;  // bitmap words per segment
@@ -492,12 +482,12 @@ __device__ void group_a(const SampleParams& P, const PipeLayout& L, const PSmem&
   int k = 0;
   for (int item = blockIdx.x; item < P.n_items; item += gridDim.x, ++k) {
     const int kb = k & 1;
-    PipeStats& st = S.stats[kb];
+    PipeStats& st = *S.stats(kb);
     // buffer kb is free once group B and producer B are done with item k-2
-    if (!timeout && !mbar_wait(&S.stats_empty[kb], ((uint32_t)(k >> 1) & 1u) ^ 1u)) timeout = true;
+    if (!timeout && !mbar_wait(&S.stats_empty()[kb], ((uint32_t)(k >> 1) & 1u) ^ 1u)) timeout = true;
     const Item it = decode_item(P, item);
     const Scalars sc = item_scalars(P, it, item);
-    int flags = mark_penalty_set(P, sc, S.bm, ta, kThreadsA);
+    int flags = mark_penalty_set(P, sc, S.bm(), ta, kThreadsA);
 
     // ---- sorted penalty list with per-segment offsets; clears the bitmap
     int count = 0;
@@ -506,26 +496,26 @@ __device__ void group_a(const SampleParams& P, const PipeLayout& L, const PSmem&
       const int wpt = (L.bm_words + kThreadsA - 1) / kThreadsA;
       const int w0 = min(L.bm_words, ta * wpt), w1 = min(L.bm_words, w0 + wpt);
       int cnt = 0;
-      for (int w = w0; w < w1; ++w) cnt += __popc(S.bm[w]);
+      for (int w = w0; w < w1; ++w) cnt += __popc(S.bm()[w]);
       const int incl = warp_incl_scan_i(cnt, lane);
-      if (lane == 31) S.scan[wa] = incl;
+      if (lane == 31) S.scan()[wa] = incl;
       named_sync(kBarA, kThreadsA);
       int base = incl - cnt, total = 0;
       for (int w2 = 0; w2 < kNA; ++w2) {
-        const int v = S.scan[w2];
+        const int v = S.scan()[w2];
         if (w2 < wa) base += v;
         total += v;
       }
       if (total <= kPipeListCap) {
         count = total;
-        int* segst = S.segst[kb];
-        int* ltok = S.ltok[kb];
+        int* segst = S.segst(kb);
+        int* ltok = S.ltok(kb);
         int pos = base;
         for (int w = w0; w < w1; ++w) {
           if (w % wps == 0) segst[w / wps] = pos;
-          uint32_t word = S.bm[w];
+          uint32_t word = S.bm()[w];
           if (word) {
-            S.bm[w] = 0u;
+            S.bm()[w] = 0u;
             while (word) {
               const int bit = __ffs(word) - 1;
               word &= word - 1;
@@ -536,7 +526,7 @@ __device__ void group_a(const SampleParams& P, const PipeLayout& L, const PSmem&
         if (ta == 0) segst[L.nseg] = total;
       } else {
         count = -1;  // too many for the list: the item is recomputed by the slow path
-        for (int w = w0; w < w1; ++w) S.bm[w] = 0u;
+        for (int w = w0; w < w1; ++w) S.bm()[w] = 0u;
       }
       named_sync(kBarA, kThreadsA);
     }
@@ -546,16 +536,16 @@ __device__ void group_a(const SampleParams& P, const PipeLayout& L, const PSmem&
     float ref[2] = {-INFINITY, -INFINITY}, run[2] = {0.f, 0.f};
     for (int stn = 0; stn < L.nst_a; ++stn) {
       const uint32_t slot = rc.slot;
-      if (!timeout && !mbar_wait(&S.full_a[slot], rc.phase)) timeout = true;
+      if (!timeout && !mbar_wait(&S.full_a()[slot], rc.phase)) timeout = true;
       rc.advance(L.slots_a);
       const int s_id = stn * kNA + wa;
       if (!skip && s_id < L.nseg) {
-        unsigned char* seg = S.ring_a + (size_t)slot * L.slot_a + wa * kPipeSegBytes;
+        unsigned char* seg = S.ring_a() + (size_t)slot * L.slot_a + wa * kPipeSegBytes;
         const int base = s_id * SEG;
         if (count > 0) {
-          const int e0 = S.segst[kb][s_id], e1 = S.segst[kb][s_id + 1];
+          const int e0 = S.segst(kb)[s_id], e1 = S.segst(kb)[s_id + 1];
           if (e1 > e0)
-            patch_segment<T, true>(seg, seg + row_bytes, sc.nrows == 2, S.ltok[kb], S.lzp[kb], S.lzq[kb], e0, e1,
+            patch_segment<T, true>(seg, seg + row_bytes, sc.nrows == 2, S.ltok(kb), S.lzp(kb), S.lzq(kb), e0, e1,
                                    base, lane);
         }
         const int nvalid = min(SEG, P.V - base);
@@ -563,7 +553,7 @@ __device__ void group_a(const SampleParams& P, const PipeLayout& L, const PSmem&
         else seg_stats<T, 1>(seg, row_bytes, lane, nvalid, sc.c, ref, run);
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(&S.empty_a[slot]);
+      if (lane == 0) mbar_arrive(&S.empty_a()[slot]);
     }
 
     // ---- hand-off to group B
@@ -577,7 +567,7 @@ __device__ void group_a(const SampleParams& P, const PipeLayout& L, const PSmem&
     if (lane == 0) st.wflags[wa] = flags;
     if (ta == 0) st.count = count;
     named_sync(kBarA, kThreadsA);
-    if (ta == 0) mbar_arrive(&S.stats_full[kb]);
+    if (ta == 0) mbar_arrive(&S.stats_full()[kb]);
   }
 }
 
@@ -585,23 +575,23 @@ __device__ void group_a(const SampleParams& P, const PipeLayout& L, const PSmem&
 // prefix of w exceeds rem, w = max(p-q, 0) or p (ponly); `take_last` or no
 // such token: the segment's last token with w > 0.  Returns -1 if none.
 template <typename T>
-__device__ int search_segment(const SampleParams& P, const PipeLayout& L, const PSmem& S, int kb, int count,
+__device__ __forceinline__ int search_segment(const SampleParams& P, const PipeLayout& L, const PSmem& S, int kb, int count,
                               const T* gp, const T* gq, bool ponly, int s, double rem, bool take_last, float c,
-                              float alpha, const float* M, const float* inv, int lane) {
+                              float alpha, float Mp, float Mq, float ip, float iq, int lane) {
   constexpr int N = Vec<T>::N;
   constexpr int LT = 4 * N;  // tokens per lane, contiguous
   const int sbase = s * L.seg;
   const int base = sbase + lane * LT;
   uint32_t pm = 0;
   if (count > 0) {
-    S.cmask[lane] = 0u;
+    S.cmask()[lane] = 0u;
     __syncwarp();
-    for (int e = S.segst[kb][s] + lane; e < S.segst[kb][s + 1]; e += 32) {
-      const int o = S.ltok[kb][e] - sbase;
-      atomicOr(&S.cmask[o / LT], 1u << (o % LT));
+    for (int e = S.segst(kb)[s] + lane; e < S.segst(kb)[s + 1]; e += 32) {
+      const int o = S.ltok(kb)[e] - sbase;
+      atomicOr(&S.cmask()[o / LT], 1u << (o % LT));
     }
     __syncwarp();
-    pm = S.cmask[lane];
+    pm = S.cmask()[lane];
   }
   uint4 vp[4], vq[4];
 #pragma unroll
@@ -627,8 +617,8 @@ __device__ int search_segment(const SampleParams& P, const PipeLayout& L, const 
       }
       float v = 0.f;
       if (base + i < P.V) {
-        const float p = prob_of(a, c, M[0], inv[0]);
-        v = ponly ? p : resid_of(p, prob_of(bq, c, M[1], inv[1]));
+        const float p = prob_of(a, c, Mp, ip);
+        v = ponly ? p : resid_of(p, prob_of(bq, c, Mq, iq));
       }
       w[i] = v;
       ls += v;
@@ -742,7 +732,7 @@ __device__ __forceinline__ double owner_search(const float* seg, int n, double u
 
 // ------------------------------------------------------------- group B
 template <typename T>
-__device__ void group_b(const SampleParams& P, const PipeLayout& L, const PSmem& S, int wb, int lane) {
+__device__ __forceinline__ void group_b(const SampleParams& P, const PipeLayout& L, const PSmem& S, int wb, int lane) {
   const int tb = wb * 32 + lane;
   const int SEG = L.seg;
   const int row_bytes = kNB * kPipeSegBytes;
@@ -751,7 +741,7 @@ __device__ void group_b(const SampleParams& P, const PipeLayout& L, const PSmem&
   int k = 0;
   for (int item = blockIdx.x; item < P.n_items; item += gridDim.x, ++k) {
     const int kb = k & 1;
-    const PipeStats& st = S.stats[kb];
+    const PipeStats& st = *S.stats(kb);
     const Item it = decode_item(P, item);
     const Scalars sc = item_scalars(P, it, item);
     int flags = sc.flags;
@@ -769,13 +759,13 @@ __device__ void group_b(const SampleParams& P, const PipeLayout& L, const PSmem&
         if (!it.bonus) u_acc = __ldg(P.uniforms + sc.off + it.i);
       }
     }
-    if (!timeout && !mbar_wait(&S.stats_full[kb], (uint32_t)(k >> 1) & 1u)) timeout = true;
+    if (!timeout && !mbar_wait(&S.stats_full()[kb], (uint32_t)(k >> 1) & 1u)) timeout = true;
     const int count = st.count;
     for (int w = 0; w < kNA; ++w) flags |= st.wflags[w];
     if (count < 0) {
-      if (tb == 0) S.defer[k >> 5] |= 1u << (k & 31);
+      if (tb == 0) S.defer()[k >> 5] |= 1u << (k & 31);
       named_sync(kBarB, kThreadsB);
-      if (tb == 0) mbar_arrive(&S.stats_empty[kb]);
+      if (tb == 0) mbar_arrive(&S.stats_empty()[kb]);
       continue;
     }
 
@@ -783,7 +773,7 @@ __device__ void group_b(const SampleParams& P, const PipeLayout& L, const PSmem&
     float pref[2] = {-INFINITY, -INFINITY}, psum[2] = {0.f, 0.f};
     int lflags = 0;
     for (int e = tb; e < count; e += kThreadsB) {
-      const float zp = S.lzp[kb][e], zq = S.lzq[kb][e];
+      const float zp = S.lzp(kb)[e], zq = S.lzq(kb)[e];
       if (is_bad_logit(zp) || (sc.nrows == 2 && is_bad_logit(zq))) lflags |= kStatusBadLogits;
       online_add(penalize(zp, sc.alpha) * sc.c, pref[0], psum[0]);
       if (sc.nrows == 2) online_add(penalize(zq, sc.alpha) * sc.c, pref[1], psum[1]);
@@ -791,22 +781,23 @@ __device__ void group_b(const SampleParams& P, const PipeLayout& L, const PSmem&
 #pragma unroll
     for (int r = 0; r < 2; ++r) {
       const float2 wv = warp_combine(pref[r], psum[r]);
-      if (lane == 0) S.bred[wb * 2 + r] = wv;
+      if (lane == 0) S.bred()[wb * 2 + r] = wv;
     }
     lflags = warp_or(lflags);
-    if (lane == 0 && lflags) atomicOr(&S.mi[0], lflags);
+    if (lane == 0 && lflags) atomicOr(&S.mi()[0], lflags);
     named_sync(kBarB, kThreadsB);
-    flags |= S.mi[0];
+    flags |= S.mi()[0];
     float M[2], Ssum[2], inv[2];
 #pragma unroll
     for (int r = 0; r < 2; ++r) {
       M[r] = -INFINITY;
       Ssum[r] = 0.f;
       for (int w = 0; w < kNA; ++w) combine_into(st.wp[w][r], M[r], Ssum[r]);
-      for (int w = 0; w < kNB; ++w) combine_into(S.bred[w * 2 + r], M[r], Ssum[r]);
+      for (int w = 0; w < kNB; ++w) combine_into(S.bred()[w * 2 + r], M[r], Ssum[r]);
     }
-    for (int r = 0; r < sc.nrows; ++r)
-      if (!(Ssum[r] > 0.f) || !(Ssum[r] < INFINITY) || !(M[r] < INFINITY)) flags |= kStatusBadLogits;
+#pragma unroll
+    for (int r = 0; r < 2; ++r)
+      if (r < sc.nrows && (!(Ssum[r] > 0.f) || !(Ssum[r] < INFINITY) || !(M[r] < INFINITY))) flags |= kStatusBadLogits;
     const bool ok_stats = !(flags & kStatusBadLogits);
 #pragma unroll
     for (int r = 0; r < 2; ++r) {
@@ -821,7 +812,7 @@ __device__ void group_b(const SampleParams& P, const PipeLayout& L, const PSmem&
       bool xpen = false;
       if (count > 0) {
         const int sx = sc.x / SEG;
-        for (int e = S.segst[kb][sx]; e < S.segst[kb][sx + 1]; ++e) xpen |= S.ltok[kb][e] == sc.x;
+        for (int e = S.segst(kb)[sx]; e < S.segst(kb)[sx + 1]; ++e) xpen |= S.ltok(kb)[e] == sc.x;
       }
       const float zp = xpen ? penalize(xzp, sc.alpha) : xzp;
       const float zq = xpen ? penalize(xzq, sc.alpha) : xzq;
@@ -832,54 +823,54 @@ __device__ void group_b(const SampleParams& P, const PipeLayout& L, const PSmem&
     // residual terms of the penalised tokens, summed per segment in list order
     if (count > 0) {
       for (int e = tb; e < count; e += kThreadsB) {
-        float r = prob_of(penalize(S.lzp[kb][e], sc.alpha), sc.c, M[0], inv[0]);
-        if (sc.nrows == 2) r = resid_of(r, prob_of(penalize(S.lzq[kb][e], sc.alpha), sc.c, M[1], inv[1]));
-        S.lzp[kb][e] = r;
+        float r = prob_of(penalize(S.lzp(kb)[e], sc.alpha), sc.c, M[0], inv[0]);
+        if (sc.nrows == 2) r = resid_of(r, prob_of(penalize(S.lzq(kb)[e], sc.alpha), sc.c, M[1], inv[1]));
+        S.lzp(kb)[e] = r;
       }
       named_sync(kBarB, kThreadsB);
     }
     for (int s = tb; s < L.nseg; s += kThreadsB) {
       float a = 0.f;
       if (count > 0)
-        for (int e = S.segst[kb][s]; e < S.segst[kb][s + 1]; ++e) a += S.lzp[kb][e];
-      S.segc[s] = a;
+        for (int e = S.segst(kb)[s]; e < S.segst(kb)[s + 1]; ++e) a += S.lzp(kb)[e];
+      S.segc()[s] = a;
     }
 
     // ---- pass 2
     for (int stn = 0; stn < L.nst_b; ++stn) {
       const uint32_t slot = rc.slot;
-      if (!timeout && !mbar_wait(&S.full_b[slot], rc.phase)) timeout = true;
+      if (!timeout && !mbar_wait(&S.full_b()[slot], rc.phase)) timeout = true;
       rc.advance(L.slots_b);
       const int s_id = stn * kNB + wb;
       if (s_id < L.nseg) {
-        unsigned char* seg = S.ring_b + (size_t)slot * L.slot_b + wb * kPipeSegBytes;
+        unsigned char* seg = S.ring_b() + (size_t)slot * L.slot_b + wb * kPipeSegBytes;
         const int base = s_id * SEG;
         if (count > 0) {
-          const int e0 = S.segst[kb][s_id], e1 = S.segst[kb][s_id + 1];
+          const int e0 = S.segst(kb)[s_id], e1 = S.segst(kb)[s_id + 1];
           if (e1 > e0)
-            patch_segment<T, false>(seg, seg + row_bytes, sc.nrows == 2, S.ltok[kb], nullptr, nullptr, e0, e1, base,
+            patch_segment<T, false>(seg, seg + row_bytes, sc.nrows == 2, S.ltok(kb), nullptr, nullptr, e0, e1, base,
                                     lane);
         }
         const int nvalid = min(SEG, P.V - base);
         const float v = it.bonus ? seg_resid<T, true>(seg, row_bytes, lane, nvalid, sc.c, M[0], M[1], inv[0], inv[1])
                                  : seg_resid<T, false>(seg, row_bytes, lane, nvalid, sc.c, M[0], M[1], inv[0], inv[1]);
-        S.part[s_id * 32 + lane] = v;
+        S.part()[s_id * 32 + lane] = v;
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(&S.empty_b[slot]);
+      if (lane == 0) mbar_arrive(&S.empty_b()[slot]);
     }
     if (timeout) flags |= kStatusTimeout;
     {
       const int f = warp_or(flags);
-      if (lane == 0 && f) atomicOr(&S.mi[0], f);
+      if (lane == 0 && f) atomicOr(&S.mi()[0], f);
     }
     named_sync(kBarB, kThreadsB);
     for (int s = wb; s < L.nseg; s += kNB) {
-      const float v = warp_sum(S.part[s * 32 + lane]);
-      if (lane == 0) S.segt[s] = v + S.segc[s];
+      const float v = warp_sum(S.part()[s * 32 + lane]);
+      if (lane == 0) S.segt()[s] = v + S.segc()[s];
     }
     named_sync(kBarB, kThreadsB);
-    flags = S.mi[0];
+    flags = S.mi()[0];
 
     // ---- sync 2, decisions, candidate (warp 0 of the group)
     bool deferred = false;
@@ -887,7 +878,7 @@ __device__ void group_b(const SampleParams& P, const PipeLayout& L, const PSmem&
       int ks;
       double rem;
       bool take_last;
-      const double R = owner_search(S.segt, L.nseg, (double)__shfl_sync(0xffffffffu, u_fin, 0), lane, ks, rem,
+      const double R = owner_search(S.segt(), L.nseg, (double)__shfl_sync(0xffffffffu, u_fin, 0), lane, ks, rem,
                                     take_last);
       const double tv = it.bonus ? 0.0 : fmin(R, 1.0);
       double theta = 1.0;
@@ -907,13 +898,13 @@ __device__ void group_b(const SampleParams& P, const PipeLayout& L, const PSmem&
         if (!it.bonus && !(R > 0.0)) {
           deferred = true;  // correction from p: recomputed by the slow path
         } else if (ks >= 0) {
-          cand = search_segment<T>(P, L, S, kb, count, gp, gq, it.bonus, ks, rem, take_last, sc.c, sc.alpha, M, inv,
+          cand = search_segment<T>(P, L, S, kb, count, gp, gq, it.bonus, ks, rem, take_last, sc.c, sc.alpha, M[0], M[1], inv[0], inv[1],
                                    lane);
         }
       }
       if (lane == 0) {
         if (deferred) {
-          S.defer[k >> 5] |= 1u << (k & 31);
+          S.defer()[k >> 5] |= 1u << (k & 31);
         } else if (sample) {
           ItemResult* res = P.results + item;
           res->acc = acc;
@@ -929,15 +920,15 @@ __device__ void group_b(const SampleParams& P, const PipeLayout& L, const PSmem&
           if (P.out_px) P.out_px[item] = bad ? NAN : px;
           if (P.out_qx) P.out_qx[item] = bad ? NAN : qx;
         }
-        S.mi[1] = deferred ? 1 : 0;
+        S.mi()[1] = deferred ? 1 : 0;
       }
     }
     named_sync(kBarB, kThreadsB);
-    deferred = S.mi[1] != 0;
-    if (tb == 0) S.mi[0] = 0;  // every B thread has read it; the next item's bits come after the barriers below
-    if (P.mode == kModeSample && !deferred) finish_item(P, it, item, flags, tb, kBarB, kThreadsB, &S.mi[2]);
+    deferred = S.mi()[1] != 0;
+    if (tb == 0) S.mi()[0] = 0;  // every B thread has read it; the next item's bits come after the barriers below
+    if (P.mode == kModeSample && !deferred) finish_item(P, it, item, flags, tb, kBarB, kThreadsB, &S.mi()[2]);
     named_sync(kBarB, kThreadsB);
-    if (tb == 0) mbar_arrive(&S.stats_empty[kb]);
+    if (tb == 0) mbar_arrive(&S.stats_empty()[kb]);
   }
 }
 
@@ -945,7 +936,7 @@ __device__ void group_b(const SampleParams& P, const PipeLayout& L, const PSmem&
 // One deferred item with all compute warps and direct global loads: the
 // same method in 256-token chunks (penalty from a bitmap).
 template <typename T>
-__device__ void slow_item(const SampleParams& P, const PipeLayout& L, const PSmem& S, int item, int warp, int lane) {
+__device__ __forceinline__ void slow_item(const SampleParams& P, const PipeLayout& L, const PSmem& S, int item, int warp, int lane) {
   constexpr int NW = kNC, NT = kThreadsC;
   const int tid = warp * 32 + lane;
   const Item it = decode_item(P, item);
@@ -954,8 +945,8 @@ __device__ void slow_item(const SampleParams& P, const PipeLayout& L, const PSme
   const int nch = (V + kChunk - 1) / kChunk;
   const T* gp = static_cast<const T*>(P.target) + (size_t)it.tgt_row * P.ld_t;
   const T* gq = it.bonus ? gp : static_cast<const T*>(P.draft) + (size_t)it.dft_row * P.ld_d;
-  if (tid == 0) S.mi[0] = 0;
-  int flags = sc.flags | mark_penalty_set(P, sc, S.bm, tid, NT);
+  if (tid == 0) S.mi()[0] = 0;
+  int flags = sc.flags | mark_penalty_set(P, sc, S.bm(), tid, NT);
   named_sync(kBarC, NT);
 
   // pass 1
@@ -963,9 +954,9 @@ __device__ void slow_item(const SampleParams& P, const PipeLayout& L, const PSme
   bool have_ref = false;
   for (int kk = warp; kk < nch; kk += NW) {
     float z[2][8];
-    global_logits<T>(gp, kk * kChunk, lane, V, S.bm, sc.pen, sc.alpha, z[0]);
+    global_logits<T>(gp, kk * kChunk, lane, V, S.bm(), sc.pen, sc.alpha, z[0]);
     if (sc.nrows == 2) {
-      global_logits<T>(gq, kk * kChunk, lane, V, S.bm, sc.pen, sc.alpha, z[1]);
+      global_logits<T>(gq, kk * kChunk, lane, V, S.bm(), sc.pen, sc.alpha, z[1]);
       chunk_stats_lane<2>(z, sc.c, refc, have_ref, Ssum);
     } else {
       chunk_stats_lane<1>(z, sc.c, refc, have_ref, Ssum);
@@ -975,7 +966,7 @@ __device__ void slow_item(const SampleParams& P, const PipeLayout& L, const PSme
   for (int r = 0; r < 2; ++r) {
     const float ref = have_ref && r < sc.nrows ? refc[r] : -INFINITY;
     const float2 wv = warp_combine(ref, ref > -INFINITY ? Ssum[r] : 0.f);
-    if (lane == 0) S.cwp[warp * 2 + r] = wv;
+    if (lane == 0) S.cwp()[warp * 2 + r] = wv;
   }
   named_sync(kBarC, NT);
   float M[2], Sr[2], inv[2];
@@ -983,10 +974,11 @@ __device__ void slow_item(const SampleParams& P, const PipeLayout& L, const PSme
   for (int r = 0; r < 2; ++r) {
     M[r] = -INFINITY;
     Sr[r] = 0.f;
-    for (int w = 0; w < NW; ++w) combine_into(S.cwp[w * 2 + r], M[r], Sr[r]);
+    for (int w = 0; w < NW; ++w) combine_into(S.cwp()[w * 2 + r], M[r], Sr[r]);
   }
-  for (int r = 0; r < sc.nrows; ++r)
-    if (!(Sr[r] > 0.f) || !(Sr[r] < INFINITY) || !(M[r] < INFINITY)) flags |= kStatusBadLogits;
+#pragma unroll
+  for (int r = 0; r < 2; ++r)
+    if (r < sc.nrows && (!(Sr[r] > 0.f) || !(Sr[r] < INFINITY) || !(M[r] < INFINITY))) flags |= kStatusBadLogits;
   const bool ok_stats = !(flags & kStatusBadLogits);
   RowProb rp[2];
 #pragma unroll
@@ -1002,7 +994,7 @@ __device__ void slow_item(const SampleParams& P, const PipeLayout& L, const PSme
   }
 
   // pass 2 (ponly: chunk sums of p instead of the residual)
-  float* seg = S.part;
+  float* seg = S.part();
   bool ponly = it.bonus;
   double R = 0.0;
   int ks = -1;
@@ -1014,14 +1006,14 @@ __device__ void slow_item(const SampleParams& P, const PipeLayout& L, const PSme
   for (int attempt = 0; attempt < 2; ++attempt) {
     for (int kk = warp; kk < nch; kk += NW) {
       float z[8], pp[8];
-      global_logits<T>(gp, kk * kChunk, lane, V, S.bm, sc.pen, sc.alpha, z);
+      global_logits<T>(gp, kk * kChunk, lane, V, S.bm(), sc.pen, sc.alpha, z);
       probs8<kPZ>(z, 0.f, rp[0], pp);
       float s;
       if (ponly) {
         s = sum8(pp);
       } else {
         float zq[8], qq[8], rr[8];
-        global_logits<T>(gq, kk * kChunk, lane, V, S.bm, sc.pen, sc.alpha, zq);
+        global_logits<T>(gq, kk * kChunk, lane, V, S.bm(), sc.pen, sc.alpha, zq);
         probs8<kPZ>(zq, 0.f, rp[1], qq);
         s = resid8(pp, qq, rr);
       }
@@ -1035,7 +1027,7 @@ __device__ void slow_item(const SampleParams& P, const PipeLayout& L, const PSme
       if (attempt == 0 && lane == 0) {
         if (!it.bonus && sc.x >= 0 && sc.x < V && ok_stats) {
           float zp = to_f32<T>(gp[sc.x]), zq = to_f32<T>(gq[sc.x]);
-          if (sc.pen && ((S.bm[sc.x >> 5] >> (sc.x & 31)) & 1u)) {
+          if (sc.pen && ((S.bm()[sc.x >> 5] >> (sc.x & 31)) & 1u)) {
             zp = penalize(zp, sc.alpha);
             zq = penalize(zq, sc.alpha);
           }
@@ -1049,11 +1041,11 @@ __device__ void slow_item(const SampleParams& P, const PipeLayout& L, const PSme
           const double pi = (1.0 - theta) * (double)px + theta * (double)qx;
           acc = ((double)ua * (double)qx < pi) ? 1 : 0;
         }
-        S.mi[4] = (P.mode == kModeSample && !it.bonus && acc == 0 && !(R > 0.0) && ok_stats) ? 1 : 0;
+        S.mi()[4] = (P.mode == kModeSample && !it.bonus && acc == 0 && !(R > 0.0) && ok_stats) ? 1 : 0;
       }
     }
     named_sync(kBarC, NT);
-    if (attempt == 0 && S.mi[4]) {
+    if (attempt == 0 && S.mi()[4]) {
       ponly = true;  // no residual mass: the correction is drawn from p
       continue;
     }
@@ -1071,14 +1063,14 @@ __device__ void slow_item(const SampleParams& P, const PipeLayout& L, const PSme
       float w[8];
       {
         float zp[8], pp[8];
-        global_logits<T>(gp, ib, lane, V, S.bm, sc.pen, sc.alpha, zp);
+        global_logits<T>(gp, ib, lane, V, S.bm(), sc.pen, sc.alpha, zp);
         probs8<kPZ>(zp, 0.f, rp[0], pp);
         if (ponly) {
 #pragma unroll
           for (int j = 0; j < 8; ++j) w[j] = pp[j];
         } else {
           float zq[8], qq[8];
-          global_logits<T>(gq, ib, lane, V, S.bm, sc.pen, sc.alpha, zq);
+          global_logits<T>(gq, ib, lane, V, S.bm(), sc.pen, sc.alpha, zq);
           probs8<kPZ>(zq, 0.f, rp[1], qq);
           resid8(pp, qq, w);
         }
@@ -1154,20 +1146,20 @@ __device__ void slow_item(const SampleParams& P, const PipeLayout& L, const PSme
   }
   {
     const int f = warp_or(flags);
-    if (lane == 0 && f) atomicOr(&S.mi[0], f);
+    if (lane == 0 && f) atomicOr(&S.mi()[0], f);
   }
   named_sync(kBarC, NT);
-  flags = S.mi[0];
-  if (P.mode == kModeSample) finish_item(P, it, item, flags, tid, kBarC, NT, &S.mi[3]);
+  flags = S.mi()[0];
+  if (P.mode == kModeSample) finish_item(P, it, item, flags, tid, kBarC, NT, &S.mi()[3]);
   // clear the bitmap for the next deferred item
   if (sc.pen) {
     for (int j = sc.h0 + tid; j < sc.h1; j += NT) {
       const int t = __ldg(P.hist + j);
-      if (t >= 0 && t < V) S.bm[t >> 5] = 0u;
+      if (t >= 0 && t < V) S.bm()[t >> 5] = 0u;
     }
     for (int j = tid; j < sc.npre; j += NT) {
       const int t = __ldg(P.draft_tokens + sc.d0 + j);
-      if (t >= 0 && t < V) S.bm[t >> 5] = 0u;
+      if (t >= 0 && t < V) S.bm()[t >> 5] = 0u;
     }
   }
   named_sync(kBarC, NT);
@@ -1176,30 +1168,29 @@ __device__ void slow_item(const SampleParams& P, const PipeLayout& L, const PSme
 // ---------------------------------------------------------------- kernel
 template <typename T>
 __global__ void __launch_bounds__(kPipeThreads, 1) pipe_verify_kernel(const __grid_constant__ SampleParams P) {
-  extern __shared__ __align__(128) unsigned char smem[];
   const PipeLayout& L = P.PL;
-  const PSmem S = carve(smem, L);
+  const PSmem S(L);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int tid = threadIdx.x;
   if (tid == 0) {
     for (int s = 0; s < L.slots_a; ++s) {
-      mbar_init(&S.full_a[s], 1);
-      mbar_init(&S.empty_a[s], kNA);
+      mbar_init(&S.full_a()[s], 1);
+      mbar_init(&S.empty_a()[s], kNA);
     }
     for (int s = 0; s < L.slots_b; ++s) {
-      mbar_init(&S.full_b[s], 1);
-      mbar_init(&S.empty_b[s], kNB);
+      mbar_init(&S.full_b()[s], 1);
+      mbar_init(&S.empty_b()[s], kNB);
     }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&S.stats_full[i], 1);
-      mbar_init(&S.stats_empty[i], 2);
+      mbar_init(&S.stats_full()[i], 1);
+      mbar_init(&S.stats_empty()[i], 2);
     }
     fence_mbar_init();
   }
-  for (int w = tid; w < L.bm_words; w += kPipeThreads) S.bm[w] = 0u;
-  for (int w = tid; w < kPipeMaxIters / 32; w += kPipeThreads) S.defer[w] = 0u;
-  if (tid < 16) S.mi[tid] = 0;
+  for (int w = tid; w < L.bm_words; w += kPipeThreads) S.bm()[w] = 0u;
+  for (int w = tid; w < kPipeMaxIters / 32; w += kPipeThreads) S.defer()[w] = 0u;
+  if (tid < 16) S.mi()[tid] = 0;
   __syncthreads();
 
   if (warp < kNA) {
@@ -1217,7 +1208,7 @@ __global__ void __launch_bounds__(kPipeThreads, 1) pipe_verify_kernel(const __gr
   named_sync(kBarC, kThreadsC);
   int k = 0;
   for (int item = blockIdx.x; item < P.n_items; item += gridDim.x, ++k)
-    if ((S.defer[k >> 5] >> (k & 31)) & 1u) slow_item<T>(P, L, S, item, warp, lane);
+    if ((S.defer()[k >> 5] >> (k & 31)) & 1u) slow_item<T>(P, L, S, item, warp, lane);
 }
 
 }  // namespace
