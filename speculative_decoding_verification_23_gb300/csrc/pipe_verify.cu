@@ -65,7 +65,12 @@ struct PSmem {
   __device__ __forceinline__ float* part() const { return reinterpret_cast<float*>(at(L.off_part)); }
   // [nseg] segment residual mass and the penalised tokens' share of it
   __device__ __forceinline__ float* segt() const { return reinterpret_cast<float*>(at(L.off_segt)); }
-  __device__ __forceinline__ float* segc() const { return reinterpret_cast<float*>(at(L.off_segc)); }
+  // [2][nseg] per item buffer
+  __device__ __forceinline__ float* segc(int kb) const {
+    return reinterpret_cast<float*>(at(L.off_segc + kb * align_up_i(L.nseg * 4, 16)));
+  }
+  // cu_draft copy (when B + 1 <= kPipeCuCap)
+  __device__ __forceinline__ int* cu() const { return reinterpret_cast<int*>(at(L.off_cu)); }
   // item buffer kb: sorted penalised tokens, their raw target logits (later
   // their residual terms), their raw draft logits, and segment offsets
   __device__ __forceinline__ int* ltok(int kb) const {
@@ -375,6 +380,42 @@ __device__ __forceinline__ void finish_item(const SampleParams& P, const Item& i
   }
 }
 
+// cu_draft as the kernel reads it: the shared-memory copy when it fits.
+__device__ __forceinline__ const int* cu_ptr(const SampleParams& P, const PSmem& S) {
+  return P.B + 1 <= kPipeCuCap ? S.cu() : P.cu_draft;
+}
+
+// The work item's request, position and rows (the same decoding as
+// decode_item, reading cu_draft through `cu`).
+__device__ __forceinline__ Item pdecode(const SampleParams& P, const int* cu, int item) {
+  Item it;
+  if (item < P.total) {
+    int lo = 0, hi = P.B;
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (cu[mid] <= item) lo = mid;
+      else hi = mid;
+    }
+    it.b = lo;
+    it.i = item - cu[lo];
+    it.bonus = false;
+    it.tgt_row = item + lo;
+    it.dft_row = item;
+    it.rows_ok = true;
+  } else {
+    const int b = item - P.total;
+    const int c0 = cu[b], c1 = cu[b + 1];
+    it.b = b;
+    it.i = c1 - c0;
+    it.bonus = true;
+    it.rows_ok = (c0 >= 0 && c0 <= c1 && c1 <= P.total);
+    it.tgt_row = it.rows_ok ? c1 + b : b;
+    it.dft_row = -1;
+  }
+  it.K = cu[it.b + 1] - cu[it.b];
+  return it;
+}
+
 // Per-request scalars and the status bits that follow from them.
 struct Scalars {
   int b, K, d0, off, nrows, x, flags;
@@ -383,11 +424,11 @@ struct Scalars {
   int h0, h1, npre;
 };
 
-__device__ __forceinline__ Scalars item_scalars(const SampleParams& P, const Item& it, int item) {
+__device__ __forceinline__ Scalars item_scalars(const SampleParams& P, const Item& it, int item, const int* cu) {
   Scalars s;
   s.b = it.b;
   s.K = it.K;
-  s.d0 = __ldg(P.cu_draft + it.b);
+  s.d0 = cu[it.b];
   s.off = s.d0 + it.b;
   s.nrows = it.bonus ? 1 : 2;
   s.flags = 0;
@@ -441,8 +482,9 @@ __device__ __forceinline__ void producer(const SampleParams& P, const PipeLayout
   RingCursor rc;
   bool to = false;
   int k = 0;
+  const int* cu = cu_ptr(P, S);
   for (int item = blockIdx.x; item < P.n_items; item += gridDim.x, ++k) {
-    const Item it = decode_item(P, item);
+    const Item it = pdecode(P, cu, item);
     if (!IS_A) {
       // pass 2 of item k starts once group A has finished its pass 1 (the
       // rows are then in L2); a deferred item is not streamed again
@@ -471,23 +513,28 @@ __device__ __forceinline__ void producer(const SampleParams& P, const PipeLayout
 }
 
 // ------------------------------------------------------------- group A
+// Per item: penalty set -> sorted list, pass 1 over the ring, then the
+// softmax combine with the penalised tokens' exact terms, p(x), q(x) and the
+// penalised tokens' residual mass per segment; all handed to group B.
 template <typename T>
 __device__ __forceinline__ void group_a(const SampleParams& P, const PipeLayout& L, const PSmem& S, int wa, int lane) {
   const int ta = wa * 32 + lane;
   const int SEG = L.seg;
   const int wps = SEG / 32;  // bitmap words per segment
   const int row_bytes = kNA * kPipeSegBytes;
+  const int* cu = cu_ptr(P, S);
   RingCursor rc;
   bool timeout = false;
   int k = 0;
   for (int item = blockIdx.x; item < P.n_items; item += gridDim.x, ++k) {
     const int kb = k & 1;
     PipeStats& st = *S.stats(kb);
+    const Item it = pdecode(P, cu, item);
+    const Scalars sc = item_scalars(P, it, item, cu);
+    // the bitmap is group A's own: mark the set before waiting for buffer kb
+    int flags = sc.flags | mark_penalty_set(P, sc, S.bm(), ta, kThreadsA);
     // buffer kb is free once group B and producer B are done with item k-2
     if (!timeout && !mbar_wait(&S.stats_empty()[kb], ((uint32_t)(k >> 1) & 1u) ^ 1u)) timeout = true;
-    const Item it = decode_item(P, item);
-    const Scalars sc = item_scalars(P, it, item);
-    int flags = mark_penalty_set(P, sc, S.bm(), ta, kThreadsA);
 
     // ---- sorted penalty list with per-segment offsets; clears the bitmap
     int count = 0;
@@ -542,6 +589,14 @@ __device__ __forceinline__ void group_a(const SampleParams& P, const PipeLayout&
       if (!skip && s_id < L.nseg) {
         unsigned char* seg = S.ring_a() + (size_t)slot * L.slot_a + wa * kPipeSegBytes;
         const int base = s_id * SEG;
+        if (sc.x >= base && sc.x < base + SEG) {
+          // the draft token's raw logits, before any patch
+          if (lane == 0) {
+            st.xz[0] = to_f32<T>(reinterpret_cast<const T*>(seg)[sc.x - base]);
+            st.xz[1] = to_f32<T>(reinterpret_cast<const T*>(seg + row_bytes)[sc.x - base]);
+          }
+          __syncwarp();
+        }
         if (count > 0) {
           const int e0 = S.segst(kb)[s_id], e1 = S.segst(kb)[s_id + 1];
           if (e1 > e0)
@@ -556,16 +611,86 @@ __device__ __forceinline__ void group_a(const SampleParams& P, const PipeLayout&
       if (lane == 0) mbar_arrive(&S.empty_a()[slot]);
     }
 
-    // ---- hand-off to group B
+    // ---- softmax combine: the pass's lanes, then the penalised tokens
     if (timeout) flags |= kStatusTimeout;
+    if (count > 0) named_sync(kBarA, kThreadsA);  // every warp's captured list values are in place
+    float pref[2] = {-INFINITY, -INFINITY}, psum[2] = {0.f, 0.f};
+    for (int e = ta; e < count; e += kThreadsA) {
+      const float zp = S.lzp(kb)[e], zq = S.lzq(kb)[e];
+      if (is_bad_logit(zp) || (sc.nrows == 2 && is_bad_logit(zq))) flags |= kStatusBadLogits;
+      online_add(penalize(zp, sc.alpha) * sc.c, pref[0], psum[0]);
+      if (sc.nrows == 2) online_add(penalize(zq, sc.alpha) * sc.c, pref[1], psum[1]);
+    }
 #pragma unroll
     for (int r = 0; r < 2; ++r) {
       const float2 wv = warp_combine(ref[r], run[r]);
-      if (lane == 0) st.wp[wa][r] = wv;
+      const float2 pv = warp_combine(pref[r], psum[r]);
+      if (lane == 0) {
+        st.wp[wa][r] = wv;
+        S.bred()[wa * 2 + r] = pv;
+      }
     }
     flags = warp_or(flags);
-    if (lane == 0) st.wflags[wa] = flags;
-    if (ta == 0) st.count = count;
+    if (lane == 0) S.scan()[kNA + wa] = flags;
+    named_sync(kBarA, kThreadsA);
+    flags = 0;
+    for (int w = 0; w < kNA; ++w) flags |= S.scan()[kNA + w];
+    float M[2], Ssum[2], inv[2];
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      M[r] = -INFINITY;
+      Ssum[r] = 0.f;
+      for (int w = 0; w < kNA; ++w) combine_into(st.wp[w][r], M[r], Ssum[r]);
+      for (int w = 0; w < kNA; ++w) combine_into(S.bred()[w * 2 + r], M[r], Ssum[r]);
+    }
+#pragma unroll
+    for (int r = 0; r < 2; ++r)
+      if (r < sc.nrows && (!(Ssum[r] > 0.f) || !(Ssum[r] < INFINITY) || !(M[r] < INFINITY))) flags |= kStatusBadLogits;
+    const bool ok_stats = !(flags & kStatusBadLogits);
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      const bool use = ok_stats && r < sc.nrows;
+      inv[r] = use ? __fdiv_rn(1.f, Ssum[r]) : 1.f;
+      if (!use) M[r] = 0.f;
+    }
+    // residual terms of the penalised tokens, summed per segment in list order
+    if (count > 0) {
+      for (int e = ta; e < count; e += kThreadsA) {
+        float r = prob_of(penalize(S.lzp(kb)[e], sc.alpha), sc.c, M[0], inv[0]);
+        if (sc.nrows == 2) r = resid_of(r, prob_of(penalize(S.lzq(kb)[e], sc.alpha), sc.c, M[1], inv[1]));
+        S.lzp(kb)[e] = r;
+      }
+      named_sync(kBarA, kThreadsA);
+    }
+    for (int s = ta; s < L.nseg; s += kThreadsA) {
+      float a = 0.f;
+      if (count > 0)
+        for (int e = S.segst(kb)[s]; e < S.segst(kb)[s + 1]; ++e) a += S.lzp(kb)[e];
+      S.segc(kb)[s] = a;
+    }
+    if (ta == 0) {
+      // p(x), q(x) (x may be penalised itself)
+      float px = 0.f, qx = 0.f;
+      if (!it.bonus && sc.x >= 0 && sc.x < P.V && ok_stats && !skip) {
+        bool xpen = false;
+        if (count > 0) {
+          const int sx = sc.x / SEG;
+          for (int e = S.segst(kb)[sx]; e < S.segst(kb)[sx + 1]; ++e) xpen |= S.ltok(kb)[e] == sc.x;
+        }
+        const float zp = xpen ? penalize(st.xz[0], sc.alpha) : st.xz[0];
+        const float zq = xpen ? penalize(st.xz[1], sc.alpha) : st.xz[1];
+        px = prob_of(zp, sc.c, M[0], inv[0]);
+        qx = prob_of(zq, sc.c, M[1], inv[1]);
+      }
+      st.M[0] = M[0];
+      st.M[1] = M[1];
+      st.inv[0] = inv[0];
+      st.inv[1] = inv[1];
+      st.px = px;
+      st.qx = qx;
+      st.flags = flags;
+      st.count = count;
+    }
     named_sync(kBarA, kThreadsA);
     if (ta == 0) mbar_arrive(&S.stats_full()[kb]);
   }
@@ -731,110 +856,41 @@ __device__ __forceinline__ double owner_search(const float* seg, int n, double u
 }
 
 // ------------------------------------------------------------- group B
+// Per item: pass 2 over the ring with group A's normalisers, the residual
+// mass per segment, the prefix over segments, the decisions, the candidate
+// and the request's finalisation.
 template <typename T>
 __device__ __forceinline__ void group_b(const SampleParams& P, const PipeLayout& L, const PSmem& S, int wb, int lane) {
   const int tb = wb * 32 + lane;
   const int SEG = L.seg;
   const int row_bytes = kNB * kPipeSegBytes;
+  const int* cu = cu_ptr(P, S);
   RingCursor rc;
   bool timeout = false;
   int k = 0;
   for (int item = blockIdx.x; item < P.n_items; item += gridDim.x, ++k) {
     const int kb = k & 1;
     const PipeStats& st = *S.stats(kb);
-    const Item it = decode_item(P, item);
-    const Scalars sc = item_scalars(P, it, item);
-    int flags = sc.flags;
+    const Item it = pdecode(P, cu, item);
+    const Scalars sc = item_scalars(P, it, item, cu);
     const T* gp = static_cast<const T*>(P.target) + (size_t)it.tgt_row * P.ld_t;
     const T* gq = it.bonus ? gp : static_cast<const T*>(P.draft) + (size_t)it.dft_row * P.ld_d;
-    // loads the decisions need, issued early
-    float xzp = 0.f, xzq = 0.f, u_acc = 0.f, u_fin = 0.f;
-    if (tb == 0) {
-      if (sc.x >= 0 && sc.x < P.V) {
-        xzp = to_f32<T>(gp[sc.x]);
-        xzq = to_f32<T>(gq[sc.x]);
-      }
-      if (P.mode == kModeSample && sc.uniforms_ok) {
-        u_fin = __ldg(P.uniforms + sc.off + sc.K);
-        if (!it.bonus) u_acc = __ldg(P.uniforms + sc.off + it.i);
-      }
+    float u_acc = 0.f, u_fin = 0.f;
+    if (tb == 0 && P.mode == kModeSample && sc.uniforms_ok) {
+      u_fin = __ldg(P.uniforms + sc.off + sc.K);
+      if (!it.bonus) u_acc = __ldg(P.uniforms + sc.off + it.i);
     }
     if (!timeout && !mbar_wait(&S.stats_full()[kb], (uint32_t)(k >> 1) & 1u)) timeout = true;
     const int count = st.count;
-    for (int w = 0; w < kNA; ++w) flags |= st.wflags[w];
+    int flags = st.flags;
     if (count < 0) {
       if (tb == 0) S.defer()[k >> 5] |= 1u << (k & 31);
       named_sync(kBarB, kThreadsB);
       if (tb == 0) mbar_arrive(&S.stats_empty()[kb]);
       continue;
     }
-
-    // ---- sync 1: penalised tokens' softmax terms, then (M, S) per row
-    float pref[2] = {-INFINITY, -INFINITY}, psum[2] = {0.f, 0.f};
-    int lflags = 0;
-    for (int e = tb; e < count; e += kThreadsB) {
-      const float zp = S.lzp(kb)[e], zq = S.lzq(kb)[e];
-      if (is_bad_logit(zp) || (sc.nrows == 2 && is_bad_logit(zq))) lflags |= kStatusBadLogits;
-      online_add(penalize(zp, sc.alpha) * sc.c, pref[0], psum[0]);
-      if (sc.nrows == 2) online_add(penalize(zq, sc.alpha) * sc.c, pref[1], psum[1]);
-    }
-#pragma unroll
-    for (int r = 0; r < 2; ++r) {
-      const float2 wv = warp_combine(pref[r], psum[r]);
-      if (lane == 0) S.bred()[wb * 2 + r] = wv;
-    }
-    lflags = warp_or(lflags);
-    if (lane == 0 && lflags) atomicOr(&S.mi()[0], lflags);
-    named_sync(kBarB, kThreadsB);
-    flags |= S.mi()[0];
-    float M[2], Ssum[2], inv[2];
-#pragma unroll
-    for (int r = 0; r < 2; ++r) {
-      M[r] = -INFINITY;
-      Ssum[r] = 0.f;
-      for (int w = 0; w < kNA; ++w) combine_into(st.wp[w][r], M[r], Ssum[r]);
-      for (int w = 0; w < kNB; ++w) combine_into(S.bred()[w * 2 + r], M[r], Ssum[r]);
-    }
-#pragma unroll
-    for (int r = 0; r < 2; ++r)
-      if (r < sc.nrows && (!(Ssum[r] > 0.f) || !(Ssum[r] < INFINITY) || !(M[r] < INFINITY))) flags |= kStatusBadLogits;
-    const bool ok_stats = !(flags & kStatusBadLogits);
-#pragma unroll
-    for (int r = 0; r < 2; ++r) {
-      const bool use = ok_stats && r < sc.nrows;
-      inv[r] = use ? __fdiv_rn(1.f, Ssum[r]) : 1.f;
-      if (!use) M[r] = 0.f;
-    }
-
-    // p(x), q(x) (one thread; x may be penalised itself)
-    float px = 0.f, qx = 0.f;
-    if (tb == 0 && !it.bonus && sc.x >= 0 && sc.x < P.V && ok_stats) {
-      bool xpen = false;
-      if (count > 0) {
-        const int sx = sc.x / SEG;
-        for (int e = S.segst(kb)[sx]; e < S.segst(kb)[sx + 1]; ++e) xpen |= S.ltok(kb)[e] == sc.x;
-      }
-      const float zp = xpen ? penalize(xzp, sc.alpha) : xzp;
-      const float zq = xpen ? penalize(xzq, sc.alpha) : xzq;
-      px = prob_of(zp, sc.c, M[0], inv[0]);
-      qx = prob_of(zq, sc.c, M[1], inv[1]);
-    }
-
-    // residual terms of the penalised tokens, summed per segment in list order
-    if (count > 0) {
-      for (int e = tb; e < count; e += kThreadsB) {
-        float r = prob_of(penalize(S.lzp(kb)[e], sc.alpha), sc.c, M[0], inv[0]);
-        if (sc.nrows == 2) r = resid_of(r, prob_of(penalize(S.lzq(kb)[e], sc.alpha), sc.c, M[1], inv[1]));
-        S.lzp(kb)[e] = r;
-      }
-      named_sync(kBarB, kThreadsB);
-    }
-    for (int s = tb; s < L.nseg; s += kThreadsB) {
-      float a = 0.f;
-      if (count > 0)
-        for (int e = S.segst(kb)[s]; e < S.segst(kb)[s + 1]; ++e) a += S.lzp(kb)[e];
-      S.segc()[s] = a;
-    }
+    const float Mp = st.M[0], Mq = st.M[1], ip = st.inv[0], iq = st.inv[1];
+    const float px = st.px, qx = st.qx;
 
     // ---- pass 2
     for (int stn = 0; stn < L.nst_b; ++stn) {
@@ -852,8 +908,8 @@ __device__ __forceinline__ void group_b(const SampleParams& P, const PipeLayout&
                                     lane);
         }
         const int nvalid = min(SEG, P.V - base);
-        const float v = it.bonus ? seg_resid<T, true>(seg, row_bytes, lane, nvalid, sc.c, M[0], M[1], inv[0], inv[1])
-                                 : seg_resid<T, false>(seg, row_bytes, lane, nvalid, sc.c, M[0], M[1], inv[0], inv[1]);
+        const float v = it.bonus ? seg_resid<T, true>(seg, row_bytes, lane, nvalid, sc.c, Mp, Mq, ip, iq)
+                                 : seg_resid<T, false>(seg, row_bytes, lane, nvalid, sc.c, Mp, Mq, ip, iq);
         S.part()[s_id * 32 + lane] = v;
       }
       __syncwarp();
@@ -867,7 +923,7 @@ __device__ __forceinline__ void group_b(const SampleParams& P, const PipeLayout&
     named_sync(kBarB, kThreadsB);
     for (int s = wb; s < L.nseg; s += kNB) {
       const float v = warp_sum(S.part()[s * 32 + lane]);
-      if (lane == 0) S.segt()[s] = v + S.segc()[s];
+      if (lane == 0) S.segt()[s] = v + S.segc(kb)[s];
     }
     named_sync(kBarB, kThreadsB);
     flags = S.mi()[0];
@@ -884,7 +940,7 @@ __device__ __forceinline__ void group_b(const SampleParams& P, const PipeLayout&
       double theta = 1.0;
       int acc = 1;
       if (lane == 0) {
-        if (tv > (double)sc.D) theta = (double)sc.D / tv;
+        if (tv > (double)sc.D) theta = (double)__fdiv_rn(sc.D, (float)tv);
         if (!it.bonus) {
           const double pi = (1.0 - theta) * (double)px + theta * (double)qx;
           acc = ((double)u_acc * (double)qx < pi) ? 1 : 0;
@@ -898,8 +954,7 @@ __device__ __forceinline__ void group_b(const SampleParams& P, const PipeLayout&
         if (!it.bonus && !(R > 0.0)) {
           deferred = true;  // correction from p: recomputed by the slow path
         } else if (ks >= 0) {
-          cand = search_segment<T>(P, L, S, kb, count, gp, gq, it.bonus, ks, rem, take_last, sc.c, sc.alpha, M[0], M[1], inv[0], inv[1],
-                                   lane);
+          cand = search_segment<T>(P, L, S, kb, count, gp, gq, it.bonus, ks, rem, take_last, sc.c, sc.alpha, Mp, Mq, ip, iq, lane);
         }
       }
       if (lane == 0) {
@@ -939,8 +994,9 @@ template <typename T>
 __device__ __forceinline__ void slow_item(const SampleParams& P, const PipeLayout& L, const PSmem& S, int item, int warp, int lane) {
   constexpr int NW = kNC, NT = kThreadsC;
   const int tid = warp * 32 + lane;
-  const Item it = decode_item(P, item);
-  const Scalars sc = item_scalars(P, it, item);
+  const int* cu = cu_ptr(P, S);
+  const Item it = pdecode(P, cu, item);
+  const Scalars sc = item_scalars(P, it, item, cu);
   const int V = P.V;
   const int nch = (V + kChunk - 1) / kChunk;
   const T* gp = static_cast<const T*>(P.target) + (size_t)it.tgt_row * P.ld_t;
@@ -1190,6 +1246,8 @@ __global__ void __launch_bounds__(kPipeThreads, 1) pipe_verify_kernel(const __gr
   }
   for (int w = tid; w < L.bm_words; w += kPipeThreads) S.bm()[w] = 0u;
   for (int w = tid; w < kPipeMaxIters / 32; w += kPipeThreads) S.defer()[w] = 0u;
+  if (P.B + 1 <= kPipeCuCap)
+    for (int i = tid; i <= P.B; i += kPipeThreads) S.cu()[i] = __ldg(P.cu_draft + i);
   if (tid < 16) S.mi()[tid] = 0;
   __syncthreads();
 

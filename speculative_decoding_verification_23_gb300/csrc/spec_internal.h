@@ -113,15 +113,18 @@ inline SmemLayout make_stream_layout(int V, int C, int elem_bytes, bool topp, in
 constexpr int kPipeWarpsA = 8;
 constexpr int kPipeWarpsB = 8;
 constexpr int kPipeSegBytes = 2048;   // one row's bytes per warp per stage (64 per lane)
-constexpr int kPipeListCap = 1024;    // distinct penalised tokens per item the pipeline handles
+constexpr int kPipeListCap = 768;     // distinct penalised tokens per item the pipeline handles
+constexpr int kPipeCuCap = 1024;      // cu_draft entries cached in shared memory (B + 1 <= this)
 constexpr int kPipeMaxIters = 8192;   // items per CTA (deferred-item bits)
 
 // Pass-1 result of one item, handed from group A to group B.
 struct PipeStats {
-  float2 wp[kPipeWarpsA][2];  // per A warp and row: (reference, sum)
-  int wflags[kPipeWarpsA];    // status bits found by each A warp
+  float2 wp[kPipeWarpsA][2];  // per A warp and row: (reference, sum) of the pass
+  float M[2], inv[2];         // per row: reference and 1 / softmax sum (units of z'c)
+  float px, qx;               // p(x), q(x) of the draft token
+  float xz[2];                // raw logits of the draft token (captured from the ring)
+  int flags;                  // status bits of the item so far
   int count;                  // penalised-token list length; -1 = too many (item deferred)
-  int pad[3];
 };
 
 struct PipeLayout {
@@ -132,7 +135,7 @@ struct PipeLayout {
   int slot_a, slot_b;   // bytes per ring slot
   int bm_words;         // bitmap words (nseg * seg / 32)
   int off_ring_a, off_ring_b, off_bm, off_part, off_segt, off_segc, off_list, off_segst, off_stats, off_misc,
-      off_defer, off_bar;
+      off_defer, off_cu, off_bar;
   int total;
 };
 
@@ -153,12 +156,13 @@ inline PipeLayout make_pipe_layout(int V, int elem_bytes, int slots_a, int slots
   L.off_bm = off;      off += align_up_i(L.bm_words * 4, 16);
   L.off_part = off;    off += L.nseg * 32 * 4;
   L.off_segt = off;    off += align_up_i(L.nseg * 4, 16);
-  L.off_segc = off;    off += align_up_i(L.nseg * 4, 16);
+  L.off_segc = off;    off += 2 * align_up_i(L.nseg * 4, 16);
   L.off_list = off;    off += 2 * kPipeListCap * 12;
   L.off_segst = off;   off += 2 * align_up_i((L.nseg + 1) * 4, 16);
   L.off_stats = off;   off += 2 * (int)sizeof(PipeStats);
   L.off_misc = off;    off += 1024;
   L.off_defer = off;   off += kPipeMaxIters / 8;
+  L.off_cu = off;      off += kPipeCuCap * 4;
   L.off_bar = off;     off += (2 * slots_a + 2 * slots_b + 4) * 8;
   L.total = align_up_i(off, 128);
   return L;
