@@ -1273,8 +1273,8 @@ __global__ void __launch_bounds__(kPipeThreads, 1) pipe_verify_kernel(const __gr
 
 // Layout for the pipelined kernel (-1 if it does not fit `max_smem`).
 int choose_pipe_layout(int V, int elem_bytes, int max_smem, PipeLayout* out) {
-  for (int slots_a = 3; slots_a >= 2; --slots_a) {
-    const PipeLayout L = make_pipe_layout(V, elem_bytes, slots_a, 2);
+  for (int slots_a = kPipeSlotsA; slots_a >= 2; --slots_a) {
+    const PipeLayout L = make_pipe_layout(V, elem_bytes, slots_a, kPipeSlotsB);
     if (L.total <= max_smem) {
       *out = L;
       return 0;

@@ -116,6 +116,8 @@ constexpr int kPipeSegBytes = 2048;   // one row's bytes per warp per stage (64 
 constexpr int kPipeListCap = 768;     // distinct penalised tokens per item the pipeline handles
 constexpr int kPipeCuCap = 1024;      // cu_draft entries cached in shared memory (B + 1 <= this)
 constexpr int kPipeMaxIters = 8192;   // items per CTA (deferred-item bits)
+constexpr int kPipeSlotsA = 3;        // ring slots of group A (HBM stream) ...
+constexpr int kPipeSlotsB = 2;        // ... and of group B (L2 re-read)
 
 // Pass-1 result of one item, handed from group A to group B.
 struct PipeStats {

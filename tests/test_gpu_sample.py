@@ -223,3 +223,63 @@ def test_chi_square_first_token_on_gpu(V, D, variant):
     ref = PR.oracle_sample(batch, range(200))
     bad, _ = PR.compare_sample(batch, (tok, acc, st), ref, range(200))
     assert not bad
+
+
+# ---------------------------------------------------------------- rare paths
+# (the streaming kernel hands these items to its slow path; the resident
+# kernel computes them in its ordinary flow)
+
+@VARIANTS
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_long_history_penalty(dtype, variant):
+    """Requests whose penalty set (history plus preceding drafts) is larger
+    than the streaming kernel's in-pipeline list, mixed with short ones."""
+    batch = W.make_batch(B=4, V=50000, K=[3, 5, 0, 2], dtype=dtype, seed=71, rho=0.9, temperature=0.8,
+                         rep_penalty=[1.3, 1.1, 1.2, 0.9], hist_len=2000, tv_budget=[0.0, 0.3, 0.6, 1.0])
+    # shorten two requests' histories so that one batch mixes both kinds
+    lens = [2000, 40, 2000, 16]
+    hist = [batch.hist[i * 2000:i * 2000 + n] for i, n in enumerate(lens)]
+    batch.hist = np.concatenate(hist).astype(np.int32)
+    batch.cu_hist = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    _check(batch, flags=variant)
+    ref = PR.oracle_sample(batch)
+    tvg = PR.run_tv(batch, flags=variant)
+    assert PR.compare_tv(batch, tvg, ref) < PR.TOL_PROB
+
+
+@VARIANTS
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_zero_residual_correction_from_p(dtype, variant):
+    """Draft rows equal to the target rows, and the drafted token has zero
+    probability under both: the draft is rejected, the residual mass is 0 and
+    the correction is drawn from p."""
+    batch = W.make_batch(B=3, V=3000, K=[2, 3, 1], dtype=dtype, seed=72, rho=0.8, temperature=0.9,
+                         rep_penalty=1.0, tv_budget=[0.0, 0.4, 1.0])
+    for b in range(batch.B):
+        d0, d1 = int(batch.cu_draft[b]), int(batch.cu_draft[b + 1])
+        off = d0 + b
+        batch.draft[d0:d1] = batch.target[off:off + (d1 - d0)]
+        # position 0 of every request drafts a token with -inf logits in both rows
+        x = int(batch.draft_tokens[d0])
+        batch.target[off, x] = -np.inf
+        batch.draft[d0, x] = -np.inf
+    got, ref = _check(batch, flags=variant)
+    tok, acc, st = got
+    assert np.all(st == 0) and list(acc) == [0, 0, 0]
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_many_requests_streaming(dtype):
+    """B = 1100 requests (more than the streaming kernel caches in shared
+    memory), K in 0..2, small V: parity on a sample, properties on all."""
+    rng = np.random.default_rng(73)
+    K = rng.integers(0, 3, size=1100)
+    batch = W.make_batch(B=1100, V=700, K=K, dtype=dtype, seed=73, rho=0.8, temperature=0.9, rep_penalty=1.1,
+                         hist_len=6, tv_budget=0.5)
+    got = PR.run_sample(batch, flags=STREAMING)
+    sample = list(range(0, 1100, 37))
+    ref = PR.oracle_sample(batch, sample)
+    bad, near = PR.compare_sample(batch, got, ref, sample)
+    assert not bad and near <= 1, (bad[:2], near)
+    tok, acc, st = got
+    assert np.all(st == 0) and np.all((acc >= 0) & (acc <= K))
