@@ -182,6 +182,24 @@ def oracle_baseline(batch, budget_s: float):
     return n / dt, n, dt
 
 
+def reduce_max(x: float, dist, device) -> float:
+    """The largest value of `x` over all ranks (the job takes as long as its
+    slowest rank); `x` itself without a process group."""
+    if dist is None:
+        return float(x)
+    import torch
+
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(units_per_rank: int, world: int, steps: int, elapsed_max: float) -> float:
+    """Whole-job units per second: every rank processes `units_per_rank` per
+    step (weak scaling), the job lasts the slowest rank's time."""
+    return world * units_per_rank * steps / elapsed_max
+
+
 def make_workload(rank: int):
     from speculative_decoding_verification_23_gb300 import workload as W
 
@@ -255,14 +273,11 @@ def bench_gpu(args, rank, world, dist):
             ev[k][1].record(stream)
         t_end.record(stream)
         torch.cuda.synchronize()
-    elapsed = t_start.elapsed_time(t_end) / 1000.0
+    elapsed = reduce_max(t_start.elapsed_time(t_end) / 1000.0, dist, dev)
     per_launch = [a.elapsed_time(b) / 1000.0 for a, b in ev]
     if dist:
-        t = torch.tensor([elapsed], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed = float(t.item())
         dist.barrier()
-    value = world * batch.B * args.steps / elapsed
+    value = job_throughput(batch.B, world, args.steps, elapsed)
     ms = 1000.0 * elapsed / args.steps
 
     # ---- end to end: pinned host inputs -> device -> call -> tokens back
@@ -301,12 +316,7 @@ def bench_gpu(args, rank, world, dist):
         e2e_step()
     b.record(stream)
     torch.cuda.synchronize()
-    e2e_s = a.elapsed_time(b) / 1000.0
-    e2e_value = world * batch.B * e_steps / e2e_s
-    if dist:
-        t = torch.tensor([e2e_s], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_value = world * batch.B * e_steps / float(t.item())
+    e2e_value = job_throughput(batch.B, world, e_steps, reduce_max(a.elapsed_time(b) / 1000.0, dist, dev))
 
     # ---- roofline of the sampling kernel (one launch per step)
     peak, peak_kind = measured_peak()
