@@ -346,12 +346,98 @@ def bench_gpu(args, rank, world, dist):
         "gpu_launches": args.steps,
         "clocks": clk.summary(),
     }
+    if rank == 0 and args.extras:
+        line["extras"] = bench_extras(dev, peak, args.cpu_seconds)
     if rank == 0 and not args.no_cpu_baseline:
         v, n, dt = oracle_baseline(batch, args.cpu_seconds)
         line["cpu_baseline"] = {"value": v, "unit": "requests/s", "cores": 1, "kind": "oracle",
                                 "sample": f"{n} whole requests cycled through the B=64 batch ({dt:.1f} s, one thread)"}
     if rank == 0:
         print(json.dumps(line), flush=True)
+
+
+def bench_extras(dev, peak: float, cpu_seconds: float) -> dict:
+    """The other configurations and entry points, one call at a time with
+    L2 flushed before each (a 256 MB write), CUDA events around the call:
+    the Qwen2.5-shaped single request (B=1, K=8, resident cluster kernel),
+    greedy verification (B=1, K in 1/2/4/8), the ragged top-p batch (B=256,
+    fp32, cluster kernel with top-p) and spec_tv_budget on the batched
+    workload.  Each with algorithmic bytes, achieved GB/s against the
+    measured peak, and the oracle's requests/s on a bounded sample."""
+    import torch
+
+    import oracle
+    import speculative_decoding_verification_23_gb300 as sv
+    from speculative_decoding_verification_23_gb300 import workload as W
+    from speculative_decoding_verification_23_gb300.device_batch import to_device
+
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def timed(call, iters=20):
+        for _ in range(3):
+            call()
+        ts = []
+        for _ in range(iters):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            call()
+            b.record(stream)
+            b.synchronize()
+            ts.append(a.elapsed_time(b) / 1000.0)
+        return float(np.median(ts))
+
+    def oracle_rate(fn, batch, budget):
+        t0 = time.perf_counter()
+        n = 0
+        while time.perf_counter() - t0 < budget:
+            fn(batch, [n % batch.B])
+            n += 1
+        return n / (time.perf_counter() - t0)
+
+    def line(name, bytes_, sec, rate, kernel):
+        ach = bytes_ / sec / 1e9
+        return {"ms": 1000.0 * sec, "bytes": int(bytes_), "achieved_gbs": ach, "frac": ach / peak,
+                "kernel": kernel, "oracle_requests_per_s": rate}
+
+    out = {}
+    budget = max(1.0, cpu_seconds / 6)
+    small = 4 * (2 * 9 + 1) + 4 * 256 + 16
+    b1 = W.qwen25_single(0.5)
+    d1 = to_device(b1, dev)
+    ws1 = sv.make_workspace(b1.B, b1.total_drafts, b1.V, dev)
+    a1 = d1.args()
+    sec = timed(lambda: sv.spec_verify_sample(a1, device=dev, workspace=ws1, stream=stream))
+    out["qwen25_single_B1_K8"] = line("qwen", b1.logit_bytes() + small, sec,
+                                      oracle_rate(oracle.verify_batch, b1, budget), "sample_verify_kernel (resident)")
+    for K in (1, 2, 4, 8):
+        bg = W.greedy_single(K)
+        dg = to_device(bg, dev)
+        wsg = sv.make_workspace(bg.B, bg.total_drafts, bg.V, dev)
+        ag = dg.args()
+        sec = timed(lambda: sv.spec_verify_greedy(ag, device=dev, workspace=wsg, stream=stream))
+        gbytes = (K + 1) * bg.V * 2 + 4 * (2 * K + 2)
+        out[f"greedy_B1_K{K}"] = line("greedy", gbytes, sec, oracle_rate(oracle.greedy_batch, bg, budget / 2),
+                                      "greedy_verify_kernel")
+        del dg, wsg
+    br = W.ragged_top_p(0)
+    dr = to_device(br, dev)
+    wsr = sv.make_workspace(br.B, br.total_drafts, br.V, dev)
+    ar = dr.args()
+    sec = timed(lambda: sv.spec_verify_sample(ar, device=dev, workspace=wsr, stream=stream), iters=10)
+    out["ragged_top_p_B256_fp32"] = line("ragged", br.logit_bytes() + 8 * (br.total_drafts + br.B) + 16 * br.B,
+                                         sec, oracle_rate(oracle.verify_batch, br, budget),
+                                         "sample_verify_kernel (streaming, top-p)")
+    del dr, wsr
+    bb = make_workload(0)
+    db = to_device(bb, dev)
+    wsb = sv.make_workspace(bb.B, bb.total_drafts, bb.V, dev)
+    ab = db.args()
+    sec = timed(lambda: sv.spec_tv_budget(ab, device=dev, workspace=wsb, stream=stream))
+    tvbytes = 2 * bb.total_drafts * bb.V * 2 + 4 * int(bb.hist.size) + 16 * bb.total_drafts
+    out["tv_budget_batched_B64_K8"] = line("tv", tvbytes, sec, None, "pipe_verify_kernel (TV only)")
+    return out
 
 
 def main():
@@ -362,6 +448,8 @@ def main():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--extras", action="store_true",
+                    help="also time the other configurations and entry points (adds about a minute)")
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
