@@ -20,6 +20,10 @@ the method in the order the pages give them:
 * "Adaptive-SpecDecode-Lab" README, section "实现" (implementation): greedy
   longest-prefix acceptance, the target's correction on a mismatch and a
   bonus token when every draft matches.
+* The same README, section "Confidence-guided early stop": after each draft
+  token the drafter reads its top-1 probability from the logits it has and
+  stops proposing below a threshold; the low-confidence token is still
+  verified.
 
 Readings where the pages are silent (each is listed in the design doc):
 
@@ -40,6 +44,10 @@ Readings where the pages are silent (each is listed in the design doc):
   same draw from p.
 * A bonus token from the last target row follows a fully accepted draft
   (``bonus=False`` emits none, as the mentored-decoding engine does).
+* Draft confidence is the largest probability of the draft distribution
+  after repetition penalty and temperature (top-p does not enter: the
+  drafter reads it from its logits); the drafter keeps the first token whose
+  confidence is below the threshold and stops after it.
 
 Near ties: every decision whose margin (in units of the uniform it consumes)
 is below ``NEAR_TIE`` is reported; the fp32 kernels may decide those either
@@ -382,6 +390,69 @@ def verify_batch(batch, requests: Optional[Iterable[int]] = None, *, bonus: bool
         out["near_tie"][b] = r["near_tie"]
         out["margin"][b] = r["margin"]
         out["computed"][b] = True
+    return out
+
+
+# ---------------------------------------------------------------------------
+# Draft confidence early stop ("Adaptive-SpecDecode-Lab" README, section
+# "Confidence-guided early stop": after each draft token the draft's own
+# top-1 probability is read from the logits it already has; below the
+# threshold, drafting stops, and that low-confidence token is still verified)
+# ---------------------------------------------------------------------------
+
+def draft_confidence_request(z_draft: np.ndarray, x: np.ndarray, hist: np.ndarray, T: float, alpha: float,
+                             threshold: float) -> Dict:
+    """Per draft row i: conf_i = max_v q_i(v), q_i the draft distribution
+    after repetition penalty (history plus the drafts before row i) and
+    temperature.  k_eff = i + 1 for the first i with conf_i < threshold, else
+    K: the number of drafts a confidence-stopped drafter would have proposed.
+    Returns conf [K], k_eff, status, and per row the margin |conf - threshold|
+    (a decision closer than NEAR_TIE is a near tie)."""
+    K = len(x)
+    V = z_draft.shape[1] if K else 0
+    st = STATUS_OK
+    if K > MAX_K:
+        st |= STATUS_BAD_K
+    if any(int(t) < 0 or int(t) >= V for t in list(x) + list(hist)):
+        st |= STATUS_BAD_TOKEN
+    a = float(np.float32(alpha))
+    Tv = float(np.float32(T))
+    if not (math.isfinite(a) and a > 0) or not (math.isfinite(Tv) and Tv > 0):
+        st |= STATUS_BAD_PARAM
+    if any(not _finite_row(r) for r in z_draft):
+        st |= STATUS_BAD_LOGITS
+    conf = np.full(K, np.nan)
+    margin = np.full(K, np.inf)
+    if st:
+        return dict(conf=conf, k_eff=-1, status=st, margin=margin)
+    k_eff = K
+    for i in range(K):
+        zp = apply_repetition_penalty(z_draft[i], penalty_set(hist, x[:i]), alpha)
+        conf[i] = float(np.max(softmax(apply_temperature(zp, T))))
+        margin[i] = abs(conf[i] - float(np.float32(threshold)))
+        if k_eff == K and conf[i] < float(np.float32(threshold)):
+            k_eff = i + 1
+    return dict(conf=conf, k_eff=k_eff, status=st, margin=margin)
+
+
+def draft_confidence_batch(batch, threshold: float, requests: Optional[Iterable[int]] = None) -> Dict:
+    """``draft_confidence_request`` over (a subset of) a packed batch:
+    conf [sum K], k_eff [B], status [B], near_tie [B] (a row whose early-stop
+    decision lies within NEAR_TIE of the threshold, up to k_eff)."""
+    B = batch.B
+    total = batch.total_drafts
+    reqs = range(B) if requests is None else list(requests)
+    out = dict(conf=np.full(total, np.nan), k_eff=np.full(B, -1, np.int64), status=np.zeros(B, np.int64),
+               near_tie=np.zeros(B, bool))
+    for b in reqs:
+        a = _unpack(batch, b)
+        r = draft_confidence_request(a["z_draft"], a["x"], a["hist"], a["T"], a["alpha"], threshold)
+        d0 = int(batch.cu_draft[b])
+        out["conf"][d0:d0 + len(a["x"])] = r["conf"]
+        out["k_eff"][b] = r["k_eff"]
+        out["status"][b] = r["status"]
+        upto = r["k_eff"] if r["k_eff"] > 0 else 0
+        out["near_tie"][b] = bool(np.any(r["margin"][:upto] < NEAR_TIE))
     return out
 
 

@@ -439,3 +439,70 @@ def test_no_bonus_variant():
     r = O.verify_request(zt, zd, np.array([1, 2]), np.zeros(0, np.int64), 1.0, 1.0, 1.0, 1.0,
                          np.array([0.1, 0.2, 0.3], np.float32), bonus=False)
     assert r["accepted"] == 2 and r["tokens"] == [1, 2, -1]
+
+
+# ------------------------------------------------ draft confidence early stop
+# ("Adaptive-SpecDecode-Lab" README, section "Confidence-guided early stop")
+
+def _conf(z, x, hist=(), T=1.0, alpha=1.0, thr=0.5):
+    return O.draft_confidence_request(np.asarray(z, np.float32), np.asarray(x, np.int64),
+                                      np.asarray(hist, np.int64), T, alpha, thr)
+
+
+def test_confidence_worked_distribution():
+    """p = [0.2, 0.5, 0.3] as logits ln p: the top-1 probability is 0.5."""
+    z = np.log([[0.2, 0.5, 0.3]])
+    r = _conf(z, [1], thr=0.4)
+    assert r["conf"][0] == pytest.approx(0.5, abs=1e-7)
+    assert r["k_eff"] == 1
+
+
+def test_confidence_uniform_is_one_over_v():
+    V = 1000
+    r = _conf(np.zeros((3, V)), [1, 2, 3], thr=0.5)
+    np.testing.assert_allclose(r["conf"], 1.0 / V, rtol=1e-12)
+    assert r["k_eff"] == 1          # the first draft is already below 0.5: stop after it
+
+
+def test_confidence_temperature_by_hand():
+    """T = 0.5 squares the probabilities: [0.04, 0.25, 0.09] / 0.38."""
+    z = np.log([[0.2, 0.5, 0.3]]).astype(np.float32)
+    r = _conf(z, [0], T=0.5)
+    p = np.array([0.2, 0.5, 0.3], np.float64)
+    zf = z.astype(np.float64)[0]   # the fp32 logits the oracle sees
+    e = np.exp(zf / 0.5)
+    assert r["conf"][0] == pytest.approx(e.max() / e.sum(), rel=1e-12)
+    assert r["conf"][0] == pytest.approx(0.25 / 0.38, abs=1e-6)
+    del p
+
+
+def test_confidence_penalty_on_history_and_preceding_drafts():
+    """alpha = 4 on a negative logit multiplies it: ln 0.8 -> 4 ln 0.8."""
+    z = np.log([[0.8, 0.2], [0.8, 0.2]]).astype(np.float32)
+    r = _conf(z, [0, 1], alpha=4.0, thr=0.5)
+    assert r["conf"][0] == pytest.approx(0.8, abs=1e-6)            # nothing penalised yet
+    pen = 0.8 ** 4
+    assert r["conf"][1] == pytest.approx(pen / (pen + 0.2), abs=1e-6)  # draft 0 penalised in row 1
+    r2 = _conf(z, [0, 1], hist=[0], alpha=4.0, thr=0.5)
+    assert r2["conf"][0] == pytest.approx(pen / (pen + 0.2), abs=1e-6)
+
+
+def test_confidence_stops_after_the_first_low_token():
+    """Two-token rows with top-1 probability 0.9, 0.7, 0.55, 0.95 and a 0.6
+    threshold: the drafter proposes three tokens (the third is the first
+    below the threshold and is still verified)."""
+    c = [0.9, 0.7, 0.55, 0.95]
+    z = np.log([[v, 1 - v] for v in c])
+    r = _conf(z, [0, 0, 1, 0], thr=0.6)
+    np.testing.assert_allclose(r["conf"], [max(v, 1 - v) for v in c], atol=1e-6)
+    assert r["k_eff"] == 3
+    assert _conf(z[[0, 1, 3]], [0, 0, 0], thr=0.6)["k_eff"] == 3   # never below: all K kept
+    assert _conf(z[:0], [], thr=0.6)["k_eff"] == 0
+
+
+def test_confidence_status():
+    z = np.zeros((2, 4), np.float32)
+    assert _conf(z, [0, 7])["status"] & O.STATUS_BAD_TOKEN
+    assert _conf(z, [0, 1], T=0.0)["status"] & O.STATUS_BAD_PARAM
+    zb = z.copy(); zb[1, 2] = np.nan
+    assert _conf(zb, [0, 1])["status"] & O.STATUS_BAD_LOGITS
