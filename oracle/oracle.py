@@ -409,7 +409,7 @@ def draft_confidence_request(z_draft: np.ndarray, x: np.ndarray, hist: np.ndarra
     Returns conf [K], k_eff, status, and per row the margin |conf - threshold|
     (a decision closer than NEAR_TIE is a near tie)."""
     K = len(x)
-    V = z_draft.shape[1] if K else 0
+    V = np.asarray(z_draft).shape[1]   # [K, V] even when K = 0
     st = STATUS_OK
     if K > MAX_K:
         st |= STATUS_BAD_K

@@ -506,3 +506,11 @@ def test_confidence_status():
     assert _conf(z, [0, 1], T=0.0)["status"] & O.STATUS_BAD_PARAM
     zb = z.copy(); zb[1, 2] = np.nan
     assert _conf(zb, [0, 1])["status"] & O.STATUS_BAD_LOGITS
+
+
+def test_confidence_no_drafts_checks_history_against_v():
+    """A request without drafts still has a vocabulary: valid history tokens
+    are valid, out-of-range ones are flagged."""
+    z = np.zeros((0, 10), np.float32)
+    assert _conf(z, [], hist=[3, 9])["status"] == 0
+    assert _conf(z, [], hist=[10])["status"] & O.STATUS_BAD_TOKEN
