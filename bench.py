@@ -361,8 +361,8 @@ def bench_extras(dev, peak: float, cpu_seconds: float) -> dict:
     L2 flushed before each (a 256 MB write), CUDA events around the call:
     the Qwen2.5-shaped single request (B=1, K=8, resident cluster kernel),
     greedy verification (B=1, K in 1/2/4/8), the ragged top-p batch (B=256,
-    fp32, cluster kernel with top-p) and spec_tv_budget on the batched
-    workload.  Each with algorithmic bytes, achieved GB/s against the
+    fp32, cluster kernel with top-p), and spec_tv_budget and
+    spec_draft_confidence on the batched workload.  Each with algorithmic bytes, achieved GB/s against the
     measured peak, and the oracle's requests/s on a bounded sample."""
     import torch
 
@@ -437,6 +437,10 @@ def bench_extras(dev, peak: float, cpu_seconds: float) -> dict:
     sec = timed(lambda: sv.spec_tv_budget(ab, device=dev, workspace=wsb, stream=stream))
     tvbytes = 2 * bb.total_drafts * bb.V * 2 + 4 * int(bb.hist.size) + 16 * bb.total_drafts
     out["tv_budget_batched_B64_K8"] = line("tv", tvbytes, sec, None, "pipe_verify_kernel (TV only)")
+    sec = timed(lambda: sv.spec_draft_confidence(ab, 0.6, device=dev, workspace=wsb, stream=stream))
+    cbytes = bb.total_drafts * bb.V * 2 + 4 * int(bb.hist.size) + 8 * bb.total_drafts
+    rate = oracle_rate(lambda batch, reqs: oracle.draft_confidence_batch(batch, 0.6, reqs), bb, budget)
+    out["draft_confidence_batched_B64_K8"] = line("conf", cbytes, sec, rate, "confidence_kernel")
     return out
 
 

@@ -176,6 +176,24 @@ int spec_verify_greedy(const spec_args *args, int32_t *out_tokens, int32_t *out_
 int spec_tv_budget(const spec_args *args, float *out_tv, float *out_theta, float *out_p_at_draft,
                    float *out_q_at_draft, void *workspace, size_t ws_bytes, spec_stream_t stream);
 
+/* Draft confidence for early stopping ("Adaptive-SpecDecode-Lab" README,
+ * section "Confidence-guided early stop": after each draft token the drafter
+ * reads its top-1 probability from the logits it already has and stops
+ * proposing below a threshold; that low-confidence token is still verified).
+ *
+ * For every draft row i of request b: out_conf[cu_draft[b] + i] =
+ * max_v q_i(v), with q_i the draft distribution after the repetition penalty
+ * (history plus the drafts before row i) and the temperature (top-p does not
+ * enter).  out_k_eff[b] = i + 1 for the first row with confidence below
+ * `threshold`, else K_b: the drafts a confidence-stopped drafter would have
+ * proposed.  Reads draft_logits, cu_draft, draft_tokens, history,
+ * temperature (NULL = 1) and rep_penalty; not the target logits.
+ * out_status [B] (may be NULL) as for sampling; an invalid request gets
+ * out_k_eff = -1 and NaN confidences.  One pass over the draft logits
+ * (HBM-bound).  Same workspace as the other entry points. */
+int spec_draft_confidence(const spec_args *args, float threshold, float *out_conf, int32_t *out_k_eff,
+                          int32_t *out_status, void *workspace, size_t ws_bytes, spec_stream_t stream);
+
 /* Fixed-scratch variant of spec_verify_sample: no workspace argument.
  *
  * The method has no counterpart to this call.  It serves callers that cannot

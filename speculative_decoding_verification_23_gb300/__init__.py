@@ -41,7 +41,7 @@ SPEC_STATUS_BAD_K = 8
 SPEC_STATUS_TIMEOUT = 16
 
 EXPORTED = ("spec_workspace_bytes", "spec_verify_sample", "spec_verify_greedy", "spec_tv_budget",
-            "spec_verify_sample_static", "spec_status_string")
+            "spec_draft_confidence", "spec_verify_sample_static", "spec_status_string")
 
 
 class SpecArgs(ctypes.Structure):
@@ -98,6 +98,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.spec_tv_budget.restype = ctypes.c_int
     lib.spec_tv_budget.argtypes = [ctypes.POINTER(SpecArgs), ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                    ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]
+    lib.spec_draft_confidence.restype = ctypes.c_int
+    lib.spec_draft_confidence.argtypes = [ctypes.POINTER(SpecArgs), ctypes.c_float, ctypes.c_void_p, ctypes.c_void_p,
+                                          ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]
     lib.spec_verify_sample_static.restype = ctypes.c_int
     lib.spec_verify_sample_static.argtypes = [ctypes.POINTER(SpecArgs), ctypes.c_void_p, ctypes.c_void_p,
                                               ctypes.c_void_p, ctypes.c_void_p]
@@ -248,6 +251,26 @@ def spec_verify_greedy(args: SpecArgs, *, device=None, workspace=None, out_token
     if rc != SPEC_OK:
         raise SpecError(rc, "spec_verify_greedy")
     return out_tokens, out_accepted, out_status
+
+
+def spec_draft_confidence(args: SpecArgs, threshold: float, *, device=None, workspace=None, stream=None):
+    """Top-1 draft probability per draft row and the confidence-stopped draft
+    count per request through ``spec_draft_confidence``.
+    Returns (conf [sum K] float32, k_eff [B] int32, status [B] int32)."""
+    import torch
+
+    lib = load_library()
+    device = device or torch.device("cuda", torch.cuda.current_device())
+    if workspace is None:
+        workspace = make_workspace(args.B, args.total_drafts, args.V, device)
+    conf = torch.empty(max(args.total_drafts, 1), dtype=torch.float32, device=device)
+    k_eff = torch.empty(args.B, dtype=torch.int32, device=device)
+    status = torch.empty(args.B, dtype=torch.int32, device=device)
+    rc = lib.spec_draft_confidence(ctypes.byref(args), float(threshold), _ptr(conf), _ptr(k_eff), _ptr(status),
+                                   _ptr(workspace), workspace.numel(), _stream_handle(stream))
+    if rc != SPEC_OK:
+        raise SpecError(rc, "spec_draft_confidence")
+    return conf[:args.total_drafts], k_eff, status
 
 
 def spec_verify_sample_static(args: SpecArgs, *, device=None, out_tokens=None, out_accepted=None, out_status=None,

@@ -235,6 +235,33 @@ struct GreedyParams {
   GreedyPartial* partials;  // [(total + B) * nck]
 };
 
+// ------------------------------------------------------ draft confidence
+struct ConfPartial {
+  float m;    // chunk maximum of the penalised logits
+  float s;    // sum over the chunk of 2^((z' - m) c)
+  int flags;
+  int pad;
+};
+
+struct ConfParams {
+  const void* draft;
+  long long ld_d;
+  const int* cu_draft;
+  const int* draft_tokens;
+  const int* cu_hist;
+  const int* hist;
+  const float* temperature;
+  const float* rep_penalty;
+  int B, V, total, max_k;
+  int nck;                 // chunks per row
+  float threshold;
+  float* out_conf;         // [total]
+  int* out_k_eff;          // [B]
+  int* out_status;         // [B] or null
+  int* counters;           // [B]
+  ConfPartial* partials;   // [total * nck]
+};
+
 // -------------------------------------------------------------- workspace
 struct WorkspaceLayout {
   size_t off_counters, off_results, off_inval, off_partials, total;

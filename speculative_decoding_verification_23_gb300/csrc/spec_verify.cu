@@ -18,6 +18,7 @@ int launch_sample_verify(SampleParams& P, bool bf16, bool topp, cudaStream_t str
 int launch_greedy_verify(const GreedyParams& P, bool bf16, cudaStream_t stream);
 int choose_pipe_layout(int V, int elem_bytes, int max_smem, PipeLayout* out);
 int launch_pipe_verify(SampleParams& P, bool bf16, int num_sms, cudaStream_t stream);
+int launch_confidence(const ConfParams& P, bool bf16, cudaStream_t stream);
 }  // namespace sv
 
 namespace {
@@ -273,6 +274,58 @@ int spec_verify_greedy(const spec_args* a, int32_t* out_tokens, int32_t* out_acc
     return SPEC_ERR_LAUNCH;
   }
   return sv::launch_greedy_verify(P, a->dtype == SPEC_BF16, s) == 0 ? SPEC_OK : SPEC_ERR_LAUNCH;
+}
+
+int spec_draft_confidence(const spec_args* a, float threshold, float* out_conf, int32_t* out_k_eff,
+                          int32_t* out_status, void* workspace, size_t ws_bytes, spec_stream_t stream) {
+  if (!a) return SPEC_ERR_NULL;
+  if (a->dtype != SPEC_F32 && a->dtype != SPEC_BF16) return SPEC_ERR_DTYPE;
+  if (a->B < 1 || a->V < 1 || a->total_drafts < 0 || a->max_k < 0) return SPEC_ERR_SHAPE;
+  if (a->max_k > SPEC_MAX_K) return SPEC_ERR_K_TOO_LARGE;
+  if ((long long)a->total_drafts > (long long)a->B * a->max_k) return SPEC_ERR_SHAPE;
+  if (!a->cu_draft || !out_k_eff) return SPEC_ERR_NULL;
+  if (a->cu_hist && !a->hist_tokens) return SPEC_ERR_NULL;
+  const int es = elem_bytes(a->dtype);
+  if (a->total_drafts > 0) {
+    if (!a->draft_logits || !a->draft_tokens || !out_conf) return SPEC_ERR_NULL;
+    if (a->ld_draft < a->V) return SPEC_ERR_SHAPE;
+    if (!aligned16(a->draft_logits) || (a->ld_draft * es) % 16 != 0) return SPEC_ERR_ALIGN;
+  }
+  int rc = check_workspace(a, workspace, ws_bytes);
+  if (rc) return rc;
+  int max_smem = 0, num_sms = 0;
+  rc = device_props(&max_smem, &num_sms);
+  if (rc) return rc;
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const sv::WorkspaceLayout W = sv::make_workspace_layout(a->B, a->total_drafts, a->V);
+  unsigned char* w = static_cast<unsigned char*>(workspace);
+  sv::ConfParams P;
+  std::memset(&P, 0, sizeof(P));
+  P.draft = a->draft_logits;
+  P.ld_d = a->ld_draft;
+  P.cu_draft = a->cu_draft;
+  P.draft_tokens = a->draft_tokens;
+  P.cu_hist = a->cu_hist;
+  P.hist = a->hist_tokens;
+  P.temperature = a->temperature;
+  P.rep_penalty = a->rep_penalty;
+  P.B = a->B;
+  P.V = a->V;
+  P.total = a->total_drafts;
+  P.max_k = a->max_k;
+  P.nck = (a->V + sv::kGreedyChunk - 1) / sv::kGreedyChunk;
+  P.threshold = threshold;
+  P.out_conf = out_conf;
+  P.out_k_eff = out_k_eff;
+  P.out_status = out_status;
+  P.counters = reinterpret_cast<int*>(w + W.off_counters);
+  P.partials = reinterpret_cast<sv::ConfPartial*>(w + W.off_partials);
+  if (cudaMemsetAsync(P.counters, 0, (size_t)a->B * sizeof(int), s) != cudaSuccess) {
+    cudaGetLastError();
+    return SPEC_ERR_LAUNCH;
+  }
+  rc = sv::launch_confidence(P, a->dtype == SPEC_BF16, s);
+  return rc == 0 ? SPEC_OK : (rc == -2 ? SPEC_ERR_SHAPE : SPEC_ERR_LAUNCH);
 }
 
 const char* spec_status_string(int code) {

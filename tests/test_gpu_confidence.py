@@ -1,0 +1,69 @@
+"""GPU parity of spec_draft_confidence against the oracle: the top-1 draft
+probability per row within 1e-5, the confidence-stopped draft count exactly
+(except rows whose confidence is within 1e-6 of the threshold)."""
+import numpy as np
+import pytest
+
+from speculative_decoding_verification_23_gb300 import workload as W
+
+import oracle
+
+pytestmark = pytest.mark.gpu
+
+
+def _run(batch, threshold):
+    import torch
+
+    import speculative_decoding_verification_23_gb300 as sv
+    from speculative_decoding_verification_23_gb300.device_batch import to_device
+
+    db = to_device(batch)
+    conf, k_eff, st = sv.spec_draft_confidence(db.args(), threshold)
+    torch.cuda.synchronize()
+    return conf.cpu().numpy().astype(np.float64), k_eff.cpu().numpy(), st.cpu().numpy()
+
+
+def _check(batch, threshold, requests=None):
+    conf, k_eff, st = _run(batch, threshold)
+    ref = oracle.draft_confidence_batch(batch, threshold, requests)
+    reqs = range(batch.B) if requests is None else requests
+    for b in reqs:
+        d0, d1 = int(batch.cu_draft[b]), int(batch.cu_draft[b + 1])
+        assert st[b] == ref["status"][b], b
+        if st[b]:
+            assert k_eff[b] == -1 and np.all(np.isnan(conf[d0:d1]))
+            continue
+        np.testing.assert_allclose(conf[d0:d1], ref["conf"][d0:d1], atol=1e-5, rtol=0)
+        if not ref["near_tie"][b]:
+            assert k_eff[b] == ref["k_eff"][b], (b, k_eff[b], ref["k_eff"][b], conf[d0:d1])
+    return conf, k_eff, st, ref
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("V", [3, 257, 8192, 8193, 50000, 152064])
+def test_confidence_shapes(dtype, V):
+    """Ragged K including 0, penalties with history, temperatures; V spans
+    one chunk, exactly one, a ragged second chunk and many."""
+    batch = W.make_batch(B=6, V=V, K=[0, 1, 3, 8, 5, 2], dtype=dtype, seed=5000 + V,
+                         rho=[0.3, 0.6, 0.8, 0.9, 0.95, 0.99], temperature=[0.5, 0.7, 1.0, 1.3, 0.9, 0.6],
+                         rep_penalty=[1.0, 1.3, 1.1, 0.8, 1.2, 1.0], hist_len=min(24, 3 * V))
+    for thr in (0.05, 0.3, 0.6):
+        _check(batch, thr)
+
+
+def test_confidence_greedy_drafts_and_k_sweep():
+    """Drafts taken as the draft argmax (the lab's greedy drafter), K 1..8."""
+    for K in (1, 2, 4, 8):
+        batch = W.greedy_single(K)
+        conf, k_eff, st, ref = _check(batch, 0.4)
+        assert 1 <= k_eff[0] <= K
+
+
+def test_confidence_invalid_requests():
+    batch = W.make_batch(B=4, V=600, K=[2, 2, 0, 2], dtype="f32", seed=9, hist_len=3, rep_penalty=1.1)
+    batch.draft_tokens[1] = 600           # request 0: token out of range
+    batch.temperature[1] = -1.0           # request 1: T < 0
+    batch.hist[2 * 3] = 9999              # request 2 (no drafts): bad history token
+    batch.draft[5, 5] = np.nan            # request 3 (rows 4, 5), row 1: NaN
+    conf, k_eff, st, ref = _check(batch, 0.5)
+    assert list(st != 0) == [True, True, True, True]
