@@ -81,6 +81,23 @@ __global__ void __launch_bounds__(kGreedyThreads) greedy_verify_kernel(const __g
   const int npre = (i >= 0 && i <= K) ? i : 0;
   const bool pen = !(flags & kStatusBadParam) && alpha != 1.f && (h1 > h0 || npre > 0);
 
+  // the chunk's logits, loaded first so that the loads are in flight while
+  // the penalty bitmap is built: thread owns 8-element groups g = tid + 256*j
+  const T* rowp = static_cast<const T*>(P.target) + (size_t)row * P.ld_t;
+  float best = -INFINITY;
+  int bidx = 0x7fffffff;
+  constexpr int kGroups = kGreedyChunk / 8 / kGreedyThreads;  // 4
+  float z[kGroups][8];
+#pragma unroll
+  for (int j = 0; j < kGroups; ++j) {
+    const int g0 = c0 + 8 * (tid + kGreedyThreads * j);
+    if (g0 + 8 <= c1) {
+      ldg8(rowp + g0, z[j]);
+    } else if (g0 < c1) {  // ragged end of the row: no read past V
+#pragma unroll
+      for (int e = 0; e < 8; ++e) z[j][e] = g0 + e < c1 ? to_f32<T>(rowp[g0 + e]) : -INFINITY;
+    }
+  }
   if (tid == 0) s_flags = 0;
   for (int w = tid; w < kGreedyChunk / 32; w += kGreedyThreads) bitmap[w] = 0u;
   __syncthreads();
@@ -97,22 +114,6 @@ __global__ void __launch_bounds__(kGreedyThreads) greedy_verify_kernel(const __g
   }
   __syncthreads();
 
-  // argmax over [c0, c1): thread owns 8-element groups g = tid + 256*j
-  const T* rowp = static_cast<const T*>(P.target) + (size_t)row * P.ld_t;
-  float best = -INFINITY;
-  int bidx = 0x7fffffff;
-  constexpr int kGroups = kGreedyChunk / 8 / kGreedyThreads;  // 4
-  float z[kGroups][8];
-#pragma unroll
-  for (int j = 0; j < kGroups; ++j) {
-    const int g0 = c0 + 8 * (tid + kGreedyThreads * j);
-    if (g0 + 8 <= c1) {
-      ldg8(rowp + g0, z[j]);
-    } else if (g0 < c1) {  // ragged end of the row: no read past V
-#pragma unroll
-      for (int e = 0; e < 8; ++e) z[j][e] = g0 + e < c1 ? to_f32<T>(rowp[g0 + e]) : -INFINITY;
-    }
-  }
 #pragma unroll
   for (int j = 0; j < kGroups; ++j) {
     const int l0 = 8 * (tid + kGreedyThreads * j);  // offset within the chunk
