@@ -3,34 +3,35 @@
 // accepting more draft tokens"), for batches with more work items than SMs.
 //
 // A work item is one draft position (target row + draft row) or one bonus
-// row, as in the cluster kernel.  One CTA per SM loops over its items; the
-// warps have four roles:
-//   group A (kPipeWarpsA warps): item k+1's penalty set, then its pass-1
-//       statistics (per lane a running reference and the sum of
-//       2^(z'c - ref), z' the penalised logit, c = log2(e)/T) from a TMA ring
-//       fed from HBM with L2 policy evict_last;
-//   group B (kPipeWarpsB warps): item k's softmax combine, pass 2 (per
-//       segment the sum of the residual max(p-q, 0), or of p for a bonus
-//       row) from a second TMA ring that re-reads the rows (L2 hits,
-//       evict_first), the prefix over segments (TV d = total residual mass),
-//       the decisions (theta, pi(x), acceptance), the inverse-CDF candidate
-//       and the request's finalisation;
+// row, as in the cluster kernel.  One CTA per SM loops over its items
+// (item k of CTA c is c + k * gridDim.x); its warps have six roles:
+//   group A streaming warps (kPipeWarpsA): pass 1 of item k from a TMA ring
+//       fed from HBM (L2 policy evict_last): per lane a running reference and
+//       the sum of 2^(z'c - ref), z' the penalised logit, c = log2(e)/T;
+//   group A setup warp: the penalty bitmap of item k+1 (history plus the
+//       drafts before the row), then item k's combine: (M, 1/S) per row,
+//       p(x) and q(x);
+//   group B streaming warps (kPipeWarpsB): pass 2 of item k-1 from a second
+//       ring that re-reads the rows (L2 hits, evict_first): the mass of
+//       max(p-q, 0) (or of p for a bonus row) per segment;
+//   group B tail warp: for item k-2 the prefix over segments (TV d = total
+//       residual mass), theta, pi(x), the acceptance decision, the
+//       inverse-CDF candidate and the request's finalisation;
 //   two producer warps (lane 0 issues the bulk copies of one ring each).
-// Only group A's ring reads HBM, so HBM keeps streaming while group B runs
-// the per-item serial steps.
+// Only ring A reads HBM, so HBM keeps streaming while the per-item serial
+// steps run on the setup and tail warps.  Per-item state (bitmap, hand-off
+// block, segment masses) is triple-buffered; mbarriers order the roles.
 //
-// Repetition penalty: group A turns the item's penalty set (history plus the
-// drafts before the row) into a sorted token list with per-segment offsets.
-// Before a warp reads its segment of a ring slot, its lanes overwrite the
-// penalised positions with -inf (group A first copies their raw logits into
-// the list), so the hot loops never test the penalty; group B adds the
-// penalised tokens' exact terms from the list: to the softmax sums and to
-// each segment's residual mass.
+// Repetition penalty: before a streaming warp reads its segment of a ring
+// slot, the lanes holding bitmap words with set bits take the penalised
+// positions out of the stream (-inf) after adding their exact terms: group A
+// their softmax terms, group B their residuals.  The hot loops never test
+// the penalty.
 //
-// Rare items leave the pipeline and are recomputed at the end by all
-// compute warps with direct global loads ("deferred"): an item with more
-// than kPipeListCap distinct penalised tokens, and a rejected position whose
-// residual mass is zero (its correction is then drawn from p).
+// A rejected position whose residual mass is exactly zero (its correction
+// is then drawn from p) leaves the pipeline; all compute warps recompute such
+// items at the end with direct global loads ("deferred").
+
 #include "common.cuh"
 #include "spec_internal.h"
 #include "verify_common.cuh"
@@ -41,7 +42,7 @@ namespace {
 
 constexpr int kNA = kPipeWarpsA;
 constexpr int kNB = kPipeWarpsB;
-constexpr int kNC = kNA + kNB;                 // compute warps
+constexpr int kNC = kNA + kNB + 2;             // compute warps (streaming + setup + tail)
 constexpr int kThreadsA = kNA * 32;
 constexpr int kThreadsB = kNB * 32;
 constexpr int kThreadsC = kNC * 32;
@@ -59,34 +60,20 @@ struct PSmem {
   __device__ __forceinline__ unsigned char* at(int off) const { return pipe_smem + off; }
   __device__ __forceinline__ unsigned char* ring_a() const { return at(L.off_ring_a); }
   __device__ __forceinline__ unsigned char* ring_b() const { return at(L.off_ring_b); }
-  // penalty bitmap: group A's scratch, then the slow path's
-  __device__ __forceinline__ uint32_t* bm() const { return reinterpret_cast<uint32_t*>(at(L.off_bm)); }
-  // [nseg][32] pass-2 lane sums (slow path: 256-token chunk sums)
+  // item buffer kb's penalty bitmap (the slow path uses buffer 0)
+  __device__ __forceinline__ uint32_t* bm(int kb) const {
+    return reinterpret_cast<uint32_t*>(at(L.off_bm + kb * align_up_i(L.bm_words * 4, 16)));
+  }
+  // slow path: 256-token chunk sums
   __device__ __forceinline__ float* part() const { return reinterpret_cast<float*>(at(L.off_part)); }
-  // [nseg] segment residual mass and the penalised tokens' share of it
-  __device__ __forceinline__ float* segt() const { return reinterpret_cast<float*>(at(L.off_segt)); }
-  // [2][nseg] per item buffer
-  __device__ __forceinline__ float* segc(int kb) const {
-    return reinterpret_cast<float*>(at(L.off_segc + kb * align_up_i(L.nseg * 4, 16)));
+  // item buffer kb: [nseg] segment residual mass
+  __device__ __forceinline__ float* segt(int kb) const {
+    return reinterpret_cast<float*>(at(L.off_segt + kb * align_up_i(L.nseg * 4, 16)));
   }
   // cu_draft copy (when B + 1 <= kPipeCuCap)
   __device__ __forceinline__ int* cu() const { return reinterpret_cast<int*>(at(L.off_cu)); }
-  // item buffer kb: sorted penalised tokens, their raw target logits (later
-  // their residual terms), their raw draft logits, and segment offsets
-  __device__ __forceinline__ int* ltok(int kb) const {
-    return reinterpret_cast<int*>(at(L.off_list + kb * kPipeListCap * 12));
-  }
-  __device__ __forceinline__ float* lzp(int kb) const {
-    return reinterpret_cast<float*>(at(L.off_list + kb * kPipeListCap * 12 + kPipeListCap * 4));
-  }
-  __device__ __forceinline__ float* lzq(int kb) const {
-    return reinterpret_cast<float*>(at(L.off_list + kb * kPipeListCap * 12 + kPipeListCap * 8));
-  }
-  __device__ __forceinline__ int* segst(int kb) const {
-    return reinterpret_cast<int*>(at(L.off_segst + kb * align_up_i((L.nseg + 1) * 4, 16)));
-  }
   __device__ __forceinline__ PipeStats* stats(int kb) const {
-    return reinterpret_cast<PipeStats*>(at(L.off_stats)) + kb;
+    return reinterpret_cast<PipeStats*>(at(L.off_stats + kb * align_up_i((int)sizeof(PipeStats), 16)));
   }
   // misc: [kNB][2] group B warp partials, [kNC][2] slow-path warp partials,
   // scan scratch, scalars, the candidate segment's penalty mask
@@ -96,16 +83,22 @@ struct PSmem {
   // mi: [0] group B status bits, [1] B deferral, [2] B finalize flag,
   //     [3] slow finalize flag, [4] slow: draw from p
   __device__ __forceinline__ int* mi() const { return reinterpret_cast<int*>(at(L.off_misc + 576)); }
-  __device__ __forceinline__ uint32_t* cmask() const { return reinterpret_cast<uint32_t*>(at(L.off_misc + 704)); }
   __device__ __forceinline__ uint32_t* defer() const { return reinterpret_cast<uint32_t*>(at(L.off_defer)); }
   __device__ __forceinline__ uint64_t* bars() const { return reinterpret_cast<uint64_t*>(at(L.off_bar)); }
   __device__ __forceinline__ uint64_t* full_a() const { return bars(); }
   __device__ __forceinline__ uint64_t* empty_a() const { return bars() + L.slots_a; }
   __device__ __forceinline__ uint64_t* full_b() const { return bars() + 2 * L.slots_a; }
   __device__ __forceinline__ uint64_t* empty_b() const { return bars() + 2 * L.slots_a + L.slots_b; }
-  // [2] A -> B: item statistics ready; B and producer B -> A: buffer free
-  __device__ __forceinline__ uint64_t* stats_full() const { return bars() + 2 * L.slots_a + 2 * L.slots_b; }
-  __device__ __forceinline__ uint64_t* stats_empty() const { return stats_full() + 2; }
+  // [kPipeBufs] each: setup warp -> A streaming warps: the item's penalty
+  // list is built; A streaming warps -> setup warp: pass 1 done; setup warp
+  // -> B streaming warps and producer B: statistics combined; B streaming
+  // warps -> tail warp: pass 2 done; tail warp and producer B -> setup warp:
+  // the item's buffers are free again
+  __device__ __forceinline__ uint64_t* list_ready() const { return bars() + 2 * L.slots_a + 2 * L.slots_b; }
+  __device__ __forceinline__ uint64_t* pass1_done() const { return list_ready() + kPipeBufs; }
+  __device__ __forceinline__ uint64_t* stats_full() const { return list_ready() + 2 * kPipeBufs; }
+  __device__ __forceinline__ uint64_t* pass2_done() const { return list_ready() + 3 * kPipeBufs; }
+  __device__ __forceinline__ uint64_t* buf_free() const { return list_ready() + 4 * kPipeBufs; }
 };
 
 __device__ __forceinline__ void fence_proxy_async_smem() {
@@ -167,29 +160,19 @@ __device__ __forceinline__ void mask_tail(float (&z)[4][N], int lane, int nvalid
       if ((j * 32 + lane) * N + e >= nvalid) z[j][e] = -INFINITY;
 }
 
-// Overwrites the penalised positions [e0, e1) of the list that fall in this
-// warp's segment with -inf, in both staged rows; with CAPTURE their raw
-// values are first copied to the list.  The writes are ordered before the
-// slot goes back to the TMA producer (proxy fence) and before the warp reads
-// the segment (__syncwarp).
-template <typename T, bool CAPTURE>
-__device__ __forceinline__ void patch_segment(unsigned char* rowp, unsigned char* rowq, bool two_rows, const int* ltok,
-                                              float* lzp, float* lzq, int e0, int e1, int base, int lane) {
-  bool wrote = false;
-  for (int e = e0 + lane; e < e1; e += 32) {
-    const int o = ltok[e] - base;
-    T* p = reinterpret_cast<T*>(rowp) + o;
-    T* q = reinterpret_cast<T*>(rowq) + o;
-    if constexpr (CAPTURE) {
-      lzp[e] = to_f32<T>(*p);
-      lzq[e] = two_rows ? to_f32<T>(*q) : 0.f;
-    }
-    *p = neg_inf<T>();
-    if (two_rows) *q = neg_inf<T>();
-    wrote = true;
+// Calls f(o) for every penalised position o of segment s (offset within
+// the segment): lane l takes bitmap word s*wps + l (l < wps), its set bits
+// one by one.  Returns whether the segment has any (warp-uniform).
+template <typename F>
+__device__ __forceinline__ bool for_penalised(const uint32_t* bm, int s, int wps, int lane, F&& f) {
+  uint32_t w = lane < wps ? bm[s * wps + lane] : 0u;
+  if (!__any_sync(0xffffffffu, w != 0u)) return false;
+  while (w) {
+    const int bit = __ffs(w) - 1;
+    w &= w - 1;
+    f(32 * lane + bit);
   }
-  if (wrote) fence_proxy_async_smem();
-  __syncwarp();
+  return true;
 }
 
 // Pass-1 statistics of one row segment for one lane: the running reference
@@ -346,7 +329,8 @@ __device__ __forceinline__ void finish_item(const SampleParams& P, const Item& i
     const int old = atomicAdd(P.counters + b, 1);
     *shflag = (old == K) && K >= 0 && it.rows_ok;
   }
-  named_sync(bar, nthr);
+  if (bar >= 0) named_sync(bar, nthr);
+  else __syncwarp();
   if (*shflag && tg < 32) {
     const int lane = tg;
     __threadfence();
@@ -454,10 +438,17 @@ __device__ __forceinline__ Scalars item_scalars(const SampleParams& P, const Ite
 // out-of-range tokens; threads t of nt.
 __device__ __forceinline__ int mark_penalty_set(const SampleParams& P, const Scalars& s, uint32_t* bm, int t, int nt) {
   int flags = 0;
-  for (int j = s.h0 + t; j < s.h1; j += nt) {
-    const int tok = __ldg(P.hist + j);
-    if (tok < 0 || tok >= P.V) flags |= kStatusBadToken;
-    else if (s.pen) atomicOr(&bm[tok >> 5], 1u << (tok & 31));
+  // eight loads in flight per thread before their bits are set
+  for (int j0 = s.h0 + t; j0 < s.h1; j0 += 8 * nt) {
+    int tok[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) tok[q] = j0 + q * nt < s.h1 ? __ldg(P.hist + j0 + q * nt) : 0;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      if (j0 + q * nt >= s.h1) continue;
+      if (tok[q] < 0 || tok[q] >= P.V) flags |= kStatusBadToken;
+      else if (s.pen) atomicOr(&bm[tok[q] >> 5], 1u << (tok[q] & 31));
+    }
   }
   for (int j = t; j < s.npre; j += nt) {
     const int tok = __ldg(P.draft_tokens + s.d0 + j);
@@ -486,13 +477,11 @@ __device__ __forceinline__ void producer(const SampleParams& P, const PipeLayout
   for (int item = blockIdx.x; item < P.n_items; item += gridDim.x, ++k) {
     const Item it = pdecode(P, cu, item);
     if (!IS_A) {
-      // pass 2 of item k starts once group A has finished its pass 1 (the
-      // rows are then in L2); a deferred item is not streamed again
-      const int kb = k & 1;
-      if (!to && !mbar_wait(&S.stats_full()[kb], (uint32_t)(k >> 1) & 1u)) to = true;
-      const int cnt = S.stats(kb)->count;
-      mbar_arrive(&S.stats_empty()[kb]);
-      if (cnt < 0) continue;
+      // pass 2 of item k starts once its statistics are combined (the rows
+      // are then in L2)
+      const int kb = k % kPipeBufs;
+      if (!to && !mbar_wait(&S.stats_full()[kb], (uint32_t)(k / kPipeBufs) & 1u)) to = true;
+      mbar_arrive(&S.buf_free()[kb]);  // this warp has seen item k's statistics
     }
     const unsigned char* rowp = static_cast<const unsigned char*>(P.target) + (size_t)it.tgt_row * P.ld_t * es;
     const unsigned char* rowq =
@@ -513,80 +502,36 @@ __device__ __forceinline__ void producer(const SampleParams& P, const PipeLayout
 }
 
 // ------------------------------------------------------------- group A
-// Per item: penalty set -> sorted list, pass 1 over the ring, then the
-// softmax combine with the penalised tokens' exact terms, p(x), q(x) and the
-// penalised tokens' residual mass per segment; all handed to group B.
+// Streaming warps: pass 1 of each item over ring A.  Before reading a
+// segment the lanes copy the penalised positions' raw logits into the list
+// and overwrite them with -inf; each lane keeps a running reference and the
+// sum of 2^(z'c - ref); the warp's (reference, sum) per row goes to the setup
+// warp.
 template <typename T>
-__device__ __forceinline__ void group_a(const SampleParams& P, const PipeLayout& L, const PSmem& S, int wa, int lane) {
-  const int ta = wa * 32 + lane;
+__device__ __forceinline__ void a_stream(const SampleParams& P, const PipeLayout& L, const PSmem& S, int wa, int lane) {
   const int SEG = L.seg;
-  const int wps = SEG / 32;  // bitmap words per segment
   const int row_bytes = kNA * kPipeSegBytes;
   const int* cu = cu_ptr(P, S);
   RingCursor rc;
   bool timeout = false;
   int k = 0;
   for (int item = blockIdx.x; item < P.n_items; item += gridDim.x, ++k) {
-    const int kb = k & 1;
+    const int kb = k % kPipeBufs;
     PipeStats& st = *S.stats(kb);
     const Item it = pdecode(P, cu, item);
     const Scalars sc = item_scalars(P, it, item, cu);
-    // the bitmap is group A's own: mark the set before waiting for buffer kb
-    int flags = sc.flags | mark_penalty_set(P, sc, S.bm(), ta, kThreadsA);
-    // buffer kb is free once group B and producer B are done with item k-2
-    if (!timeout && !mbar_wait(&S.stats_empty()[kb], ((uint32_t)(k >> 1) & 1u) ^ 1u)) timeout = true;
-
-    // ---- sorted penalty list with per-segment offsets; clears the bitmap
-    int count = 0;
-    if (sc.pen) {
-      named_sync(kBarA, kThreadsA);
-      const int wpt = (L.bm_words + kThreadsA - 1) / kThreadsA;
-      const int w0 = min(L.bm_words, ta * wpt), w1 = min(L.bm_words, w0 + wpt);
-      int cnt = 0;
-      for (int w = w0; w < w1; ++w) cnt += __popc(S.bm()[w]);
-      const int incl = warp_incl_scan_i(cnt, lane);
-      if (lane == 31) S.scan()[wa] = incl;
-      named_sync(kBarA, kThreadsA);
-      int base = incl - cnt, total = 0;
-      for (int w2 = 0; w2 < kNA; ++w2) {
-        const int v = S.scan()[w2];
-        if (w2 < wa) base += v;
-        total += v;
-      }
-      if (total <= kPipeListCap) {
-        count = total;
-        int* segst = S.segst(kb);
-        int* ltok = S.ltok(kb);
-        int pos = base;
-        for (int w = w0; w < w1; ++w) {
-          if (w % wps == 0) segst[w / wps] = pos;
-          uint32_t word = S.bm()[w];
-          if (word) {
-            S.bm()[w] = 0u;
-            while (word) {
-              const int bit = __ffs(word) - 1;
-              word &= word - 1;
-              ltok[pos++] = 32 * w + bit;
-            }
-          }
-        }
-        if (ta == 0) segst[L.nseg] = total;
-      } else {
-        count = -1;  // too many for the list: the item is recomputed by the slow path
-        for (int w = w0; w < w1; ++w) S.bm()[w] = 0u;
-      }
-      named_sync(kBarA, kThreadsA);
-    }
-
-    // ---- pass 1
-    const bool skip = count < 0;
+    if (!timeout && !mbar_wait(&S.list_ready()[kb], (uint32_t)(k / kPipeBufs) & 1u)) timeout = true;
+    const bool pen = st.pen != 0;
+    const int wps = SEG / 32;
     float ref[2] = {-INFINITY, -INFINITY}, run[2] = {0.f, 0.f};
+    float pref[2] = {-INFINITY, -INFINITY}, psum[2] = {0.f, 0.f};
+    int pflags = 0;
     for (int stn = 0; stn < L.nst_a; ++stn) {
       const uint32_t slot = rc.slot;
       if (!timeout && !mbar_wait(&S.full_a()[slot], rc.phase)) timeout = true;
       rc.advance(L.slots_a);
       const int s_id = stn * kNA + wa;
-      if (!skip && s_id < L.nseg) {
+      if (s_id < L.nseg) {
         unsigned char* seg = S.ring_a() + (size_t)slot * L.slot_a + wa * kPipeSegBytes;
         const int base = s_id * SEG;
         if (sc.x >= base && sc.x < base + SEG) {
@@ -597,11 +542,26 @@ __device__ __forceinline__ void group_a(const SampleParams& P, const PipeLayout&
           }
           __syncwarp();
         }
-        if (count > 0) {
-          const int e0 = S.segst(kb)[s_id], e1 = S.segst(kb)[s_id + 1];
-          if (e1 > e0)
-            patch_segment<T, true>(seg, seg + row_bytes, sc.nrows == 2, S.ltok(kb), S.lzp(kb), S.lzq(kb), e0, e1,
-                                   base, lane);
+        if (pen) {
+          // penalised positions: add their exact terms, then take them out
+          // of the stream (-inf)
+          const bool two = sc.nrows == 2;
+          bool wrote = false;
+          const bool any = for_penalised(S.bm(kb), s_id, wps, lane, [&](int o) {
+            T* pp = reinterpret_cast<T*>(seg) + o;
+            T* qq = reinterpret_cast<T*>(seg + row_bytes) + o;
+            const float zp = to_f32<T>(*pp), zq = two ? to_f32<T>(*qq) : 0.f;
+            if (is_bad_logit(zp) || (two && is_bad_logit(zq))) pflags |= kStatusBadLogits;
+            online_add(penalize(zp, sc.alpha) * sc.c, pref[0], psum[0]);
+            if (two) online_add(penalize(zq, sc.alpha) * sc.c, pref[1], psum[1]);
+            *pp = neg_inf<T>();
+            if (two) *qq = neg_inf<T>();
+            wrote = true;
+          });
+          if (any) {
+            if (wrote) fence_proxy_async_smem();
+            __syncwarp();
+          }
         }
         const int nvalid = min(SEG, P.V - base);
         if (sc.nrows == 2) seg_stats<T, 2>(seg, row_bytes, lane, nvalid, sc.c, ref, run);
@@ -610,78 +570,95 @@ __device__ __forceinline__ void group_a(const SampleParams& P, const PipeLayout&
       __syncwarp();
       if (lane == 0) mbar_arrive(&S.empty_a()[slot]);
     }
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      // the lane's stream terms and its penalised tokens' terms, then the warp's
+      float M = ref[r], Sl = run[r];
+      combine_into(make_float2(pref[r], psum[r]), M, Sl);
+      const float2 wv = warp_combine(M, Sl);
+      if (lane == 0) st.wp[wa][r] = wv;
+    }
+    pflags = warp_or(pflags);
+    if (lane == 0) st.aflags[wa] = pflags | (timeout ? kStatusTimeout : 0);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&S.pass1_done()[kb]);
+  }
+}
 
-    // ---- softmax combine: the pass's lanes, then the penalised tokens
-    if (timeout) flags |= kStatusTimeout;
-    if (count > 0) named_sync(kBarA, kThreadsA);  // every warp's captured list values are in place
-    float pref[2] = {-INFINITY, -INFINITY}, psum[2] = {0.f, 0.f};
-    for (int e = ta; e < count; e += kThreadsA) {
-      const float zp = S.lzp(kb)[e], zq = S.lzq(kb)[e];
-      if (is_bad_logit(zp) || (sc.nrows == 2 && is_bad_logit(zq))) flags |= kStatusBadLogits;
-      online_add(penalize(zp, sc.alpha) * sc.c, pref[0], psum[0]);
-      if (sc.nrows == 2) online_add(penalize(zq, sc.alpha) * sc.c, pref[1], psum[1]);
-    }
-#pragma unroll
-    for (int r = 0; r < 2; ++r) {
-      const float2 wv = warp_combine(ref[r], run[r]);
-      const float2 pv = warp_combine(pref[r], psum[r]);
-      if (lane == 0) {
-        st.wp[wa][r] = wv;
-        S.bred()[wa * 2 + r] = pv;
-      }
-    }
+// Group A's setup warp, per item k: the penalty list of item k+1 (bitmap,
+// then compaction into a list sorted by segment), then item k's softmax
+// combine with the penalised tokens' exact terms, p(x), q(x) and the
+// penalised tokens' residual mass per segment.
+template <typename T>
+__device__ __forceinline__ void a_setup(const SampleParams& P, const PipeLayout& L, const PSmem& S, int lane) {
+  const int SEG = L.seg;
+  const int wshift = __ffs(SEG / 32) - 1;  // log2(bitmap words per segment)
+  const int* cu = cu_ptr(P, S);
+  bool timeout = false;
+  const int n_local = (int)blockIdx.x < P.n_items ? (P.n_items - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x : 0;
+
+  auto build = [&](int k) {
+    const int item = blockIdx.x + k * gridDim.x;
+    const int kb = k % kPipeBufs;
+    const Item it = pdecode(P, cu, item);
+    const Scalars sc = item_scalars(P, it, item, cu);
+    // buffer kb is free once item k-3's tail and producer B are done with it
+    if (!timeout && !mbar_wait(&S.buf_free()[kb], ((uint32_t)(k / kPipeBufs) & 1u) ^ 1u)) timeout = true;
+    PipeStats& st = *S.stats(kb);
+    uint32_t* bm = S.bm(kb);
+    if (sc.pen)
+      for (int q = lane; q < L.bm_words / 4; q += 32) reinterpret_cast<uint4*>(bm)[q] = make_uint4(0u, 0u, 0u, 0u);
+    __syncwarp();
+    int flags = sc.flags | mark_penalty_set(P, sc, bm, lane, 32) | (timeout ? kStatusTimeout : 0);
     flags = warp_or(flags);
-    if (lane == 0) S.scan()[kNA + wa] = flags;
-    named_sync(kBarA, kThreadsA);
-    flags = 0;
-    for (int w = 0; w < kNA; ++w) flags |= S.scan()[kNA + w];
-    float M[2], Ssum[2], inv[2];
-#pragma unroll
-    for (int r = 0; r < 2; ++r) {
-      M[r] = -INFINITY;
-      Ssum[r] = 0.f;
-      for (int w = 0; w < kNA; ++w) combine_into(st.wp[w][r], M[r], Ssum[r]);
-      for (int w = 0; w < kNA; ++w) combine_into(S.bred()[w * 2 + r], M[r], Ssum[r]);
+    if (lane == 0) {
+      st.flags = flags;
+      st.pen = sc.pen ? 1 : 0;
     }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&S.list_ready()[kb]);
+  };
+
+  auto combine = [&](int k) {
+    const int item = blockIdx.x + k * gridDim.x;
+    const int kb = k % kPipeBufs;
+    const Item it = pdecode(P, cu, item);
+    const Scalars sc = item_scalars(P, it, item, cu);
+    PipeStats& st = *S.stats(kb);
+    if (!timeout && !mbar_wait(&S.pass1_done()[kb], (uint32_t)(k / kPipeBufs) & 1u)) timeout = true;
+    int flags = st.flags | (timeout ? kStatusTimeout : 0);
+    for (int w = 0; w < kNA; ++w) flags |= st.aflags[w];
+    float M[2] = {0.f, 0.f}, inv[2] = {1.f, 1.f};
+    float px = 0.f, qx = 0.f;
+    {
+      float Ssum[2];
 #pragma unroll
-    for (int r = 0; r < 2; ++r)
-      if (r < sc.nrows && (!(Ssum[r] > 0.f) || !(Ssum[r] < INFINITY) || !(M[r] < INFINITY))) flags |= kStatusBadLogits;
-    const bool ok_stats = !(flags & kStatusBadLogits);
-#pragma unroll
-    for (int r = 0; r < 2; ++r) {
-      const bool use = ok_stats && r < sc.nrows;
-      inv[r] = use ? __fdiv_rn(1.f, Ssum[r]) : 1.f;
-      if (!use) M[r] = 0.f;
-    }
-    // residual terms of the penalised tokens, summed per segment in list order
-    if (count > 0) {
-      for (int e = ta; e < count; e += kThreadsA) {
-        float r = prob_of(penalize(S.lzp(kb)[e], sc.alpha), sc.c, M[0], inv[0]);
-        if (sc.nrows == 2) r = resid_of(r, prob_of(penalize(S.lzq(kb)[e], sc.alpha), sc.c, M[1], inv[1]));
-        S.lzp(kb)[e] = r;
+      for (int r = 0; r < 2; ++r) {
+        M[r] = -INFINITY;
+        Ssum[r] = 0.f;
+        for (int w = 0; w < kNA; ++w) combine_into(st.wp[w][r], M[r], Ssum[r]);
       }
-      named_sync(kBarA, kThreadsA);
-    }
-    for (int s = ta; s < L.nseg; s += kThreadsA) {
-      float a = 0.f;
-      if (count > 0)
-        for (int e = S.segst(kb)[s]; e < S.segst(kb)[s + 1]; ++e) a += S.lzp(kb)[e];
-      S.segc(kb)[s] = a;
-    }
-    if (ta == 0) {
-      // p(x), q(x) (x may be penalised itself)
-      float px = 0.f, qx = 0.f;
-      if (!it.bonus && sc.x >= 0 && sc.x < P.V && ok_stats && !skip) {
-        bool xpen = false;
-        if (count > 0) {
-          const int sx = sc.x / SEG;
-          for (int e = S.segst(kb)[sx]; e < S.segst(kb)[sx + 1]; ++e) xpen |= S.ltok(kb)[e] == sc.x;
-        }
+#pragma unroll
+      for (int r = 0; r < 2; ++r)
+        if (r < sc.nrows && (!(Ssum[r] > 0.f) || !(Ssum[r] < INFINITY) || !(M[r] < INFINITY)))
+          flags |= kStatusBadLogits;
+      const bool ok_stats = !(flags & kStatusBadLogits);
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        const bool use = ok_stats && r < sc.nrows;
+        inv[r] = use ? __fdiv_rn(1.f, Ssum[r]) : 1.f;
+        if (!use) M[r] = 0.f;
+      }
+      if (lane == 0 && !it.bonus && sc.x >= 0 && sc.x < P.V && ok_stats) {
+        // p(x), q(x) (x may be penalised itself)
+        const bool xpen = st.pen && ((S.bm(kb)[sc.x >> 5] >> (sc.x & 31)) & 1u);
         const float zp = xpen ? penalize(st.xz[0], sc.alpha) : st.xz[0];
         const float zq = xpen ? penalize(st.xz[1], sc.alpha) : st.xz[1];
         px = prob_of(zp, sc.c, M[0], inv[0]);
         qx = prob_of(zq, sc.c, M[1], inv[1]);
       }
+    }
+    if (lane == 0) {
       st.M[0] = M[0];
       st.M[1] = M[1];
       st.inv[0] = inv[0];
@@ -689,10 +666,15 @@ __device__ __forceinline__ void group_a(const SampleParams& P, const PipeLayout&
       st.px = px;
       st.qx = qx;
       st.flags = flags;
-      st.count = count;
     }
-    named_sync(kBarA, kThreadsA);
-    if (ta == 0) mbar_arrive(&S.stats_full()[kb]);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&S.stats_full()[kb]);
+  };
+
+  if (n_local > 0) build(0);
+  for (int k = 0; k < n_local; ++k) {
+    if (k + 1 < n_local) build(k + 1);
+    combine(k);
   }
 }
 
@@ -700,23 +682,18 @@ __device__ __forceinline__ void group_a(const SampleParams& P, const PipeLayout&
 // prefix of w exceeds rem, w = max(p-q, 0) or p (ponly); `take_last` or no
 // such token: the segment's last token with w > 0.  Returns -1 if none.
 template <typename T>
-__device__ __forceinline__ int search_segment(const SampleParams& P, const PipeLayout& L, const PSmem& S, int kb, int count,
-                              const T* gp, const T* gq, bool ponly, int s, double rem, bool take_last, float c,
-                              float alpha, float Mp, float Mq, float ip, float iq, int lane) {
+__device__ __forceinline__ int search_segment(const SampleParams& P, const PipeLayout& L, const uint32_t* bm,
+                                              const T* gp, const T* gq, bool ponly, int s, double rem, bool take_last,
+                                              float c, float alpha, float Mp, float Mq, float ip, float iq, int lane) {
   constexpr int N = Vec<T>::N;
   constexpr int LT = 4 * N;  // tokens per lane, contiguous
   const int sbase = s * L.seg;
   const int base = sbase + lane * LT;
+  // this lane's penalised tokens (bitmap bits base .. base + LT - 1)
   uint32_t pm = 0;
-  if (count > 0) {
-    S.cmask()[lane] = 0u;
-    __syncwarp();
-    for (int e = S.segst(kb)[s] + lane; e < S.segst(kb)[s + 1]; e += 32) {
-      const int o = S.ltok(kb)[e] - sbase;
-      atomicOr(&S.cmask()[o / LT], 1u << (o % LT));
-    }
-    __syncwarp();
-    pm = S.cmask()[lane];
+  if (bm) {
+    const uint32_t w = bm[base >> 5];
+    pm = LT == 32 ? w : (w >> (base & 31)) & ((1u << LT) - 1u);
   }
   uint4 vp[4], vq[4];
 #pragma unroll
@@ -856,12 +833,11 @@ __device__ __forceinline__ double owner_search(const float* seg, int n, double u
 }
 
 // ------------------------------------------------------------- group B
-// Per item: pass 2 over the ring with group A's normalisers, the residual
-// mass per segment, the prefix over segments, the decisions, the candidate
-// and the request's finalisation.
+// Streaming warps: pass 2 of each item over ring B with the setup warp's
+// normalisers; per lane and segment the sum of max(p-q, 0) (or p for a bonus
+// row); then the segment masses for the tail warp.
 template <typename T>
-__device__ __forceinline__ void group_b(const SampleParams& P, const PipeLayout& L, const PSmem& S, int wb, int lane) {
-  const int tb = wb * 32 + lane;
+__device__ __forceinline__ void b_stream(const SampleParams& P, const PipeLayout& L, const PSmem& S, int wb, int lane) {
   const int SEG = L.seg;
   const int row_bytes = kNB * kPipeSegBytes;
   const int* cu = cu_ptr(P, S);
@@ -869,92 +845,107 @@ __device__ __forceinline__ void group_b(const SampleParams& P, const PipeLayout&
   bool timeout = false;
   int k = 0;
   for (int item = blockIdx.x; item < P.n_items; item += gridDim.x, ++k) {
-    const int kb = k & 1;
+    const int kb = k % kPipeBufs;
+    PipeStats& st = *S.stats(kb);
+    const Item it = pdecode(P, cu, item);
+    const Scalars sc = item_scalars(P, it, item, cu);
+    if (!timeout && !mbar_wait(&S.stats_full()[kb], (uint32_t)(k / kPipeBufs) & 1u)) timeout = true;
+    {
+      const bool pen = st.pen != 0;
+      const int wps = SEG / 32;
+      const float Mp = st.M[0], Mq = st.M[1], ip = st.inv[0], iq = st.inv[1];
+      for (int stn = 0; stn < L.nst_b; ++stn) {
+        const uint32_t slot = rc.slot;
+        if (!timeout && !mbar_wait(&S.full_b()[slot], rc.phase)) timeout = true;
+        rc.advance(L.slots_b);
+        const int s_id = stn * kNB + wb;
+        if (s_id < L.nseg) {
+          unsigned char* seg = S.ring_b() + (size_t)slot * L.slot_b + wb * kPipeSegBytes;
+          const int base = s_id * SEG;
+          float extra = 0.f;
+          if (pen) {
+            // penalised positions: their exact residual (or p), then out of
+            // the stream (-inf)
+            const bool two = sc.nrows == 2;
+            bool wrote = false;
+            const bool any = for_penalised(S.bm(kb), s_id, wps, lane, [&](int o) {
+              T* pp = reinterpret_cast<T*>(seg) + o;
+              T* qq = reinterpret_cast<T*>(seg + row_bytes) + o;
+              const float p = prob_of(penalize(to_f32<T>(*pp), sc.alpha), sc.c, Mp, ip);
+              extra += it.bonus ? p : resid_of(p, prob_of(penalize(to_f32<T>(*qq), sc.alpha), sc.c, Mq, iq));
+              *pp = neg_inf<T>();
+              if (two) *qq = neg_inf<T>();
+              wrote = true;
+            });
+            if (any) {
+              if (wrote) fence_proxy_async_smem();
+              __syncwarp();
+            }
+          }
+          const int nvalid = min(SEG, P.V - base);
+          const float v = it.bonus ? seg_resid<T, true>(seg, row_bytes, lane, nvalid, sc.c, Mp, Mq, ip, iq)
+                                   : seg_resid<T, false>(seg, row_bytes, lane, nvalid, sc.c, Mp, Mq, ip, iq);
+          const float tot = warp_sum(v + extra);
+          if (lane == 0) S.segt(kb)[s_id] = tot;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&S.empty_b()[slot]);
+      }
+      if (lane == 0 && timeout) atomicOr(&st.flags, kStatusTimeout);
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&S.pass2_done()[kb]);
+  }
+}
+
+// Group B's tail warp, per item: the prefix over segments (TV d = total
+// residual mass), theta, pi(x), the acceptance decision, the inverse-CDF
+// candidate and the request's finalisation; then the item's buffers go back
+// to the setup warp.
+template <typename T>
+__device__ __forceinline__ void b_tail(const SampleParams& P, const PipeLayout& L, const PSmem& S, int lane) {
+  const int* cu = cu_ptr(P, S);
+  bool timeout = false;
+  int k = 0;
+  for (int item = blockIdx.x; item < P.n_items; item += gridDim.x, ++k) {
+    const int kb = k % kPipeBufs;
     const PipeStats& st = *S.stats(kb);
     const Item it = pdecode(P, cu, item);
     const Scalars sc = item_scalars(P, it, item, cu);
     const T* gp = static_cast<const T*>(P.target) + (size_t)it.tgt_row * P.ld_t;
     const T* gq = it.bonus ? gp : static_cast<const T*>(P.draft) + (size_t)it.dft_row * P.ld_d;
     float u_acc = 0.f, u_fin = 0.f;
-    if (tb == 0 && P.mode == kModeSample && sc.uniforms_ok) {
+    if (P.mode == kModeSample && sc.uniforms_ok) {
       u_fin = __ldg(P.uniforms + sc.off + sc.K);
       if (!it.bonus) u_acc = __ldg(P.uniforms + sc.off + it.i);
     }
-    if (!timeout && !mbar_wait(&S.stats_full()[kb], (uint32_t)(k >> 1) & 1u)) timeout = true;
-    const int count = st.count;
-    int flags = st.flags;
-    if (count < 0) {
-      if (tb == 0) S.defer()[k >> 5] |= 1u << (k & 31);
-      named_sync(kBarB, kThreadsB);
-      if (tb == 0) mbar_arrive(&S.stats_empty()[kb]);
-      continue;
-    }
-    const float Mp = st.M[0], Mq = st.M[1], ip = st.inv[0], iq = st.inv[1];
-    const float px = st.px, qx = st.qx;
-
-    // ---- pass 2
-    for (int stn = 0; stn < L.nst_b; ++stn) {
-      const uint32_t slot = rc.slot;
-      if (!timeout && !mbar_wait(&S.full_b()[slot], rc.phase)) timeout = true;
-      rc.advance(L.slots_b);
-      const int s_id = stn * kNB + wb;
-      if (s_id < L.nseg) {
-        unsigned char* seg = S.ring_b() + (size_t)slot * L.slot_b + wb * kPipeSegBytes;
-        const int base = s_id * SEG;
-        if (count > 0) {
-          const int e0 = S.segst(kb)[s_id], e1 = S.segst(kb)[s_id + 1];
-          if (e1 > e0)
-            patch_segment<T, false>(seg, seg + row_bytes, sc.nrows == 2, S.ltok(kb), nullptr, nullptr, e0, e1, base,
-                                    lane);
-        }
-        const int nvalid = min(SEG, P.V - base);
-        const float v = it.bonus ? seg_resid<T, true>(seg, row_bytes, lane, nvalid, sc.c, Mp, Mq, ip, iq)
-                                 : seg_resid<T, false>(seg, row_bytes, lane, nvalid, sc.c, Mp, Mq, ip, iq);
-        S.part()[s_id * 32 + lane] = v;
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&S.empty_b()[slot]);
-    }
-    if (timeout) flags |= kStatusTimeout;
+    if (!timeout && !mbar_wait(&S.pass2_done()[kb], (uint32_t)(k / kPipeBufs) & 1u)) timeout = true;
     {
-      const int f = warp_or(flags);
-      if (lane == 0 && f) atomicOr(&S.mi()[0], f);
-    }
-    named_sync(kBarB, kThreadsB);
-    for (int s = wb; s < L.nseg; s += kNB) {
-      const float v = warp_sum(S.part()[s * 32 + lane]);
-      if (lane == 0) S.segt()[s] = v + S.segc(kb)[s];
-    }
-    named_sync(kBarB, kThreadsB);
-    flags = S.mi()[0];
-
-    // ---- sync 2, decisions, candidate (warp 0 of the group)
-    bool deferred = false;
-    if (wb == 0) {
+      const int flags = st.flags | (timeout ? kStatusTimeout : 0);
+      const float Mp = st.M[0], Mq = st.M[1], ip = st.inv[0], iq = st.inv[1];
+      const float px = st.px, qx = st.qx;
       int ks;
       double rem;
       bool take_last;
-      const double R = owner_search(S.segt(), L.nseg, (double)__shfl_sync(0xffffffffu, u_fin, 0), lane, ks, rem,
-                                    take_last);
+      const double R = owner_search(S.segt(kb), L.nseg, (double)u_fin, lane, ks, rem, take_last);
       const double tv = it.bonus ? 0.0 : fmin(R, 1.0);
       double theta = 1.0;
+      if (tv > (double)sc.D) theta = (double)__fdiv_rn(sc.D, (float)tv);
       int acc = 1;
-      if (lane == 0) {
-        if (tv > (double)sc.D) theta = (double)__fdiv_rn(sc.D, (float)tv);
-        if (!it.bonus) {
-          const double pi = (1.0 - theta) * (double)px + theta * (double)qx;
-          acc = ((double)u_acc * (double)qx < pi) ? 1 : 0;
-        }
+      if (!it.bonus) {
+        const double pi = (1.0 - theta) * (double)px + theta * (double)qx;
+        acc = ((double)u_acc * (double)qx < pi) ? 1 : 0;
       }
-      acc = __shfl_sync(0xffffffffu, acc, 0);
       const bool sample = P.mode == kModeSample;
       const bool need_cand = sample && flags == 0 && (it.bonus ? !(P.flags & 1u) : acc == 0);
+      bool deferred = false;
       int cand = -1;
       if (need_cand) {
         if (!it.bonus && !(R > 0.0)) {
           deferred = true;  // correction from p: recomputed by the slow path
         } else if (ks >= 0) {
-          cand = search_segment<T>(P, L, S, kb, count, gp, gq, it.bonus, ks, rem, take_last, sc.c, sc.alpha, Mp, Mq, ip, iq, lane);
+          cand = search_segment<T>(P, L, st.pen ? S.bm(kb) : nullptr, gp, gq, it.bonus, ks, rem, take_last, sc.c,
+                                   sc.alpha, Mp, Mq, ip, iq, lane);
         }
       }
       if (lane == 0) {
@@ -975,15 +966,11 @@ __device__ __forceinline__ void group_b(const SampleParams& P, const PipeLayout&
           if (P.out_px) P.out_px[item] = bad ? NAN : px;
           if (P.out_qx) P.out_qx[item] = bad ? NAN : qx;
         }
-        S.mi()[1] = deferred ? 1 : 0;
       }
+      if (sample && !deferred) finish_item(P, it, item, flags, lane, -1, 32, &S.mi()[2]);
     }
-    named_sync(kBarB, kThreadsB);
-    deferred = S.mi()[1] != 0;
-    if (tb == 0) S.mi()[0] = 0;  // every B thread has read it; the next item's bits come after the barriers below
-    if (P.mode == kModeSample && !deferred) finish_item(P, it, item, flags, tb, kBarB, kThreadsB, &S.mi()[2]);
-    named_sync(kBarB, kThreadsB);
-    if (tb == 0) mbar_arrive(&S.stats_empty()[kb]);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&S.buf_free()[kb]);
   }
 }
 
@@ -1002,7 +989,7 @@ __device__ __forceinline__ void slow_item(const SampleParams& P, const PipeLayou
   const T* gp = static_cast<const T*>(P.target) + (size_t)it.tgt_row * P.ld_t;
   const T* gq = it.bonus ? gp : static_cast<const T*>(P.draft) + (size_t)it.dft_row * P.ld_d;
   if (tid == 0) S.mi()[0] = 0;
-  int flags = sc.flags | mark_penalty_set(P, sc, S.bm(), tid, NT);
+  int flags = sc.flags | mark_penalty_set(P, sc, S.bm(0), tid, NT);
   named_sync(kBarC, NT);
 
   // pass 1
@@ -1010,9 +997,9 @@ __device__ __forceinline__ void slow_item(const SampleParams& P, const PipeLayou
   bool have_ref = false;
   for (int kk = warp; kk < nch; kk += NW) {
     float z[2][8];
-    global_logits<T>(gp, kk * kChunk, lane, V, S.bm(), sc.pen, sc.alpha, z[0]);
+    global_logits<T>(gp, kk * kChunk, lane, V, S.bm(0), sc.pen, sc.alpha, z[0]);
     if (sc.nrows == 2) {
-      global_logits<T>(gq, kk * kChunk, lane, V, S.bm(), sc.pen, sc.alpha, z[1]);
+      global_logits<T>(gq, kk * kChunk, lane, V, S.bm(0), sc.pen, sc.alpha, z[1]);
       chunk_stats_lane<2>(z, sc.c, refc, have_ref, Ssum);
     } else {
       chunk_stats_lane<1>(z, sc.c, refc, have_ref, Ssum);
@@ -1062,14 +1049,14 @@ __device__ __forceinline__ void slow_item(const SampleParams& P, const PipeLayou
   for (int attempt = 0; attempt < 2; ++attempt) {
     for (int kk = warp; kk < nch; kk += NW) {
       float z[8], pp[8];
-      global_logits<T>(gp, kk * kChunk, lane, V, S.bm(), sc.pen, sc.alpha, z);
+      global_logits<T>(gp, kk * kChunk, lane, V, S.bm(0), sc.pen, sc.alpha, z);
       probs8<kPZ>(z, 0.f, rp[0], pp);
       float s;
       if (ponly) {
         s = sum8(pp);
       } else {
         float zq[8], qq[8], rr[8];
-        global_logits<T>(gq, kk * kChunk, lane, V, S.bm(), sc.pen, sc.alpha, zq);
+        global_logits<T>(gq, kk * kChunk, lane, V, S.bm(0), sc.pen, sc.alpha, zq);
         probs8<kPZ>(zq, 0.f, rp[1], qq);
         s = resid8(pp, qq, rr);
       }
@@ -1083,7 +1070,7 @@ __device__ __forceinline__ void slow_item(const SampleParams& P, const PipeLayou
       if (attempt == 0 && lane == 0) {
         if (!it.bonus && sc.x >= 0 && sc.x < V && ok_stats) {
           float zp = to_f32<T>(gp[sc.x]), zq = to_f32<T>(gq[sc.x]);
-          if (sc.pen && ((S.bm()[sc.x >> 5] >> (sc.x & 31)) & 1u)) {
+          if (sc.pen && ((S.bm(0)[sc.x >> 5] >> (sc.x & 31)) & 1u)) {
             zp = penalize(zp, sc.alpha);
             zq = penalize(zq, sc.alpha);
           }
@@ -1119,14 +1106,14 @@ __device__ __forceinline__ void slow_item(const SampleParams& P, const PipeLayou
       float w[8];
       {
         float zp[8], pp[8];
-        global_logits<T>(gp, ib, lane, V, S.bm(), sc.pen, sc.alpha, zp);
+        global_logits<T>(gp, ib, lane, V, S.bm(0), sc.pen, sc.alpha, zp);
         probs8<kPZ>(zp, 0.f, rp[0], pp);
         if (ponly) {
 #pragma unroll
           for (int j = 0; j < 8; ++j) w[j] = pp[j];
         } else {
           float zq[8], qq[8];
-          global_logits<T>(gq, ib, lane, V, S.bm(), sc.pen, sc.alpha, zq);
+          global_logits<T>(gq, ib, lane, V, S.bm(0), sc.pen, sc.alpha, zq);
           probs8<kPZ>(zq, 0.f, rp[1], qq);
           resid8(pp, qq, w);
         }
@@ -1211,11 +1198,11 @@ __device__ __forceinline__ void slow_item(const SampleParams& P, const PipeLayou
   if (sc.pen) {
     for (int j = sc.h0 + tid; j < sc.h1; j += NT) {
       const int t = __ldg(P.hist + j);
-      if (t >= 0 && t < V) S.bm()[t >> 5] = 0u;
+      if (t >= 0 && t < V) S.bm(0)[t >> 5] = 0u;
     }
     for (int j = tid; j < sc.npre; j += NT) {
       const int t = __ldg(P.draft_tokens + sc.d0 + j);
-      if (t >= 0 && t < V) S.bm()[t >> 5] = 0u;
+      if (t >= 0 && t < V) S.bm(0)[t >> 5] = 0u;
     }
   }
   named_sync(kBarC, NT);
@@ -1238,13 +1225,15 @@ __global__ void __launch_bounds__(kPipeThreads, 1) pipe_verify_kernel(const __gr
       mbar_init(&S.full_b()[s], 1);
       mbar_init(&S.empty_b()[s], kNB);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kPipeBufs; ++i) {
+      mbar_init(&S.list_ready()[i], 1);
+      mbar_init(&S.pass1_done()[i], kNA);
       mbar_init(&S.stats_full()[i], 1);
-      mbar_init(&S.stats_empty()[i], 2);
+      mbar_init(&S.pass2_done()[i], kNB);
+      mbar_init(&S.buf_free()[i], 2);
     }
     fence_mbar_init();
   }
-  for (int w = tid; w < L.bm_words; w += kPipeThreads) S.bm()[w] = 0u;
   for (int w = tid; w < kPipeMaxIters / 32; w += kPipeThreads) S.defer()[w] = 0u;
   if (P.B + 1 <= kPipeCuCap)
     for (int i = tid; i <= P.B; i += kPipeThreads) S.cu()[i] = __ldg(P.cu_draft + i);
@@ -1252,9 +1241,13 @@ __global__ void __launch_bounds__(kPipeThreads, 1) pipe_verify_kernel(const __gr
   __syncthreads();
 
   if (warp < kNA) {
-    group_a<T>(P, L, S, warp, lane);
-  } else if (warp < kNC) {
-    group_b<T>(P, L, S, warp - kNA, lane);
+    a_stream<T>(P, L, S, warp, lane);
+  } else if (warp == kNA) {
+    a_setup<T>(P, L, S, lane);
+  } else if (warp < kNA + 1 + kNB) {
+    b_stream<T>(P, L, S, warp - kNA - 1, lane);
+  } else if (warp == kNA + 1 + kNB) {
+    b_tail<T>(P, L, S, lane);
   } else {
     if (lane == 0) {
       if (warp == kNC) producer<T, true>(P, L, S);
@@ -1262,7 +1255,10 @@ __global__ void __launch_bounds__(kPipeThreads, 1) pipe_verify_kernel(const __gr
     }
     return;
   }
-  // deferred items of this CTA, after the pipeline has drained
+  // deferred items of this CTA, after the pipeline has drained (bitmap 0
+  // serves their penalty sets)
+  named_sync(kBarC, kThreadsC);
+  for (int q = tid; q < L.bm_words; q += kThreadsC) S.bm(0)[q] = 0u;
   named_sync(kBarC, kThreadsC);
   int k = 0;
   for (int item = blockIdx.x; item < P.n_items; item += gridDim.x, ++k)

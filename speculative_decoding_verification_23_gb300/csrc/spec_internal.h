@@ -106,27 +106,30 @@ inline SmemLayout make_stream_layout(int V, int C, int elem_bytes, bool topp, in
 }
 
 // ------------------------------------------- pipelined streaming sampling
-// One CTA per SM, persistent over its items.  Warp group A computes the
-// pass-1 statistics of item k+1 from HBM while warp group B runs pass 2 (an
-// L2 re-read), the decisions and the candidate search of item k; each group
-// has its own TMA producer warp and shared-memory ring.
-constexpr int kPipeWarpsA = 8;
-constexpr int kPipeWarpsB = 8;
+// One CTA per SM, persistent over its items.  Four warp roles: group A's
+// streaming warps compute pass-1 statistics of item k from HBM while group
+// B's streaming warps run pass 2 (an L2 re-read) of item k-1; group A's setup
+// warp builds the penalty list of item k+1 and combines item k's statistics,
+// group B's tail warp takes the decisions and the candidate of item k-2.
+// Each streaming group has its own TMA producer warp and ring.
+constexpr int kPipeWarpsA = 7;        // group A streaming warps (+ 1 setup warp)
+constexpr int kPipeWarpsB = 7;        // group B streaming warps (+ 1 tail warp)
+constexpr int kPipeBufs = 3;          // per-item buffers in flight
 constexpr int kPipeSegBytes = 2048;   // one row's bytes per warp per stage (64 per lane)
-constexpr int kPipeListCap = 768;     // distinct penalised tokens per item the pipeline handles
 constexpr int kPipeCuCap = 1024;      // cu_draft entries cached in shared memory (B + 1 <= this)
 constexpr int kPipeMaxIters = 8192;   // items per CTA (deferred-item bits)
 constexpr int kPipeSlotsA = 3;        // ring slots of group A (HBM stream) ...
 constexpr int kPipeSlotsB = 2;        // ... and of group B (L2 re-read)
 
-// Pass-1 result of one item, handed from group A to group B.
+// One item's hand-offs between the roles.
 struct PipeStats {
-  float2 wp[kPipeWarpsA][2];  // per A warp and row: (reference, sum) of the pass
+  float2 wp[kPipeWarpsA][2];  // per A streaming warp and row: (reference, sum) of pass 1
+  int aflags[kPipeWarpsA];    // status bits seen by each A streaming warp
   float M[2], inv[2];         // per row: reference and 1 / softmax sum (units of z'c)
   float px, qx;               // p(x), q(x) of the draft token
   float xz[2];                // raw logits of the draft token (captured from the ring)
-  int flags;                  // status bits of the item so far
-  int count;                  // penalised-token list length; -1 = too many (item deferred)
+  int flags;                  // status bits of the item
+  int pen;                    // the repetition penalty applies (bitmap kb holds the set)
 };
 
 struct PipeLayout {
@@ -136,7 +139,7 @@ struct PipeLayout {
   int slots_a, slots_b;
   int slot_a, slot_b;   // bytes per ring slot
   int bm_words;         // bitmap words (nseg * seg / 32)
-  int off_ring_a, off_ring_b, off_bm, off_part, off_segt, off_segc, off_list, off_segst, off_stats, off_misc,
+  int off_ring_a, off_ring_b, off_bm, off_part, off_segt, off_stats, off_misc,
       off_defer, off_cu, off_bar;
   int total;
 };
@@ -152,20 +155,18 @@ inline PipeLayout make_pipe_layout(int V, int elem_bytes, int slots_a, int slots
   L.slot_a = 2 * kPipeWarpsA * kPipeSegBytes;
   L.slot_b = 2 * kPipeWarpsB * kPipeSegBytes;
   L.bm_words = L.nseg * L.seg / 32;
+  const int segv = align_up_i(L.nseg * 4, 16);
   int off = 0;
   L.off_ring_a = off;  off += slots_a * L.slot_a;
   L.off_ring_b = off;  off += slots_b * L.slot_b;
-  L.off_bm = off;      off += align_up_i(L.bm_words * 4, 16);
-  L.off_part = off;    off += L.nseg * 32 * 4;
-  L.off_segt = off;    off += align_up_i(L.nseg * 4, 16);
-  L.off_segc = off;    off += 2 * align_up_i(L.nseg * 4, 16);
-  L.off_list = off;    off += 2 * kPipeListCap * 12;
-  L.off_segst = off;   off += 2 * align_up_i((L.nseg + 1) * 4, 16);
-  L.off_stats = off;   off += 2 * (int)sizeof(PipeStats);
+  L.off_bm = off;      off += kPipeBufs * align_up_i(L.bm_words * 4, 16);  // one penalty bitmap per item buffer
+  L.off_part = off;    off += align_up_i((V + 255) / 256 * 4, 16);  // slow path: 256-token chunk sums
+  L.off_segt = off;    off += kPipeBufs * segv;
+  L.off_stats = off;   off += kPipeBufs * align_up_i((int)sizeof(PipeStats), 16);
   L.off_misc = off;    off += 1024;
   L.off_defer = off;   off += kPipeMaxIters / 8;
   L.off_cu = off;      off += kPipeCuCap * 4;
-  L.off_bar = off;     off += (2 * slots_a + 2 * slots_b + 4) * 8;
+  L.off_bar = off;     off += (2 * slots_a + 2 * slots_b + 5 * kPipeBufs) * 8;
   L.total = align_up_i(off, 128);
   return L;
 }
