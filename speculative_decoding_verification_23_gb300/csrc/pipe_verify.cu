@@ -75,11 +75,8 @@ struct PSmem {
   __device__ __forceinline__ PipeStats* stats(int kb) const {
     return reinterpret_cast<PipeStats*>(at(L.off_stats + kb * align_up_i((int)sizeof(PipeStats), 16)));
   }
-  // misc: [kNB][2] group B warp partials, [kNC][2] slow-path warp partials,
-  // scan scratch, scalars, the candidate segment's penalty mask
-  __device__ __forceinline__ float2* bred() const { return reinterpret_cast<float2*>(at(L.off_misc)); }
-  __device__ __forceinline__ float2* cwp() const { return reinterpret_cast<float2*>(at(L.off_misc + 128)); }
-  __device__ __forceinline__ int* scan() const { return reinterpret_cast<int*>(at(L.off_misc + 384)); }
+  // misc: [compute warps][2] slow-path warp partials (up to 64), then scalars
+  __device__ __forceinline__ float2* cwp() const { return reinterpret_cast<float2*>(at(L.off_misc)); }
   // mi: [0] group B status bits, [1] B deferral, [2] B finalize flag,
   //     [3] slow finalize flag, [4] slow: draw from p
   __device__ __forceinline__ int* mi() const { return reinterpret_cast<int*>(at(L.off_misc + 576)); }

@@ -112,8 +112,8 @@ inline SmemLayout make_stream_layout(int V, int C, int elem_bytes, bool topp, in
 // warp builds the penalty list of item k+1 and combines item k's statistics,
 // group B's tail warp takes the decisions and the candidate of item k-2.
 // Each streaming group has its own TMA producer warp and ring.
-constexpr int kPipeWarpsA = 7;        // group A streaming warps (+ 1 setup warp)
-constexpr int kPipeWarpsB = 7;        // group B streaming warps (+ 1 tail warp)
+constexpr int kPipeWarpsA = 8;        // group A streaming warps (+ 1 setup warp)
+constexpr int kPipeWarpsB = 8;        // group B streaming warps (+ 1 tail warp)
 constexpr int kPipeBufs = 3;          // per-item buffers in flight
 constexpr int kPipeSegBytes = 2048;   // one row's bytes per warp per stage (64 per lane)
 constexpr int kPipeCuCap = 1024;      // cu_draft entries cached in shared memory (B + 1 <= this)
