@@ -204,17 +204,18 @@ int spec_draft_confidence(const spec_args *args, float threshold, float *out_con
  *
  * Arguments, checks, kernels and results are those of spec_verify_sample;
  * the workspace is replaced by one buffer per device that the library holds
- * as a file-scope __device__ array of SPEC_STATIC_SCRATCH_BYTES (16 MiB).  The
+ * as a file-scope __device__ array of SPEC_STATIC_SCRATCH_BYTES (1 MiB).  The
  * call allocates and frees nothing.
  *
- * Size limit: a batch fits when spec_workspace_bytes(B, total_drafts, V) is
- * at most SPEC_STATIC_SCRATCH_BYTES (e.g. B = 64 requests of 8 drafts over a
- * 152064-token vocabulary need about 3.4 MB).  A batch that does not fit
- * returns SPEC_ERR_STATIC_SCRATCH and enqueues nothing.
+ * Size limit: with n = total_drafts + B the batch needs
+ * align256(4 B) + align256(32 n) + align256(64 n) bytes; every batch with
+ * n <= 10000 fits.  A batch that does not fit returns SPEC_ERR_STATIC_SCRATCH
+ * and enqueues nothing.
  *
- * Zeroing: the counters and flags the kernels count on must be zero when
- * they start; each call clears them on `stream` before its main launch.
- * Everything else in the buffer is written before it is read.
+ * Zeroing: only the B per-request arrival counters at the start of the
+ * buffer must be zero when the kernel starts; each call clears them on
+ * `stream` (cudaMemsetAsync) before its launch.  Everything else in the
+ * buffer is written before it is read.
  *
  * First call on a device: it looks the buffer's address up with
  * cudaGetSymbolAddress (that device current) and caches it; make this first
@@ -223,7 +224,7 @@ int spec_draft_confidence(const spec_args *args, float threshold, float *out_con
  * Races: all calls on one device share the buffer.  They must be ordered
  * (one stream, or synchronised); two calls in flight at once, on two streams
  * or from two host threads, race and corrupt each other's results. */
-#define SPEC_STATIC_SCRATCH_BYTES (16u << 20)
+#define SPEC_STATIC_SCRATCH_BYTES (1u << 20)
 int spec_verify_sample_static(const spec_args *args, int32_t *out_tokens, int32_t *out_accepted,
                               int32_t *out_status, spec_stream_t stream);
 

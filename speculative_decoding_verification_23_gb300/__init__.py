@@ -32,7 +32,7 @@ SPEC_ERR_ALIGN = -6
 SPEC_ERR_LAUNCH = -7
 SPEC_ERR_DEVICE = -8
 SPEC_ERR_STATIC_SCRATCH = -9
-SPEC_STATIC_SCRATCH_BYTES = 16 << 20
+SPEC_STATIC_SCRATCH_BYTES = 1 << 20
 
 SPEC_STATUS_BAD_TOKEN = 1
 SPEC_STATUS_BAD_PARAM = 2

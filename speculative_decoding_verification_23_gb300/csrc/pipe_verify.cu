@@ -366,6 +366,71 @@ __device__ __forceinline__ const int* cu_ptr(const SampleParams& P, const PSmem&
   return P.B + 1 <= kPipeCuCap ? S.cu() : P.cu_draft;
 }
 
+// The work item's request, position and rows (the same decoding as
+// decode_item, reading cu_draft through `cu`).
+__device__ __forceinline__ Item pdecode(const SampleParams& P, const int* cu, int item) {
+  Item it;
+  if (item < P.total) {
+    int lo = 0, hi = P.B;
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (cu[mid] <= item) lo = mid;
+      else hi = mid;
+    }
+    it.b = lo;
+    it.i = item - cu[lo];
+    it.bonus = false;
+    it.tgt_row = item + lo;
+    it.dft_row = item;
+    it.rows_ok = true;
+  } else {
+    const int b = item - P.total;
+    const int c0 = cu[b], c1 = cu[b + 1];
+    it.b = b;
+    it.i = c1 - c0;
+    it.bonus = true;
+    it.rows_ok = (c0 >= 0 && c0 <= c1 && c1 <= P.total);
+    it.tgt_row = it.rows_ok ? c1 + b : b;
+    it.dft_row = -1;
+  }
+  it.K = cu[it.b + 1] - cu[it.b];
+  return it;
+}
+
+// Per-request scalars and the status bits that follow from them.
+struct Scalars {
+  int b, K, d0, off, nrows, x, flags;
+  float alpha, c, D;
+  bool params_ok, pen, uniforms_ok;
+  int h0, h1, npre;
+};
+
+__device__ __forceinline__ Scalars item_scalars(const SampleParams& P, const Item& it, int item, const int* cu) {
+  Scalars s;
+  s.b = it.b;
+  s.K = it.K;
+  s.d0 = cu[it.b];
+  s.off = s.d0 + it.b;
+  s.nrows = it.bonus ? 1 : 2;
+  s.flags = 0;
+  if (!it.rows_ok || s.K < 0 || s.K > P.max_k || s.K > kMaxK) s.flags |= kStatusBadK;
+  const float T_ = P.temperature ? __ldg(P.temperature + s.b) : 1.f;
+  s.alpha = P.rep_penalty ? __ldg(P.rep_penalty + s.b) : 1.f;
+  s.D = P.tv_budget ? __ldg(P.tv_budget + s.b) : 0.f;
+  s.params_ok = item_params_ok(P, s.b);
+  if (!s.params_ok) s.flags |= kStatusBadParam;
+  // invalid scalars are reported; the statistics then use T = 1, no penalty
+  s.c = __fdiv_rn(1.44269504088896341f, s.params_ok ? T_ : 1.f);
+  s.x = it.bonus ? -1 : __ldg(P.draft_tokens + item);
+  if (!it.bonus && (s.x < 0 || s.x >= P.V)) s.flags |= kStatusBadToken;
+  s.h0 = P.cu_hist ? __ldg(P.cu_hist + s.b) : 0;
+  s.h1 = P.cu_hist ? __ldg(P.cu_hist + s.b + 1) : 0;
+  s.npre = it.bonus ? (it.rows_ok ? s.K : 0) : it.i;
+  s.pen = s.params_ok && s.alpha != 1.f && (s.h1 > s.h0 || s.npre > 0);
+  s.uniforms_ok = !(s.flags & kStatusBadK);
+  return s;
+}
+
 // Marks the penalty set of a request row in `bm` (if pen) and reports
 // out-of-range tokens; threads t of nt.
 __device__ __forceinline__ int mark_penalty_set(const SampleParams& P, const Scalars& s, uint32_t* bm, int t, int nt) {

@@ -171,84 +171,6 @@ inline PipeLayout make_pipe_layout(int V, int elem_bytes, int slots_a, int slots
   return L;
 }
 
-
-// ---------------------------------------- dataflow streaming sampling kernel
-// Each pass over a work item's rows is cut into tasks of one vocabulary
-// chunk; every CTA (one per SM) takes tasks from one global counter, so the
-// whole GPU works on a few items at a time.  Pass-2 tasks of an item are
-// placed `lag_items` items behind its pass-1 tasks, so its rows are still in
-// L2 when they are read again.
-constexpr int kFlowConsumers = 16;      // streaming warps per CTA, in groups of kFlowUnits
-constexpr int kFlowUnits = 8;           // warps (units) per task; groups take alternate slots
-constexpr int kFlowSlots = 4;           // ring slots, one task each
-constexpr int kFlowSlotBytes = 51200;   // two rows of one chunk
-constexpr int kFlowLagRings = 5;        // pass-2 lag, in GPU-wide rings of tasks
-
-// Per ring slot: the task and everything its consumers need.
-struct FlowHdr {
-  int task;       // index in the task sequence, -1 = no more tasks
-  int type;       // 1 = pass 1, 2 = pass 2
-  int item, chunk;
-  int lo_line;    // first 256-token line of the chunk
-  int nlines;     // lines in the chunk
-  int nrows;      // 2 (draft position) or 1 (bonus row)
-  int pen;        // the repetition penalty applies (slot bitmap holds the set)
-  int x;          // draft token (-1 for a bonus row)
-  float c;        // log2(e) / T
-  float alpha;    // repetition penalty
-  float Mt, it, Md, id;  // pass 2: per row reference and 1 / sum
-  int pad[3];
-};
-
-struct FlowLayout {
-  int lpc;         // lines (256 tokens) per chunk
-  int nlines;      // lines per row
-  int nck;         // chunks per row
-  int nu;          // units per row (nck * kFlowUnits): one consumer warp's lines of a chunk
-  int row_bytes;   // one row of a slot
-  int slot_bytes;  // two rows
-  int bm_words;    // penalty bitmap words per slot (lpc * 8)
-  int lag_items;   // pass-2 lag in items
-  int off_ring, off_bm, off_hdr, off_cu, off_tw, off_bar;
-  int total;
-};
-
-inline FlowLayout make_flow_layout(int V, int elem_bytes) {
-  FlowLayout L{};
-  const int maxl = kFlowSlotBytes / (2 * 256 * elem_bytes);
-  L.nlines = (V + 255) / 256;
-  L.nck = (L.nlines + maxl - 1) / maxl;
-  L.lpc = (L.nlines + L.nck - 1) / L.nck;
-  L.nu = L.nck * kFlowUnits;
-  L.row_bytes = L.lpc * 256 * elem_bytes;
-  L.slot_bytes = 2 * L.row_bytes;
-  L.bm_words = L.lpc * 8;
-  int off = 0;
-  L.off_ring = off;  off += kFlowSlots * L.slot_bytes;
-  L.off_bm = off;    off += kFlowSlots * L.bm_words * 4;
-  L.off_hdr = off;   off += kFlowSlots * (int)sizeof(FlowHdr);
-  L.off_cu = off;    off += 1024 * 4;                                  // cu_draft copy (B + 1 <= 1024)
-  L.off_tw = off;    off += align_up_i(L.nu * 4, 16);                  // tail warp's unit masses
-  L.off_bar = off;   off += 3 * kFlowSlots * 8;
-  L.total = align_up_i(off, 128);
-  return L;
-}
-
-// Global workspace of the dataflow kernel (part of the caller's workspace).
-struct FlowWs {
-  uint32_t* hbm;      // [B][hbm_words] history bitmaps
-  int hbm_words;
-  int* rflags;        // [B] status bits of the history tokens
-  int* zero;          // start of the region cleared before each launch:
-  int zero_words;     //   req[B], cnt[2][n_items], ctl[8]
-  int* req;           // [B] decided items per request
-  int* cnt;           // [2][n_items] finished pass-1 / pass-2 tasks per item
-  int* ctl;           // [0] next task, [1] error bits, [2] CTAs done
-  float4* p1;         // [n_items][nu] pass-1 (reference, sum) per unit: target, draft
-  float* p2;          // [n_items][nu] pass-2 residual mass per unit
-  float2* xz;         // [n_items] raw logits of the draft token (target, draft)
-};
-
 struct SampleParams {
   const void* target;
   long long ld_t;
@@ -284,9 +206,6 @@ struct SampleParams {
   int n_clusters;
   SmemLayout L;
   PipeLayout PL;   // pipelined streaming kernel only
-  FlowLayout FL;   // dataflow kernel only
-  FlowWs F;        // dataflow kernel only
-  int n_p2;        // items with a pass 2 (draft positions)
 };
 
 // ------------------------------------------------------------------- greedy
@@ -346,10 +265,7 @@ struct ConfParams {
 
 // -------------------------------------------------------------- workspace
 struct WorkspaceLayout {
-  size_t off_counters, off_results, off_inval, off_partials;
-  size_t off_hbm, off_rflags, off_zero, off_p1, off_p2, off_xz;  // dataflow kernel
-  int hbm_words, nu, zero_words;
-  size_t total;
+  size_t off_counters, off_results, off_inval, off_partials, total;
 };
 
 inline size_t align_up_z(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -366,24 +282,6 @@ inline WorkspaceLayout make_workspace_layout(int B, int total, int V) {
   off = align_up_z(off + items * kMaxCluster * 4, 256);
   W.off_partials = off;
   off = align_up_z(off + items * nck * sizeof(GreedyPartial), 256);
-  // dataflow kernel: units per row of the finer (fp32) chunking covers both dtypes
-  const FlowLayout f4 = make_flow_layout(V, 4), f2 = make_flow_layout(V, 2);
-  W.nu = f4.nu > f2.nu ? f4.nu : f2.nu;
-  W.hbm_words = align_up_i((V + 31) / 32, 8);
-  W.off_hbm = off;
-  off = align_up_z(off + (size_t)B * W.hbm_words * 4, 256);
-  W.off_rflags = off;
-  off = align_up_z(off + (size_t)B * 4, 256);
-  W.off_zero = off;
-  const size_t zw = (size_t)B + 2 * items + 8;
-  W.zero_words = (int)zw;
-  off = align_up_z(off + zw * 4, 256);
-  W.off_p1 = off;
-  off = align_up_z(off + items * W.nu * 16, 256);
-  W.off_p2 = off;
-  off = align_up_z(off + items * W.nu * 4, 256);
-  W.off_xz = off;
-  off = align_up_z(off + items * 8, 256);
   W.total = off;
   return W;
 }

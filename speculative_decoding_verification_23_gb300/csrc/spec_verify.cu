@@ -16,7 +16,8 @@ int choose_stream_layout(int V, int C, int elem_bytes, bool topp, int max_smem, 
                          SmemLayout* L_out);
 int launch_sample_verify(SampleParams& P, bool bf16, bool topp, cudaStream_t stream);
 int launch_greedy_verify(const GreedyParams& P, bool bf16, cudaStream_t stream);
-int launch_flow_verify(SampleParams& P, bool bf16, int num_sms, cudaStream_t stream);
+int choose_pipe_layout(int V, int elem_bytes, int max_smem, PipeLayout* out);
+int launch_pipe_verify(SampleParams& P, bool bf16, int num_sms, cudaStream_t stream);
 int launch_confidence(const ConfParams& P, bool bf16, cudaStream_t stream);
 }  // namespace sv
 
@@ -92,9 +93,9 @@ void fill_sample_inputs(sv::SampleParams& P, const spec_args* a) {
 
 // Picks the kernel variant.  Resident (each logit read once, values kept in
 // the shared memory of a C-CTA cluster) when every work item gets its own
-// cluster in one wave; streaming otherwise: the dataflow kernel (both passes
-// of every item cut into vocabulary-chunk tasks shared by all SMs) without
-// top-p, the cluster kernel's streaming variant with top-p.
+// cluster in one wave; streaming otherwise: the pipelined kernel (one CTA
+// per SM, pass 1 of the next item overlapping pass 2 of the current one)
+// without top-p, the cluster kernel's streaming variant with top-p.
 // SPEC_PREFER_* flags override the choice between resident and streaming.
 int run_sample(sv::SampleParams& P, const spec_args* a, void* ws, cudaStream_t stream) {
   int max_smem = 0, num_sms = 0, smem_per_sm = 0;
@@ -110,36 +111,27 @@ int run_sample(sv::SampleParams& P, const spec_args* a, void* ws, cudaStream_t s
          sv::choose_stream_layout(a->V, C_str, es, topp, max_smem, smem_per_sm, &L_str) != 0)
     C_str *= 2;
   const bool str_ok = C_str <= sv::kMaxCluster;
-  const sv::FlowLayout L_flow = sv::make_flow_layout(a->V, es);
-  const bool flow_ok = !topp && L_flow.total <= max_smem;
-  const bool stream_ok = flow_ok || str_ok;
   bool resident;
   if ((a->flags & SPEC_PREFER_RESIDENT) && res_ok) resident = true;
-  else if ((a->flags & SPEC_PREFER_STREAMING) && stream_ok) resident = false;
-  else resident = res_ok && (!stream_ok || (long long)P.n_items * C_res <= num_sms);
-  if (!resident && !stream_ok) return SPEC_ERR_SHAPE;
+  else if ((a->flags & SPEC_PREFER_STREAMING) && str_ok) resident = false;
+  else resident = res_ok && (!str_ok || (long long)P.n_items * C_res <= num_sms);
+  sv::PipeLayout L_pipe{};
+  const bool pipe_ok = !topp && sv::choose_pipe_layout(a->V, es, max_smem, &L_pipe) == 0 &&
+                       (long long)P.n_items <= (long long)num_sms * sv::kPipeMaxIters;
+  if (!resident && !str_ok && !pipe_ok) return SPEC_ERR_SHAPE;
   const sv::WorkspaceLayout W = sv::make_workspace_layout(a->B, a->total_drafts, a->V);
   unsigned char* w = static_cast<unsigned char*>(ws);
   P.counters = reinterpret_cast<int*>(w + W.off_counters);
   P.results = reinterpret_cast<sv::ItemResult*>(w + W.off_results);
   P.inval = reinterpret_cast<int*>(w + W.off_inval);
-  if (!resident && flow_ok) {
-    const size_t items = (size_t)P.n_items;
-    P.FL = L_flow;
-    P.n_p2 = a->total_drafts;
-    P.F.hbm = reinterpret_cast<uint32_t*>(w + W.off_hbm);
-    P.F.hbm_words = W.hbm_words;
-    P.F.rflags = reinterpret_cast<int*>(w + W.off_rflags);
-    int* z = reinterpret_cast<int*>(w + W.off_zero);
-    P.F.zero = z;
-    P.F.zero_words = (int)((size_t)a->B + 2 * items + 8);
-    P.F.req = z;
-    P.F.cnt = P.F.req + a->B;
-    P.F.ctl = P.F.cnt + 2 * items;
-    P.F.p1 = reinterpret_cast<float4*>(w + W.off_p1);
-    P.F.p2 = reinterpret_cast<float*>(w + W.off_p2);
-    P.F.xz = reinterpret_cast<float2*>(w + W.off_xz);
-    return sv::launch_flow_verify(P, a->dtype == SPEC_BF16, num_sms, stream);
+  if (!resident && pipe_ok) {
+    P.PL = L_pipe;
+    if (P.mode == sv::kModeSample &&
+        cudaMemsetAsync(P.counters, 0, (size_t)a->B * sizeof(int), stream) != cudaSuccess) {
+      cudaGetLastError();
+      return SPEC_ERR_LAUNCH;
+    }
+    return sv::launch_pipe_verify(P, a->dtype == SPEC_BF16, num_sms, stream);
   }
   P.C = resident ? C_res : C_str;
   P.L = resident ? L_res : L_str;
@@ -209,7 +201,8 @@ int spec_verify_sample_static(const spec_args* a, int32_t* out_tokens, int32_t* 
   int rc = check_common(a, true);
   if (rc) return rc;
   if (!out_tokens || !out_accepted || !a->temperature || !a->tv_budget || !a->uniforms) return SPEC_ERR_NULL;
-  if (sv::make_workspace_layout(a->B, a->total_drafts, a->V).total > SPEC_STATIC_SCRATCH_BYTES)
+  // the sampling kernel uses the counters, results and flags regions only
+  if (sv::make_workspace_layout(a->B, a->total_drafts, a->V).off_partials > SPEC_STATIC_SCRATCH_BYTES)
     return SPEC_ERR_STATIC_SCRATCH;
   void* scratch = nullptr;
   rc = static_scratch_address(&scratch);
