@@ -441,7 +441,45 @@ def bench_extras(dev, peak: float, cpu_seconds: float) -> dict:
     cbytes = bb.total_drafts * bb.V * 2 + 4 * int(bb.hist.size) + 8 * bb.total_drafts
     rate = oracle_rate(lambda batch, reqs: oracle.draft_confidence_batch(batch, 0.6, reqs), bb, budget)
     out["draft_confidence_batched_B64_K8"] = line("conf", cbytes, sec, rate, "confidence_kernel")
+    del db, wsb
+    out["acceptance_qwen25_K8"] = acceptance_sweep(dev)
     return out
+
+
+def acceptance_sweep(dev, batches: int = 8, per: int = 32) -> dict:
+    """Acceptance statistics of the GPU path on the Qwen2.5-shaped rows
+    (V=152064, bf16, K=8, rho=0.9, T=0.7, no repetition penalty so that the
+    drafts are draws from q): for each TV budget D, batches * per rounds over
+    the same rows with fresh drafts and uniforms; per position the observed
+    acceptance rate against 1 - max(0, d_i - D) (d_i from spec_tv_budget),
+    and per K' in 1/2/4/8 the accepted and emitted tokens per round, with and
+    without the bonus."""
+    import speculative_decoding_verification_23_gb300 as sv
+    from speculative_decoding_verification_23_gb300 import acceptance as A
+    from speculative_decoding_verification_23_gb300 import workload as W
+    from speculative_decoding_verification_23_gb300.device_batch import to_device
+
+    res = {}
+    for D in (0.0, 0.5, 0.75, 1.0):
+        one = to_device(W.acceptance_trials(D, 1), dev)
+        d = sv.spec_tv_budget(one.args(), device=dev)[0].cpu().numpy().astype(np.float64)
+        accs = []
+        for t in range(batches):
+            db = to_device(W.acceptance_trials(D, per, draws=1 + t), dev)
+            _, acc, st = sv.spec_verify_sample(db.args(), device=dev)
+            assert int(st.abs().max()) == 0
+            accs.append(acc.cpu().numpy())
+            del db
+        rep = A.acceptance_report(np.concatenate(accs), d, D)
+        res[f"D{D}"] = {
+            "rounds": rep["rounds"],
+            "d": [round(x, 5) for x in rep["d"]],
+            "rate": [round(p["rate"], 4) for p in rep["positions"]],
+            "expected": [round(p["expected"], 4) for p in rep["positions"]],
+            "max_abs_z": round(max((abs(p["z"]) for p in rep["positions"] if p["z"] == p["z"]), default=0.0), 2),
+            "k_sweep": [{k: (round(v, 4) if isinstance(v, float) else v) for k, v in s.items()} for s in rep["k_sweep"]],
+        }
+    return res
 
 
 def main():

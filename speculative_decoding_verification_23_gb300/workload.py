@@ -284,6 +284,38 @@ def ragged_top_p(round_: int = 0, B: int = 256) -> Batch:
                       draft_topk=16, name="ragged_top_p")
 
 
+def acceptance_trials(D: float, n: int, round_: int = 0, V: int = QWEN25_VOCAB, K: int = 8,
+                      dtype: str = DTYPE_BF16, rho: float = 0.9, temperature: float = 0.7, draws: int = 0) -> Batch:
+    """``n`` verification rounds over the same rows (the Qwen2.5-shaped
+    request: rho = 0.9, T = 0.7; no repetition penalty, so the draft
+    distribution does not depend on earlier drafts): request t is one round,
+    its drafts drawn afresh by the draft sampler (Gumbel-max over the draft
+    rows / T), its uniforms fresh.  The rounds' accepted counts then sample
+    the acceptance law of these rows."""
+    base = make_batch(B=1, V=V, K=K, dtype=dtype, seed=5 * 10 ** 6 + round_, rho=rho, temperature=temperature,
+                      rep_penalty=1.0, hist_len=0, tv_budget=D, name="acceptance_base")
+    rng = np.random.Generator(np.random.PCG64(6 * 10 ** 6 + 1000 * round_ + draws))
+    tokens = np.empty((n, K), dtype=np.int32)
+    for i in range(K):
+        z = base.draft[i, :V].astype(np.float64) / float(temperature)
+        for t0 in range(0, n, 64):
+            m = min(64, n - t0)
+            g = -np.log(-np.log(rng.random((m, V))))
+            tokens[t0:t0 + m, i] = np.argmax(z[None, :] + g, axis=1)
+    cu_draft = (np.arange(n + 1, dtype=np.int64) * K).astype(np.int32)
+    target = np.tile(base.target, (n, 1))
+    draft = np.tile(base.draft, (n, 1))
+    uniforms = uniforms_from_bits(rng.integers(0, 2 ** 32, size=n * (K + 1), dtype=np.uint64))
+
+    def full(v):
+        return np.full(n, v, dtype=np.float32)
+
+    return Batch(B=n, V=V, ld=base.ld, dtype=dtype, cu_draft=cu_draft, target=target, draft=draft,
+                 draft_tokens=tokens.reshape(-1), cu_hist=np.zeros(n + 1, dtype=np.int32),
+                 hist=np.zeros(0, dtype=np.int32), temperature=full(temperature), rep_penalty=full(1.0),
+                 top_p=full(1.0), tv_budget=full(D), uniforms=uniforms, name=f"acceptance_D{D}")
+
+
 WORKLOADS = {
     "tiny": tiny,
     "qwen25_single": qwen25_single,
