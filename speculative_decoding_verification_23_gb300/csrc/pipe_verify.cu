@@ -488,12 +488,15 @@ __device__ __forceinline__ void producer(const SampleParams& P, const PipeLayout
       // first use of a slot: the phase "before" its first completes at once
       if (!to && !mbar_wait(&empty[slot], rc.phase ^ 1u)) to = true;
       rc.advance(nslots);
-      const int n = min(stage, P.V - st * stage);
+      // ring B takes the stages in reverse: the lines ring A read last are
+      // re-read first, while they are the least likely to have left L2
+      const int sx = IS_A ? st : nst - 1 - st;
+      const int n = min(stage, P.V - sx * stage);
       const uint32_t bytes = (uint32_t)((n * es + 15) & ~15);
       unsigned char* dst = ring + (size_t)slot * slot_bytes;
       mbar_arrive_expect_tx(&full[slot], it.bonus ? bytes : 2 * bytes);
-      bulk_g2s(dst, rowp + (size_t)st * stage * es, bytes, &full[slot], pol);
-      if (!it.bonus) bulk_g2s(dst + (size_t)stage * es, rowq + (size_t)st * stage * es, bytes, &full[slot], pol);
+      bulk_g2s(dst, rowp + (size_t)sx * stage * es, bytes, &full[slot], pol);
+      if (!it.bonus) bulk_g2s(dst + (size_t)stage * es, rowq + (size_t)sx * stage * es, bytes, &full[slot], pol);
     }
   }
 }
@@ -855,7 +858,7 @@ __device__ __forceinline__ void b_stream(const SampleParams& P, const PipeLayout
         const uint32_t slot = rc.slot;
         if (!timeout && !mbar_wait(&S.full_b()[slot], rc.phase)) timeout = true;
         rc.advance(L.slots_b);
-        const int s_id = stn * kNB + wb;
+        const int s_id = (L.nst_b - 1 - stn) * kNB + wb;  // stages in reverse (producer B)
         if (s_id < L.nseg) {
           unsigned char* seg = S.ring_b() + (size_t)slot * L.slot_b + wb * kPipeSegBytes;
           const int base = s_id * SEG;

@@ -283,3 +283,28 @@ def test_many_requests_streaming(dtype):
     assert not bad and near <= 1, (bad[:2], near)
     tok, acc, st = got
     assert np.all(st == 0) and np.all((acc >= 0) & (acc <= K))
+
+
+@pytest.mark.parametrize("dtype,V", [("bf16", 152064), ("f32", 65536), ("bf16", 50000), ("bf16", 262144),
+                                     ("f32", 7)])
+def test_pipeline_shapes(dtype, V):
+    """The pipelined kernel with several items per CTA over vocabularies from
+    7 to 262144 tokens (ragged last stage and segment), ragged K (incl. 0),
+    penalties and budgets: sampled requests against the oracle, the TV path
+    on the same batch, properties on all."""
+    rng = np.random.default_rng(V)
+    B = 24
+    K = [int(k) for k in rng.integers(0, 9, size=B)]
+    K[3] = 0
+    batch = W.make_batch(B=B, V=V, K=K, dtype=dtype, seed=4000 + V, rho=0.9, temperature=0.8,
+                         rep_penalty=[1.0, 1.2, 0.9, 1.1] * 6, hist_len=min(300, 3 * V),
+                         tv_budget=[0.0, 0.25, 0.5, 0.75, 1.0, 0.1] * 4)
+    got = PR.run_sample(batch, flags=STREAMING)
+    sample = [0, 3, 5, 10, 17, 23]
+    ref = PR.oracle_sample(batch, sample)
+    bad, near = PR.compare_sample(batch, got, ref, sample)
+    assert not bad and near <= 1, (bad[:2], near)
+    tok, acc, st = got
+    assert np.all(st == 0) and np.all((acc >= 0) & (acc <= np.array(K)))
+    tvg = PR.run_tv(batch, flags=STREAMING)
+    assert PR.compare_tv(batch, tvg, ref, sample) < PR.TOL_PROB
