@@ -96,6 +96,8 @@ struct PSmem {
   __device__ __forceinline__ uint64_t* stats_full() const { return list_ready() + 2 * kPipeBufs; }
   __device__ __forceinline__ uint64_t* pass2_done() const { return list_ready() + 3 * kPipeBufs; }
   __device__ __forceinline__ uint64_t* buf_free() const { return list_ready() + 4 * kPipeBufs; }
+  // A streaming warps -> tail warp: their share of the last item's pass 2 is done
+  __device__ __forceinline__ uint64_t* pass2a_done() const { return list_ready() + 5 * kPipeBufs; }
 };
 
 __device__ __forceinline__ void fence_proxy_async_smem() {
@@ -361,6 +363,16 @@ __device__ __forceinline__ void finish_item(const SampleParams& P, const Item& i
   }
 }
 
+// Items of this CTA (item k is blockIdx.x + k * gridDim.x).
+__device__ __forceinline__ int n_local_items(const SampleParams& P) {
+  return (int)blockIdx.x < P.n_items ? (P.n_items - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x : 0;
+}
+
+// The last item's pass 2 is shared: ring B / group B take the even
+// positions of its (reversed) stage order, ring A / group A the odd ones,
+// once group A has no pass 1 left.
+__device__ __forceinline__ bool b_skips(int k, int n_local, int stn) { return k == n_local - 1 && (stn & 1); }
+
 // cu_draft as the kernel reads it: the shared-memory copy when it fits.
 __device__ __forceinline__ const int* cu_ptr(const SampleParams& P, const PSmem& S) {
   return P.B + 1 <= kPipeCuCap ? S.cu() : P.cu_draft;
@@ -471,6 +483,7 @@ __device__ __forceinline__ void producer(const SampleParams& P, const PipeLayout
   bool to = false;
   int k = 0;
   const int* cu = cu_ptr(P, S);
+  const int n_local = n_local_items(P);
   for (int item = blockIdx.x; item < P.n_items; item += gridDim.x, ++k) {
     const Item it = pdecode(P, cu, item);
     if (!IS_A) {
@@ -484,6 +497,7 @@ __device__ __forceinline__ void producer(const SampleParams& P, const PipeLayout
     const unsigned char* rowq =
         it.bonus ? rowp : static_cast<const unsigned char*>(P.draft) + (size_t)it.dft_row * P.ld_d * es;
     for (int st = 0; st < nst; ++st) {
+      if (!IS_A && b_skips(k, n_local, st)) continue;
       const uint32_t slot = rc.slot;
       // first use of a slot: the phase "before" its first completes at once
       if (!to && !mbar_wait(&empty[slot], rc.phase ^ 1u)) to = true;
@@ -499,7 +513,71 @@ __device__ __forceinline__ void producer(const SampleParams& P, const PipeLayout
       if (!it.bonus) bulk_g2s(dst + (size_t)stage * es, rowq + (size_t)sx * stage * es, bytes, &full[slot], pol);
     }
   }
+  if (IS_A && n_local > 0) {
+    // ring A then carries the last item's odd pass-2 stages (a re-read, in
+    // ring B's reversed order), once its statistics are combined
+    const int kl = n_local - 1;
+    if (!to && !mbar_wait(&S.stats_full()[kl % kPipeBufs], (uint32_t)(kl / kPipeBufs) & 1u)) to = true;
+    const Item it = pdecode(P, cu, blockIdx.x + kl * gridDim.x);
+    const unsigned char* rowp = static_cast<const unsigned char*>(P.target) + (size_t)it.tgt_row * P.ld_t * es;
+    const unsigned char* rowq =
+        it.bonus ? rowp : static_cast<const unsigned char*>(P.draft) + (size_t)it.dft_row * P.ld_d * es;
+    const uint64_t pol2 = l2_policy_evict_first();
+    for (int st = 1; st < L.nst_b; st += 2) {
+      const uint32_t slot = rc.slot;
+      if (!to && !mbar_wait(&empty[slot], rc.phase ^ 1u)) to = true;
+      rc.advance(nslots);
+      const int sx = L.nst_b - 1 - st;
+      const int n = min(stage, P.V - sx * stage);
+      const uint32_t bytes = (uint32_t)((n * es + 15) & ~15);
+      unsigned char* dst = ring + (size_t)slot * slot_bytes;
+      mbar_arrive_expect_tx(&full[slot], it.bonus ? bytes : 2 * bytes);
+      bulk_g2s(dst, rowp + (size_t)sx * stage * es, bytes, &full[slot], pol2);
+      if (!it.bonus) bulk_g2s(dst + (size_t)stage * es, rowq + (size_t)sx * stage * es, bytes, &full[slot], pol2);
+    }
+  }
 }
+
+// Pass 2 of segment s_id of item buffer kb from a staged ring segment (both
+// rows, kNB * kPipeSegBytes apart): the penalised tokens' exact residuals
+// (or p), their copies -inf, then the segment's mass of max(p-q, 0) (or of
+// p for a bonus row) to segt.
+template <typename T>
+__device__ __forceinline__ void pass2_seg(const SampleParams& P, const PipeLayout& L, const PSmem& S, int kb,
+                                          const Item& it, const Scalars& sc, unsigned char* seg, int s_id, int lane) {
+  const int SEG = L.seg;
+  const int wps = SEG / 32;
+  const int row_bytes = kNB * kPipeSegBytes;
+  const PipeStats& st = *S.stats(kb);
+  const float Mp = st.M[0], Mq = st.M[1], ip = st.inv[0], iq = st.inv[1];
+  float extra = 0.f;
+  if (st.pen) {
+    // penalised positions: their exact residual (or p), then out of the
+    // stream (-inf)
+    const bool two = sc.nrows == 2;
+    bool wrote = false;
+    const bool any = for_penalised(S.bm(kb), s_id, wps, lane, [&](int o) {
+      T* pp = reinterpret_cast<T*>(seg) + o;
+      T* qq = reinterpret_cast<T*>(seg + row_bytes) + o;
+      const float p = prob_of(penalize(to_f32<T>(*pp), sc.alpha), sc.c, Mp, ip);
+      extra += it.bonus ? p : resid_of(p, prob_of(penalize(to_f32<T>(*qq), sc.alpha), sc.c, Mq, iq));
+      *pp = neg_inf<T>();
+      if (two) *qq = neg_inf<T>();
+      wrote = true;
+    });
+    if (any) {
+      if (wrote) fence_proxy_async_smem();
+      __syncwarp();
+    }
+  }
+  const int nvalid = min(SEG, P.V - s_id * SEG);
+  const float v = it.bonus ? seg_resid<T, true>(seg, row_bytes, lane, nvalid, sc.c, Mp, Mq, ip, iq)
+                           : seg_resid<T, false>(seg, row_bytes, lane, nvalid, sc.c, Mp, Mq, ip, iq);
+  const float tot = warp_sum(v + extra);
+  if (lane == 0) S.segt(kb)[s_id] = tot;
+}
+
+static_assert(kPipeWarpsA == kPipeWarpsB, "the rings share a stage size");
 
 // ------------------------------------------------------------- group A
 // Streaming warps: pass 1 of each item over ring A.  Before reading a
@@ -582,6 +660,29 @@ __device__ __forceinline__ void a_stream(const SampleParams& P, const PipeLayout
     if (lane == 0) st.aflags[wa] = pflags | (timeout ? kStatusTimeout : 0);
     __syncwarp();
     if (lane == 0) mbar_arrive(&S.pass1_done()[kb]);
+  }
+  const int n_local = n_local_items(P);
+  if (n_local > 0) {
+    // the odd positions of the last item's pass 2, from ring A
+    const int kl = n_local - 1;
+    const int kb = kl % kPipeBufs;
+    const int item = blockIdx.x + kl * gridDim.x;
+    const Item it = pdecode(P, cu, item);
+    const Scalars sc = item_scalars(P, it, item, cu);
+    if (!timeout && !mbar_wait(&S.stats_full()[kb], (uint32_t)(kl / kPipeBufs) & 1u)) timeout = true;
+    for (int st = 1; st < L.nst_b; st += 2) {
+      const uint32_t slot = rc.slot;
+      if (!timeout && !mbar_wait(&S.full_a()[slot], rc.phase)) timeout = true;
+      rc.advance(L.slots_a);
+      const int s_id = (L.nst_b - 1 - st) * kNA + wa;
+      if (s_id < L.nseg)
+        pass2_seg<T>(P, L, S, kb, it, sc, S.ring_a() + (size_t)slot * L.slot_a + wa * kPipeSegBytes, s_id, lane);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&S.empty_a()[slot]);
+    }
+    if (lane == 0 && timeout) atomicOr(&S.stats(kb)->flags, kStatusTimeout);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&S.pass2a_done()[0]);
   }
 }
 
@@ -833,14 +934,14 @@ __device__ __forceinline__ double owner_search(const float* seg, int n, double u
 }
 
 // ------------------------------------------------------------- group B
+
 // Streaming warps: pass 2 of each item over ring B with the setup warp's
 // normalisers; per lane and segment the sum of max(p-q, 0) (or p for a bonus
 // row); then the segment masses for the tail warp.
 template <typename T>
 __device__ __forceinline__ void b_stream(const SampleParams& P, const PipeLayout& L, const PSmem& S, int wb, int lane) {
-  const int SEG = L.seg;
-  const int row_bytes = kNB * kPipeSegBytes;
   const int* cu = cu_ptr(P, S);
+  const int n_local = n_local_items(P);
   RingCursor rc;
   bool timeout = false;
   int k = 0;
@@ -851,43 +952,14 @@ __device__ __forceinline__ void b_stream(const SampleParams& P, const PipeLayout
     const Scalars sc = item_scalars(P, it, item, cu);
     if (!timeout && !mbar_wait(&S.stats_full()[kb], (uint32_t)(k / kPipeBufs) & 1u)) timeout = true;
     {
-      const bool pen = st.pen != 0;
-      const int wps = SEG / 32;
-      const float Mp = st.M[0], Mq = st.M[1], ip = st.inv[0], iq = st.inv[1];
       for (int stn = 0; stn < L.nst_b; ++stn) {
+        if (b_skips(k, n_local, stn)) continue;
         const uint32_t slot = rc.slot;
         if (!timeout && !mbar_wait(&S.full_b()[slot], rc.phase)) timeout = true;
         rc.advance(L.slots_b);
         const int s_id = (L.nst_b - 1 - stn) * kNB + wb;  // stages in reverse (producer B)
-        if (s_id < L.nseg) {
-          unsigned char* seg = S.ring_b() + (size_t)slot * L.slot_b + wb * kPipeSegBytes;
-          const int base = s_id * SEG;
-          float extra = 0.f;
-          if (pen) {
-            // penalised positions: their exact residual (or p), then out of
-            // the stream (-inf)
-            const bool two = sc.nrows == 2;
-            bool wrote = false;
-            const bool any = for_penalised(S.bm(kb), s_id, wps, lane, [&](int o) {
-              T* pp = reinterpret_cast<T*>(seg) + o;
-              T* qq = reinterpret_cast<T*>(seg + row_bytes) + o;
-              const float p = prob_of(penalize(to_f32<T>(*pp), sc.alpha), sc.c, Mp, ip);
-              extra += it.bonus ? p : resid_of(p, prob_of(penalize(to_f32<T>(*qq), sc.alpha), sc.c, Mq, iq));
-              *pp = neg_inf<T>();
-              if (two) *qq = neg_inf<T>();
-              wrote = true;
-            });
-            if (any) {
-              if (wrote) fence_proxy_async_smem();
-              __syncwarp();
-            }
-          }
-          const int nvalid = min(SEG, P.V - base);
-          const float v = it.bonus ? seg_resid<T, true>(seg, row_bytes, lane, nvalid, sc.c, Mp, Mq, ip, iq)
-                                   : seg_resid<T, false>(seg, row_bytes, lane, nvalid, sc.c, Mp, Mq, ip, iq);
-          const float tot = warp_sum(v + extra);
-          if (lane == 0) S.segt(kb)[s_id] = tot;
-        }
+        if (s_id < L.nseg)
+          pass2_seg<T>(P, L, S, kb, it, sc, S.ring_b() + (size_t)slot * L.slot_b + wb * kPipeSegBytes, s_id, lane);
         __syncwarp();
         if (lane == 0) mbar_arrive(&S.empty_b()[slot]);
       }
@@ -920,6 +992,7 @@ __device__ __forceinline__ void b_tail(const SampleParams& P, const PipeLayout& 
       if (!it.bonus) u_acc = __ldg(P.uniforms + sc.off + it.i);
     }
     if (!timeout && !mbar_wait(&S.pass2_done()[kb], (uint32_t)(k / kPipeBufs) & 1u)) timeout = true;
+    if (k == n_local_items(P) - 1 && !timeout && !mbar_wait(&S.pass2a_done()[0], 0u)) timeout = true;
     {
       const int flags = st.flags | (timeout ? kStatusTimeout : 0);
       const float Mp = st.M[0], Mq = st.M[1], ip = st.inv[0], iq = st.inv[1];
@@ -1232,6 +1305,7 @@ __global__ void __launch_bounds__(kPipeThreads, 1) pipe_verify_kernel(const __gr
       mbar_init(&S.pass2_done()[i], kNB);
       mbar_init(&S.buf_free()[i], 2);
     }
+    mbar_init(&S.pass2a_done()[0], kNA);
     fence_mbar_init();
   }
   for (int w = tid; w < kPipeMaxIters / 32; w += kPipeThreads) S.defer()[w] = 0u;

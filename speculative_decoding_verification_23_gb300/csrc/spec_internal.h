@@ -166,7 +166,7 @@ inline PipeLayout make_pipe_layout(int V, int elem_bytes, int slots_a, int slots
   L.off_misc = off;    off += 1024;
   L.off_defer = off;   off += kPipeMaxIters / 8;
   L.off_cu = off;      off += kPipeCuCap * 4;
-  L.off_bar = off;     off += (2 * slots_a + 2 * slots_b + 5 * kPipeBufs) * 8;
+  L.off_bar = off;     off += (2 * slots_a + 2 * slots_b + 5 * kPipeBufs + 1) * 8;
   L.total = align_up_i(off, 128);
   return L;
 }
