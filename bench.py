@@ -39,6 +39,7 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 KERNEL_SOURCES = ["speculative_decoding_verification_23_gb300/csrc/pipe_verify.cu",
+                  "speculative_decoding_verification_23_gb300/csrc/stream_common.cuh",
                   "speculative_decoding_verification_23_gb300/csrc/verify_common.cuh",
                   "speculative_decoding_verification_23_gb300/csrc/common.cuh",
                   "speculative_decoding_verification_23_gb300/csrc/spec_internal.h"]
@@ -440,7 +441,7 @@ def bench_extras(dev, peak: float, cpu_seconds: float) -> dict:
     sec = timed(lambda: sv.spec_draft_confidence(ab, 0.6, device=dev, workspace=wsb, stream=stream))
     cbytes = bb.total_drafts * bb.V * 2 + 4 * int(bb.hist.size) + 8 * bb.total_drafts
     rate = oracle_rate(lambda batch, reqs: oracle.draft_confidence_batch(batch, 0.6, reqs), bb, budget)
-    out["draft_confidence_batched_B64_K8"] = line("conf", cbytes, sec, rate, "confidence_kernel")
+    out["draft_confidence_batched_B64_K8"] = line("conf", cbytes, sec, rate, "conf_pipe_kernel (pipelined)")
     del db, wsb
     out["acceptance_qwen25_K8"] = acceptance_sweep(dev)
     return out

@@ -92,6 +92,17 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity
   }
 }
 
+// Position in the ring: slot index and the parity of its current use.
+struct RingCursor {
+  uint32_t slot = 0, phase = 0;
+  __device__ __forceinline__ void advance(int nslots) {
+    if (++slot == (uint32_t)nslots) {
+      slot = 0;
+      phase ^= 1u;
+    }
+  }
+};
+
 // ------------------------------------------------------ TMA bulk (1-D) copy
 // Global -> this CTA's shared memory, completion signalled on `bar` as
 // transaction bytes.  dst, src and bytes must be multiples of 16.

@@ -16,8 +16,13 @@
 // counter) combines them per row and writes conf and k_eff.  B extra CTAs
 // report the requests without drafts.  The bound is HBM: every draft logit
 // is read once.
+//
+// Batches with at least one draft row per SM take the pipelined kernel
+// instead (conf_pipe_kernel below): one CTA per SM streams whole rows
+// through a TMA ring, so that the loads never wait on a CTA's serial steps.
 #include "common.cuh"
 #include "spec_internal.h"
+#include "stream_common.cuh"
 
 namespace sv {
 
@@ -243,6 +248,385 @@ __global__ void __launch_bounds__(kGreedyThreads) confidence_kernel(const __grid
     if (P.out_status) P.out_status[b] = st;
   }
   for (int r = tid; r < K; r += kGreedyThreads) P.out_conf[d0 + r] = s_flags ? NAN : s_conf[r];
+}
+
+// ------------------------------------------------------------- pipelined
+// One CTA per SM; draft row k of CTA c is row c + k * gridDim.x.  Warps:
+//   streaming warps (kConfWarps): stage st of a row is segments
+//       st * kConfWarps + w (2 KB each) in one ring slot; warp w keeps per
+//       lane a running reference, the sum of 2^(z'c - ref) and the largest
+//       z' (z' the penalised logit, c = log2(e)/T);
+//   setup warp: the penalty bitmap of row k+1, then row k's combine:
+//       conf = 2^(max z' * c - M) / S with M the largest reference and S
+//       the sum relative to it, the row's status bits, and the request's
+//       k_eff once its last row is done (an atomic counter per request);
+//   producer warp: lane 0 issues one bulk copy per stage (evict_first:
+//       every logit is read once).
+// The penalised positions leave the stream as in the sampling kernels: the
+// lanes holding their bitmap words add their exact terms and overwrite them
+// with -inf before the hot loop reads the segment.
+
+namespace {
+
+constexpr int kCW = kConfWarps;
+constexpr int kConfThreads = (kCW + 2) * 32;
+
+extern __shared__ __align__(128) unsigned char conf_smem[];
+
+struct CSmem {
+  const ConfLayout& L;
+  __device__ __forceinline__ explicit CSmem(const ConfLayout& l) : L(l) {}
+  __device__ __forceinline__ unsigned char* at(int off) const { return conf_smem + off; }
+  __device__ __forceinline__ unsigned char* ring() const { return at(L.off_ring); }
+  __device__ __forceinline__ uint32_t* bm(int kb) const {
+    return reinterpret_cast<uint32_t*>(at(L.off_bm + kb * align_up_i(L.bm_words * 4, 16)));
+  }
+  __device__ __forceinline__ ConfStats* stats(int kb) const {
+    return reinterpret_cast<ConfStats*>(at(L.off_stats + kb * align_up_i((int)sizeof(ConfStats), 16)));
+  }
+  __device__ __forceinline__ int* cu() const { return reinterpret_cast<int*>(at(L.off_cu)); }
+  __device__ __forceinline__ uint64_t* bars() const { return reinterpret_cast<uint64_t*>(at(L.off_bar)); }
+  __device__ __forceinline__ uint64_t* full() const { return bars(); }
+  __device__ __forceinline__ uint64_t* empty() const { return bars() + L.slots; }
+  // [kConfBufs] each: setup warp -> streaming warps: the row's bitmap is
+  // built; streaming warps -> setup warp: the row is streamed
+  __device__ __forceinline__ uint64_t* bm_ready() const { return bars() + 2 * L.slots; }
+  __device__ __forceinline__ uint64_t* row_done() const { return bm_ready() + kConfBufs; }
+};
+
+__device__ __forceinline__ const int* conf_cu(const ConfParams& P, const CSmem& S) {
+  return S.L.cu_ints ? S.cu() : P.cu_draft;
+}
+
+// Rows of this CTA.
+__device__ __forceinline__ int conf_n_local(const ConfParams& P) {
+  return (int)blockIdx.x < P.total ? (P.total - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x : 0;
+}
+
+// Draft row d: its request, position and scalars.
+struct CRow {
+  int b, d0, K, i, h0, h1, flags;
+  float c, alpha;
+  bool valid;  // the request's draft count is valid and d is one of its rows
+  bool pen;    // the repetition penalty applies to the row
+};
+
+__device__ __forceinline__ CRow conf_row(const ConfParams& P, const int* cu, int d) {
+  CRow r;
+  int lo = 0, hi = P.B;  // the largest b with cu_draft[b] <= d
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (cu[mid] <= d) lo = mid;
+    else hi = mid;
+  }
+  r.b = lo;
+  r.d0 = cu[lo];
+  r.K = cu[lo + 1] - r.d0;
+  r.i = d - r.d0;
+  r.valid = r.K >= 0 && r.K <= P.max_k && r.K <= kMaxK && r.i >= 0 && r.i < r.K;
+  r.flags = conf_params(P, r.b, r.c, r.alpha) | (r.valid ? 0 : kStatusBadK);
+  r.h0 = P.cu_hist ? __ldg(P.cu_hist + r.b) : 0;
+  r.h1 = P.cu_hist ? __ldg(P.cu_hist + r.b + 1) : 0;
+  r.pen = !(r.flags & kStatusBadParam) && r.alpha != 1.f && (r.h1 > r.h0 || (r.valid && r.i > 0));
+  return r;
+}
+
+// Row d's penalty set (history plus the drafts before the row) into bm when
+// the penalty applies; reports out-of-range tokens of the history and the
+// row's own draft token (the request's rows together cover all its drafts).
+// One warp.
+__device__ __forceinline__ int conf_mark(const ConfParams& P, const CRow& r, int d, uint32_t* bm, int lane) {
+  int flags = 0;
+  // eight loads in flight per lane before their bits are set
+  for (int j0 = r.h0 + lane; j0 < r.h1; j0 += 8 * 32) {
+    int tok[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) tok[q] = j0 + 32 * q < r.h1 ? __ldg(P.hist + j0 + 32 * q) : 0;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      if (j0 + 32 * q >= r.h1) continue;
+      if (tok[q] < 0 || tok[q] >= P.V) flags |= kStatusBadToken;
+      else if (r.pen) atomicOr(&bm[tok[q] >> 5], 1u << (tok[q] & 31));
+    }
+  }
+  const int npre = r.valid ? r.i : 0;
+  for (int j = lane; j < npre; j += 32) {
+    const int t = __ldg(P.draft_tokens + r.d0 + j);
+    if (r.pen && t >= 0 && t < P.V) atomicOr(&bm[t >> 5], 1u << (t & 31));
+  }
+  if (lane == 0) {
+    const int x = __ldg(P.draft_tokens + d);
+    if (x < 0 || x >= P.V) flags |= kStatusBadToken;
+  }
+  return flags;
+}
+
+// One staged 2 KB segment for one lane: the largest value and the pass-1
+// statistics (reference, sum of 2^(z'c - ref)).
+template <typename T>
+__device__ __forceinline__ void seg_stats_max(const unsigned char* seg, int lane, int nvalid, float c, float& ref,
+                                              float& run, float& zmax) {
+  constexpr int N = Vec<T>::N;
+  uint4 v[4];
+  lds_seg(seg, lane, v);
+  float z[4][N];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) cvt16(v[j], z[j]);
+  if (nvalid < 128 * N) mask_tail<N>(z, lane, nvalid);
+  float m0 = zmax, m1 = -INFINITY;
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+#pragma unroll
+    for (int e = 0; e < N; e += 2) {
+      m0 = fmaxf(m0, z[j][e]);
+      m1 = fmaxf(m1, z[j][e + 1]);
+    }
+  zmax = fmaxf(m0, m1);
+  stats_row<N>(z, c, ref, run);
+}
+
+template <typename T>
+__device__ __forceinline__ void conf_stream(const ConfParams& P, const CSmem& S, int w, int lane) {
+  const ConfLayout& L = S.L;
+  const int SEG = L.seg, wps = SEG / 32;
+  const int* cu = conf_cu(P, S);
+  const int n_local = conf_n_local(P);
+  RingCursor rc;
+  bool to = false;
+  for (int k = 0; k < n_local; ++k) {
+    const int kb = k % kConfBufs;
+    const CRow r = conf_row(P, cu, blockIdx.x + k * gridDim.x);
+    if (!to && !mbar_wait(&S.bm_ready()[kb], (uint32_t)(k / kConfBufs) & 1u)) to = true;
+    ConfStats& st = *S.stats(kb);
+    const bool pen = st.pen != 0;
+    float ref = -INFINITY, run = 0.f, pref = -INFINITY, psum = 0.f, zmax = -INFINITY;
+    int pflags = 0;
+    for (int stn = 0; stn < L.nst; ++stn) {
+      const uint32_t slot = rc.slot;
+      if (!to && !mbar_wait(&S.full()[slot], rc.phase)) to = true;
+      rc.advance(L.slots);
+      const int s_id = stn * kCW + w;
+      if (s_id < L.nseg) {
+        unsigned char* seg = S.ring() + (size_t)slot * L.slot_bytes + w * 2048;
+        if (pen) {
+          // penalised positions: their exact terms, then out of the stream
+          bool wrote = false;
+          const bool any = for_penalised(S.bm(kb), s_id, wps, lane, [&](int o) {
+            T* pp = reinterpret_cast<T*>(seg) + o;
+            const float z = to_f32<T>(*pp);
+            if (is_bad_logit(z)) pflags |= kStatusBadLogits;
+            const float zp = penalize(z, r.alpha);
+            zmax = fmaxf(zmax, zp);
+            online_add(zp * r.c, pref, psum);
+            *pp = neg_inf<T>();
+            wrote = true;
+          });
+          if (any) {
+            if (wrote) fence_proxy_async_smem();
+            __syncwarp();
+          }
+        }
+        seg_stats_max<T>(seg, lane, min(SEG, P.V - s_id * SEG), r.c, ref, run, zmax);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&S.empty()[slot]);
+    }
+    combine_into(make_float2(pref, psum), ref, run);
+    const float2 wv = warp_combine(ref, run);
+    zmax = warp_max(zmax);
+    pflags = warp_or(pflags);
+    if (lane == 0) {
+      st.wp[w] = wv;
+      st.zmax[w] = zmax;
+      st.wflags[w] = pflags | (to ? kStatusTimeout : 0);
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&S.row_done()[kb]);
+  }
+}
+
+template <typename T>
+__device__ __forceinline__ void conf_setup(const ConfParams& P, const CSmem& S, int lane) {
+  const ConfLayout& L = S.L;
+  const int* cu = conf_cu(P, S);
+  const int n_local = conf_n_local(P);
+  bool to = false;
+
+  auto build = [&](int k) {
+    // buffer k % kConfBufs was last used by row k - 2, combined already
+    const int d = blockIdx.x + k * gridDim.x;
+    const int kb = k % kConfBufs;
+    const CRow r = conf_row(P, cu, d);
+    uint32_t* bm = S.bm(kb);
+    if (r.pen)
+      for (int q = lane; q < L.bm_words / 4; q += 32) reinterpret_cast<uint4*>(bm)[q] = make_uint4(0u, 0u, 0u, 0u);
+    __syncwarp();
+    const int flags = warp_or(r.flags | conf_mark(P, r, d, bm, lane));
+    ConfStats& st = *S.stats(kb);
+    if (lane == 0) {
+      st.flags = flags;
+      st.pen = r.pen ? 1 : 0;
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&S.bm_ready()[kb]);
+  };
+
+  auto combine = [&](int k) {
+    const int d = blockIdx.x + k * gridDim.x;
+    const int kb = k % kConfBufs;
+    const CRow r = conf_row(P, cu, d);
+    if (!to && !mbar_wait(&S.row_done()[kb], (uint32_t)(k / kConfBufs) & 1u)) to = true;
+    const ConfStats& st = *S.stats(kb);
+    const float2 v = lane < kCW ? st.wp[lane] : make_float2(-INFINITY, 0.f);
+    const float2 t = warp_combine(v.x, v.y);  // (M, S)
+    const float zm = warp_max(lane < kCW ? st.zmax[lane] : -INFINITY);
+    int flags = st.flags | (to ? kStatusTimeout : 0) | warp_or(lane < kCW ? st.wflags[lane] : 0);
+    if (!(t.y > 0.f) || !(t.y < INFINITY) || !(t.x < INFINITY) || !(zm < INFINITY)) flags |= kStatusBadLogits;
+    const float conf = flags ? NAN : __fdiv_rn(ex2(fmaf(zm, r.c, -t.x)), t.y);
+    int last = 0;
+    if (lane == 0 && r.valid) {
+      P.out_conf[d] = conf;
+      ConfPartial cp;
+      cp.m = conf;
+      cp.s = 0.f;
+      cp.flags = flags;
+      cp.pad = 0;
+      P.partials[d] = cp;
+      __threadfence();
+      last = atomicAdd(P.counters + r.b, 1) == r.K - 1;
+    }
+    if (__shfl_sync(0xffffffffu, last, 0)) {
+      // the request's last row: status and the confidence-stopped count
+      __threadfence();
+      int f = 0;
+      float cf = 0.f;
+      if (lane < r.K) {
+        f = __ldcg(&P.partials[r.d0 + lane].flags);
+        cf = __ldcg(&P.partials[r.d0 + lane].m);
+      }
+      f = warp_or(f);
+      const unsigned below = __ballot_sync(0xffffffffu, lane < r.K && cf < P.threshold);
+      if (lane == 0) {
+        P.out_k_eff[r.b] = f ? -1 : (below ? __ffs(below) : r.K);
+        if (P.out_status) P.out_status[r.b] = f;
+      }
+      if (f && lane < r.K) P.out_conf[r.d0 + lane] = NAN;
+    }
+  };
+
+  if (n_local > 0) build(0);
+  for (int k = 0; k < n_local; ++k) {
+    if (k + 1 < n_local) build(k + 1);
+    combine(k);
+  }
+
+  // requests without drafts, or with an invalid draft count (their rows
+  // wrote nothing)
+  for (int b = blockIdx.x; b < P.B; b += gridDim.x) {
+    const int d0 = cu[b];
+    const int K = cu[b + 1] - d0;
+    const bool bad_k = K < 0 || K > P.max_k || K > kMaxK;
+    if (K != 0 && !bad_k) continue;
+    float c, alpha;
+    int flags = conf_params(P, b, c, alpha) | (bad_k ? kStatusBadK : 0);
+    if (bad_k)
+      for (int r = max(d0, 0) + lane; r < min(d0 + K, P.total); r += 32) P.out_conf[r] = NAN;
+    const int h0 = P.cu_hist ? __ldg(P.cu_hist + b) : 0;
+    const int h1 = P.cu_hist ? __ldg(P.cu_hist + b + 1) : 0;
+    for (int j = h0 + lane; j < h1; j += 32) {
+      const int t = __ldg(P.hist + j);
+      if (t < 0 || t >= P.V) flags |= kStatusBadToken;
+    }
+    flags = warp_or(flags);
+    if (lane == 0) {
+      P.out_k_eff[b] = flags ? -1 : 0;
+      if (P.out_status) P.out_status[b] = flags;
+    }
+  }
+}
+
+template <typename T>
+__device__ __forceinline__ void conf_producer(const ConfParams& P, const CSmem& S) {
+  const ConfLayout& L = S.L;
+  constexpr int es = (int)sizeof(T);
+  const uint64_t pol = l2_policy_evict_first();
+  const int stage = kCW * L.seg;  // tokens per stage
+  const int n_local = conf_n_local(P);
+  RingCursor rc;
+  bool to = false;
+  for (int k = 0; k < n_local; ++k) {
+    const int d = blockIdx.x + k * gridDim.x;
+    const unsigned char* row = static_cast<const unsigned char*>(P.draft) + (size_t)d * P.ld_d * es;
+    for (int st = 0; st < L.nst; ++st) {
+      const uint32_t slot = rc.slot;
+      // first use of a slot: the phase "before" its first completes at once
+      if (!to && !mbar_wait(&S.empty()[slot], rc.phase ^ 1u)) to = true;
+      rc.advance(L.slots);
+      // the row's padded stride (a multiple of 16 bytes) covers the rounding
+      const int n = min(stage, P.V - st * stage);
+      const uint32_t bytes = (uint32_t)((n * es + 15) & ~15);
+      mbar_arrive_expect_tx(&S.full()[slot], bytes);
+      bulk_g2s(S.ring() + (size_t)slot * L.slot_bytes, row + (size_t)st * stage * es, bytes, &S.full()[slot], pol);
+    }
+  }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kConfThreads, 1) conf_pipe_kernel(const __grid_constant__ ConfParams P) {
+  const ConfLayout& L = P.CL;
+  const CSmem S(L);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
+  if (tid == 0) {
+    for (int s = 0; s < L.slots; ++s) {
+      mbar_init(&S.full()[s], 1);
+      mbar_init(&S.empty()[s], kCW);
+    }
+    for (int i = 0; i < kConfBufs; ++i) {
+      mbar_init(&S.bm_ready()[i], 1);
+      mbar_init(&S.row_done()[i], kCW);
+    }
+    fence_mbar_init();
+  }
+  for (int i = tid; i < L.cu_ints; i += kConfThreads) S.cu()[i] = __ldg(P.cu_draft + i);
+  __syncthreads();
+  if (warp < kCW) conf_stream<T>(P, S, warp, lane);
+  else if (warp == kCW) conf_setup<T>(P, S, lane);
+  else if (lane == 0) conf_producer<T>(P, S);
+}
+
+}  // namespace
+
+// Layout of the pipelined kernel (-1 if it does not fit `max_smem`).
+int choose_conf_layout(int V, int elem_bytes, int B, int max_smem, ConfLayout* out) {
+  for (int slots = kConfSlots; slots >= 2; --slots) {
+    const ConfLayout L = make_conf_layout(V, elem_bytes, slots, B);
+    if (L.total <= max_smem) {
+      *out = L;
+      return 0;
+    }
+  }
+  return -1;
+}
+
+int launch_conf_pipe(const ConfParams& P, bool bf16, int num_sms, cudaStream_t stream) {
+  const int smem = P.CL.total;
+  const int grid = P.total < 1 ? 1 : (P.total < num_sms ? P.total : num_sms);
+  if (bf16) {
+    auto kern = conf_pipe_kernel<__nv_bfloat16>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) {
+      cudaGetLastError();
+      return -8;
+    }
+    kern<<<grid, kConfThreads, smem, stream>>>(P);
+  } else {
+    auto kern = conf_pipe_kernel<float>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) {
+      cudaGetLastError();
+      return -8;
+    }
+    kern<<<grid, kConfThreads, smem, stream>>>(P);
+  }
+  return cudaGetLastError() == cudaSuccess ? 0 : -7;
 }
 
 int launch_confidence(const ConfParams& P, bool bf16, cudaStream_t stream) {

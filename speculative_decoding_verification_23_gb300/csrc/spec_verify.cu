@@ -19,6 +19,8 @@ int launch_greedy_verify(const GreedyParams& P, bool bf16, cudaStream_t stream);
 int choose_pipe_layout(int V, int elem_bytes, int max_smem, PipeLayout* out);
 int launch_pipe_verify(SampleParams& P, bool bf16, int num_sms, cudaStream_t stream);
 int launch_confidence(const ConfParams& P, bool bf16, cudaStream_t stream);
+int choose_conf_layout(int V, int elem_bytes, int B, int max_smem, ConfLayout* out);
+int launch_conf_pipe(const ConfParams& P, bool bf16, int num_sms, cudaStream_t stream);
 }  // namespace sv
 
 namespace {
@@ -324,7 +326,12 @@ int spec_draft_confidence(const spec_args* a, float threshold, float* out_conf, 
     cudaGetLastError();
     return SPEC_ERR_LAUNCH;
   }
-  rc = sv::launch_confidence(P, a->dtype == SPEC_BF16, s);
+  // at least one draft row per SM: the pipelined kernel (whole rows per
+  // CTA); smaller batches spread each row over 8192-token chunks
+  if (a->total_drafts >= num_sms && sv::choose_conf_layout(a->V, es, a->B, max_smem, &P.CL) == 0)
+    rc = sv::launch_conf_pipe(P, a->dtype == SPEC_BF16, num_sms, s);
+  else
+    rc = sv::launch_confidence(P, a->dtype == SPEC_BF16, s);
   return rc == 0 ? SPEC_OK : (rc == -2 ? SPEC_ERR_SHAPE : SPEC_ERR_LAUNCH);
 }
 

@@ -214,17 +214,6 @@ __device__ __forceinline__ float max8(const float* z) {
   return fmaxf(m, fmaxf(fmaxf(z[4], z[5]), fmaxf(z[6], z[7])));
 }
 
-// Position in the ring: slot index and the parity of its current use.
-struct RingCursor {
-  uint32_t slot = 0, phase = 0;
-  __device__ __forceinline__ void advance(int nslots) {
-    if (++slot == (uint32_t)nslots) {
-      slot = 0;
-      phase ^= 1u;
-    }
-  }
-};
-
 // Streaming pass-1 statistics of one chunk of NR rows with a per-lane running
 // reference (no warp-wide step in the hot loop): each lane keeps refc, the
 // running maximum of z'c it has seen when a chunk would overflow (sum above

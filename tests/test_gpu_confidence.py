@@ -67,3 +67,55 @@ def test_confidence_invalid_requests():
     batch.draft[5, 5] = np.nan            # request 3 (rows 4, 5), row 1: NaN
     conf, k_eff, st, ref = _check(batch, 0.5)
     assert list(st != 0) == [True, True, True, True]
+
+
+def _sms():
+    import torch
+
+    return torch.cuda.get_device_properties(0).multi_processor_count
+
+
+_KS = [0, 8, 3, 6, 1, 8, 5, 7]
+
+
+def _wide(V, dtype, seed, **kw):
+    """A batch with more draft rows than SMs: the pipelined kernel, one CTA
+    per SM streaming whole rows."""
+    B = len(_KS) * (_sms() // sum(_KS) + 1)
+    reps = B // len(_KS)
+    args = dict(rho=[0.3, 0.6, 0.8, 0.9, 0.95, 0.99, 0.5, 0.7] * reps,
+                temperature=[0.5, 0.7, 1.0, 1.3, 0.9, 0.6, 2.0, 0.8] * reps,
+                rep_penalty=[1.0, 1.3, 1.1, 0.8, 1.2, 1.0, 1.5, 0.9] * reps, hist_len=min(24, 3 * V))
+    args.update(kw)
+    batch = W.make_batch(B=B, V=V, K=_KS * reps, dtype=dtype, seed=seed, **args)
+    assert batch.total_drafts >= _sms()
+    return batch
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("V", [3, 1000, 8193, 50000])
+def test_confidence_pipelined_shapes(dtype, V):
+    """Ragged K including 0, penalties with history, temperatures; V spans
+    one partial segment, one stage, a ragged last stage and many stages."""
+    batch = _wide(V, dtype, 7000 + V)
+    for thr in (0.05, 0.3, 0.6):
+        _check(batch, thr)
+
+
+def test_confidence_pipelined_batched_workload():
+    """The batched workload (B=64, K=8, V=152064, bf16, 512-token histories
+    with a 1.1 penalty): 512 rows over the SMs, several rows per CTA."""
+    _check(W.batched(), 0.45)
+
+
+def test_confidence_pipelined_invalid_requests():
+    batch = _wide(600, "f32", 11, hist_len=3, rep_penalty=1.1)
+    cu = batch.cu_draft
+    batch.draft_tokens[int(cu[1]) + 1] = 600          # request 1: token out of range
+    batch.temperature[2] = -1.0                        # request 2: T < 0
+    batch.hist[8 * 3] = 9999                           # request 8 (no drafts): bad history token
+    batch.draft[int(cu[3]) + 2, 5] = np.nan            # request 3, row 2: NaN
+    batch.draft[int(cu[5]) + 4, 7] = np.inf            # request 5, row 4: +inf
+    conf, k_eff, st, ref = _check(batch, 0.5)
+    assert st[1] and st[2] and st[3] and st[5] and st[8]
+    assert not st[4] and not st[6]
