@@ -22,6 +22,7 @@
 // through a TMA ring, so that the loads never wait on a CTA's serial steps.
 #include "common.cuh"
 #include "spec_internal.h"
+#include "conf_internal.h"
 #include "stream_common.cuh"
 
 namespace sv {
@@ -334,27 +335,27 @@ __device__ __forceinline__ CRow conf_row(const ConfParams& P, const int* cu, int
 // Row d's penalty set (history plus the drafts before the row) into bm when
 // the penalty applies; reports out-of-range tokens of the history and the
 // row's own draft token (the request's rows together cover all its drafts).
-// One warp.
-__device__ __forceinline__ int conf_mark(const ConfParams& P, const CRow& r, int d, uint32_t* bm, int lane) {
+// Thread t of nt.
+__device__ __forceinline__ int conf_mark(const ConfParams& P, const CRow& r, int d, uint32_t* bm, int t, int nt) {
   int flags = 0;
-  // eight loads in flight per lane before their bits are set
-  for (int j0 = r.h0 + lane; j0 < r.h1; j0 += 8 * 32) {
+  // eight loads in flight per thread before their bits are set
+  for (int j0 = r.h0 + t; j0 < r.h1; j0 += 8 * nt) {
     int tok[8];
 #pragma unroll
-    for (int q = 0; q < 8; ++q) tok[q] = j0 + 32 * q < r.h1 ? __ldg(P.hist + j0 + 32 * q) : 0;
+    for (int q = 0; q < 8; ++q) tok[q] = j0 + nt * q < r.h1 ? __ldg(P.hist + j0 + nt * q) : 0;
 #pragma unroll
     for (int q = 0; q < 8; ++q) {
-      if (j0 + 32 * q >= r.h1) continue;
+      if (j0 + nt * q >= r.h1) continue;
       if (tok[q] < 0 || tok[q] >= P.V) flags |= kStatusBadToken;
       else if (r.pen) atomicOr(&bm[tok[q] >> 5], 1u << (tok[q] & 31));
     }
   }
   const int npre = r.valid ? r.i : 0;
-  for (int j = lane; j < npre; j += 32) {
-    const int t = __ldg(P.draft_tokens + r.d0 + j);
-    if (r.pen && t >= 0 && t < P.V) atomicOr(&bm[t >> 5], 1u << (t & 31));
+  for (int j = t; j < npre; j += nt) {
+    const int tk = __ldg(P.draft_tokens + r.d0 + j);
+    if (r.pen && tk >= 0 && tk < P.V) atomicOr(&bm[tk >> 5], 1u << (tk & 31));
   }
-  if (lane == 0) {
+  if (t == 0) {
     const int x = __ldg(P.draft_tokens + d);
     if (x < 0 || x >= P.V) flags |= kStatusBadToken;
   }
@@ -389,16 +390,15 @@ template <typename T>
 __device__ __forceinline__ void conf_stream(const ConfParams& P, const CSmem& S, int w, int lane) {
   const ConfLayout& L = S.L;
   const int SEG = L.seg, wps = SEG / 32;
-  const int* cu = conf_cu(P, S);
   const int n_local = conf_n_local(P);
   RingCursor rc;
   bool to = false;
   for (int k = 0; k < n_local; ++k) {
     const int kb = k % kConfBufs;
-    const CRow r = conf_row(P, cu, blockIdx.x + k * gridDim.x);
     if (!to && !mbar_wait(&S.bm_ready()[kb], (uint32_t)(k / kConfBufs) & 1u)) to = true;
     ConfStats& st = *S.stats(kb);
     const bool pen = st.pen != 0;
+    const float c = st.c, alpha = st.alpha;
     float ref = -INFINITY, run = 0.f, pref = -INFINITY, psum = 0.f, zmax = -INFINITY;
     int pflags = 0;
     for (int stn = 0; stn < L.nst; ++stn) {
@@ -415,9 +415,9 @@ __device__ __forceinline__ void conf_stream(const ConfParams& P, const CSmem& S,
             T* pp = reinterpret_cast<T*>(seg) + o;
             const float z = to_f32<T>(*pp);
             if (is_bad_logit(z)) pflags |= kStatusBadLogits;
-            const float zp = penalize(z, r.alpha);
+            const float zp = penalize(z, alpha);
             zmax = fmaxf(zmax, zp);
-            online_add(zp * r.c, pref, psum);
+            online_add(zp * c, pref, psum);
             *pp = neg_inf<T>();
             wrote = true;
           });
@@ -426,7 +426,7 @@ __device__ __forceinline__ void conf_stream(const ConfParams& P, const CSmem& S,
             __syncwarp();
           }
         }
-        seg_stats_max<T>(seg, lane, min(SEG, P.V - s_id * SEG), r.c, ref, run, zmax);
+        seg_stats_max<T>(seg, lane, min(SEG, P.V - s_id * SEG), c, ref, run, zmax);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&S.empty()[slot]);
@@ -461,11 +461,13 @@ __device__ __forceinline__ void conf_setup(const ConfParams& P, const CSmem& S, 
     if (r.pen)
       for (int q = lane; q < L.bm_words / 4; q += 32) reinterpret_cast<uint4*>(bm)[q] = make_uint4(0u, 0u, 0u, 0u);
     __syncwarp();
-    const int flags = warp_or(r.flags | conf_mark(P, r, d, bm, lane));
+    const int flags = warp_or(r.flags | conf_mark(P, r, d, bm, lane, 32));
     ConfStats& st = *S.stats(kb);
     if (lane == 0) {
       st.flags = flags;
       st.pen = r.pen ? 1 : 0;
+      st.c = r.c;
+      st.alpha = r.alpha;
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&S.bm_ready()[kb]);
@@ -514,7 +516,8 @@ __device__ __forceinline__ void conf_setup(const ConfParams& P, const CSmem& S, 
     }
   };
 
-  if (n_local > 0) build(0);
+  // row 0's set was built by all compute warps
+  if (n_local > 0 && lane == 0) mbar_arrive(&S.bm_ready()[0]);
   for (int k = 0; k < n_local; ++k) {
     if (k + 1 < n_local) build(k + 1);
     combine(k);
@@ -589,6 +592,25 @@ __global__ void __launch_bounds__(kConfThreads, 1) conf_pipe_kernel(const __grid
   }
   for (int i = tid; i < L.cu_ints; i += kConfThreads) S.cu()[i] = __ldg(P.cu_draft + i);
   __syncthreads();
+  if (warp <= kCW && conf_n_local(P) > 0) {
+    // the first row's penalty set, by all compute warps while the producer
+    // fills the ring (the setup warp builds the later ones alone)
+    constexpr int nt = (kCW + 1) * 32;
+    const CRow r = conf_row(P, conf_cu(P, S), blockIdx.x);
+    ConfStats& st = *S.stats(0);
+    if (r.pen)
+      for (int q = tid; q < L.bm_words / 4; q += nt) reinterpret_cast<uint4*>(S.bm(0))[q] = make_uint4(0u, 0u, 0u, 0u);
+    if (tid == 0) {
+      st.flags = r.flags;
+      st.pen = r.pen ? 1 : 0;
+      st.c = r.c;
+      st.alpha = r.alpha;
+    }
+    named_sync(1, nt);
+    const int f = warp_or(conf_mark(P, r, blockIdx.x, S.bm(0), tid, nt));
+    if (lane == 0 && f) atomicOr(&st.flags, f);
+    named_sync(1, nt);
+  }
   if (warp < kCW) conf_stream<T>(P, S, warp, lane);
   else if (warp == kCW) conf_setup<T>(P, S, lane);
   else if (lane == 0) conf_producer<T>(P, S);

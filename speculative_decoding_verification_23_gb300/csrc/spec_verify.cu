@@ -9,6 +9,7 @@
 
 #include "spec_verify.h"
 #include "spec_internal.h"
+#include "conf_internal.h"
 
 namespace sv {
 int choose_resident_layout(int V, int elem_bytes, bool topp, int max_smem, int* C_out, SmemLayout* L_out);
