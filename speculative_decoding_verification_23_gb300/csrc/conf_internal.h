@@ -7,10 +7,12 @@
 namespace sv {
 
 // ------------------------------------------------------ draft confidence
+// Chunked kernel: one partial per (row, chunk).  Pipelined kernel: one per
+// row, m holding the row's confidence (s and pad unused).
 struct ConfPartial {
   float m;    // chunk maximum of the penalised logits
   float s;    // sum over the chunk of 2^((z' - m) c)
-  int flags;
+  int flags;  // status bits
   int pad;
 };
 

@@ -257,7 +257,8 @@ __global__ void __launch_bounds__(kGreedyThreads) confidence_kernel(const __grid
 //       st * kConfWarps + w (2 KB each) in one ring slot; warp w keeps per
 //       lane a running reference, the sum of 2^(z'c - ref) and the largest
 //       z' (z' the penalised logit, c = log2(e)/T);
-//   setup warp: the penalty bitmap of row k+1, then row k's combine:
+//   setup warp: the penalty bitmap of row k+1 (all compute warps build
+//       row 0's together at the start), then row k's combine:
 //       conf = 2^(max z' * c - M) / S with M the largest reference and S
 //       the sum relative to it, the row's status bits, and the request's
 //       k_eff once its last row is done (an atomic counter per request);
