@@ -119,3 +119,43 @@ def test_confidence_pipelined_invalid_requests():
     conf, k_eff, st, ref = _check(batch, 0.5)
     assert st[1] and st[2] and st[3] and st[5] and st[8]
     assert not st[4] and not st[6]
+
+
+def _run_args(db, args, threshold):
+    import torch
+
+    import speculative_decoding_verification_23_gb300 as sv
+
+    conf, k_eff, st = sv.spec_draft_confidence(args, threshold)
+    torch.cuda.synchronize()
+    return conf.cpu().numpy().astype(np.float64), k_eff.cpu().numpy(), st.cpu().numpy()
+
+
+@pytest.mark.parametrize("wide", [False, True], ids=["chunked", "pipelined"])
+def test_confidence_draft_count_above_max_k(wide):
+    """A request with more drafts than the call's max_k is reported (status
+    bit 8, k_eff = -1, NaN confidences); the other requests are unaffected."""
+    from speculative_decoding_verification_23_gb300.device_batch import to_device
+
+    if wide:
+        batch = _wide(3000, "bf16", 21, rep_penalty=1.2)
+        max_k = 5
+    else:
+        batch = W.make_batch(B=6, V=3000, K=[0, 1, 3, 8, 5, 2], dtype="bf16", seed=22, hist_len=9,
+                             rep_penalty=1.2)
+        max_k = 4
+    assert batch.total_drafts <= batch.B * max_k
+    db = to_device(batch)
+    args = db.args()
+    args.max_k = max_k
+    conf, k_eff, st = _run_args(db, args, 0.4)
+    ref = oracle.draft_confidence_batch(batch, 0.4, None)
+    for b in range(batch.B):
+        d0, d1 = int(batch.cu_draft[b]), int(batch.cu_draft[b + 1])
+        if d1 - d0 > max_k:
+            assert st[b] & 8 and k_eff[b] == -1 and np.all(np.isnan(conf[d0:d1])), b
+            continue
+        assert st[b] == ref["status"][b], b
+        np.testing.assert_allclose(conf[d0:d1], ref["conf"][d0:d1], atol=1e-5, rtol=0)
+        if not ref["near_tie"][b]:
+            assert k_eff[b] == ref["k_eff"][b], b
