@@ -25,7 +25,7 @@ the method in the order the pages give them:
   stops proposing below a threshold; the low-confidence token is still
   verified.
 
-Readings where the pages are silent (each is listed in the design doc):
+Readings where the pages are silent (the same readings the kernels implement):
 
 * Repetition penalty (named only): for every distinct token of the request's
   history plus the drafts that precede the row, z' = z/alpha if z > 0 else
