@@ -129,9 +129,13 @@ enum {
    every logit once; it suits batches whose work items (sum K_b + B) all fit
    in one wave of clusters.  STREAMING re-reads each slice from L2 for the
    second pass and keeps about one item per SM in flight; it suits large
-   batches.  Without a hint the library picks by batch size. */
+   batches.  SPLIT (without top-p) cuts every row into vocabulary segments
+   spread over all SMs: one read of each logit for the softmax statistics,
+   and a second read of only the rows of positions whose decision those
+   statistics leave open.  Without a hint the library picks by batch size. */
 #define SPEC_PREFER_RESIDENT 2u
 #define SPEC_PREFER_STREAMING 4u
+#define SPEC_PREFER_SPLIT 8u
 
 typedef struct {
   int32_t B;             /* requests, >= 1                                   */
@@ -204,27 +208,32 @@ int spec_draft_confidence(const spec_args *args, float threshold, float *out_con
  *
  * Arguments, checks, kernels and results are those of spec_verify_sample;
  * the workspace is replaced by one buffer per device that the library holds
- * as a file-scope __device__ array of SPEC_STATIC_SCRATCH_BYTES (1 MiB).  The
+ * as a file-scope __device__ array of SPEC_STATIC_SCRATCH_BYTES (8 MiB).  The
  * call allocates and frees nothing.
  *
- * Size limit: with n = total_drafts + B the batch needs
- * align256(4 B) + align256(32 n) + align256(64 n) bytes; every batch with
- * n <= 10000 fits.  A batch that does not fit returns SPEC_ERR_STATIC_SCRATCH
- * and enqueues nothing.
+ * Size limit: the batch needs the scratch of the kernel the call runs.
+ * Without top-p (the split-vocabulary kernel) that is about 160 bytes per
+ * logit row (2 total_drafts + B rows), 64 bytes per row and vocabulary
+ * segment (segments of 15360 bf16 or 7680 fp32 logits), V/8 bytes of
+ * penalty bitmap per request and 64 bytes per vocabulary segment and draft;
+ * for B = 64, K = 8, V = 152064 it is 2.4 MiB in bf16 and 3.3 MiB in fp32.
+ * With top-p (the cluster kernel) it is 96 bytes per work item
+ * (total_drafts + B).  A batch that does not fit returns
+ * SPEC_ERR_STATIC_SCRATCH and enqueues nothing.
  *
- * Zeroing: only the B per-request arrival counters at the start of the
- * buffer must be zero when the kernel starts; each call clears them on
- * `stream` (cudaMemsetAsync) before its launch.  Everything else in the
+ * Zeroing: the call's counters at the start of the buffer are cleared on
+ * `stream` (cudaMemsetAsync) before its launch; everything else in the
  * buffer is written before it is read.
  *
- * First call on a device: it looks the buffer's address up with
- * cudaGetSymbolAddress (that device current) and caches it; make this first
- * call outside any stream capture.  A failed lookup returns SPEC_ERR_DEVICE.
+ * Address: every call looks the buffer up with cudaGetSymbolAddress for the
+ * current device (a host-side lookup that allocates nothing).  The first
+ * call on a device may load the library's device code; make it outside any
+ * stream capture.  A failed lookup returns SPEC_ERR_DEVICE.
  *
  * Races: all calls on one device share the buffer.  They must be ordered
  * (one stream, or synchronised); two calls in flight at once, on two streams
  * or from two host threads, race and corrupt each other's results. */
-#define SPEC_STATIC_SCRATCH_BYTES (1u << 20)
+#define SPEC_STATIC_SCRATCH_BYTES (8u << 20)
 int spec_verify_sample_static(const spec_args *args, int32_t *out_tokens, int32_t *out_accepted,
                               int32_t *out_status, spec_stream_t stream);
 

@@ -21,6 +21,7 @@ SPEC_MAX_K = 32
 SPEC_NO_BONUS = 1
 SPEC_PREFER_RESIDENT = 2
 SPEC_PREFER_STREAMING = 4
+SPEC_PREFER_SPLIT = 8
 
 SPEC_OK = 0
 SPEC_ERR_NULL = -1
@@ -32,7 +33,7 @@ SPEC_ERR_ALIGN = -6
 SPEC_ERR_LAUNCH = -7
 SPEC_ERR_DEVICE = -8
 SPEC_ERR_STATIC_SCRATCH = -9
-SPEC_STATIC_SCRATCH_BYTES = 1 << 20
+SPEC_STATIC_SCRATCH_BYTES = 8 << 20
 
 SPEC_STATUS_BAD_TOKEN = 1
 SPEC_STATUS_BAD_PARAM = 2

@@ -3,13 +3,13 @@
 // work is enqueued on the caller's stream.
 #include <cstdint>
 #include <cstring>
-#include <mutex>
 
 #include <cuda_runtime.h>
 
 #include "spec_verify.h"
 #include "spec_internal.h"
 #include "conf_internal.h"
+#include "seg_internal.h"
 
 namespace sv {
 int choose_resident_layout(int V, int elem_bytes, bool topp, int max_smem, int* C_out, SmemLayout* L_out);
@@ -22,6 +22,8 @@ int launch_pipe_verify(SampleParams& P, bool bf16, int num_sms, cudaStream_t str
 int launch_confidence(const ConfParams& P, bool bf16, cudaStream_t stream);
 int choose_conf_layout(int V, int elem_bytes, int B, int max_smem, ConfLayout* out);
 int launch_conf_pipe(const ConfParams& P, bool bf16, int num_sms, cudaStream_t stream);
+int launch_seg_verify(const SegParams& P, bool bf16, int num_sms, cudaStream_t stream);
+int seg_smem_bytes();
 }  // namespace sv
 
 namespace {
@@ -94,6 +96,81 @@ void fill_sample_inputs(sv::SampleParams& P, const spec_args* a) {
   P.flags = a->flags;
 }
 
+// Default bound on every wait of the split-vocabulary kernel, in SM clock
+// cycles (about two seconds at any clock this part runs).
+constexpr long long kSegWaitLimit = 4000000000ll;
+
+// The split-vocabulary kernel serves sampling without top-p when the caller
+// asks for it and a row has at most kSegMaxSegs segments (V <= 491520 bf16,
+// 245760 fp32); other batches go to the kernels below.
+bool use_seg(const spec_args* a) {
+  return !a->top_p && (a->flags & SPEC_PREFER_SPLIT) &&
+         sv::make_seg_geom(a->V, elem_bytes(a->dtype)).nseg <= sv::kSegMaxSegs;
+}
+
+// The split-vocabulary kernel (no top-p): sampling or the TV quantities.
+int run_seg(const sv::SampleParams& S, const spec_args* a, void* ws, int num_sms, int max_smem,
+            cudaStream_t stream) {
+  if (sv::seg_smem_bytes() > max_smem) return SPEC_ERR_DEVICE;
+  const int es = elem_bytes(a->dtype);
+  const sv::SegWorkspace W = sv::make_seg_workspace(a->B, a->total_drafts, a->V, es);
+  unsigned char* w = static_cast<unsigned char*>(ws);
+  sv::SegParams P;
+  std::memset(&P, 0, sizeof(P));
+  P.target = a->target_logits;
+  P.ld_t = a->ld_target;
+  P.draft = a->draft_logits;
+  P.ld_d = a->ld_draft;
+  P.cu_draft = a->cu_draft;
+  P.draft_tokens = a->draft_tokens;
+  P.cu_hist = a->cu_hist;
+  P.hist = a->hist_tokens;
+  P.temperature = a->temperature;
+  P.rep_penalty = a->rep_penalty;
+  P.tv_budget = a->tv_budget;
+  P.uniforms = S.uniforms;
+  P.B = a->B;
+  P.V = a->V;
+  P.total = a->total_drafts;
+  P.max_k = a->max_k;
+  P.flags = a->flags;
+  P.mode = S.mode;
+  P.out_tokens = S.out_tokens;
+  P.out_accepted = S.out_accepted;
+  P.out_status = S.out_status;
+  P.out_tv = S.out_tv;
+  P.out_theta = S.out_theta;
+  P.out_px = S.out_px;
+  P.out_qx = S.out_qx;
+  P.g = sv::make_seg_geom(a->V, es);
+  P.NT = a->total_drafts + a->B;
+  P.NR = 2 * a->total_drafts + a->B;
+  P.wait_limit = kSegWaitLimit;
+  P.ctl = reinterpret_cast<unsigned*>(w + W.off_ctl);
+  P.row_cnt = reinterpret_cast<unsigned*>(w + W.off_row_cnt);
+  P.req_rows = reinterpret_cast<unsigned*>(w + W.off_req_rows);
+  P.req_pend = reinterpret_cast<unsigned*>(w + W.off_req_pend);
+  P.req_done = reinterpret_cast<unsigned*>(w + W.off_req_done);
+  P.job_cnt = reinterpret_cast<unsigned*>(w + W.off_job_cnt);
+  P.jobs = reinterpret_cast<int*>(w + W.off_jobs);
+  P.bitmap = reinterpret_cast<uint32_t*>(w + W.off_bitmap);
+  P.rowdesc = reinterpret_cast<sv::SegRowDesc*>(w + W.off_rowdesc);
+  P.part1 = reinterpret_cast<float2*>(w + W.off_part1);
+  P.rowstat = reinterpret_cast<sv::SegRowStat*>(w + W.off_rowstat);
+  P.zx = reinterpret_cast<float*>(w + W.off_zx);
+  P.pos = reinterpret_cast<sv::SegPos*>(w + W.off_pos);
+  P.part2 = reinterpret_cast<float*>(w + W.off_part2);
+  P.jobdesc = reinterpret_cast<sv::SegJobDesc*>(w + W.off_jobdesc);
+  P.req_status = reinterpret_cast<int*>(w + W.off_req_status);
+  P.req_need = reinterpret_cast<unsigned*>(w + W.off_req_need);
+  P.posdesc = reinterpret_cast<sv::SegRowDesc*>(w + W.off_posdesc);
+  if (cudaMemsetAsync(w + W.off_zero, 0, W.zero_bytes, stream) != cudaSuccess) {
+    cudaGetLastError();
+    return SPEC_ERR_LAUNCH;
+  }
+  return sv::launch_seg_verify(P, a->dtype == SPEC_BF16, num_sms, stream) == 0 ? SPEC_OK : SPEC_ERR_LAUNCH;
+}
+
 // Picks the kernel variant.  Resident (each logit read once, values kept in
 // the shared memory of a C-CTA cluster) when every work item gets its own
 // cluster in one wave; streaming otherwise: the pipelined kernel (one CTA
@@ -114,6 +191,8 @@ int run_sample(sv::SampleParams& P, const spec_args* a, void* ws, cudaStream_t s
          sv::choose_stream_layout(a->V, C_str, es, topp, max_smem, smem_per_sm, &L_str) != 0)
     C_str *= 2;
   const bool str_ok = C_str <= sv::kMaxCluster;
+  // Without top-p, when asked for: the split-vocabulary kernel.
+  if (use_seg(a)) return run_seg(P, a, ws, num_sms, max_smem, stream);
   bool resident;
   if ((a->flags & SPEC_PREFER_RESIDENT) && res_ok) resident = true;
   else if ((a->flags & SPEC_PREFER_STREAMING) && str_ok) resident = false;
@@ -149,28 +228,29 @@ int run_sample(sv::SampleParams& P, const spec_args* a, void* ws, cudaStream_t s
 
 // ---- fixed device scratch of spec_verify_sample_static
 // One buffer per device, placed by the CUDA runtime when this module loads;
-// no call of this library allocates it.  Its address is looked up once per
-// device (cudaGetSymbolAddress with that device current) and cached.
+// no call of this library allocates it.  Its address is looked up on every
+// call (cudaGetSymbolAddress with the caller's device current): a host-side
+// lookup that allocates nothing, and stays right after a device reset
+// reloads the module.
 static __device__ __align__(256) unsigned char g_static_scratch[SPEC_STATIC_SCRATCH_BYTES];
 
-constexpr int kScratchCacheDevices = 64;
-std::mutex g_scratch_mu;
-void* g_scratch_addr[kScratchCacheDevices] = {};
-
 int static_scratch_address(void** out) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) { cudaGetLastError(); return SPEC_ERR_DEVICE; }
-  std::lock_guard<std::mutex> lock(g_scratch_mu);
-  void* p = (dev >= 0 && dev < kScratchCacheDevices) ? g_scratch_addr[dev] : nullptr;
-  if (!p) {
-    if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || !p) {
-      cudaGetLastError();
-      return SPEC_ERR_DEVICE;
-    }
-    if (dev >= 0 && dev < kScratchCacheDevices) g_scratch_addr[dev] = p;
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || !p) {
+    cudaGetLastError();
+    return SPEC_ERR_DEVICE;
   }
   *out = p;
   return SPEC_OK;
+}
+
+// Scratch the sampling call needs: the split-vocabulary kernel's records
+// without top-p (unless the resident cluster kernel is asked for), the
+// cluster kernel's counters, results and flags with it.
+size_t sample_scratch_bytes(const spec_args* a) {
+  if (use_seg(a))
+    return sv::make_seg_workspace(a->B, a->total_drafts, a->V, elem_bytes(a->dtype)).total;
+  return sv::make_workspace_layout(a->B, a->total_drafts, a->V).off_partials;
 }
 
 }  // namespace
@@ -179,7 +259,12 @@ extern "C" {
 
 size_t spec_workspace_bytes(int32_t B, int32_t total_drafts, int32_t V) {
   if (B < 0 || total_drafts < 0 || V < 0) return 0;
-  return sv::make_workspace_layout(B, total_drafts, V).total;
+  size_t n = sv::make_workspace_layout(B, total_drafts, V).total;
+  for (int es : {2, 4}) {
+    const size_t m = sv::make_seg_workspace(B, total_drafts, V, es).total;
+    if (m > n) n = m;
+  }
+  return n;
 }
 
 int spec_verify_sample(const spec_args* a, int32_t* out_tokens, int32_t* out_accepted, int32_t* out_status,
@@ -204,9 +289,7 @@ int spec_verify_sample_static(const spec_args* a, int32_t* out_tokens, int32_t* 
   int rc = check_common(a, true);
   if (rc) return rc;
   if (!out_tokens || !out_accepted || !a->temperature || !a->tv_budget || !a->uniforms) return SPEC_ERR_NULL;
-  // the sampling kernel uses the counters, results and flags regions only
-  if (sv::make_workspace_layout(a->B, a->total_drafts, a->V).off_partials > SPEC_STATIC_SCRATCH_BYTES)
-    return SPEC_ERR_STATIC_SCRATCH;
+  if (sample_scratch_bytes(a) > SPEC_STATIC_SCRATCH_BYTES) return SPEC_ERR_STATIC_SCRATCH;
   void* scratch = nullptr;
   rc = static_scratch_address(&scratch);
   if (rc) return rc;

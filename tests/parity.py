@@ -6,6 +6,14 @@ import oracle
 
 TOL_PROB = 1e-5     # probabilities, TV and theta: absolute, fp32 kernels vs fp64 oracle
 
+# Near ties seen by the GPU parity tests: (case, near ties, requests
+# compared).  The test session prints them at its end (conftest.py).
+NEAR_TIES = []
+
+
+def record_near(case, near, n):
+    NEAR_TIES.append((str(case), int(near), int(n)))
+
 
 def run_sample(batch, *, flags=0, device="cuda", db=None):
     import torch

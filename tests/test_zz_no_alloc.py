@@ -29,7 +29,7 @@ def test_oversize_batch_is_rejected_on_the_host():
 
     __graft_entry__.build()
     lib = sv.load_library()
-    a = _fake_args(B=11000, total=0, V=10)
+    a = _fake_args(B=200000, total=0, V=10)
     rc = lib.spec_verify_sample_static(ctypes.byref(a), 1 << 20, 1 << 20, 1 << 20, None)
     assert rc == sv.SPEC_ERR_STATIC_SCRATCH
     assert "SPEC_STATIC_SCRATCH_BYTES" in sv.status_string(rc)
@@ -74,7 +74,7 @@ def test_two_calls_in_a_row_match_the_workspace_path():
 def test_oversize_batch_with_device_tensors_leaves_outputs_untouched():
     import torch
 
-    B, V = 11000, 8
+    B, V = 200000, 8
     target = torch.zeros((B, V), dtype=torch.float32, device="cuda")
     cu = torch.zeros(B + 1, dtype=torch.int32, device="cuda")
     ones = torch.ones(B, dtype=torch.float32, device="cuda")
