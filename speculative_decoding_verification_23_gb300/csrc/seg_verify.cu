@@ -48,13 +48,11 @@ extern __shared__ __align__(128) unsigned char seg_smem[];
 
 constexpr int seg_al16(int x) { return (x + 15) / 16 * 16; }
 constexpr int kOffBars = kSegSlots * kSegSlotBytes;                     // full[kSegSlots], empty[kSegSlots]
-constexpr int kOffGk = seg_al16(kOffBars + 2 * kSegSlots * 8);          // [group][2]: the unit a group claimed
-constexpr int kOffRec = seg_al16(kOffGk + kSegGroups * 2 * 4);          // unit records (kSegRecN)
+constexpr int kOffRec = seg_al16(kOffBars + 2 * kSegSlots * 8);        // unit records (kSegRecN)
 constexpr int kOffMisc = seg_al16(kOffRec + kSegRecN * (int)sizeof(SegUnitRec));  // control words
-constexpr int kOffTab = seg_al16(kOffMisc + 64);                        // penalty bits of a vector -> -inf masks
-constexpr int kOffCu = kOffTab + 256 * 16;                               // cu_draft copy (B + 1 <= kSegCuCap)
+constexpr int kOffCu = seg_al16(kOffMisc + 64);                         // cu_draft copy (B + 1 <= kSegCuCap)
 constexpr int kSegSmem = kOffCu + kSegCuCap * 4;
-static_assert(kSegSlotBytes % 128 == 0 && kOffBars % 8 == 0 && kOffRec % 16 == 0 && kOffTab % 16 == 0,
+static_assert(kSegSlotBytes % 128 == 0 && kOffBars % 8 == 0 && kOffRec % 16 == 0 && kOffCu % 16 == 0,
               "shared-memory regions keep the alignment of their widest access");
 
 constexpr float kTiny = 5.421010862427522e-20f;  // 2^-64
@@ -138,12 +136,10 @@ struct Ring {
   __device__ unsigned char* slot(int s) const { return seg_smem + (size_t)s * kSegSlotBytes; }
   __device__ uint64_t* full() const { return reinterpret_cast<uint64_t*>(seg_smem + kOffBars); }
   __device__ uint64_t* empty() const { return full() + kSegSlots; }
-  __device__ int* gk() const { return reinterpret_cast<int*>(seg_smem + kOffGk); }
   __device__ SegUnitRec* rec(int k) const {
     return reinterpret_cast<SegUnitRec*>(seg_smem + kOffRec) + (k % kSegRecN);
   }
   __device__ unsigned* misc() const { return reinterpret_cast<unsigned*>(seg_smem + kOffMisc); }
-  __device__ uint4* tab() const { return reinterpret_cast<uint4*>(seg_smem + kOffTab); }
   __device__ int* cu() const { return reinterpret_cast<int*>(seg_smem + kOffCu); }
 };
 
@@ -717,33 +713,17 @@ __device__ void producer(const SegParams& P, const Ring& R, Prod& st, int pre, i
 // ------------------------------------------------------------ the consumers
 // A consumer warp owns a contiguous range of each unit (pass 1: wr tokens
 // of one row; pass 2: wr2 tokens of both rows), and lane l a contiguous run
-// of it (kTpl tokens in pass 1, kTpl / 2 in pass 2), so that the run's
-// penalty bits are one 64- or 32-bit word of the slot's bitmap.  Lanes read
-// their 16-byte vectors in a rotated order that keeps every quarter-warp on
-// distinct banks.
-
-// The 16-byte mask that turns the logits of vector elements with set bits
-// into -inf (with a LOP3 per word): 8 bf16 or 4 fp32 elements.
-template <int N>
-__device__ __forceinline__ uint4 bits_to_mask(uint32_t b) {
-  uint32_t w[4];
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    if constexpr (N == 8) {
-      w[j] = (((b >> (2 * j)) & 1u) ? 0x0000FFFFu : 0u) | (((b >> (2 * j + 1)) & 1u) ? 0xFFFF0000u : 0u);
-    } else {
-      w[j] = ((b >> j) & 1u) ? 0xFFFFFFFFu : 0u;
-    }
-  }
-  return make_uint4(w[0], w[1], w[2], w[3]);
-}
-
-__device__ __forceinline__ void apply_mask(uint4& v, const uint4& m, uint32_t neg) {
-  v.x = (v.x & ~m.x) | (neg & m.x);
-  v.y = (v.y & ~m.y) | (neg & m.y);
-  v.z = (v.z & ~m.z) | (neg & m.z);
-  v.w = (v.w & ~m.w) | (neg & m.w);
-}
+// of it (64 bf16 / 32 fp32 tokens in pass 1, half that per row in pass 2):
+// 128 or 64 bytes, so that the run's penalty bits are one word of the
+// slot's bitmap.  A lane reads its 16-byte vectors in the order m ^ L (L
+// from the lane index), which keeps the eight lanes of every quarter-warp
+// on distinct banks.
+//
+// Penalised tokens: before it loads its run, a lane reads each of its
+// penalised tokens (the bits of its run in the slot's bitmap, plus the
+// row's extras), adds that token's penalised term to a side sum and
+// overwrites the token with -inf in the slot; the hot loop then sums the
+// run as it stands.  Every lane touches only its own run.
 
 template <int N>
 __device__ __forceinline__ uint32_t neg_word();
@@ -773,11 +753,30 @@ __device__ __forceinline__ float ldz(const unsigned char* p) {
   return to_f32<T>(*reinterpret_cast<const T*>(p));
 }
 
-// Penalty bits of a lane's run of `bits` tokens (64 or 32) starting at bit
-// `bit0` of the slot's bitmap (bit0 a multiple of `bits`), with the row's
-// extras (drafts before the row outside the history) folded in.  Tokens of
-// the warp's range are [first_tok, first_tok + wn); lane l's run starts at
-// first_tok + l * bits.
+// A logit of the slot becomes -inf.
+template <typename T>
+__device__ __forceinline__ void set_neg_inf(unsigned char* p) {
+  if constexpr (sizeof(T) == 2) *reinterpret_cast<uint16_t*>(p) = 0xFF80u;
+  else *reinterpret_cast<uint32_t*>(p) = 0xFF800000u;
+}
+
+// 16 bytes of shared memory at a 32-bit shared-window address.  Volatile
+// with a memory clobber: no load moves past the slot's release, nor ahead of
+// the lane's own -inf stores.
+__device__ __forceinline__ uint4 lds16(uint32_t a) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(a)
+               : "memory");
+  return v;
+}
+
+// Penalty bits of a lane's run of `bits` tokens (64, 32 or 16) starting at
+// bit `bit0` of the slot's bitmap (bit0 a multiple of `bits`), with the
+// row's extras (drafts before the row outside the history) folded in.
+// Tokens of the warp's range are [first_tok, first_tok + wn); lane l's run
+// starts at first_tok + l * bits.
 template <int BITS>
 __device__ __forceinline__ unsigned long long run_bits(const unsigned char* bm, int bit0, const SegRowDesc* d,
                                                        int first_tok, int wn, int lane) {
@@ -802,26 +801,41 @@ __device__ __forceinline__ unsigned long long run_bits(const unsigned char* bm, 
   return pm;
 }
 
-// Sum of 2^(z c - ref) over the 8 (bf16) or 4 (fp32) logits of a vector.
+// The lane's run (VPL vectors at shared address `run`, `ln` valid tokens)
+// into registers, vector m of the result being the run's vector m ^ L;
+// tokens past `ln` read as -inf.
+template <int N, int VPL>
+__device__ __forceinline__ void load_run(uint4 (&v)[VPL], uint32_t run, int L, int ln) {
+  if (ln == N * VPL) {
+    const uint32_t sw = run | ((uint32_t)L << 4);
+#pragma unroll
+    for (int m = 0; m < VPL; ++m) v[m] = lds16(sw ^ ((uint32_t)m << 4));
+  } else {
+    const uint32_t NW = neg_word<N>();
+#pragma unroll
+    for (int m = 0; m < VPL; ++m) {
+      const int vi = m ^ L;
+      v[m] = make_uint4(NW, NW, NW, NW);
+      if (vi * N < ln) {
+        v[m] = lds16(run + (uint32_t)vi * 16u);
+        if (vi * N + N > ln) mask_vec<N>(v[m], ln - vi * N);
+      }
+    }
+  }
+}
+
+// Sum of 2^(z c) over the 8 (bf16) or 4 (fp32) logits of a vector.
 template <int N>
-__device__ __forceinline__ float2 vec_exp_sum(const uint4& v, float2 c2, float2 nr, float2 acc) {
+__device__ __forceinline__ float2 vec_exp_sum(const uint4& v, float2 c2, float2 acc) {
   float z[N];
   cvt16(v, z);
+  const float2 z2 = make_float2(0.f, 0.f);
 #pragma unroll
   for (int e = 0; e < N; e += 2) {
-    const float2 y = __ffma2_rn(make_float2(z[e], z[e + 1]), c2, nr);
+    const float2 y = __ffma2_rn(make_float2(z[e], z[e + 1]), c2, z2);
     acc = __fadd2_rn(acc, make_float2(ex2(y.x), ex2(y.y)));
   }
   return acc;
-}
-
-template <int N>
-__device__ __forceinline__ float vec_max(const uint4& v, float m) {
-  float z[N];
-  cvt16(v, z);
-#pragma unroll
-  for (int e = 0; e < N; ++e) m = fmaxf(m, z[e]);
-  return m;
 }
 
 // A per-lane sum of 2^(z'c) (reference 0) is trusted inside [2^-100, 2^100]:
@@ -833,8 +847,8 @@ constexpr float kSumLo = 7.888609052210118e-31f;   // 2^-100
 
 // Pass 1 of one unit for consumer warp w (0..7 of its group): the sum of
 // 2^(z'c) over the warp's tokens, and the row's draft-token logit.  All
-// reads of the slot come first (penalty bits, the penalised tokens' terms,
-// the lane's run into registers); the slot goes back to the producer
+// reads of the slot come first (the draft token, the penalised tokens, the
+// lane's run into registers); the slot goes back to the producer
 // (`release`) before the arithmetic.
 template <typename T, typename Rel>
 __device__ __forceinline__ void unit_row(const SegParams& P, unsigned char* slot, const SegUnitHdr& h, int w,
@@ -858,31 +872,26 @@ __device__ __forceinline__ void unit_row(const SegParams& P, unsigned char* slot
       rc->has_zx = 1;
     }
   }
+  // penalised tokens: their own terms, then -inf in the slot
   const unsigned long long pm = run_bits<TPL>(slot + kSegLogitBytes, wt0 + lane * TPL, d, h.tok0 + wt0, wn, lane);
-  // penalised tokens: their own terms, reference 0
   float side = 0.f;
   for (unsigned long long mm = pm; mm; mm &= mm - 1) {
     const int e = __ffsll((long long)mm) - 1;
-    if (e < ln) side += ex2(penalize(ldz<T>(run + (size_t)e * sizeof(T)), alpha) * c);
+    if (e < ln) {
+      unsigned char* q = const_cast<unsigned char*>(run) + (size_t)e * sizeof(T);
+      side += ex2(__fmul_rn(penalize(ldz<T>(q), alpha), c));
+      set_neg_inf<T>(q);
+    }
   }
-  // the run (penalised tokens and the tail -inf)
-  const uint32_t NW = neg_word<N>();
-  const uint4* tab = reinterpret_cast<const uint4*>(seg_smem + kOffTab);
   uint4 v[VPL];
-#pragma unroll
-  for (int m = 0; m < VPL; ++m) {
-    const int vi = (m + lane) & (VPL - 1);
-    v[m] = vi * N < ln ? *reinterpret_cast<const uint4*>(run + (size_t)vi * 16) : make_uint4(NW, NW, NW, NW);
-    if (pm) apply_mask(v[m], tab[(uint32_t)(pm >> (vi * N)) & ((1u << N) - 1u)], NW);
-    if (vi * N < ln && vi * N + N > ln) mask_vec<N>(v[m], ln - vi * N);
-  }
+  load_run<N, VPL>(v, (uint32_t)__cvta_generic_to_shared(run), lane & 7, ln);
   release();
-  const float2 c2 = make_float2(c, c), z2 = make_float2(0.f, 0.f);
+  const float2 c2 = make_float2(c, c);
   float2 a0 = make_float2(0.f, 0.f), a1 = make_float2(0.f, 0.f);
 #pragma unroll
   for (int m = 0; m < VPL; m += 2) {
-    a0 = vec_exp_sum<N>(v[m], c2, z2, a0);
-    a1 = vec_exp_sum<N>(v[m + 1], c2, z2, a1);
+    a0 = vec_exp_sum<N>(v[m], c2, a0);
+    a1 = vec_exp_sum<N>(v[m + 1], c2, a1);
   }
   const float s = (a0.x + a0.y) + (a1.x + a1.y) + side;
   // a lane outside the trusted range flags the warp's partial (S < 0)
@@ -891,8 +900,25 @@ __device__ __forceinline__ void unit_row(const SegParams& P, unsigned char* slot
   if (lane == 0) rc->r[w] = bad ? make_float2(0.f, -1.f) : make_float2(0.f, S);
 }
 
+// Residual terms of two packed token pairs in units of fp: max(p - q, 0) / fp
+// with p = 2^(zp c - Lp) fp and q = 2^(zq c - Lq) fq, as max(eq * -r + ep, 0)
+// (ep, eq the two powers, r = fq / fp) in one fused step.  Rows that agree
+// give exactly 0 whichever way the compiler schedules it.
+__device__ __forceinline__ float2 pair_terms(float2 zp, float2 zq, float2 c2, float2 np2, float2 nq2, float2 mr2) {
+  const float2 a = __ffma2_rn(zp, c2, np2);
+  const float2 bq = __ffma2_rn(zq, c2, nq2);
+  const float2 df = __ffma2_rn(make_float2(ex2(bq.x), ex2(bq.y)), mr2, make_float2(ex2(a.x), ex2(a.y)));
+  return make_float2(fmaxf(df.x, 0.f), fmaxf(df.y, 0.f));
+}
+
+// One token's residual term in units of fp, as pair_terms computes it.
+__device__ __forceinline__ float pair_term(float zp, float zq, float c, float Lp, float Lq, float r) {
+  return fmaxf(__fmaf_rn(ex2(fmaf(zq, c, -Lq)), -r, ex2(fmaf(zp, c, -Lp))), 0.f);
+}
+
 // Pass 2 of one half-segment unit for consumer warp w: the warp's share of
-// sum max(p - q, 0), p = 2^(z'c - Lp), q = 2^(z'c - Lq).
+// sum max(p - q, 0), p = 2^(z'c - Lp) fp, q = 2^(z'c - Lq) fq (summed in
+// units of fp, then scaled).
 template <typename T, typename Rel>
 __device__ __forceinline__ void unit_pair(const SegParams& P, unsigned char* slot, const SegUnitHdr& h, int w,
                                           int lane, SegUnitRec* rc, Rel&& release) {
@@ -901,48 +927,34 @@ __device__ __forceinline__ void unit_pair(const SegParams& P, unsigned char* slo
   constexpr int TPL = N * VPL;             // tokens per lane: 32 bf16, 16 fp32
   const SegRowDesc* d = reinterpret_cast<const SegRowDesc*>(slot + kSegDescOff);
   const SegJobDesc* jd = reinterpret_cast<const SegJobDesc*>(slot + kSegDescOff + sizeof(SegRowDesc));
-  const float c = d->c, alpha = d->alpha, Lp = jd->Lp, Lq = jd->Lq, fp = jd->fp, fq = jd->fq;
+  const float c = d->c, alpha = d->alpha, Lp = jd->Lp, Lq = jd->Lq, fp = jd->fp;
+  const float r = __fdiv_rn(jd->fq, fp);
   const int wt0 = w * P.g.wr2;
   const int wn = max(0, min(P.g.wr2, h.n - wt0));
   const int ln = max(0, min(TPL, wn - lane * TPL));
   const unsigned char* rp = slot + (size_t)(wt0 + lane * TPL) * sizeof(T);
   const unsigned char* rq = rp + kSegLogitBytes / 2;
+  // penalised tokens: their own residual terms, then -inf in both rows
   const unsigned long long pm = run_bits<TPL>(slot + kSegLogitBytes, wt0 + lane * TPL, d, h.tok0 + wt0, wn, lane);
-  const uint32_t NW = neg_word<N>();
-  const uint4* tab = reinterpret_cast<const uint4*>(seg_smem + kOffTab);
-  const float2 c2 = make_float2(c, c), np2 = make_float2(-Lp, -Lp), nq2 = make_float2(-Lq, -Lq);
-  const float2 fp2 = make_float2(fp, fp), mfq2 = make_float2(-fq, -fq);
-  // penalised tokens: their own residuals
   float side = 0.f;
-  unsigned long long mm = pm;
-  while (mm) {
+  for (unsigned long long mm = pm; mm; mm &= mm - 1) {
     const int e = __ffsll((long long)mm) - 1;
-    mm &= mm - 1;
     if (e < ln) {
-      const float zp = penalize(ldz<T>(rp + (size_t)e * sizeof(T)), alpha);
-      const float zq = penalize(ldz<T>(rq + (size_t)e * sizeof(T)), alpha);
-      const float pv = ex2(fmaf(zp, c, -Lp)) * fp, qv = ex2(fmaf(zq, c, -Lq)) * fq;
-      side += fmaxf(pv - qv, 0.f);
+      unsigned char* qp = const_cast<unsigned char*>(rp) + (size_t)e * sizeof(T);
+      unsigned char* qq = const_cast<unsigned char*>(rq) + (size_t)e * sizeof(T);
+      side += pair_term(penalize(ldz<T>(qp), alpha), penalize(ldz<T>(qq), alpha), c, Lp, Lq, r);
+      set_neg_inf<T>(qp);
+      set_neg_inf<T>(qq);
     }
   }
   // the lane's run of both rows into registers, then the slot goes back
   uint4 vp[VPL], vq[VPL];
-#pragma unroll
-  for (int m = 0; m < VPL; ++m) {
-    const int vi = (m + (lane >> 1)) & (VPL - 1);
-    vp[m] = vi * N < ln ? *reinterpret_cast<const uint4*>(rp + (size_t)vi * 16) : make_uint4(NW, NW, NW, NW);
-    vq[m] = vi * N < ln ? *reinterpret_cast<const uint4*>(rq + (size_t)vi * 16) : make_uint4(NW, NW, NW, NW);
-    if (pm) {
-      const uint4 mk = tab[(uint32_t)(pm >> (vi * N)) & ((1u << N) - 1u)];
-      apply_mask(vp[m], mk, NW);
-      apply_mask(vq[m], mk, NW);
-    }
-    if (vi * N < ln && vi * N + N > ln) {
-      mask_vec<N>(vp[m], ln - vi * N);
-      mask_vec<N>(vq[m], ln - vi * N);
-    }
-  }
+  const uint32_t sp = (uint32_t)__cvta_generic_to_shared(rp);
+  load_run<N, VPL>(vp, sp, (lane >> 1) & 3, ln);
+  load_run<N, VPL>(vq, sp + (uint32_t)(kSegLogitBytes / 2), (lane >> 1) & 3, ln);
   release();
+  const float2 c2 = make_float2(c, c), np2 = make_float2(-Lp, -Lp), nq2 = make_float2(-Lq, -Lq);
+  const float2 mr2 = make_float2(-r, -r);
   float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
   for (int m = 0; m < VPL; ++m) {
@@ -950,17 +962,12 @@ __device__ __forceinline__ void unit_pair(const SegParams& P, unsigned char* slo
     cvt16(vp[m], zp);
     cvt16(vq[m], zq);
 #pragma unroll
-    for (int e = 0; e < N; e += 2) {
-      const float2 a = __ffma2_rn(make_float2(zp[e], zp[e + 1]), c2, np2);
-      const float2 bq = __ffma2_rn(make_float2(zq[e], zq[e + 1]), c2, nq2);
-      const float2 pv = __fmul2_rn(make_float2(ex2(a.x), ex2(a.y)), fp2);
-      const float2 qn = __fmul2_rn(make_float2(ex2(bq.x), ex2(bq.y)), mfq2);
-      const float2 df = __fadd2_rn(pv, qn);
-      acc = __fadd2_rn(acc, make_float2(fmaxf(df.x, 0.f), fmaxf(df.y, 0.f)));
-    }
+    for (int e = 0; e < N; e += 2)
+      acc = __fadd2_rn(acc, pair_terms(make_float2(zp[e], zp[e + 1]), make_float2(zq[e], zq[e + 1]), c2, np2, nq2,
+                                       mr2));
   }
-  const float s = warp_sum(acc.x + acc.y + side);
-  if (lane == 0) rc->r[w] = make_float2(s, 0.f);
+  const float S = warp_sum(acc.x + acc.y + side) * fp;
+  if (lane == 0) rc->r[w] = make_float2(S, 0.f);
 }
 
 // Group g's warps take units g, g + kSegGroups, ...: each warp its own share
@@ -1025,11 +1032,9 @@ template <typename T, bool PAIR>
 __device__ __forceinline__ float draw_term(float zp, float zq, bool pen, const SegRowDesc& d, float Lp, float fp,
                                            float Lq, float fq) {
   if (pen) zp = penalize(zp, d.alpha);
-  const float pv = ex2(fmaf(zp, d.c, -Lp)) * fp;
-  if (!PAIR) return pv;
+  if (!PAIR) return __fmul_rn(ex2(fmaf(zp, d.c, -Lp)), fp);
   if (pen) zq = penalize(zq, d.alpha);
-  const float qv = ex2(fmaf(zq, d.c, -Lq)) * fq;
-  return fmaxf(pv - qv, 0.f);
+  return __fmul_rn(pair_term(zp, zq, d.c, Lp, Lq, __fdiv_rn(fq, fp)), fp);
 }
 
 // Inverse CDF inside the token range [a, a + n) (a a multiple of 32) of a
@@ -1655,9 +1660,7 @@ __global__ void __launch_bounds__(kSegThreads, 1) seg_verify_kernel(const __grid
     }
     fence_mbar_init();
   }
-  if (threadIdx.x < kSegGroups * 2) R.gk()[threadIdx.x] = 0;
   if (threadIdx.x < 16) R.misc()[threadIdx.x] = 0u;
-  for (int i = threadIdx.x; i < 256; i += blockDim.x) R.tab()[i] = bits_to_mask<Vec<T>::N>((uint32_t)i);
   __syncthreads();
   Prod st;
 #pragma unroll
