@@ -50,12 +50,14 @@ constexpr int seg_al16(int x) { return (x + 15) / 16 * 16; }
 constexpr int kOffBars = kSegSlots * kSegSlotBytes;                     // full[kSegSlots], empty[kSegSlots]
 constexpr int kOffRec = seg_al16(kOffBars + 2 * kSegSlots * 8);        // unit records (kSegRecN)
 constexpr int kOffMisc = seg_al16(kOffRec + kSegRecN * (int)sizeof(SegUnitRec));  // control words
-constexpr int kOffCu = seg_al16(kOffMisc + 64);                         // cu_draft copy (B + 1 <= kSegCuCap)
+constexpr int kSegJq = 64;                                              // second-pass candidates found, not yet issued
+constexpr int kOffJq = seg_al16(kOffMisc + 64);                         // their job entries (kSegJq, 8 bytes each)
+constexpr int kOffCu = kOffJq + kSegJq * 8;                             // cu_draft copy (B + 1 <= kSegCuCap)
 constexpr int kSegSmem = kOffCu + kSegCuCap * 4;
-static_assert(kSegSlotBytes % 128 == 0 && kOffBars % 8 == 0 && kOffRec % 16 == 0 && kOffCu % 16 == 0,
+static_assert(kSegSlotBytes % 128 == 0 && kOffBars % 8 == 0 && kOffRec % 16 == 0 && kOffJq % 16 == 0 &&
+                  kOffCu % 16 == 0,
               "shared-memory regions keep the alignment of their widest access");
 
-constexpr float kTiny = 5.421010862427522e-20f;  // 2^-64
 
 // ------------------------------------------------------------------ PTX
 __device__ __forceinline__ void mbar_expect(uint64_t* bar, uint32_t bytes) {
@@ -81,11 +83,6 @@ __device__ __forceinline__ void red_add_gpu(unsigned* p, unsigned v) {
 __device__ __forceinline__ unsigned ld_acq_gpu(const unsigned* p) {
   unsigned v;
   asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-__device__ __forceinline__ unsigned long long ld_acq_gpu64(const void* p) {
-  unsigned long long v;
-  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
   return v;
 }
 __device__ __forceinline__ void st_rel_gpu64(void* p, unsigned long long v) {
@@ -140,6 +137,7 @@ struct Ring {
     return reinterpret_cast<SegUnitRec*>(seg_smem + kOffRec) + (k % kSegRecN);
   }
   __device__ unsigned* misc() const { return reinterpret_cast<unsigned*>(seg_smem + kOffMisc); }
+  __device__ unsigned long long* jq() const { return reinterpret_cast<unsigned long long*>(seg_smem + kOffJq); }
   __device__ int* cu() const { return reinterpret_cast<int*>(seg_smem + kOffCu); }
 };
 
@@ -398,101 +396,130 @@ __device__ __forceinline__ int static_units(const SegParams& P) {
 }
 __device__ __forceinline__ int unit_of(int ks) { return (int)blockIdx.x + ks * (int)gridDim.x; }
 
-// Producer state (lane 0 of warp 0).
+// Producer state, the same in every lane of warp 0.
 struct Prod {
-  uint32_t fill_par[kSegSlots];  // parity of each slot's last fill
-  bool filled[kSegSlots];
+  uint32_t filled = 0;    // slots filled at least once (bit s)
+  uint32_t par = 0;       // parity of each slot's last fill (bit s)
+  int rec_seen = 0;       // records the recorder had taken when last looked
+  __device__ __forceinline__ void fill(int k) {
+    const int s = k % kSegSlots;
+    filled |= 1u << s;
+    par = (par & ~(1u << s)) | ((uint32_t)((k / kSegSlots) & 1) << s);
+  }
 };
 
-// Unit k may go into the ring: its slot is free and the finisher has taken
-// the record unit k - kSegRecN left.
-__device__ __forceinline__ bool wait_slot(const SegParams& P, const Ring& R, int k) {
-  if (k >= kSegRecN) {
-    const long long t0 = clock64();
-    while ((int)ld_acq_cta(R.misc() + 1) <= k - kSegRecN) {
-      if (aborted(P) || clock64() - t0 > P.wait_limit) {
-        raise_abort(P);
-        return false;
+// Unit k may go into the ring: the recorder has taken the record unit
+// k - kSegRecN left, and the consumers have released the slot.  Waited by
+// lane 0; every lane gets the outcome (false: a wait ran out).
+__device__ __forceinline__ bool wait_slot(const SegParams& P, const Ring& R, Prod& st, int k, int lane) {
+  bool ok = true;
+  if (k >= kSegRecN && st.rec_seen <= k - kSegRecN) {
+    if (lane == 0) {
+      const long long t0 = clock64();
+      while ((int)ld_acq_cta(R.misc() + 1) <= k - kSegRecN) {
+        if (aborted(P) || clock64() - t0 > P.wait_limit) {
+          raise_abort(P);
+          ok = false;
+          break;
+        }
+        __nanosleep(32);
       }
-      __nanosleep(32);
+      st.rec_seen = (int)ld_acq_cta(R.misc() + 1);
     }
+    st.rec_seen = __shfl_sync(0xffffffffu, st.rec_seen, 0);
   }
-  if (k < kSegSlots) return true;
-  const int s = k % kSegSlots;
-  return ring_wait(P, R.empty() + s, (uint32_t)((k / kSegSlots - 1) & 1));
+  if (k >= kSegSlots && lane == 0 && ok) {
+    const int s = k % kSegSlots;
+    ok = ring_wait(P, R.empty() + s, (uint32_t)((k / kSegSlots - 1) & 1));
+  }
+  return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
 
-__device__ __forceinline__ void set_rec(const Ring& R, int k, int kind, int id, int part) {
-  SegUnitRec* rc = R.rec(k);
-  rc->kind = kind;
-  rc->id = id;
-  rc->part = part;
-  rc->has_zx = 0;
-  rc->ndone = 0u;
-  st_rel_cta(R.misc() + 6, (unsigned)(k + 1));   // records 0 .. k are set
+// Arrive on a full barrier, raising the bytes it waits for first.
+__device__ __forceinline__ void mbar_arrive_expect(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
 }
 
-// Pass-1 unit of static index ks as ring unit k: the logits copy (phase 1),
-// then the penalty bits and the row descriptor (phase 2, once the prologue
-// is done everywhere); the slot's single arrival comes last.
-template <typename T>
-__device__ __forceinline__ void issue_row_logits(const SegParams& P, const Ring& R, Prod& st, int k, int ks, int src,
-                                                 uint64_t pol) {
-  const int s = k % kSegSlots;
-  unsigned char* slot = R.slot(s);
-  const int u = unit_of(ks);
-  const int sg = u % P.g.nseg;
-  const int tok0 = sg * P.g.seg;
-  const int n = min(P.g.seg, P.V - tok0);
+// The slot header and the unit record of ring unit k (plain stores: the
+// slot's arrival releases them to the consumers, and the recorder reads the
+// record only after the consumers have counted the unit done).
+__device__ __forceinline__ void put_unit(const Ring& R, int k, int kind, int id, int part, int tok0, int n) {
+  unsigned char* slot = R.slot(k % kSegSlots);
   SegUnitHdr* h = hdr_of(slot);
-  h->kind = kUnitRow;
-  h->id = u;
-  h->part = 0;
-  h->tok0 = tok0;
+  *reinterpret_cast<int4*>(h) = make_int4(kind, id, part, tok0);
   h->n = n;
-  set_rec(R, k, kUnitRow, u, 0);
-  const uint32_t bytes = tma_bytes(n, sizeof(T));
-  mbar_expect(R.full() + s, bytes);
-  bulk_g2s(slot, row_ptr<T>(P, src) + (size_t)tok0 * sizeof(T), bytes, R.full() + s, pol);
-  st.fill_par[s] = (uint32_t)((k / kSegSlots) & 1);
-  st.filled[s] = true;
+  *reinterpret_cast<int4*>(R.rec(k)) = make_int4(kind, id, part, 0);
 }
 
-__device__ __forceinline__ void issue_row_desc(const SegParams& P, const Ring& R, int k, int ks, int b,
-                                               uint64_t pol) {
+// Pass-1 unit geometry: static unit ks of this CTA is unit u =
+// blockIdx.x + ks * gridDim.x, i.e. segment u % nseg of logical row
+// u / nseg.  Lane l of the producer holds the geometry of static unit
+// 32 j + l of the current batch j of 32, and issues that unit.
+struct RowUnit {
+  const unsigned char* logits;   // the segment's first logit
+  const unsigned char* bits;     // the segment's penalty bits (its request's bitmap)
+  const SegRowDesc* desc;        // the row's descriptor
+  int u, tok0, n;                // n < 0: no such unit
+};
+
+template <typename T>
+__device__ __forceinline__ RowUnit row_unit(const SegParams& P, const int* cu, int ks, int n_static) {
+  RowUnit x{};
+  x.n = -1;
+  if (ks >= n_static) return x;
+  x.u = unit_of(ks);
+  const int r = x.u / P.g.nseg, sg = x.u - r * P.g.nseg;
+  x.tok0 = sg * P.g.seg;
+  x.n = min(P.g.seg, P.V - x.tok0);
+  const int2 bs = row_src(P, cu, r);
+  x.logits = row_ptr<T>(P, bs.y) + (size_t)x.tok0 * sizeof(T);
+  x.bits = reinterpret_cast<const unsigned char*>(P.bitmap) + (size_t)bs.x * P.g.bm_bytes + (size_t)sg * (P.g.seg / 8);
+  x.desc = P.rowdesc + r;
+  return x;
+}
+
+// The logits copy of a pass-1 unit (ring unit k), ahead of the rest.
+template <typename T>
+__device__ __forceinline__ void issue_row_logits(const Ring& R, int k, const RowUnit& x, uint64_t pol) {
+  const int s = k % kSegSlots;
+  put_unit(R, k, kUnitRow, x.u, 0, x.tok0, x.n);
+  const uint32_t bytes = tma_bytes(x.n, sizeof(T));
+  mbar_expect(R.full() + s, bytes);
+  bulk_g2s(R.slot(s), x.logits, bytes, R.full() + s, pol);
+}
+
+// A pass-1 unit as ring unit k: the logits (unless already on their way),
+// the penalty bits and the row descriptor, with the slot's single arrival
+// first (it raises the bytes the slot waits for).
+template <typename T>
+__device__ __forceinline__ void issue_row(const SegParams& P, const Ring& R, int k, const RowUnit& x,
+                                          bool logits_issued, uint64_t pol_s, uint64_t pol_k) {
   const int s = k % kSegSlots;
   unsigned char* slot = R.slot(s);
-  const int u = unit_of(ks);
-  const int r = u / P.g.nseg, sg = u % P.g.nseg;
+  if (!logits_issued) put_unit(R, k, kUnitRow, x.u, 0, x.tok0, x.n);
+  const uint32_t lb = logits_issued ? 0u : tma_bytes(x.n, sizeof(T));
   const uint32_t bmb = (uint32_t)(P.g.seg / 8);
-  mbar_expect(R.full() + s, bmb + (uint32_t)sizeof(SegRowDesc));
-  bulk_g2s(slot + kSegLogitBytes,
-           reinterpret_cast<const unsigned char*>(P.bitmap) + (size_t)b * P.g.bm_bytes + (size_t)sg * bmb, bmb,
-           R.full() + s, pol);
-  bulk_g2s(slot + kSegDescOff, P.rowdesc + r, (uint32_t)sizeof(SegRowDesc), R.full() + s, pol);
-  mbar_arrive(R.full() + s);
+  mbar_arrive_expect(R.full() + s, lb + bmb + (uint32_t)sizeof(SegRowDesc));
+  if (lb) bulk_g2s(slot, x.logits, lb, R.full() + s, pol_s);
+  bulk_g2s(slot + kSegLogitBytes, x.bits, bmb, R.full() + s, pol_k);
+  bulk_g2s(slot + kSegDescOff, x.desc, (uint32_t)sizeof(SegRowDesc), R.full() + s, pol_k);
 }
 
 // Pass-2 unit: half-segment `part` of position p (request b).
 template <typename T>
-__device__ __forceinline__ void issue_pair(const SegParams& P, const Ring& R, Prod& st, int k, int p, int b,
-                                           int part, uint64_t pol_s, uint64_t pol_k) {
+__device__ __forceinline__ void issue_pair(const SegParams& P, const Ring& R, int k, int p, int b, int part,
+                                           uint64_t pol_s, uint64_t pol_k) {
   const int s = k % kSegSlots;
   unsigned char* slot = R.slot(s);
   const int sg = part >> 1, hh = part & 1;
   const int half = P.g.seg / 2;
   const int tok0 = sg * P.g.seg + hh * half;
   const int n = max(0, min(half, P.V - tok0));
-  SegUnitHdr* h = hdr_of(slot);
-  h->kind = kUnitPair;
-  h->id = p;
-  h->part = part;
-  h->tok0 = tok0;
-  h->n = n;
-  set_rec(R, k, kUnitPair, p, part);
+  put_unit(R, k, kUnitPair, p, part, tok0, n);
   const uint32_t bytes = tma_bytes(n, sizeof(T));
   const uint32_t bmb = (uint32_t)(half / 8);
-  mbar_expect(R.full() + s, 2 * bytes + bmb + (uint32_t)(sizeof(SegRowDesc) + sizeof(SegJobDesc)));
+  mbar_arrive_expect(R.full() + s, 2 * bytes + bmb + (uint32_t)(sizeof(SegRowDesc) + sizeof(SegJobDesc)));
   if (bytes) {
     bulk_g2s(slot, row_ptr<T>(P, p + b) + (size_t)tok0 * sizeof(T), bytes, R.full() + s, pol_s);
     bulk_g2s(slot + kSegLogitBytes / 2, row_ptr<T>(P, P.NT + p) + (size_t)tok0 * sizeof(T), bytes, R.full() + s,
@@ -504,41 +531,33 @@ __device__ __forceinline__ void issue_pair(const SegParams& P, const Ring& R, Pr
   bulk_g2s(slot + kSegDescOff, P.posdesc + p, (uint32_t)sizeof(SegRowDesc), R.full() + s, pol_k);
   bulk_g2s(slot + kSegDescOff + sizeof(SegRowDesc), P.jobdesc + p, (uint32_t)sizeof(SegJobDesc), R.full() + s,
            pol_k);
-  mbar_arrive(R.full() + s);
-  st.fill_par[s] = (uint32_t)((k / kSegSlots) & 1);
-  st.filled[s] = true;
 }
 
-__device__ __forceinline__ void issue_stop(const Ring& R, Prod& st, int k) {
+__device__ __forceinline__ void issue_stop(const Ring& R, int k) {
   const int s = k % kSegSlots;
   hdr_of(R.slot(s))->kind = kUnitStop;
   mbar_arrive(R.full() + s);
-  st.fill_par[s] = (uint32_t)((k / kSegSlots) & 1);
-  st.filled[s] = true;
 }
-
 
 // cu_draft as the producer reads it: the shared-memory copy when it fits.
 __device__ __forceinline__ const int* cu_of(const SegParams& P, const Ring& R) {
   return P.B + 1 <= kSegCuCap ? R.cu() : P.cu_draft;
 }
 
-// The producer warp, before the prologue: caches cu_draft, then lane 0
-// issues the logits of the first ring-full of static units (their slots
-// stay open until issue_row_desc).
+// The producer warp, before the prologue: caches cu_draft, computes the
+// geometry of its first 32 static units (lane l: unit l) and starts the
+// logits copies of the first kSegSlots of them, one lane each.  Returns how
+// many copies it started.
 template <typename T>
-__device__ int producer_prefetch(const SegParams& P, const Ring& R, Prod& st, int lane) {
+__device__ int producer_prefetch(const SegParams& P, const Ring& R, Prod& st, RowUnit& mine, int lane) {
   if (P.B + 1 <= kSegCuCap)
     for (int j = lane; j <= P.B; j += 32) R.cu()[j] = __ldg(P.cu_draft + j);
   __syncwarp();
-  const int pre = min(static_units(P), kSegSlots);
-  int src = 0;
-  if (lane < pre) src = row_src(P, cu_of(P, R), unit_of(lane) / P.g.nseg).y;
-  const uint64_t pol = lane == 0 ? l2_policy_evict_first() : 0;
-  for (int k = 0; k < pre; ++k) {
-    const int sk = __shfl_sync(0xffffffffu, src, k);
-    if (lane == 0) issue_row_logits<T>(P, R, st, k, k, sk, pol);
-  }
+  const int n_static = static_units(P);
+  const int pre = min(n_static, kSegSlots);
+  mine = row_unit<T>(P, cu_of(P, R), lane, n_static);
+  if (lane < pre) issue_row_logits<T>(R, lane, mine, l2_policy_evict_first());
+  for (int k = 0; k < pre; ++k) st.fill(k);
   return pre;
 }
 
@@ -562,20 +581,16 @@ __device__ __forceinline__ unsigned long long ld_relaxed_gpu64(const void* p) {
 // producer keeps its next one's job entry loading in the background and
 // puts it into the ring, ahead of the next static unit, as soon as the job
 // is published; after its static units it waits for the rest.
+// The producer warp: puts units into the ring in order.  Static (pass-1)
+// units go in as their slots come free, each issued by the lane that holds
+// its geometry; second-pass units go ahead of them as soon as the recorder
+// has queued one.  At the end, one stop per consumer group.
 template <typename T>
-__device__ void producer(const SegParams& P, const Ring& R, Prod& st, int pre, int lane) {
+__device__ void producer(const SegParams& P, const Ring& R, Prod& st, RowUnit mine, int pre, int lane) {
   const int G = gridDim.x;
   const int n_static = static_units(P);
   const int* cu = cu_of(P, R);
-  auto req_of = [&](int ks) -> int2 {
-    if (ks >= n_static) return make_int2(0, 0);
-    return row_src(P, cu, unit_of(ks) / P.g.nseg);
-  };
-  uint64_t pol_s = 0, pol_k = 0;
-  if (lane == 0) {
-    pol_s = l2_policy_evict_first();
-    pol_k = l2_policy_evict_last();
-  }
+  const uint64_t pol_s = l2_policy_evict_first(), pol_k = l2_policy_evict_last();
   // every CTA's prologue is done: descriptors and bitmaps exist
   bool ok = true;
   if (lane == 0) ok = poll_gpu(P, P.ctl + kCtlPrepDone, [G](unsigned v) { return v >= (unsigned)G; });
@@ -584,129 +599,98 @@ __device__ void producer(const SegParams& P, const Ring& R, Prod& st, int pre, i
   const bool broken = ok && ld_acq_gpu(P.ctl + kCtlBroken) != 0u;
   int k = 0;        // units put into the ring (static and second-pass)
   int real = 0;     // of which real units (the rest are stops)
+  int stops = 0;    // stop units in the ring (one per group ends the consumers)
   long long t_idle = clock64();   // the last unit issued (bounds the wait for jobs)
-  int stops = 0;           // stop units in the ring (one per group ends the consumers)
   if (ok && !broken) {
     const unsigned upj = (unsigned)P.g.upj;
-    const unsigned njob = (unsigned)P.total;           // job slots in the list
     int ks = 0;               // static units issued
-    // Second-pass candidates: lane j watches this CTA's candidate cb + j
-    // (unit g = blockIdx.x + (cb + j) * G of the job list); `ent` is its
-    // job entry (0 until published), reloaded by all lanes at once.  A load
-    // is looked at only two static units after it was issued, so that its
-    // round trip overlaps the ring waits.
-    unsigned cb = 0;
-    unsigned long long ent = 0;
-    auto cand_job = [&](unsigned j) -> unsigned { return (blockIdx.x + (cb + j) * (unsigned)G) / upj; };
-    auto reload = [&]() {
-      const unsigned jg = cand_job(lane);
-      ent = jg < njob ? ld_relaxed_gpu64(P.jobs + 2 * jg) : 0ull;
-    };
-    reload();
-    int age = 0;              // static units since the last reload
-    int2 win = req_of(lane);              // static units 0..31: (request, logits row)
-    int2 nxt = req_of(32 + lane);         // static units 32..63
+    // Second-pass units: this CTA's candidates g = blockIdx.x + c * G of the
+    // job list (unit g: part g % upj of job g / upj), taken in order c =
+    // 0, 1, ...  The recorder warp watches the job list and queues each
+    // candidate's entry once published (misc[8] counts them); the producer
+    // issues no global load while static units remain, so that none of its
+    // releases waits on one.
+    unsigned head = 0;        // candidates issued
     for (;;) {
-      const bool fresh = age >= 2 || ks >= n_static;
-      // the first candidate (lane 0's) is published: it goes next
-      const unsigned long long e0 = fresh ? __shfl_sync(0xffffffffu, ent, 0) : 0ull;
-      if ((unsigned)(e0 & 0xffffffffull) != 0u && cand_job(0) < njob) {
-        // lane 1 takes the acquire (the job's descriptors were written and
-        // fenced for the async proxy before the entry was released); lane 0,
-        // which has copies in flight, issues the unit
-        if (lane == 1) asm volatile("fence.acq_rel.gpu;" ::: "memory");
-        __syncwarp();
-        if (lane == 0) {
-          ok = wait_slot(P, R, k);
-          if (ok)
-            issue_pair<T>(P, R, st, k, (int)(e0 & 0xffffffffull) - 1, (int)(e0 >> 32),
-                          (int)((blockIdx.x + cb * (unsigned)G) % upj), pol_s, pol_k);
-        }
-        ok = __shfl_sync(0xffffffffu, ok, 0) != 0;
+      const unsigned tail = *reinterpret_cast<volatile unsigned*>(R.misc() + 8);
+      if (head < tail) {
+        (void)ld_acq_cta(R.misc() + 8);      // the queued entry and its job's descriptors
+        const unsigned long long e0 = R.jq()[head % kSegJq];
+        ok = wait_slot(P, R, st, k, lane);
         if (!ok) break;
+        if (lane == 0)
+          issue_pair<T>(P, R, k, (int)(e0 & 0xffffffffull) - 1, (int)(e0 >> 32),
+                        (int)((blockIdx.x + head * (unsigned)G) % upj), pol_s, pol_k);
+        st.fill(k);
         ++k;
-        ++cb;
-        ent = __shfl_down_sync(0xffffffffu, ent, 1);
-        if (lane == 31) ent = 0ull;     // reloaded with the others
+        ++head;
+        if (lane == 0) st_rel_cta(R.misc() + 9, head);   // the queue entry is free again
         t_idle = clock64();
         continue;
       }
       if (ks < n_static) {
-        if (ks > 0 && (ks & 31) == 0) {
-          win = nxt;
-          nxt = req_of(ks + 32 + lane);
+        if (ks > 0 && (ks & 31) == 0) mine = row_unit<T>(P, cu, ks + lane, n_static);
+        if (ks >= pre) {
+          ok = wait_slot(P, R, st, k, lane);
+          if (!ok) break;
+          st.fill(k);
         }
-        const int bs = __shfl_sync(0xffffffffu, win.x, ks & 31);
-        const int ss = __shfl_sync(0xffffffffu, win.y, ks & 31);
-        if (lane == 0) {
-          if (ks >= pre) {
-            ok = wait_slot(P, R, k);
-            if (ok) issue_row_logits<T>(P, R, st, k, ks, ss, pol_s);
-          }
-          if (ok) issue_row_desc(P, R, k, ks, bs, pol_k);
-        }
-        ok = __shfl_sync(0xffffffffu, ok, 0) != 0;
-        if (!ok) break;
+        if (lane == (ks & 31)) issue_row<T>(P, R, k, mine, ks < pre, pol_s, pol_k);
         ++k;
         ++ks;
         t_idle = clock64();
-        if (++age > 2) {
-          reload();
-          age = 0;
-        }
         continue;
       }
-      // static units done: the first candidate is not published yet
-      if (cand_job(0) >= njob) break;          // no job slot left for this CTA
+      // static units done and no candidate queued: finished once every
+      // request is decided and the next candidate lies past the jobs reserved
       bool done = false;
       if (lane == 0) {
-        const unsigned jg = cand_job(0);
-        if (ld_acq_gpu(P.ctl + kCtlDecided) >= (unsigned)P.B && jg >= ld_acq_gpu(P.ctl + kCtlJobTail)) done = true;
+        const unsigned jg = (blockIdx.x + head * (unsigned)G) / upj;
+        if (jg >= (unsigned)P.total ||
+            (ld_acq_gpu(P.ctl + kCtlDecided) >= (unsigned)P.B && jg >= ld_acq_gpu(P.ctl + kCtlJobTail)))
+          done = true;
         else if (aborted(P)) ok = false;
-      }
-      done = __shfl_sync(0xffffffffu, done, 0) != 0;
-      ok = __shfl_sync(0xffffffffu, ok, 0) != 0;
-      if (done || !ok) break;
-      __nanosleep(200);
-      reload();
-      if (ent == 0ull && lane == 0) {
-        // bounded: the wait ends with the job or with every request decided
-        if (clock64() - t_idle > P.wait_limit) {
+        else if (clock64() - t_idle > P.wait_limit) {
+          // bounded: the wait ends with the job or with every request decided
           raise_abort(P);
           ok = false;
         }
       }
+      done = __shfl_sync(0xffffffffu, done, 0) != 0;
       ok = __shfl_sync(0xffffffffu, ok, 0) != 0;
-      if (!ok) break;
+      if (done || !ok) break;
+      __nanosleep(100);
     }
     real = k;
-  } else if (lane == 0) {
+  } else {
     // nothing to stream: the prefetched slots become stops once their bytes land
-    for (int j = 0; j < pre; ++j) {
-      hdr_of(R.slot(j))->kind = kUnitStop;
-      mbar_arrive(R.full() + j);
-      ++stops;
-    }
+    if (lane == 0)
+      for (int j = 0; j < pre; ++j) {
+        hdr_of(R.slot(j))->kind = kUnitStop;
+        mbar_arrive(R.full() + j);
+      }
+    stops = pre;
     k = pre;
   }
-  k = __shfl_sync(0xffffffffu, k, 0);
-  real = __shfl_sync(0xffffffffu, real, 0);
   if (lane == 0) {
     R.misc()[0] = (unsigned)real;          // units the finisher will see
     R.misc()[4] = (ok && !broken) ? 0u : 1u;  // rows and requests will not complete
     st_rel_cta(R.misc() + 2, 1u);
-    // one stop per group (each group leaves at the first stop it claims)
-    for (int j = k; stops < kSegGroups; ++j, ++stops)
-      if (!wait_slot(P, R, j)) break;
-      else issue_stop(R, st, j);
-    // nothing may land in shared memory after the CTA exits
+  }
+  // one stop per group (each group leaves at the first stop it claims)
+  for (int j = k; stops < kSegGroups; ++j, ++stops) {
+    if (!wait_slot(P, R, st, j, lane)) break;
+    if (lane == 0) issue_stop(R, j);
+    st.fill(j);
+  }
+  // nothing may land in shared memory after the CTA exits
+  if (lane == 0)
     for (int s2 = 0; s2 < kSegSlots; ++s2)
-      if (st.filled[s2]) {
+      if ((st.filled >> s2) & 1u) {
         const long long t0 = clock64();
-        while (!mbar_test(R.full() + s2, st.fill_par[s2]) && clock64() - t0 < P.wait_limit) {
+        while (!mbar_test(R.full() + s2, (st.par >> s2) & 1u) && clock64() - t0 < P.wait_limit) {
         }
       }
-  }
   __syncwarp();
 }
 
@@ -1480,12 +1464,20 @@ template <typename T>
 __device__ void recorder(const SegParams& P, const Ring& R, int lane) {
   int k = 0;
   long long t_last = clock64();
+  // the producer's second-pass candidates (see the producer): lane j loads
+  // the job entry of candidate cb + j; the published ones, in order, are
+  // queued for the producer
+  const unsigned G = gridDim.x, upj = (unsigned)P.g.upj, njob = (unsigned)P.total;
+  unsigned cb = 0, jtail = 0;
+  unsigned long long ent = 0;
+  bool pend = false, jq_done = false;
   for (;;) {
     bool progress = false;
     // 1. units finished by all their warps, in ring order
-    const int issued = (int)ld_acq_cta(R.misc() + 6);
-    bool fin = false;
-    if (k + lane < issued) fin = ld_acq_cta(&R.rec(k + lane)->ndone) == (unsigned)kSegGroupWarps;
+    // record slot i counts kSegGroupWarps per use: unit k is done once its
+    // slot's count reaches kSegGroupWarps * (k / kSegRecN + 1)
+    const bool fin = ld_acq_cta(&R.rec(k + lane)->ndone) ==
+                     (unsigned)(kSegGroupWarps * ((k + lane) / kSegRecN + 1));
     const unsigned fm = __ballot_sync(0xffffffffu, fin);
     const int done = k + (fm == 0xffffffffu ? 32 : __ffs(~fm) - 1);
     const int nd = min(done - k, 32);
@@ -1521,6 +1513,33 @@ __device__ void recorder(const SegParams& P, const Ring& R, int lane) {
       __syncwarp();
       k += nd;
       if (lane == 0) st_rel_cta(R.misc() + 1, (unsigned)k);
+    }
+    // 2. second-pass candidates: last round's published entries join the
+    //    queue (as far as it has room), then the next window is loaded
+    if (!jq_done) {
+      if (pend) {
+        const unsigned jg = (blockIdx.x + (cb + lane) * G) / upj;
+        const bool pub = jg < njob && (unsigned)(ent & 0xffffffffull) != 0u;
+        const unsigned pm = __ballot_sync(0xffffffffu, pub);
+        int n = pm == 0xffffffffu ? 32 : __ffs(~pm) - 1;
+        n = min(n, kSegJq - (int)(jtail - ld_acq_cta(R.misc() + 9)));
+        if (n > 0) {
+          asm volatile("fence.acq_rel.gpu;" ::: "memory");   // each entry's release happens before the queue's
+          if (lane < n) R.jq()[(jtail + lane) % kSegJq] = ent;
+          __syncwarp();
+          jtail += n;
+          cb += n;
+          if (lane == 0) st_rel_cta(R.misc() + 8, jtail);
+        }
+        pend = false;
+      }
+      if ((blockIdx.x + cb * G) / upj >= njob || ld_acq_cta(R.misc() + 2) != 0u) {
+        jq_done = true;       // no candidate left, or the producer has finished
+      } else {
+        const unsigned jg = (blockIdx.x + (cb + lane) * G) / upj;
+        ent = jg < njob ? ld_relaxed_gpu64(P.jobs + 2 * jg) : 0ull;
+        pend = true;
+      }
     }
     if (progress) {
       t_last = clock64();
@@ -1661,15 +1680,12 @@ __global__ void __launch_bounds__(kSegThreads, 1) seg_verify_kernel(const __grid
     fence_mbar_init();
   }
   if (threadIdx.x < 16) R.misc()[threadIdx.x] = 0u;
+  for (int i = threadIdx.x; i < kSegRecN; i += blockDim.x) R.rec(i)->ndone = 0u;
   __syncthreads();
   Prod st;
-#pragma unroll
-  for (int s = 0; s < kSegSlots; ++s) {
-    st.filled[s] = false;
-    st.fill_par[s] = 0u;
-  }
+  RowUnit mine{};
   int pre = 0;
-  if (warp == 0) pre = producer_prefetch<T>(P, R, st, lane);
+  if (warp == 0) pre = producer_prefetch<T>(P, R, st, mine, lane);
   // the prologue: request b on CTA b mod gridDim (warps 1 .. 26; warp 0 has
   // started the first copies)
   if (blockIdx.x == 0 && threadIdx.x == 0) {
@@ -1687,8 +1703,7 @@ __global__ void __launch_bounds__(kSegThreads, 1) seg_verify_kernel(const __grid
     red_add_gpu(P.ctl + kCtlPrepDone, 1u);
   }
   if (warp == 0) {
-    pre = __shfl_sync(0xffffffffu, pre, 0);
-    producer<T>(P, R, st, pre, lane);
+    producer<T>(P, R, st, mine, pre, lane);
   } else if (warp == 1) {
     recorder<T>(P, R, lane);
   } else if (warp == 2) {
