@@ -435,6 +435,17 @@ __device__ __forceinline__ bool wait_slot(const SegParams& P, const Ring& R, Pro
   return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
 
+// Whether an mbarrier phase has completed, without waiting for it.
+__device__ __forceinline__ bool mbar_done(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{ .reg .pred p; mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Arrive on a full barrier, raising the bytes it waits for first.
 __device__ __forceinline__ void mbar_arrive_expect(uint64_t* bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
@@ -573,14 +584,6 @@ __device__ __forceinline__ unsigned long long ld_relaxed_gpu64(const void* p) {
   return v;
 }
 
-// The producer warp after the prologue.  Lane 0 issues; the warp loads the
-// requests of the coming static units, 32 at a time, one window ahead.
-//
-// Second-pass units are dealt out deterministically: unit g of the job list
-// (job g / upj, half-segment g % upj) belongs to CTA g mod gridDim.  The
-// producer keeps its next one's job entry loading in the background and
-// puts it into the ring, ahead of the next static unit, as soon as the job
-// is published; after its static units it waits for the rest.
 // The producer warp: puts units into the ring in order.  Static (pass-1)
 // units go in as their slots come free, each issued by the lane that holds
 // its geometry; second-pass units go ahead of them as soon as the recorder
@@ -628,16 +631,37 @@ __device__ void producer(const SegParams& P, const Ring& R, Prod& st, RowUnit mi
         t_idle = clock64();
         continue;
       }
+      if (ks < pre) {
+        // the prefetched units: penalty bits, descriptors and arrivals, one
+        // lane each (their slots are fresh)
+        if (lane < pre) issue_row<T>(P, R, lane, mine, true, pol_s, pol_k);
+        k = ks = pre;
+        t_idle = clock64();
+        continue;
+      }
       if (ks < n_static) {
-        if (ks > 0 && (ks & 31) == 0) mine = row_unit<T>(P, cu, ks + lane, n_static);
-        if (ks >= pre) {
+        if ((ks & 31) == 0 && ks > 0) mine = row_unit<T>(P, cu, ks + lane, n_static);
+        // the next units whose slots are free and whose records the
+        // recorder has taken (to the end of this batch of 32) go in
+        // together, one lane each; with none free, wait for the first
+        const int lim = min(min(kSegSlots, n_static - ks), 32 - (ks & 31));
+        const int kk = k + lane;
+        bool fr = false;
+        if (lane < lim)
+          fr = (kk < kSegRecN || st.rec_seen > kk - kSegRecN) &&
+               (kk < kSegSlots || mbar_done(R.empty() + kk % kSegSlots, (uint32_t)((kk / kSegSlots - 1) & 1)));
+        const unsigned fm = __ballot_sync(0xffffffffu, fr);
+        int n = fm == 0xffffffffu ? 32 : __ffs(~fm) - 1;
+        if (n == 0) {
           ok = wait_slot(P, R, st, k, lane);
           if (!ok) break;
-          st.fill(k);
+          n = 1;
         }
-        if (lane == (ks & 31)) issue_row<T>(P, R, k, mine, ks < pre, pol_s, pol_k);
-        ++k;
-        ++ks;
+        __syncwarp();     // the slots' releases, seen by the testing lanes, before the copies
+        if (((lane - ks) & 31) < n) issue_row<T>(P, R, k + ((lane - ks) & 31), mine, false, pol_s, pol_k);
+        for (int j = 0; j < n; ++j) st.fill(k + j);
+        k += n;
+        ks += n;
         t_idle = clock64();
         continue;
       }
