@@ -15,7 +15,8 @@ namespace sv {
 constexpr int kSegGroupWarps = 8;                  // consumer warps per group (one unit at a time)
 constexpr int kSegGroups = 3;                      // unit k goes to group k % kSegGroups
 constexpr int kSegConsumers = kSegGroups * kSegGroupWarps;
-constexpr int kSegThreads = (kSegConsumers + 3) * 32;  // + producer, recorder and decider warps
+constexpr int kSegCtlWarps = 4;                    // producer, recorder, decider and finisher warps
+constexpr int kSegThreads = (kSegConsumers + kSegCtlWarps) * 32;
 constexpr int kSegSlots = 6;                       // TMA ring slots
 static_assert(kSegSlots % kSegGroups == 0, "slot k % kSegSlots belongs to group k % kSegGroups");
 constexpr int kSegLogitBytes = 30720;              // logit bytes per slot (one segment of one row)

@@ -10,9 +10,10 @@
 //
 // Pass 1 (every row, every logit read once): softmax statistics per
 // (unit, warp): a reference and the sum of 2^(z'c - ref), z' the penalised
-// logit, c = log2(e)/T.  When a row's last unit is in, the finisher warp of
-// that CTA combines the row; when a request's last row is in, it takes the
-// request's decisions from pass-1 quantities alone wherever they are fixed:
+// logit, c = log2(e)/T.  When a row's last unit is in, the decider warp of
+// the CTA that owns the row combines it; when a request's last row is in,
+// the owner of the request takes its decisions from pass-1 quantities
+// alone wherever they are fixed:
 //   theta = min(1, D/d) lies in [D, min(1, D/(q(x)-p(x)))] because
 //   q(x) - p(x) <= d <= 1, so pi(x) = p(x) + theta (q(x) - p(x)) is bounded
 //   by p + D (q - p) and min(q, p + D) when q(x) > p(x), and pi(x) >= q(x)
@@ -21,19 +22,21 @@
 // Pass 2 (a "job"): only for the positions whose test the bounds leave open
 // before the first certain rejection, and for that rejection itself (its
 // residual draw).  A job re-reads the position's two rows in half-segment
-// units claimed by any CTA and sums max(p - q, 0) per (unit, warp); its last
-// unit gives d = TV(p, q), theta, pi(x) and the exact decision.  The
-// request's finaliser then draws the correction from the residual's
-// (unit, warp) masses and one re-read range, or the bonus token from the
-// last target row's pass-1 masses, and writes the tokens.
+// units, unit g of the job list going to CTA g mod gridDim, and sums
+// max(p - q, 0) per (unit, warp); its last unit gives d = TV(p, q), theta,
+// pi(x) and the exact decision.  The finisher warp of the request's owner
+// then draws the correction from the residual's (unit, warp) masses and one
+// re-read range, or the bonus token from the last target row's pass-1
+// masses, and writes the tokens.
 //
-// Warp roles: warp 0 producer (lane 0 issues the TMA bulk copies of a
-// 6-slot ring; a free group of 8 consumer warps takes the next unit), warp 1
-// recorder (stores the consumers' partials and counts units), warp 2
-// decider (row combines, decisions, second passes' ends, tokens), warps
-// 3..26 consumers.  Every wait is bounded;
-// a wait that runs out raises a global abort flag, everyone leaves, and the
-// last CTA marks unfinished requests SPEC_STATUS_TIMEOUT.
+// Warp roles: warp 0 producer (TMA bulk copies into a 6-slot ring; slot s
+// feeds consumer group s mod 3), warp 1 recorder (stores the consumers'
+// partials, counts units, finds published second-pass units for the
+// producer), warp 2 decider (row combines, decisions, second passes' ends),
+// warp 3 finisher (draws and tokens), warps 4.. consumers in 3 groups of 8.
+// Every wait is bounded; a wait that runs out raises a global abort flag,
+// everyone leaves, and the last CTA marks unfinished requests
+// SPEC_STATUS_TIMEOUT.
 
 #include "common.cuh"
 #include "spec_internal.h"
@@ -52,10 +55,12 @@ constexpr int kOffRec = seg_al16(kOffBars + 2 * kSegSlots * 8);        // unit r
 constexpr int kOffMisc = seg_al16(kOffRec + kSegRecN * (int)sizeof(SegUnitRec));  // control words
 constexpr int kSegJq = 64;                                              // second-pass candidates found, not yet issued
 constexpr int kOffJq = seg_al16(kOffMisc + 64);                         // their job entries (kSegJq, 8 bytes each)
-constexpr int kOffCu = kOffJq + kSegJq * 8;                             // cu_draft copy (B + 1 <= kSegCuCap)
+constexpr int kSegFq = 64;                                              // requests ready for their tokens
+constexpr int kOffFq = kOffJq + kSegJq * 8;                             // their indices (kSegFq)
+constexpr int kOffCu = kOffFq + kSegFq * 4;                             // cu_draft copy (B + 1 <= kSegCuCap)
 constexpr int kSegSmem = kOffCu + kSegCuCap * 4;
 static_assert(kSegSlotBytes % 128 == 0 && kOffBars % 8 == 0 && kOffRec % 16 == 0 && kOffJq % 16 == 0 &&
-                  kOffCu % 16 == 0,
+                  kOffFq % 16 == 0 && kOffCu % 16 == 0,
               "shared-memory regions keep the alignment of their widest access");
 
 
@@ -138,6 +143,7 @@ struct Ring {
   }
   __device__ unsigned* misc() const { return reinterpret_cast<unsigned*>(seg_smem + kOffMisc); }
   __device__ unsigned long long* jq() const { return reinterpret_cast<unsigned long long*>(seg_smem + kOffJq); }
+  __device__ int* fq() const { return reinterpret_cast<int*>(seg_smem + kOffFq); }
   __device__ int* cu() const { return reinterpret_cast<int*>(seg_smem + kOffCu); }
 };
 
@@ -222,13 +228,13 @@ __device__ __forceinline__ int bound_decision(float px, float qx, float D, float
 }
 
 // ------------------------------------------------------------ prologue
-// Request b's prologue, by the CTA's warps 1 .. kSegConsumers + 2 (`tid` in
+// Request b's prologue, by the CTA's warps 1 .. kSegThreads / 32 - 1 (`tid` in
 // 0 .. kPrepThreads-1; the producer warp is busy with the first copies):
 // status bits, the history bitmap (every token of the request's history)
 // and the descriptors of the request's rows.  With alpha = 1 the penalty is
 // the identity and the set stays empty.  `sh` is a shared word for the
 // status bits.
-constexpr int kPrepThreads = (kSegConsumers + 2) * 32;
+constexpr int kPrepThreads = kSegThreads - 32;
 constexpr int kPrepBar = 15;
 
 __device__ __forceinline__ void prep_sync() { named_sync(kPrepBar, kPrepThreads); }
@@ -697,7 +703,7 @@ __device__ void producer(const SegParams& P, const Ring& R, Prod& st, RowUnit mi
     k = pre;
   }
   if (lane == 0) {
-    R.misc()[0] = (unsigned)real;          // units the finisher will see
+    R.misc()[0] = (unsigned)real;          // units the recorder will see
     R.misc()[4] = (ok && !broken) ? 0u : 1u;  // rows and requests will not complete
     st_rel_cta(R.misc() + 2, 1u);
   }
@@ -848,7 +854,7 @@ __device__ __forceinline__ float2 vec_exp_sum(const uint4& v, float2 c2, float2 
 
 // A per-lane sum of 2^(z'c) (reference 0) is trusted inside [2^-100, 2^100]:
 // a row's total then stays far inside fp32.  Outside it (or NaN), the
-// warp's partial is flagged and the finisher recomputes that range with the
+// warp's partial is flagged and the recorder recomputes that range with the
 // range's largest logit as the reference.
 constexpr float kSumHi = 1.2676506002282294e30f;   // 2^100
 constexpr float kSumLo = 7.888609052210118e-31f;   // 2^-100
@@ -1006,7 +1012,7 @@ __device__ void consumer(const SegParams& P, const Ring& R, int cw, int lane) {
   }
 }
 
-// ------------------------------------------------------------ the finisher
+// ------------------------------------------------------------ draws and records
 // Inverse CDF inside the token range [a, a + n) (a a multiple of 32) of a
 // row, or of the residual max(p - q, 0) of a row pair: the smallest v whose
 // prefix mass (from a) exceeds t; the last token with mass if t is out of
@@ -1304,7 +1310,8 @@ __device__ void finalize(const SegParams& P, int b, int lane) {
 // the jobs (second passes) for the rest.  Returns the positions whose job
 // the caller then waits for (0: the request is finished).
 template <typename T>
-__device__ unsigned request_decide(const SegParams& P, int b, int lane) {
+__device__ unsigned request_decide(const SegParams& P, int b, int lane, bool& ready) {
+  ready = false;
   const int d0 = __ldg(P.cu_draft + b), K = __ldg(P.cu_draft + b + 1) - d0, off = d0 + b;
   const int base = 2 * d0 + b;      // the request's first row
   int st = __ldcg(P.req_status + b);
@@ -1379,7 +1386,7 @@ __device__ unsigned request_decide(const SegParams& P, int b, int lane) {
       }
       if (lane == 0) P.req_done[b] = 1u;
     } else if (!tv_only) {
-      finalize<T>(P, b, lane);
+      ready = true;       // every decision is known: the tokens can be drawn
     } else if (lane == 0) {
       P.req_done[b] = 1u;
     }
@@ -1580,6 +1587,48 @@ __device__ void recorder(const SegParams& P, const Ring& R, int lane) {
   }
 }
 
+// A request whose decisions are all known goes to the finisher warp, which
+// draws its last token and emits its tokens; with the queue full, the
+// decider does it itself.
+template <typename T>
+__device__ __forceinline__ void queue_final(const SegParams& P, const Ring& R, unsigned& tail, int b, int lane) {
+  if (tail - ld_acq_cta(R.misc() + 11) >= (unsigned)kSegFq) {
+    finalize<T>(P, b, lane);
+    return;
+  }
+  __syncwarp();
+  if (lane == 0) {
+    R.fq()[tail % kSegFq] = b;
+    st_rel_cta(R.misc() + 10, tail + 1);   // the request's decisions and its entry, then the count
+  }
+  ++tail;
+}
+
+// The finisher warp: the requests the decider queued, in order; done once
+// the decider has finished (misc[12]) and the queue is empty.
+template <typename T>
+__device__ void finisher(const SegParams& P, const Ring& R, int lane) {
+  unsigned head = 0;
+  long long t_last = clock64();
+  for (;;) {
+    if (head < ld_acq_cta(R.misc() + 10)) {
+      finalize<T>(P, R.fq()[head % kSegFq], lane);
+      ++head;
+      __syncwarp();
+      if (lane == 0) st_rel_cta(R.misc() + 11, head);
+      t_last = clock64();
+      continue;
+    }
+    if (ld_acq_cta(R.misc() + 12) != 0u && head == ld_acq_cta(R.misc() + 10)) break;
+    if (aborted(P)) break;
+    if (clock64() - t_last > P.wait_limit) {
+      raise_abort(P);
+      break;
+    }
+    __nanosleep(200);
+  }
+}
+
 // The decider warp: for the rows and requests this CTA owns (the i-th is
 // c + i * gridDim), combines a row once all its units are counted, decides a
 // request once all its rows are combined, waits for its positions' second
@@ -1590,6 +1639,7 @@ __device__ void decider(const SegParams& P, const Ring& R, int lane) {
   const int* cu = cu_of(P, R);
   Owned rows, reqs;
   int jp = -1, jb = -1;     // a position of an owned request waiting for its second pass (per lane)
+  unsigned fq_tail = 0;     // requests handed to the finisher
   rows.n = c < P.NR ? (P.NR - 1 - c) / G + 1 : 0;
   reqs.n = c < P.B ? (P.B - 1 - c) / G + 1 : 0;
   // nothing completes when cu_draft is not a valid packing
@@ -1639,7 +1689,9 @@ __device__ void decider(const SegParams& P, const Ring& R, int lane) {
         if (min(KL, 32) > room) break;    // decided later, once jobs have finished
         reqs.done |= 1u << L;
         const int bb = c + (reqs.next + L) * G;
-        const unsigned need = request_decide<T>(P, bb, lane);
+        bool ready;
+        const unsigned need = request_decide<T>(P, bb, lane, ready);
+        if (ready) queue_final<T>(P, R, fq_tail, bb, lane);
         if (need) {
           // the request's positions with a job join the wait list
           const int d0 = cu[bb];
@@ -1674,7 +1726,7 @@ __device__ void decider(const SegParams& P, const Ring& R, int lane) {
         if (P.mode == kModeTvOnly) {
           if (lane == 0) P.req_done[b] = 1u;
         } else {
-          finalize<T>(P, b, lane);
+          queue_final<T>(P, R, fq_tail, b, lane);
         }
       }
     }
@@ -1710,7 +1762,7 @@ __global__ void __launch_bounds__(kSegThreads, 1) seg_verify_kernel(const __grid
   RowUnit mine{};
   int pre = 0;
   if (warp == 0) pre = producer_prefetch<T>(P, R, st, mine, lane);
-  // the prologue: request b on CTA b mod gridDim (warps 1 .. 26; warp 0 has
+  // the prologue: request b on CTA b mod gridDim (warps 1 and up; warp 0 has
   // started the first copies)
   if (blockIdx.x == 0 && threadIdx.x == 0) {
     if (__ldg(P.cu_draft) != 0 || __ldg(P.cu_draft + P.B) != P.total) atomicOr(P.ctl + kCtlBroken, 1u);
@@ -1732,8 +1784,12 @@ __global__ void __launch_bounds__(kSegThreads, 1) seg_verify_kernel(const __grid
     recorder<T>(P, R, lane);
   } else if (warp == 2) {
     decider<T>(P, R, lane);
+    __syncwarp();
+    if (lane == 0) st_rel_cta(R.misc() + 12, 1u);   // the finisher's queue is complete
+  } else if (warp == 3) {
+    finisher<T>(P, R, lane);
   } else {
-    consumer<T>(P, R, warp - 3, lane);
+    consumer<T>(P, R, warp - kSegCtlWarps, lane);
   }
   __syncthreads();
   if (threadIdx.x == 0) {
