@@ -14,7 +14,10 @@ Prints one JSON line:
   cpu_baseline  the CPU oracle on a bounded sample of the same workload
 
 ``--impl reference`` times the CPU oracle itself (one bounded sample per
-step) and prints its line with "impl": "reference".
+step) and prints its line with "impl": "reference".  ``--profile`` runs the
+ncu launch list and one capture of the sampling kernel and writes
+profiles/seg_verify_kernel_batched.json.  ``--gpus N`` outside torchrun
+starts N ranks itself (or refuses when fewer GPUs are visible).
 
 Multi-GPU: one process per GPU under torchrun; requests are independent, so
 each rank verifies its own batch (weak scaling, no data-path collective; a
@@ -38,12 +41,15 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
-KERNEL_SOURCES = ["speculative_decoding_verification_23_gb300/csrc/pipe_verify.cu",
+KERNEL_SOURCES = ["speculative_decoding_verification_23_gb300/csrc/seg_verify.cu",
+                  "speculative_decoding_verification_23_gb300/csrc/seg_internal.h",
                   "speculative_decoding_verification_23_gb300/csrc/stream_common.cuh",
-                  "speculative_decoding_verification_23_gb300/csrc/verify_common.cuh",
                   "speculative_decoding_verification_23_gb300/csrc/common.cuh",
                   "speculative_decoding_verification_23_gb300/csrc/spec_internal.h"]
-PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "sample_verify_batched.json")
+KERNEL = "seg_verify_kernel"
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "seg_verify_kernel_batched.json")
+WORKLOAD = "batched B=64 K=8 V=152064 bf16 logits"
+CLOCK_WINDOW_S = 0.2           # the K-step window repeats until this much time has passed
 METRIC = "spec-verify rows/s and logits HBM GB/s (% of GB300 peak) at B=64 K=8 V=152064"
 
 
@@ -167,20 +173,65 @@ class ClockSampler:
                 "samples": len(self.samples), "source": self.source}
 
 
-def oracle_baseline(batch, budget_s: float):
+def oracle_baseline(batch, budget_s: float, results=None):
     """Requests/s of the CPU oracle on a bounded sample: whole requests of the
-    batch in order, cycling through the batch until `budget_s` has passed."""
+    batch in order, cycling through the batch until `budget_s` has passed.
+    With `results` (a dict), each request's oracle outputs are kept there."""
     import oracle
 
     t0 = time.perf_counter()
     n = 0
     while True:
-        oracle.verify_batch(batch, [n % batch.B])
+        b = n % batch.B
+        r = oracle.verify_batch(batch, [b])
+        if results is not None and b not in results:
+            off = int(batch.cu_draft[b]) + b
+            results[b] = (r["tokens"][off:off + batch.k(b) + 1].copy(), int(r["accepted"][b]),
+                          int(r["status"][b]), bool(r["near_tie"][b]))
         n += 1
         if time.perf_counter() - t0 > budget_s:
             break
     dt = time.perf_counter() - t0
     return n / dt, n, dt
+
+
+def _oracle_worker(args):
+    round_, first, budget_s = args
+    import oracle
+
+    batch = make_workload(round_)
+    t0 = time.perf_counter()
+    n = 0
+    while time.perf_counter() - t0 < budget_s:
+        oracle.verify_batch(batch, [(first + n) % batch.B])
+        n += 1
+    return n, time.perf_counter() - t0
+
+
+def oracle_all_cores(round_: int, budget_s: float):
+    """The same oracle on every host core at once (one process per core,
+    started with spawn): requests/s summed over the workers, and the cores."""
+    import multiprocessing as mp
+
+    cores = os.cpu_count() or 1
+    with mp.get_context("spawn").Pool(cores) as pool:
+        res = pool.map(_oracle_worker, [(round_, i, budget_s) for i in range(cores)])
+    return sum(n / dt for n, dt in res), cores
+
+
+def parity_sample(got, results, batch):
+    """GPU outputs against the oracle's on the requests the CPU sample ran:
+    (requests compared, mismatches, near ties)."""
+    tok, acc, st = got
+    bad = near = 0
+    for b, (rt, ra, rs, nt) in results.items():
+        if nt:
+            near += 1
+            continue
+        off = int(batch.cu_draft[b]) + b
+        if not (np.array_equal(tok[off:off + batch.k(b) + 1], rt) and acc[b] == ra and st[b] == rs):
+            bad += 1
+    return len(results), bad, near
 
 
 def reduce_max(x: float, dist, device) -> float:
@@ -207,6 +258,13 @@ def make_workload(rank: int):
     return W.batched(round_=rank)
 
 
+def bench_config(world: int) -> dict:
+    """The workload the line is quoted on (the same for both arms)."""
+    return {"workload": WORKLOAD, "B": 64, "K": 8, "V": 152064, "logit_bytes_per_step": 330891264,
+            "parallelism": f"replicas x{world}",
+            "l2": "inputs 330.9 MB > 129 MB L2; two input copies alternate"}
+
+
 def bench_reference(args, rank, world):
     batch = make_workload(rank)
     per_step_budget = max(1.0, 150.0 / max(1, args.steps + args.warmup))
@@ -223,8 +281,7 @@ def bench_reference(args, rank, world):
         "impl": "reference", "metric": METRIC, "value": value, "unit": "requests/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * wall / max(1, args.steps),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": {"workload": "batched B=64 K=8 V=152064 bf16 logits", "B": 64, "K": 8,
-                                        "V": 152064},
+        "data": "synthetic", "config": bench_config(world),
         "cpu_baseline": {"value": value, "unit": "requests/s", "cores": 1, "kind": "oracle",
                          "sample": f"whole requests of the B=64 batch, ~{per_step_budget:.1f} s of CPU per step"},
         "e2e": {"value": value, "unit": "requests/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -255,33 +312,46 @@ def bench_gpu(args, rank, world, dist):
         sv.spec_verify_sample(argv[k % 2], device=dev, workspace=ws, out_tokens=outs[0], out_accepted=outs[1],
                               out_status=outs[2], stream=stream)
 
-    for k in range(max(3, args.warmup)):
+    warm = max(3, args.warmup)
+    for k in range(warm):
         step(k)
     torch.cuda.synchronize()
     assert int(outs[2].max().item()) == 0, "bench inputs flagged invalid"
 
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    if dist:
-        dist.barrier()
-    torch.cuda.synchronize()
+    # ---- timed windows of exactly K steps, repeated (the same count on
+    # every rank) until CLOCK_WINDOW_S of wall time has passed, clocks
+    # sampled throughout
+    per_launch, win_s = [], []
+    n_win = 0
+    t_wall = time.perf_counter()
     with ClockSampler(dev) as clk:
-        t_start = torch.cuda.Event(enable_timing=True)
-        t_end = torch.cuda.Event(enable_timing=True)
-        t_start.record(stream)
-        for k in range(args.steps):
-            ev[k][0].record(stream)
-            step(k)
-            ev[k][1].record(stream)
-        t_end.record(stream)
-        torch.cuda.synchronize()
-    elapsed = reduce_max(t_start.elapsed_time(t_end) / 1000.0, dist, dev)
-    per_launch = [a.elapsed_time(b) / 1000.0 for a, b in ev]
+        while n_win == 0 or reduce_max(float(time.perf_counter() - t_wall < CLOCK_WINDOW_S), dist, dev) > 0:
+            n_win += 1
+            ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                  for _ in range(args.steps)]
+            if dist:
+                dist.barrier()
+            torch.cuda.synchronize()
+            t_start = torch.cuda.Event(enable_timing=True)
+            t_end = torch.cuda.Event(enable_timing=True)
+            t_start.record(stream)
+            for k in range(args.steps):
+                ev[k][0].record(stream)
+                step(k)
+                ev[k][1].record(stream)
+            t_end.record(stream)
+            torch.cuda.synchronize()
+            win_s.append(reduce_max(t_start.elapsed_time(t_end) / 1000.0, dist, dev))
+            per_launch += [x.elapsed_time(y) / 1000.0 for x, y in ev]
+    elapsed = float(np.median(win_s))
     if dist:
         dist.barrier()
     value = job_throughput(batch.B, world, args.steps, elapsed)
     ms = 1000.0 * elapsed / args.steps
+    got = [t.cpu().numpy() for t in outs]
 
-    # ---- end to end: pinned host inputs -> device -> call -> tokens back
+    # ---- end to end over the same K steps: pinned host inputs -> device ->
+    # call -> tokens and accepted counts back
     host = {
         "target": copies[0].target.cpu().pin_memory(), "draft": copies[0].draft.cpu().pin_memory(),
         "small": [t.cpu().pin_memory() for t in (copies[0].cu_draft, copies[0].draft_tokens, copies[0].cu_hist,
@@ -310,16 +380,18 @@ def bench_gpu(args, rank, world, dist):
     for _ in range(2):
         e2e_step()
     torch.cuda.synchronize()
-    e_steps = max(3, min(args.steps, 20))
+    if dist:
+        dist.barrier()
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     a.record(stream)
-    for _ in range(e_steps):
+    for _ in range(args.steps):
         e2e_step()
     b.record(stream)
     torch.cuda.synchronize()
-    e2e_value = job_throughput(batch.B, world, e_steps, reduce_max(a.elapsed_time(b) / 1000.0, dist, dev))
+    e2e_value = job_throughput(batch.B, world, args.steps, reduce_max(a.elapsed_time(b) / 1000.0, dist, dev))
 
-    # ---- roofline of the sampling kernel (one launch per step)
+    # ---- roofline of the sampling kernel (one launch per step, after the
+    # call's clear of its counters)
     peak, peak_kind = measured_peak()
     alg_bytes = batch.logit_bytes() + 4 * (batch.total_drafts + batch.B) * 2 + 4 * int(batch.hist.size) + 4 * 4 * batch.B
     launch_s = float(np.mean(per_launch))
@@ -333,26 +405,36 @@ def bench_gpu(args, rank, world, dist):
 
     line = {
         "metric": METRIC, "value": value, "unit": "requests/s", "n_gpus": world, "steps": args.steps,
-        "warmup": max(3, args.warmup), "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": "batched B=64 K=8 V=152064 bf16 logits", "B": batch.B, "K": 8, "V": batch.V,
-                   "logit_bytes_per_step": batch.logit_bytes(), "parallelism": f"replicas x{world}",
-                   "l2": "inputs 330.9 MB > 129 MB L2; two input copies alternate"},
+        "warmup": warm, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": bench_config(world),
+        "windows": {"count": n_win, "ms_per_step": [round(1000.0 * w / args.steps, 4) for w in win_s],
+                    "value_from": "median window"},
         "logit_rows_per_s": value * (2 * 8 + 1),
         "hbm_gbs": achieved,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "traffic": traffic, "peak_kind": peak_kind, "kernel": "pipe_verify_kernel",
-                     "algorithmic_bytes_per_launch": alg_bytes, "launch_ms": 1000 * launch_s},
-        "e2e": {"value": e2e_value, "unit": "requests/s", "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
-        "gpu_launches": args.steps,
+                     "traffic": traffic, "peak_kind": peak_kind, "kernel": KERNEL,
+                     "algorithmic_bytes_per_launch": alg_bytes, "launch_ms": 1000 * launch_s,
+                     "launch_timing": "CUDA events around each call on its stream (counter clear and kernel)"},
+        "e2e": {"value": e2e_value, "unit": "requests/s", "h2d_bytes_per_step": int(h2d),
+                "d2h_bytes_per_step": int(d2h), "steps": args.steps},
+        "gpu_launches": args.steps * n_win,
         "clocks": clk.summary(),
     }
     if rank == 0 and args.extras:
         line["extras"] = bench_extras(dev, peak, args.cpu_seconds)
     if rank == 0 and not args.no_cpu_baseline:
-        v, n, dt = oracle_baseline(batch, args.cpu_seconds)
+        results = {}
+        v, n, dt = oracle_baseline(batch, args.cpu_seconds, results)
+        v_all, cores = oracle_all_cores(rank, max(2.0, args.cpu_seconds / 3))
         line["cpu_baseline"] = {"value": v, "unit": "requests/s", "cores": 1, "kind": "oracle",
-                                "sample": f"{n} whole requests cycled through the B=64 batch ({dt:.1f} s, one thread)"}
+                                "sample": f"{n} whole requests cycled through the B=64 batch ({dt:.1f} s, one thread)",
+                                "all_cores": {"value": v_all, "cores": cores,
+                                              "sample": "one spawned process per core, each cycling through the batch"}}
+        checked, bad, near = parity_sample(got, results, batch)
+        line["parity"] = {"requests_checked": checked, "mismatches": bad, "near_ties": near,
+                          "rule": "tokens, accepted and status equal to the oracle's for every request "
+                                  "not within 1e-6 of a decision threshold"}
+        line["near_ties"] = near
     if rank == 0:
         print(json.dumps(line), flush=True)
 
@@ -437,7 +519,7 @@ def bench_extras(dev, peak: float, cpu_seconds: float) -> dict:
     ab = db.args()
     sec = timed(lambda: sv.spec_tv_budget(ab, device=dev, workspace=wsb, stream=stream))
     tvbytes = 2 * bb.total_drafts * bb.V * 2 + 4 * int(bb.hist.size) + 16 * bb.total_drafts
-    out["tv_budget_batched_B64_K8"] = line("tv", tvbytes, sec, None, "pipe_verify_kernel (TV only)")
+    out["tv_budget_batched_B64_K8"] = line("tv", tvbytes, sec, None, "seg_verify_kernel (TV only)")
     sec = timed(lambda: sv.spec_draft_confidence(ab, 0.6, device=dev, workspace=wsb, stream=stream))
     cbytes = bb.total_drafts * bb.V * 2 + 4 * int(bb.hist.size) + 8 * bb.total_drafts
     rate = oracle_rate(lambda batch, reqs: oracle.draft_confidence_batch(batch, 0.6, reqs), bb, budget)
@@ -483,6 +565,81 @@ def acceptance_sweep(dev, batches: int = 8, per: int = 32) -> dict:
     return res
 
 
+def relaunch(args) -> int:
+    """`--gpus N` outside torchrun: run N ranks of this script, one per GPU
+    (torch.distributed.run on 127.0.0.1), or refuse when there are fewer
+    GPUs.  Returns the exit code."""
+    import torch
+
+    have = torch.cuda.device_count()
+    if have < args.gpus:
+        print(json.dumps({"error": f"--gpus {args.gpus} asked for, {have} GPU(s) visible; refusing"}), flush=True)
+        return 2
+    import socket
+
+    with socket.socket() as so:
+        so.bind(("127.0.0.1", 0))
+        port = so.getsockname()[1]
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={args.gpus}",
+           "--master-addr=127.0.0.1", f"--master-port={port}", os.path.abspath(__file__)] + sys.argv[1:]
+    return subprocess.call(cmd)
+
+
+def profile(args) -> int:
+    """`--profile`: the launch list of a short bench run and one full capture
+    of the sampling kernel under ncu (clocks left alone), summarised into
+    profiles/<kernel>_batched.json (DRAM bytes per launch, duration, the
+    kernel's share of the launches) with the kernel sources' hash.  Run
+    only where the same command has run cleanly without ncu."""
+    import csv
+
+    os.makedirs(os.path.join(ROOT, "gpurun_out"), exist_ok=True)
+    base = [sys.executable, os.path.abspath(__file__), "--steps", "3", "--warmup", "3", "--no-cpu-baseline"]
+    if subprocess.call(base, stdout=subprocess.DEVNULL) != 0:
+        print("plain run failed; not profiling", file=sys.stderr)
+        return 1
+    launches = os.path.join(ROOT, "gpurun_out", "launches.csv")
+    rc = subprocess.call(["ncu", "--metrics", "gpu__time_duration.sum", "--clock-control", "none", "-c", "400",
+                          "--csv", "--log-file", launches] + base, stdout=subprocess.DEVNULL)
+    if rc:
+        return rc
+    rep = os.path.join(ROOT, "gpurun_out", "prof_" + KERNEL)
+    rc = subprocess.call(["ncu", "--set", "full", "--clock-control", "none", "-k", "regex:" + KERNEL, "-s", "4",
+                          "-c", "1", "-f", "-o", rep] + base, stdout=subprocess.DEVNULL)
+    if rc:
+        return rc
+    raw = subprocess.run(["ncu", "-i", rep + ".ncu-rep", "--page", "raw", "--csv"], capture_output=True,
+                         text=True).stdout
+    rows = list(csv.reader(raw.splitlines()))
+    hdr, vals = rows[0], rows[2]
+    get = lambda k: float(vals[hdr.index(k)].replace(",", ""))
+    names, times = [], []
+    per_ns = {"nsecond": 1.0, "ns": 1.0, "usecond": 1e3, "us": 1e3, "msecond": 1e6, "ms": 1e6, "second": 1e9,
+              "s": 1e9}
+    with open(launches) as f:
+        lines = [l for l in f if l.startswith('"')]
+    for r in csv.DictReader(lines):
+        if r.get("Metric Name") == "gpu__time_duration.sum":
+            names.append(r["Kernel Name"])
+            times.append(float(r["Metric Value"].replace(",", "")) * per_ns.get(r.get("Metric Unit", ""), 1.0))
+    tot = sum(times) or 1.0
+    mine = [t for n, t in zip(names, times) if KERNEL in n]
+    rd, wr = get("dram__bytes_read.sum"), get("dram__bytes_write.sum")
+    scale = {"byte": 1, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9}.get(rows[1][hdr.index("dram__bytes_read.sum")], 1)
+    dur = get("gpu__time_duration.sum") * per_ns.get(rows[1][hdr.index("gpu__time_duration.sum")], 1.0) / 1e3
+    out = {"kernel": KERNEL, "workload": WORKLOAD, "kernel_hash": kernel_hash(),
+           "dram_bytes_per_launch": int((rd + wr) * scale), "dram_read_bytes": int(rd * scale),
+           "dram_write_bytes": int(wr * scale),
+           "duration_us_under_ncu": dur,
+           "launch_list": {"launches": len(names), "kernel_launches": len(mine), "kernel_share": sum(mine) / tot},
+           "command": "python bench.py --profile"}
+    for path in (PROFILE_SUMMARY, os.path.join(ROOT, "gpurun_out", os.path.basename(PROFILE_SUMMARY))):
+        with open(path, "w") as f:
+            json.dump(out, f, indent=2)
+    print(json.dumps(out), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -493,9 +650,15 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--extras", action="store_true",
                     help="also time the other configurations and entry points (adds about a minute)")
+    ap.add_argument("--profile", action="store_true",
+                    help="ncu launch list and one capture of the sampling kernel -> profiles/")
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
+    if args.profile:
+        sys.exit(profile(args))
+    if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
+        sys.exit(relaunch(args))
     if args.impl == "reference":
         if rank == 0:
             bench_reference(args, rank, world)

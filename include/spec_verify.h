@@ -127,12 +127,15 @@ enum {
    definition either way; fp32 rounding may differ in the last bits).
    RESIDENT keeps each CTA's slice of both rows in shared memory and reads
    every logit once; it suits batches whose work items (sum K_b + B) all fit
-   in one wave of clusters.  STREAMING re-reads each slice from L2 for the
-   second pass and keeps about one item per SM in flight; it suits large
-   batches.  SPLIT (without top-p) cuts every row into vocabulary segments
-   spread over all SMs: one read of each logit for the softmax statistics,
-   and a second read of only the rows of positions whose decision those
-   statistics leave open.  Without a hint the library picks by batch size. */
+   in one wave of clusters.  SPLIT (without top-p) cuts every row into
+   vocabulary segments spread over all SMs: one read of each logit for the
+   softmax statistics, and a second read of only the rows of positions whose
+   decision those statistics leave open.  STREAMING without top-p names the
+   pipelined kernel (about one work item per SM in flight, each item's
+   second pass re-read from L2); with top-p, the cluster kernel's streaming
+   variant.  Without a hint: RESIDENT when the batch fits in one wave, else
+   SPLIT without top-p (rows of at most 32 segments: V <= 491520 bf16,
+   245760 fp32) and the streaming cluster kernel with top-p. */
 #define SPEC_PREFER_RESIDENT 2u
 #define SPEC_PREFER_STREAMING 4u
 #define SPEC_PREFER_SPLIT 8u

@@ -156,14 +156,27 @@ __device__ __forceinline__ bool aborted(const SegParams& P) {
 }
 __device__ __forceinline__ void raise_abort(const SegParams& P) { atomicExch(P.ctl + kCtlAbort, 1u); }
 
+// One try of an mbarrier phase that may suspend the thread for up to
+// `ns` nanoseconds (it resumes early once the phase completes), so that a
+// waiting warp takes no issue slots from the working ones.
+__device__ __forceinline__ bool mbar_try(uint64_t* bar, uint32_t parity, uint32_t ns) {
+  uint32_t ok;
+  asm volatile(
+      "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3; selp.u32 %0, 1, 0, p; }"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(ns)
+      : "memory");
+  return ok != 0;
+}
+
 // Bounded wait on an mbarrier phase; false if it ran out or another CTA
 // raised the abort flag.
 __device__ __forceinline__ bool ring_wait(const SegParams& P, uint64_t* bar, uint32_t parity) {
-  if (mbar_test(bar, parity)) return true;
+  if (mbar_try(bar, parity, 20000u)) return true;
   const long long t0 = clock64();
   for (int n = 1;; ++n) {
-    if (mbar_test(bar, parity)) return true;
-    if ((n & 63) == 0 && aborted(P)) return false;
+    if (mbar_try(bar, parity, 20000u)) return true;
+    if ((n & 3) == 0 && aborted(P)) return false;
     if (clock64() - t0 > P.wait_limit) {
       raise_abort(P);
       return false;

@@ -100,12 +100,21 @@ void fill_sample_inputs(sv::SampleParams& P, const spec_args* a) {
 // cycles (about two seconds at any clock this part runs).
 constexpr long long kSegWaitLimit = 4000000000ll;
 
-// The split-vocabulary kernel serves sampling without top-p when the caller
-// asks for it and a row has at most kSegMaxSegs segments (V <= 491520 bf16,
-// 245760 fp32); other batches go to the kernels below.
-bool use_seg(const spec_args* a) {
-  return !a->top_p && (a->flags & SPEC_PREFER_SPLIT) &&
-         sv::make_seg_geom(a->V, elem_bytes(a->dtype)).nseg <= sv::kSegMaxSegs;
+// The split-vocabulary kernel can serve sampling without top-p when a row
+// has at most kSegMaxSegs segments (V <= 491520 bf16, 245760 fp32).
+bool seg_fits(const spec_args* a) {
+  return !a->top_p && sv::make_seg_geom(a->V, elem_bytes(a->dtype)).nseg <= sv::kSegMaxSegs;
+}
+
+// It does when asked for, and by default for batches the resident cluster
+// kernel would not take in one wave (`resident_pick`: the choice made
+// without hints).  SPEC_PREFER_RESIDENT and SPEC_PREFER_STREAMING keep the
+// kernels they name.
+bool use_seg(const spec_args* a, bool resident_pick) {
+  if (!seg_fits(a)) return false;
+  if (a->flags & SPEC_PREFER_SPLIT) return true;
+  if (a->flags & (SPEC_PREFER_RESIDENT | SPEC_PREFER_STREAMING)) return false;
+  return !resident_pick;
 }
 
 // The split-vocabulary kernel (no top-p): sampling or the TV quantities.
@@ -173,10 +182,11 @@ int run_seg(const sv::SampleParams& S, const spec_args* a, void* ws, int num_sms
 
 // Picks the kernel variant.  Resident (each logit read once, values kept in
 // the shared memory of a C-CTA cluster) when every work item gets its own
-// cluster in one wave; streaming otherwise: the pipelined kernel (one CTA
-// per SM, pass 1 of the next item overlapping pass 2 of the current one)
-// without top-p, the cluster kernel's streaming variant with top-p.
-// SPEC_PREFER_* flags override the choice between resident and streaming.
+// cluster in one wave; otherwise the split-vocabulary kernel without top-p
+// and the cluster kernel's streaming variant with top-p.  SPEC_PREFER_*
+// flags override the choice; SPEC_PREFER_STREAMING without top-p names the
+// pipelined kernel (one CTA per SM, pass 1 of the next item overlapping
+// pass 2 of the current one).
 int run_sample(sv::SampleParams& P, const spec_args* a, void* ws, cudaStream_t stream) {
   int max_smem = 0, num_sms = 0, smem_per_sm = 0;
   int rc = device_props(&max_smem, &num_sms, &smem_per_sm);
@@ -191,12 +201,12 @@ int run_sample(sv::SampleParams& P, const spec_args* a, void* ws, cudaStream_t s
          sv::choose_stream_layout(a->V, C_str, es, topp, max_smem, smem_per_sm, &L_str) != 0)
     C_str *= 2;
   const bool str_ok = C_str <= sv::kMaxCluster;
-  // Without top-p, when asked for: the split-vocabulary kernel.
-  if (use_seg(a)) return run_seg(P, a, ws, num_sms, max_smem, stream);
+  const bool resident_pick = res_ok && (!str_ok || (long long)P.n_items * C_res <= num_sms);
+  if (use_seg(a, resident_pick)) return run_seg(P, a, ws, num_sms, max_smem, stream);
   bool resident;
   if ((a->flags & SPEC_PREFER_RESIDENT) && res_ok) resident = true;
   else if ((a->flags & SPEC_PREFER_STREAMING) && str_ok) resident = false;
-  else resident = res_ok && (!str_ok || (long long)P.n_items * C_res <= num_sms);
+  else resident = resident_pick;
   sv::PipeLayout L_pipe{};
   const bool pipe_ok = !topp && sv::choose_pipe_layout(a->V, es, max_smem, &L_pipe) == 0 &&
                        (long long)P.n_items <= (long long)num_sms * sv::kPipeMaxIters;
@@ -244,13 +254,15 @@ int static_scratch_address(void** out) {
   return SPEC_OK;
 }
 
-// Scratch the sampling call needs: the split-vocabulary kernel's records
-// without top-p (unless the resident cluster kernel is asked for), the
-// cluster kernel's counters, results and flags with it.
+// Scratch the sampling call needs: the cluster kernels' counters, results
+// and flags, or the split-vocabulary kernel's records when it may serve the
+// batch (the larger of the two then, as the choice between them depends on
+// the device).
 size_t sample_scratch_bytes(const spec_args* a) {
-  if (use_seg(a))
-    return sv::make_seg_workspace(a->B, a->total_drafts, a->V, elem_bytes(a->dtype)).total;
-  return sv::make_workspace_layout(a->B, a->total_drafts, a->V).off_partials;
+  const size_t n = sv::make_workspace_layout(a->B, a->total_drafts, a->V).off_partials;
+  if (!seg_fits(a) || (a->flags & (SPEC_PREFER_RESIDENT | SPEC_PREFER_STREAMING))) return n;
+  const size_t m = sv::make_seg_workspace(a->B, a->total_drafts, a->V, elem_bytes(a->dtype)).total;
+  return m > n ? m : n;
 }
 
 }  // namespace
