@@ -574,9 +574,13 @@ __device__ __forceinline__ const int* cu_of(const SegParams& P, const Ring& R) {
   return P.B + 1 <= kSegCuCap ? R.cu() : P.cu_draft;
 }
 
+// Pass-1 units whose logits copies start before the prologue's end: more
+// of them only slow the prologue's own loads.
+constexpr int kSegPre = 3;
+
 // The producer warp, before the prologue: caches cu_draft, computes the
 // geometry of its first 32 static units (lane l: unit l) and starts the
-// logits copies of the first kSegSlots of them, one lane each.  Returns how
+// logits copies of the first kSegPre of them, one lane each.  Returns how
 // many copies it started.
 template <typename T>
 __device__ int producer_prefetch(const SegParams& P, const Ring& R, Prod& st, RowUnit& mine, int lane) {
@@ -584,7 +588,7 @@ __device__ int producer_prefetch(const SegParams& P, const Ring& R, Prod& st, Ro
     for (int j = lane; j <= P.B; j += 32) R.cu()[j] = __ldg(P.cu_draft + j);
   __syncwarp();
   const int n_static = static_units(P);
-  const int pre = min(n_static, kSegSlots);
+  const int pre = min(n_static, kSegPre);
   mine = row_unit<T>(P, cu_of(P, R), lane, n_static);
   if (lane < pre) issue_row_logits<T>(R, lane, mine, l2_policy_evict_first());
   for (int k = 0; k < pre; ++k) st.fill(k);
@@ -830,10 +834,13 @@ __device__ __forceinline__ unsigned long long run_bits(const unsigned char* bm, 
 
 // The lane's run (VPL vectors at shared address `run`, `ln` valid tokens)
 // into registers, vector m of the result being the run's vector m ^ L;
-// tokens past `ln` read as -inf.
+// tokens past `ln` read as -inf.  A lane with no tokens (ln == 0) reads a
+// whole run's worth of the slot beyond its warp's range (still inside the
+// slot) and the caller drops its sum: the lanes of a full unit then all
+// take the same path.
 template <int N, int VPL>
 __device__ __forceinline__ void load_run(uint4 (&v)[VPL], uint32_t run, int L, int ln) {
-  if (ln == N * VPL) {
+  if (ln == N * VPL || ln == 0) {
     const uint32_t sw = run | ((uint32_t)L << 4);
 #pragma unroll
     for (int m = 0; m < VPL; ++m) v[m] = lds16(sw ^ ((uint32_t)m << 4));
@@ -920,7 +927,7 @@ __device__ __forceinline__ void unit_row(const SegParams& P, unsigned char* slot
     a0 = vec_exp_sum<N>(v[m], c2, a0);
     a1 = vec_exp_sum<N>(v[m + 1], c2, a1);
   }
-  const float s = (a0.x + a0.y) + (a1.x + a1.y) + side;
+  const float s = ln > 0 ? (a0.x + a0.y) + (a1.x + a1.y) + side : 0.f;
   // a lane outside the trusted range flags the warp's partial (S < 0)
   const bool bad = __any_sync(0xffffffffu, !(s <= kSumHi) || (s < kSumLo && ln > 0));
   const float S = warp_sum(s);
@@ -993,7 +1000,7 @@ __device__ __forceinline__ void unit_pair(const SegParams& P, unsigned char* slo
       acc = __fadd2_rn(acc, pair_terms(make_float2(zp[e], zp[e + 1]), make_float2(zq[e], zq[e + 1]), c2, np2, nq2,
                                        mr2));
   }
-  const float S = warp_sum(acc.x + acc.y + side) * fp;
+  const float S = warp_sum(ln > 0 ? acc.x + acc.y + side : 0.f) * fp;
   if (lane == 0) rc->r[w] = make_float2(S, 0.f);
 }
 
