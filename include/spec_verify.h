@@ -26,7 +26,11 @@
  *                       correction on the first mismatch, or as the bonus
  *                       when every draft matches.
  *   spec_tv_budget      the per-position quantities alone: d, theta, p(x),
- *                       q(x).
+ *                       q(x) ("What I Gave Up to Make Speculative Decoding
+ *                       Faster", section "A knob for accepting more draft
+ *                       tokens": the total variation d between the
+ *                       processed target and draft rows, and the mixing
+ *                       weight theta = min(1, D/d) it sets).
  *
  * Conventions shared by every entry point
  * ---------------------------------------
@@ -176,10 +180,14 @@ int spec_verify_sample(const spec_args *args, int32_t *out_tokens, int32_t *out_
 int spec_verify_greedy(const spec_args *args, int32_t *out_tokens, int32_t *out_accepted,
                        int32_t *out_status, void *workspace, size_t ws_bytes, spec_stream_t stream);
 
-/* Per-position mentored-decoding quantities, [total_drafts] each:
-   out_tv = d = TV(p_i, q_i), out_theta = theta_i, out_p_at_draft = p_i(x_i),
-   out_q_at_draft = q_i(x_i) (the last two may be NULL).  Invalid positions
-   get NaN.  Reads no uniforms. */
+/* Per-position mentored-decoding quantities ("What I Gave Up to Make
+   Speculative Decoding Faster", section "A knob for accepting more draft
+   tokens"), [total_drafts] each: out_tv = d = TV(p_i, q_i) = sum_v
+   max(p_i(v) - q_i(v), 0), out_theta = theta_i = min(1, D_b / d) (1 when
+   d <= D_b), out_p_at_draft = p_i(x_i), out_q_at_draft = q_i(x_i) (the last
+   two may be NULL).  p_i and q_i are the target and draft rows after the
+   repetition penalty, the temperature and top-p, as for sampling.  Invalid
+   positions get NaN.  Reads no uniforms.  Same workspace as sampling. */
 int spec_tv_budget(const spec_args *args, float *out_tv, float *out_theta, float *out_p_at_draft,
                    float *out_q_at_draft, void *workspace, size_t ws_bytes, spec_stream_t stream);
 
@@ -242,6 +250,17 @@ int spec_verify_sample_static(const spec_args *args, int32_t *out_tokens, int32_
 
 /* A static description of a return code. */
 const char *spec_status_string(int code);
+
+/* Diagnostic hook: the bound, in SM clock cycles, on every wait of the
+   split-vocabulary sampling kernel (SPEC_PREFER_SPLIT, and the default
+   without top-p).  Each wait that runs out sets a global abort flag; every
+   CTA then stops, and the requests left unfinished get
+   SPEC_STATUS_TIMEOUT (tokens -1, accepted -1) while the call itself still
+   returns SPEC_OK.  cycles <= 0 restores the default of 4e9 cycles (about
+   two seconds).  Process-wide; applies to calls launched afterwards.
+   Returns the previous bound.  The wait for copies in flight before a CTA
+   exits keeps its own fixed bound of about two seconds. */
+int64_t spec_set_wait_cycles(int64_t cycles);
 
 #ifdef __cplusplus
 }

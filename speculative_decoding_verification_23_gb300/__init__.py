@@ -42,7 +42,7 @@ SPEC_STATUS_BAD_K = 8
 SPEC_STATUS_TIMEOUT = 16
 
 EXPORTED = ("spec_workspace_bytes", "spec_verify_sample", "spec_verify_greedy", "spec_tv_budget",
-            "spec_draft_confidence", "spec_verify_sample_static", "spec_status_string")
+            "spec_draft_confidence", "spec_verify_sample_static", "spec_status_string", "spec_set_wait_cycles")
 
 
 class SpecArgs(ctypes.Structure):
@@ -107,6 +107,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
                                               ctypes.c_void_p, ctypes.c_void_p]
     lib.spec_status_string.restype = ctypes.c_char_p
     lib.spec_status_string.argtypes = [ctypes.c_int]
+    lib.spec_set_wait_cycles.restype = ctypes.c_int64
+    lib.spec_set_wait_cycles.argtypes = [ctypes.c_int64]
     _lib = lib
     return lib
 
@@ -116,6 +118,16 @@ def status_string(code: int) -> str:
 
 
 spec_status_string = status_string
+
+
+def set_wait_cycles(cycles: int) -> int:
+    """Bound (SM clock cycles) on every wait of the split-vocabulary kernel;
+    <= 0 restores the default.  Returns the previous bound (a diagnostic
+    hook: see ``spec_set_wait_cycles``)."""
+    return int(load_library().spec_set_wait_cycles(int(cycles)))
+
+
+spec_set_wait_cycles = set_wait_cycles
 
 
 def spec_workspace_bytes(B: int, total_drafts: int, V: int) -> int:

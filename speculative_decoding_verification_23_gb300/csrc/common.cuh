@@ -92,6 +92,22 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity
   }
 }
 
+// The fills a producer put into a ring of at most 32 slots (bit s: slot s
+// filled at least once; parity bit s: the phase of its last fill).  A
+// producer whose wait ran out stops issuing and, before its CTA may exit,
+// waits (bounded) for the copies it already started to land.
+struct RingFills {
+  uint32_t filled = 0, par = 0;
+  __device__ __forceinline__ void note(uint32_t slot, uint32_t phase) {
+    filled |= 1u << slot;
+    par = (par & ~(1u << slot)) | ((phase & 1u) << slot);
+  }
+  __device__ __forceinline__ void drain(uint64_t* full, int nslots) const {
+    for (int s = 0; s < nslots; ++s)
+      if ((filled >> s) & 1u) (void)mbar_wait(&full[s], (par >> s) & 1u);
+  }
+};
+
 // Position in the ring: slot index and the parity of its current use.
 struct RingCursor {
   uint32_t slot = 0, phase = 0;

@@ -557,15 +557,20 @@ __device__ __forceinline__ void conf_producer(const ConfParams& P, const CSmem& 
   const int stage = kCW * L.seg;  // tokens per stage
   const int n_local = conf_n_local(P);
   RingCursor rc;
-  bool to = false;
-  for (int k = 0; k < n_local; ++k) {
+  RingFills fills;
+  bool to = false;   // a wait ran out: nothing more is issued (the compute warps' own waits then run out)
+  for (int k = 0; k < n_local && !to; ++k) {
     const int d = blockIdx.x + k * gridDim.x;
     const unsigned char* row = static_cast<const unsigned char*>(P.draft) + (size_t)d * P.ld_d * es;
     for (int st = 0; st < L.nst; ++st) {
-      const uint32_t slot = rc.slot;
+      const uint32_t slot = rc.slot, phase = rc.phase;
       // first use of a slot: the phase "before" its first completes at once
-      if (!to && !mbar_wait(&S.empty()[slot], rc.phase ^ 1u)) to = true;
+      if (!mbar_wait(&S.empty()[slot], rc.phase ^ 1u)) {
+        to = true;
+        break;
+      }
       rc.advance(L.slots);
+      fills.note(slot, phase);
       // the row's padded stride (a multiple of 16 bytes) covers the rounding
       const int n = min(stage, P.V - st * stage);
       const uint32_t bytes = (uint32_t)((n * es + 15) & ~15);
@@ -573,6 +578,9 @@ __device__ __forceinline__ void conf_producer(const ConfParams& P, const CSmem& 
       bulk_g2s(S.ring() + (size_t)slot * L.slot_bytes, row + (size_t)st * stage * es, bytes, &S.full()[slot], pol);
     }
   }
+  // after a wait ran out: the copies already started land before the CTA
+  // may exit
+  if (to) fills.drain(S.full(), L.slots);
 }
 
 template <typename T>

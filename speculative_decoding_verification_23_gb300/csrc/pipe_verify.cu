@@ -266,17 +266,21 @@ __device__ __forceinline__ void producer(const SampleParams& P, const PipeLayout
   uint64_t* full = IS_A ? S.full_a() : S.full_b();
   uint64_t* empty = IS_A ? S.empty_a() : S.empty_b();
   RingCursor rc;
-  bool to = false;
+  RingFills fills;
+  bool to = false;   // a wait ran out: nothing more is issued (the consumers' own waits then run out)
   int k = 0;
   const int* cu = cu_ptr(P, S);
   const int n_local = n_local_items(P);
-  for (int item = blockIdx.x; item < P.n_items; item += gridDim.x, ++k) {
+  for (int item = blockIdx.x; item < P.n_items && !to; item += gridDim.x, ++k) {
     const Item it = pdecode(P, cu, item);
     if (!IS_A) {
       // pass 2 of item k starts once its statistics are combined (the rows
       // are then in L2)
       const int kb = k % kPipeBufs;
-      if (!to && !mbar_wait(&S.stats_full()[kb], (uint32_t)(k / kPipeBufs) & 1u)) to = true;
+      if (!mbar_wait(&S.stats_full()[kb], (uint32_t)(k / kPipeBufs) & 1u)) {
+        to = true;
+        break;
+      }
       mbar_arrive(&S.buf_free()[kb]);  // this warp has seen item k's statistics
     }
     const unsigned char* rowp = static_cast<const unsigned char*>(P.target) + (size_t)it.tgt_row * P.ld_t * es;
@@ -284,10 +288,14 @@ __device__ __forceinline__ void producer(const SampleParams& P, const PipeLayout
         it.bonus ? rowp : static_cast<const unsigned char*>(P.draft) + (size_t)it.dft_row * P.ld_d * es;
     for (int st = 0; st < nst; ++st) {
       if (!IS_A && b_skips(k, n_local, st)) continue;
-      const uint32_t slot = rc.slot;
+      const uint32_t slot = rc.slot, phase = rc.phase;
       // first use of a slot: the phase "before" its first completes at once
-      if (!to && !mbar_wait(&empty[slot], rc.phase ^ 1u)) to = true;
+      if (!mbar_wait(&empty[slot], rc.phase ^ 1u)) {
+        to = true;
+        break;
+      }
       rc.advance(nslots);
+      fills.note(slot, phase);
       // ring B takes the stages in reverse: the lines ring A read last are
       // re-read first, while they are the least likely to have left L2
       const int sx = IS_A ? st : nst - 1 - st;
@@ -299,20 +307,24 @@ __device__ __forceinline__ void producer(const SampleParams& P, const PipeLayout
       if (!it.bonus) bulk_g2s(dst + (size_t)stage * es, rowq + (size_t)sx * stage * es, bytes, &full[slot], pol);
     }
   }
-  if (IS_A && n_local > 0) {
+  if (IS_A && n_local > 0 && !to) {
     // ring A then carries the last item's odd pass-2 stages (a re-read, in
     // ring B's reversed order), once its statistics are combined
     const int kl = n_local - 1;
-    if (!to && !mbar_wait(&S.stats_full()[kl % kPipeBufs], (uint32_t)(kl / kPipeBufs) & 1u)) to = true;
+    if (!mbar_wait(&S.stats_full()[kl % kPipeBufs], (uint32_t)(kl / kPipeBufs) & 1u)) to = true;
     const Item it = pdecode(P, cu, blockIdx.x + kl * gridDim.x);
     const unsigned char* rowp = static_cast<const unsigned char*>(P.target) + (size_t)it.tgt_row * P.ld_t * es;
     const unsigned char* rowq =
         it.bonus ? rowp : static_cast<const unsigned char*>(P.draft) + (size_t)it.dft_row * P.ld_d * es;
     const uint64_t pol2 = l2_policy_evict_first();
-    for (int st = 1; st < L.nst_b; st += 2) {
-      const uint32_t slot = rc.slot;
-      if (!to && !mbar_wait(&empty[slot], rc.phase ^ 1u)) to = true;
+    for (int st = 1; st < L.nst_b && !to; st += 2) {
+      const uint32_t slot = rc.slot, phase = rc.phase;
+      if (!mbar_wait(&empty[slot], rc.phase ^ 1u)) {
+        to = true;
+        break;
+      }
       rc.advance(nslots);
+      fills.note(slot, phase);
       const int sx = L.nst_b - 1 - st;
       const int n = min(stage, P.V - sx * stage);
       const uint32_t bytes = (uint32_t)((n * es + 15) & ~15);
@@ -322,6 +334,9 @@ __device__ __forceinline__ void producer(const SampleParams& P, const PipeLayout
       if (!it.bonus) bulk_g2s(dst + (size_t)stage * es, rowq + (size_t)sx * stage * es, bytes, &full[slot], pol2);
     }
   }
+  // after a wait ran out: the copies already started land before the CTA
+  // may exit (the consumers' own waits run out and mark their items)
+  if (to) fills.drain(full, nslots);
 }
 
 // Pass 2 of segment s_id of item buffer kb from a staged ring segment (both

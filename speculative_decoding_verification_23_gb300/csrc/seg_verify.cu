@@ -415,6 +415,10 @@ __device__ __forceinline__ int static_units(const SegParams& P) {
 }
 __device__ __forceinline__ int unit_of(int ks) { return (int)blockIdx.x + ks * (int)gridDim.x; }
 
+// The wait for the producer's copies in flight before its CTA exits: a fixed
+// bound (about two seconds), whatever wait limit the call runs with.
+constexpr long long kSegDrainCycles = 4000000000ll;
+
 // Producer state, the same in every lane of warp 0.
 struct Prod {
   uint32_t filled = 0;    // slots filled at least once (bit s)
@@ -735,7 +739,7 @@ __device__ void producer(const SegParams& P, const Ring& R, Prod& st, RowUnit mi
     for (int s2 = 0; s2 < kSegSlots; ++s2)
       if ((st.filled >> s2) & 1u) {
         const long long t0 = clock64();
-        while (!mbar_test(R.full() + s2, (st.par >> s2) & 1u) && clock64() - t0 < P.wait_limit) {
+        while (!mbar_test(R.full() + s2, (st.par >> s2) & 1u) && clock64() - t0 < kSegDrainCycles) {
         }
       }
   __syncwarp();

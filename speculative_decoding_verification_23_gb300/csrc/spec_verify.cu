@@ -2,6 +2,7 @@
 // launches.  No entry point allocates, frees or synchronises; all device
 // work is enqueued on the caller's stream.
 #include <cstdint>
+#include <atomic>
 #include <cstring>
 
 #include <cuda_runtime.h>
@@ -97,8 +98,10 @@ void fill_sample_inputs(sv::SampleParams& P, const spec_args* a) {
 }
 
 // Default bound on every wait of the split-vocabulary kernel, in SM clock
-// cycles (about two seconds at any clock this part runs).
+// cycles (about two seconds at any clock this part runs); the calls use
+// g_seg_wait_limit, which spec_set_wait_cycles changes.
 constexpr long long kSegWaitLimit = 4000000000ll;
+std::atomic<long long> g_seg_wait_limit{kSegWaitLimit};
 
 // The split-vocabulary kernel can serve sampling without top-p when a row
 // has at most kSegMaxSegs segments (V <= 491520 bf16, 245760 fp32).
@@ -154,7 +157,7 @@ int run_seg(const sv::SampleParams& S, const spec_args* a, void* ws, int num_sms
   P.g = sv::make_seg_geom(a->V, es);
   P.NT = a->total_drafts + a->B;
   P.NR = 2 * a->total_drafts + a->B;
-  P.wait_limit = kSegWaitLimit;
+  P.wait_limit = g_seg_wait_limit.load(std::memory_order_relaxed);
   P.ctl = reinterpret_cast<unsigned*>(w + W.off_ctl);
   P.row_cnt = reinterpret_cast<unsigned*>(w + W.off_row_cnt);
   P.req_rows = reinterpret_cast<unsigned*>(w + W.off_req_rows);
@@ -429,6 +432,11 @@ int spec_draft_confidence(const spec_args* a, float threshold, float* out_conf, 
   else
     rc = sv::launch_confidence(P, a->dtype == SPEC_BF16, s);
   return rc == 0 ? SPEC_OK : (rc == -2 ? SPEC_ERR_SHAPE : SPEC_ERR_LAUNCH);
+}
+
+int64_t spec_set_wait_cycles(int64_t cycles) {
+  const long long v = cycles > 0 ? (long long)cycles : kSegWaitLimit;
+  return (int64_t)g_seg_wait_limit.exchange(v, std::memory_order_relaxed);
 }
 
 const char* spec_status_string(int code) {

@@ -23,7 +23,7 @@ def lib():
 
 def _declared_symbols():
     text = open(os.path.join(ROOT, "include", "spec_verify.h")).read()
-    return sorted(set(re.findall(r"^\s*(?:size_t|int|const char \*)\s*\**(spec_\w+)\(", text, re.M)))
+    return sorted(set(re.findall(r"^\s*(?:size_t|int64_t|int|const char \*)\s*\**(spec_\w+)\(", text, re.M)))
 
 
 def test_header_declares_the_python_names():
