@@ -78,8 +78,10 @@
  * the launch.  No entry point ever traps on the device.
  *
  * Workspace: spec_workspace_bytes(B, total_drafts, V) bytes of device
- * memory, at least 256-byte aligned.  Its contents need no initialisation;
- * each call clears what it needs on `stream`.  Calls that share one
+ * memory, at least 256-byte aligned.  Its contents need no initialisation:
+ * the split-vocabulary sampling kernel clears its counters itself at its
+ * start (one launch per call); the other kernels' calls clear theirs with a
+ * cudaMemsetAsync on `stream` before their launch.  Calls that share one
  * workspace must be ordered (same stream, or synchronised).
  */
 #ifndef SPEC_VERIFY_H
@@ -232,8 +234,9 @@ int spec_draft_confidence(const spec_args *args, float threshold, float *out_con
  * (total_drafts + B).  A batch that does not fit returns
  * SPEC_ERR_STATIC_SCRATCH and enqueues nothing.
  *
- * Zeroing: the call's counters at the start of the buffer are cleared on
- * `stream` (cudaMemsetAsync) before its launch; everything else in the
+ * Zeroing: as for the workspace entry point (the split-vocabulary kernel
+ * clears its counters at its start; the cluster kernel's counters are
+ * cleared with a cudaMemsetAsync before its launch); everything else in the
  * buffer is written before it is read.
  *
  * Address: every call looks the buffer up with cudaGetSymbolAddress for the

@@ -139,7 +139,7 @@ __host__ __device__ inline SegGeom make_seg_geom(int V, int es) {
 
 // Workspace regions of the kernel (offsets in bytes, 256-byte aligned).
 struct SegWorkspace {
-  size_t off_zero, zero_bytes;    // counters cleared before every call
+  size_t off_zero, zero_bytes;    // counters the kernel clears at its start (from off_jobs)
   size_t off_ctl, off_row_cnt, off_req_rows, off_req_pend, off_job_cnt, off_jobs, off_req_done;
   size_t off_bitmap, off_rowdesc, off_part1, off_rowstat, off_zx, off_pos, off_part2, off_jobdesc, off_req_status,
       off_req_need, off_posdesc;
@@ -208,8 +208,12 @@ struct SegParams {
   int NT;                   // target rows (total + B); draft row k is physical row NT + k
   int NR;                   // all rows
   long long wait_limit;     // cycles a bounded wait may spin
-  // workspace
+  // control words: a per-device array, zero between calls (the call's last
+  // CTA clears it before it exits)
   unsigned* ctl;
+  // workspace
+  unsigned char* zero;      // the per-call counters [zero, zero + zero_bytes): cleared by the CTAs
+  size_t zero_bytes;        // before the prologue's grid-wide wait (a multiple of 16)
   unsigned* row_cnt;
   unsigned* req_rows;
   unsigned* req_pend;

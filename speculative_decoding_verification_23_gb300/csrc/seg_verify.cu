@@ -627,6 +627,8 @@ __device__ void producer(const SegParams& P, const Ring& R, Prod& st, RowUnit mi
   ok = __shfl_sync(0xffffffffu, ok, 0) != 0;
   fence_proxy_async_global();
   const bool broken = ok && ld_acq_gpu(P.ctl + kCtlBroken) != 0u;
+  // the job list is cleared and may be watched (misc[5], for the recorder)
+  if (lane == 0 && ok && !broken) st_rel_cta(R.misc() + 5, 1u);
   int k = 0;        // units put into the ring (static and second-pass)
   int real = 0;     // of which real units (the rest are stops)
   int stops = 0;    // stop units in the ring (one per group ends the consumers)
@@ -1571,7 +1573,8 @@ __device__ void recorder(const SegParams& P, const Ring& R, int lane) {
     }
     // 2. second-pass candidates: last round's published entries join the
     //    queue (as far as it has room), then the next window is loaded
-    if (!jq_done) {
+    //    (once every CTA has cleared its part of the job list: misc[5])
+    if (!jq_done && ld_acq_cta(R.misc() + 5) != 0u) {
       if (pend) {
         const unsigned jg = (blockIdx.x + (cb + lane) * G) / upj;
         const bool pub = jg < njob && (unsigned)(ent & 0xffffffffull) != 0u;
@@ -1791,6 +1794,14 @@ __global__ void __launch_bounds__(kSegThreads, 1) seg_verify_kernel(const __grid
   if (blockIdx.x == 0 && threadIdx.x == 0) {
     if (__ldg(P.cu_draft) != 0 || __ldg(P.cu_draft + P.B) != P.total) atomicOr(P.ctl + kCtlBroken, 1u);
   }
+  // this CTA's stripe of the per-call counters, before the grid-wide wait
+  // that ends the prologue (nothing reads or writes them before it)
+  {
+    const size_t n16 = P.zero_bytes / 16;
+    uint4* z = reinterpret_cast<uint4*>(P.zero);
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n16; i += (size_t)gridDim.x * blockDim.x)
+      z[i] = make_uint4(0u, 0u, 0u, 0u);
+  }
   if (warp >= 1)
     for (int b = blockIdx.x; b < P.B; b += gridDim.x) {
       prep_request(P, b, threadIdx.x - 32, R.misc() + 7);
@@ -1844,12 +1855,30 @@ __global__ void __launch_bounds__(kSegThreads, 1) seg_verify_kernel(const __grid
       P.out_accepted[b] = -1;
       if (P.out_status) P.out_status[b] = ab ? kStatusTimeout : kStatusBadK;
     }
+    // every other CTA has left: the control words go back to zero for the
+    // next call
+    __syncthreads();
+    if (threadIdx.x < kCtlWords) P.ctl[threadIdx.x] = 0u;
   }
 }
 
 }  // namespace
 
+// Control words of the kernel (kCtlWords per device), zero between calls.
+// One call at a time uses them: a launch takes every SM for its cooperative
+// grid, so a second one starts only after the first has left.
+__device__ unsigned g_seg_ctl[kCtlWords];
+
 int seg_smem_bytes() { return kSegSmem; }
+
+unsigned* seg_ctl_address() {
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_seg_ctl) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  return static_cast<unsigned*>(p);
+}
 
 int launch_seg_verify(const SegParams& P, bool bf16, int num_sms, cudaStream_t stream) {
   auto kern = bf16 ? seg_verify_kernel<__nv_bfloat16> : seg_verify_kernel<float>;

@@ -25,6 +25,7 @@ int choose_conf_layout(int V, int elem_bytes, int B, int max_smem, ConfLayout* o
 int launch_conf_pipe(const ConfParams& P, bool bf16, int num_sms, cudaStream_t stream);
 int launch_seg_verify(const SegParams& P, bool bf16, int num_sms, cudaStream_t stream);
 int seg_smem_bytes();
+unsigned* seg_ctl_address();
 }  // namespace sv
 
 namespace {
@@ -158,7 +159,10 @@ int run_seg(const sv::SampleParams& S, const spec_args* a, void* ws, int num_sms
   P.NT = a->total_drafts + a->B;
   P.NR = 2 * a->total_drafts + a->B;
   P.wait_limit = g_seg_wait_limit.load(std::memory_order_relaxed);
-  P.ctl = reinterpret_cast<unsigned*>(w + W.off_ctl);
+  P.ctl = sv::seg_ctl_address();
+  if (!P.ctl) return SPEC_ERR_DEVICE;
+  P.zero = w + W.off_jobs;
+  P.zero_bytes = W.zero_bytes - (W.off_jobs - W.off_zero);
   P.row_cnt = reinterpret_cast<unsigned*>(w + W.off_row_cnt);
   P.req_rows = reinterpret_cast<unsigned*>(w + W.off_req_rows);
   P.req_pend = reinterpret_cast<unsigned*>(w + W.off_req_pend);
@@ -176,10 +180,6 @@ int run_seg(const sv::SampleParams& S, const spec_args* a, void* ws, int num_sms
   P.req_status = reinterpret_cast<int*>(w + W.off_req_status);
   P.req_need = reinterpret_cast<unsigned*>(w + W.off_req_need);
   P.posdesc = reinterpret_cast<sv::SegRowDesc*>(w + W.off_posdesc);
-  if (cudaMemsetAsync(w + W.off_zero, 0, W.zero_bytes, stream) != cudaSuccess) {
-    cudaGetLastError();
-    return SPEC_ERR_LAUNCH;
-  }
   return sv::launch_seg_verify(P, a->dtype == SPEC_BF16, num_sms, stream) == 0 ? SPEC_OK : SPEC_ERR_LAUNCH;
 }
 
