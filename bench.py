@@ -324,6 +324,7 @@ def bench_gpu(args, rank, world, dist):
     per_launch, win_s = [], []
     n_win = 0
     t_wall = time.perf_counter()
+    torch.cuda.nvtx.range_push("bench: timed windows")
     with ClockSampler(dev) as clk:
         while n_win == 0 or reduce_max(float(time.perf_counter() - t_wall < CLOCK_WINDOW_S), dist, dev) > 0:
             n_win += 1
@@ -343,6 +344,7 @@ def bench_gpu(args, rank, world, dist):
             torch.cuda.synchronize()
             win_s.append(reduce_max(t_start.elapsed_time(t_end) / 1000.0, dist, dev))
             per_launch += [x.elapsed_time(y) / 1000.0 for x, y in ev]
+    torch.cuda.nvtx.range_pop()
     elapsed = float(np.median(win_s))
     if dist:
         dist.barrier()
@@ -383,11 +385,13 @@ def bench_gpu(args, rank, world, dist):
     if dist:
         dist.barrier()
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.nvtx.range_push("bench: end to end")
     a.record(stream)
     for _ in range(args.steps):
         e2e_step()
     b.record(stream)
     torch.cuda.synchronize()
+    torch.cuda.nvtx.range_pop()
     e2e_value = job_throughput(batch.B, world, args.steps, reduce_max(a.elapsed_time(b) / 1000.0, dist, dev))
 
     # ---- roofline of the sampling kernel (one launch per step, after the
@@ -494,6 +498,7 @@ def bench_extras(dev, peak: float, cpu_seconds: float) -> dict:
     sec = timed(lambda: sv.spec_verify_sample(a1, device=dev, workspace=ws1, stream=stream))
     out["qwen25_single_B1_K8"] = line("qwen", b1.logit_bytes() + small, sec,
                                       oracle_rate(oracle.verify_batch, b1, budget), "sample_verify_kernel (resident)")
+    out["qwen25_single_B1_K8_breakdown"] = small_batch_breakdown(dev, d1, ws1, stream)
     for K in (1, 2, 4, 8):
         bg = W.greedy_single(K)
         dg = to_device(bg, dev)
@@ -527,6 +532,59 @@ def bench_extras(dev, peak: float, cpu_seconds: float) -> dict:
     del db, wsb
     out["acceptance_qwen25_K8"] = acceptance_sweep(dev)
     return out
+
+
+def small_batch_breakdown(dev, db, ws, stream, iters: int = 200) -> dict:
+    """Where a B=1 call's time goes, per kernel choice: the host's time to
+    check the arguments and enqueue the work (no synchronisation), the GPU
+    span of one call (CUDA events around it, L2 warm), the GPU span of the
+    same calls issued back to back (launches overlap the host), and the
+    span of an empty device operation on the stream (the floor any launch
+    pays)."""
+    import torch
+
+    import speculative_decoding_verification_23_gb300 as sv
+
+    res = {}
+    for name, flags in (("resident (default)", 0), ("split", 8)):
+        args = db.args(flags=flags)
+        call = lambda: sv.spec_verify_sample(args, device=dev, workspace=ws, stream=stream)
+        for _ in range(10):
+            call()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(iters):
+            call()
+        host_us = 1e6 * (time.perf_counter() - t0) / iters
+        torch.cuda.synchronize()
+        spans = []
+        for _ in range(50):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            call()
+            b.record(stream)
+            b.synchronize()
+            spans.append(a.elapsed_time(b) * 1000.0)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(iters):
+            call()
+        b.record(stream)
+        b.synchronize()
+        res[name] = {"host_enqueue_us": round(host_us, 2), "gpu_span_us": round(float(np.median(spans)), 2),
+                     "back_to_back_us": round(a.elapsed_time(b) * 1000.0 / iters, 2),
+                     "launches_per_call": 2 if flags == 0 else 1}
+    x = torch.empty(1, device=dev)
+    spans = []
+    for _ in range(50):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        x.zero_()
+        b.record(stream)
+        b.synchronize()
+        spans.append(a.elapsed_time(b) * 1000.0)
+    res["empty_operation_us"] = round(float(np.median(spans)), 2)
+    return res
 
 
 def acceptance_sweep(dev, batches: int = 8, per: int = 32) -> dict:

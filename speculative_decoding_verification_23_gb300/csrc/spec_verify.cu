@@ -6,6 +6,7 @@
 #include <cstring>
 
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include "spec_verify.h"
 #include "spec_internal.h"
@@ -97,6 +98,16 @@ void fill_sample_inputs(sv::SampleParams& P, const spec_args* a) {
   P.max_k = a->max_k;
   P.flags = a->flags;
 }
+
+// An NVTX range around each entry point's host work and launches (named
+// after the entry point), for timelines taken with a profiler; without one
+// attached the push and pop do nothing.
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
 
 // Default bound on every wait of the split-vocabulary kernel, in SM clock
 // cycles (about two seconds at any clock this part runs); the calls use
@@ -284,6 +295,7 @@ size_t spec_workspace_bytes(int32_t B, int32_t total_drafts, int32_t V) {
 
 int spec_verify_sample(const spec_args* a, int32_t* out_tokens, int32_t* out_accepted, int32_t* out_status,
                        void* workspace, size_t ws_bytes, spec_stream_t stream) {
+  NvtxRange nvtx("spec_verify_sample");
   int rc = check_common(a, true);
   if (rc) return rc;
   if (!out_tokens || !out_accepted || !a->temperature || !a->tv_budget || !a->uniforms) return SPEC_ERR_NULL;
@@ -301,6 +313,7 @@ int spec_verify_sample(const spec_args* a, int32_t* out_tokens, int32_t* out_acc
 
 int spec_verify_sample_static(const spec_args* a, int32_t* out_tokens, int32_t* out_accepted, int32_t* out_status,
                               spec_stream_t stream) {
+  NvtxRange nvtx("spec_verify_sample_static");
   int rc = check_common(a, true);
   if (rc) return rc;
   if (!out_tokens || !out_accepted || !a->temperature || !a->tv_budget || !a->uniforms) return SPEC_ERR_NULL;
@@ -320,6 +333,7 @@ int spec_verify_sample_static(const spec_args* a, int32_t* out_tokens, int32_t* 
 
 int spec_tv_budget(const spec_args* a, float* out_tv, float* out_theta, float* out_p_at_draft,
                    float* out_q_at_draft, void* workspace, size_t ws_bytes, spec_stream_t stream) {
+  NvtxRange nvtx("spec_tv_budget");
   int rc = check_common(a, true);
   if (rc) return rc;
   if (!out_tv || !out_theta || !a->temperature || !a->tv_budget) return SPEC_ERR_NULL;
@@ -340,6 +354,7 @@ int spec_tv_budget(const spec_args* a, float* out_tv, float* out_theta, float* o
 
 int spec_verify_greedy(const spec_args* a, int32_t* out_tokens, int32_t* out_accepted, int32_t* out_status,
                        void* workspace, size_t ws_bytes, spec_stream_t stream) {
+  NvtxRange nvtx("spec_verify_greedy");
   int rc = check_common(a, false);
   if (rc) return rc;
   if (!out_tokens || !out_accepted) return SPEC_ERR_NULL;
@@ -379,6 +394,7 @@ int spec_verify_greedy(const spec_args* a, int32_t* out_tokens, int32_t* out_acc
 
 int spec_draft_confidence(const spec_args* a, float threshold, float* out_conf, int32_t* out_k_eff,
                           int32_t* out_status, void* workspace, size_t ws_bytes, spec_stream_t stream) {
+  NvtxRange nvtx("spec_draft_confidence");
   if (!a) return SPEC_ERR_NULL;
   if (a->dtype != SPEC_F32 && a->dtype != SPEC_BF16) return SPEC_ERR_DTYPE;
   if (a->B < 1 || a->V < 1 || a->total_drafts < 0 || a->max_k < 0) return SPEC_ERR_SHAPE;
