@@ -110,6 +110,7 @@ enum : int {
   kCtlDecided,       // requests decided after pass 1
   kCtlExited,        // CTAs finished
   kCtlAbort,         // a bounded wait ran out somewhere
+  kCtlSteal,         // pass-1 units past the dealt ones claimed
   kCtlWords = 16
 };
 

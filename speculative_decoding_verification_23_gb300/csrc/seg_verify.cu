@@ -55,12 +55,27 @@ constexpr int kOffRec = seg_al16(kOffBars + 2 * kSegSlots * 8);        // unit r
 constexpr int kOffMisc = seg_al16(kOffRec + kSegRecN * (int)sizeof(SegUnitRec));  // control words
 constexpr int kSegJq = 64;                                              // second-pass candidates found, not yet issued
 constexpr int kOffJq = seg_al16(kOffMisc + 64);                         // their job entries (kSegJq, 8 bytes each)
+// Claimed pass-1 units queued for the producer, with their geometry.
+struct SegSteal {
+  unsigned long long logits, bits, desc;   // global addresses
+  int u, tok0, n, pad;
+};
+constexpr int kSegSq = 32;
+constexpr int kStealChunk = 8;                                          // pass-1 units per claim
+constexpr int kStealAhead = 16;                                         // queued claimed units kept ahead
+constexpr int kStealLead = 8;                                           // dealt units left when claiming starts
+static_assert(kStealAhead <= kSegSq && kStealChunk <= 32, "claims fit the queue and a warp");
+constexpr int kOffSq = kOffJq + kSegJq * 8;                             // the claimed units (kSegSq)
 constexpr int kSegFq = 64;                                              // requests ready for their tokens
-constexpr int kOffFq = kOffJq + kSegJq * 8;                             // their indices (kSegFq)
-constexpr int kOffCu = kOffFq + kSegFq * 4;                             // cu_draft copy (B + 1 <= kSegCuCap)
+constexpr int kOffFq = kOffSq + kSegSq * (int)sizeof(SegSteal);         // their indices (kSegFq)
+constexpr int kDrawBytes = 4096;                                         // a draw's staged logits (both rows of a pair)
+constexpr int kOffDraw = kOffFq + kSegFq * 4;                           // [2]: the finisher's and the decider's draw areas
+constexpr int kDrawArea = kDrawBytes + 256 + 16;                        // logits, penalty words, mbarrier + phase
+constexpr int kOffCu = kOffDraw + 2 * kDrawArea;                        // cu_draft copy (B + 1 <= kSegCuCap)
 constexpr int kSegSmem = kOffCu + kSegCuCap * 4;
 static_assert(kSegSlotBytes % 128 == 0 && kOffBars % 8 == 0 && kOffRec % 16 == 0 && kOffJq % 16 == 0 &&
-                  kOffFq % 16 == 0 && kOffCu % 16 == 0,
+                  kOffSq % 16 == 0 && kOffFq % 16 == 0 && kOffDraw % 16 == 0 && kDrawArea % 16 == 0 &&
+                  kOffCu % 16 == 0,
               "shared-memory regions keep the alignment of their widest access");
 
 
@@ -144,7 +159,9 @@ struct Ring {
   __device__ unsigned* misc() const { return reinterpret_cast<unsigned*>(seg_smem + kOffMisc); }
   __device__ unsigned long long* jq() const { return reinterpret_cast<unsigned long long*>(seg_smem + kOffJq); }
   __device__ int* fq() const { return reinterpret_cast<int*>(seg_smem + kOffFq); }
+  __device__ SegSteal* sq() const { return reinterpret_cast<SegSteal*>(seg_smem + kOffSq); }
   __device__ int* cu() const { return reinterpret_cast<int*>(seg_smem + kOffCu); }
+  __device__ unsigned char* draw_area(int i) const { return seg_smem + kOffDraw + i * kDrawArea; }
 };
 
 __device__ __forceinline__ SegUnitHdr* hdr_of(unsigned char* slot) {
@@ -407,11 +424,23 @@ __device__ __forceinline__ int2 row_src(const SegParams& P, const int* cu, int r
   return make_int2(b, src);
 }
 
-// Static (pass-1) units of this CTA: u = blockIdx.x + ks * gridDim.x, so
-// that all CTAs sweep the rows together (requests complete in order).
-__device__ __forceinline__ int static_units(const SegParams& P) {
+// Pass-1 units: u = 0 .. NR * nseg - 1 in row order.  The first ones, in
+// whole waves of gridDim (kDealtNum / kDealtDen of the waves when there are
+// at least kDealtDen), are dealt out: CTA c takes u = c + ks * gridDim.x, so
+// that all CTAs sweep the rows together (requests complete in order).  The
+// rest go to whichever CTA claims them first (a global counter), in chunks
+// of kStealChunk: CTAs that ran slower take fewer of them, which evens out
+// the end of the pass.
+constexpr int kDealtNum = 3, kDealtDen = 4;
+__device__ __forceinline__ int dealt_units(const SegParams& P) {
   const long long U = (long long)P.NR * P.g.nseg;
-  return (long long)blockIdx.x < U ? (int)((U - 1 - blockIdx.x) / gridDim.x + 1) : 0;
+  const long long waves = (U + gridDim.x - 1) / gridDim.x;
+  const long long own = waves >= kDealtDen ? waves * kDealtNum / kDealtDen : waves;
+  return (int)(own * gridDim.x < U ? own * gridDim.x : U);
+}
+__device__ __forceinline__ int static_units(const SegParams& P) {
+  const long long D = dealt_units(P);
+  return (long long)blockIdx.x < D ? (int)((D - 1 - blockIdx.x) / gridDim.x + 1) : 0;
 }
 __device__ __forceinline__ int unit_of(int ks) { return (int)blockIdx.x + ks * (int)gridDim.x; }
 
@@ -643,6 +672,13 @@ __device__ void producer(const SegParams& P, const Ring& R, Prod& st, RowUnit mi
     // issues no global load while static units remain, so that none of its
     // releases waits on one.
     unsigned head = 0;        // candidates issued
+    unsigned shead = 0;       // claimed pass-1 units issued
+    if (pre > 0) {
+      // first the prefetched units (ring units 0 .. pre-1, their slots
+      // fresh): penalty bits, descriptors and arrivals, one lane each
+      if (lane < pre) issue_row<T>(P, R, lane, mine, true, pol_s, pol_k);
+      k = ks = pre;
+    }
     for (;;) {
       const unsigned tail = *reinterpret_cast<volatile unsigned*>(R.misc() + 8);
       if (head < tail) {
@@ -657,14 +693,6 @@ __device__ void producer(const SegParams& P, const Ring& R, Prod& st, RowUnit mi
         ++k;
         ++head;
         if (lane == 0) st_rel_cta(R.misc() + 9, head);   // the queue entry is free again
-        t_idle = clock64();
-        continue;
-      }
-      if (ks < pre) {
-        // the prefetched units: penalty bits, descriptors and arrivals, one
-        // lane each (their slots are fresh)
-        if (lane < pre) issue_row<T>(P, R, lane, mine, true, pol_s, pol_k);
-        k = ks = pre;
         t_idle = clock64();
         continue;
       }
@@ -691,16 +719,57 @@ __device__ void producer(const SegParams& P, const Ring& R, Prod& st, RowUnit mi
         for (int j = 0; j < n; ++j) st.fill(k + j);
         k += n;
         ks += n;
+        if (lane == 0) *reinterpret_cast<volatile unsigned*>(R.misc() + 13) = (unsigned)ks;   // for the claims
         t_idle = clock64();
         continue;
       }
-      // static units done and no candidate queued: finished once every
-      // request is decided and the next candidate lies past the jobs reserved
+      // then the claimed pass-1 units the recorder queued (misc[6]), those
+      // whose slots are free together, one lane each
+      const unsigned stail = *reinterpret_cast<volatile unsigned*>(R.misc() + 6);
+      if (shead < stail) {
+        (void)ld_acq_cta(R.misc() + 6);
+        const int lim = min((int)(stail - shead), kSegSlots);
+        const int kk = k + lane;
+        bool fr = false;
+        if (lane < lim)
+          fr = (kk < kSegRecN || st.rec_seen > kk - kSegRecN) &&
+               (kk < kSegSlots || mbar_done(R.empty() + kk % kSegSlots, (uint32_t)((kk / kSegSlots - 1) & 1)));
+        const unsigned fm = __ballot_sync(0xffffffffu, fr);
+        int n = fm == 0xffffffffu ? 32 : __ffs(~fm) - 1;
+        if (n == 0) {
+          ok = wait_slot(P, R, st, k, lane);
+          if (!ok) break;
+          n = 1;
+        }
+        __syncwarp();
+        if (lane < n) {
+          const SegSteal e = R.sq()[(shead + lane) % kSegSq];
+          RowUnit x;
+          x.logits = reinterpret_cast<const unsigned char*>(e.logits);
+          x.bits = reinterpret_cast<const unsigned char*>(e.bits);
+          x.desc = reinterpret_cast<const SegRowDesc*>(e.desc);
+          x.u = e.u;
+          x.tok0 = e.tok0;
+          x.n = e.n;
+          issue_row<T>(P, R, k + lane, x, false, pol_s, pol_k);
+        }
+        for (int j = 0; j < n; ++j) st.fill(k + j);
+        k += n;
+        shead += n;
+        __syncwarp();
+        if (lane == 0) st_rel_cta(R.misc() + 14, shead);   // the queue entries are free again
+        t_idle = clock64();
+        continue;
+      }
+      // dealt units done and nothing queued: finished once no claimed
+      // pass-1 unit will come (misc[15]), every request is decided and the
+      // next candidate lies past the jobs reserved
       bool done = false;
       if (lane == 0) {
         const unsigned jg = (blockIdx.x + head * (unsigned)G) / upj;
-        if (jg >= (unsigned)P.total ||
-            (ld_acq_gpu(P.ctl + kCtlDecided) >= (unsigned)P.B && jg >= ld_acq_gpu(P.ctl + kCtlJobTail)))
+        if (ld_acq_cta(R.misc() + 15) != 0u && shead == ld_acq_cta(R.misc() + 6) &&
+            (jg >= (unsigned)P.total ||
+             (ld_acq_gpu(P.ctl + kCtlDecided) >= (unsigned)P.B && jg >= ld_acq_gpu(P.ctl + kCtlJobTail))))
           done = true;
         else if (aborted(P)) ok = false;
         else if (clock64() - t_idle > P.wait_limit) {
@@ -1077,42 +1146,85 @@ __device__ __forceinline__ float draw_term(float zp, float zq, bool pen, const S
   return __fmul_rn(pair_term(zp, zq, d.c, Lp, Lq, __fdiv_rn(fq, fp)), fp);
 }
 
+// A warp's staging area for one draw: the range's logits (a row's range at
+// `p`, or both rows' at `p` and `q`), its penalty words, and the mbarrier the
+// bulk copies complete on, with the parity of its next phase.
+struct DrawBuf {
+  unsigned char* p;
+  unsigned char* q;
+  uint32_t* bits;
+  uint64_t* bar;
+  unsigned* phase;
+};
+
+__device__ __forceinline__ DrawBuf draw_buf(const Ring& R, int i) {
+  unsigned char* area = R.draw_area(i);
+  DrawBuf db;
+  db.p = area;
+  db.q = area + kDrawBytes / 2;
+  db.bits = reinterpret_cast<uint32_t*>(area + kDrawBytes);
+  db.bar = reinterpret_cast<uint64_t*>(area + kDrawBytes + 256);
+  db.phase = reinterpret_cast<unsigned*>(area + kDrawBytes + 256 + 8);
+  return db;
+}
+
 // Inverse CDF inside the token range [a, a + n) (a a multiple of 32) of a
 // row, or of the residual max(p - q, 0) of a row pair: the smallest v whose
 // prefix mass (from a) exceeds t; the last token with mass if t is out of
 // reach.  p = 2^(z'c - Lp) * fp and q = 2^(z'c - Lq) * fq, as in the
-// streaming passes.  Each lane loads its 32 tokens at once (one round trip
-// per 1024 tokens, and one more for the lane that holds the draw).
+// streaming passes.  The range (at most kDrawBytes per row) comes into the
+// warp's DrawBuf with one bulk copy per row, its penalty words with plain
+// loads alongside; the walk then reads shared memory only.
 template <typename T, bool PAIR>
-__device__ int range_draw(const SegParams& P, int rp_row, int rq_row, int a, int n, const SegRowDesc& d, float Lp,
-                          float fp, float Lq, float fq, int b, double t, int lane) {
-  const T* rowp = reinterpret_cast<const T*>(row_ptr<T>(P, rp_row));
-  const T* rowq = PAIR ? reinterpret_cast<const T*>(row_ptr<T>(P, rq_row)) : nullptr;
-  const uint32_t* bm = P.bitmap + (size_t)b * (P.g.bm_bytes / 4);
+__device__ int range_draw(const SegParams& P, const DrawBuf& db, int rp_row, int rq_row, int a, int n,
+                          const SegRowDesc& d, float Lp, float fp, float Lq, float fq, int b, double t, int lane) {
+  const uint32_t bytes = tma_bytes(n, sizeof(T));
+  unsigned par = 0;
+  if (lane == 0) {
+    par = *db.phase;
+    mbar_arrive_expect(db.bar, PAIR ? 2 * bytes : bytes);
+    const uint64_t pol = l2_policy_evict_first();
+    bulk_g2s(db.p, row_ptr<T>(P, rp_row) + (size_t)a * sizeof(T), bytes, db.bar, pol);
+    if (PAIR) bulk_g2s(db.q, row_ptr<T>(P, rq_row) + (size_t)a * sizeof(T), bytes, db.bar, pol);
+  }
+  // penalty words of the range, with the row's extras
+  const uint32_t* bm = P.bitmap + (size_t)b * (P.g.bm_bytes / 4) + (a >> 5);
+  const int nw = (n + 31) >> 5;
+  for (int w = lane; w < nw; w += 32) db.bits[w] = __ldcg(bm + w);
+  __syncwarp();
+  if (lane < d.n_extra) {
+    const int e = d.extras[lane] - a;
+    if (e >= 0 && e < n) atomicOr(db.bits + (e >> 5), 1u << (e & 31));
+  }
+  par = __shfl_sync(0xffffffffu, par, 0);
+  bool ok = true;
+  if (lane == 0) {
+    ok = ring_wait(P, db.bar, par);
+    *db.phase = par ^ 1u;
+  }
+  ok = __shfl_sync(0xffffffffu, (int)ok, 0) != 0;
+  __syncwarp();
+  if (!ok) return -1;
+  auto zp_at = [&](int i) { return ldz<T>(db.p + (size_t)i * sizeof(T)); };
+  auto zq_at = [&](int i) { return PAIR ? ldz<T>(db.q + (size_t)i * sizeof(T)) : 0.f; };
   int found = -1, lastpos = -1;
   double carry = 0.0;
-  for (int base = a; base < a + n && found < 0; base += 1024) {
+  for (int base = 0; base < n && found < 0; base += 1024) {
     const int t0 = base + 32 * lane;
-    const int end = a + n;
-    const int cnt = max(0, min(32, end - t0));
-    Run32<T> rp, rq;
-    rp.load(rowp, t0, end);
-    if (PAIR) rq.load(rowq, t0, end);
-    uint32_t pw = cnt > 0 ? __ldcg(bm + (t0 >> 5)) : 0u;
-    for (int k = 0; k < d.n_extra; ++k) {
-      const int e = d.extras[k];
-      if (e >= t0 && e < t0 + 32) pw |= 1u << (e - t0);
-    }
-    double lsum = 0.0;
+    const int cnt = max(0, min(32, n - t0));
+    const uint32_t pw = cnt > 0 ? db.bits[t0 >> 5] : 0u;
+    // the lane's 32 terms summed in fp32 with compensation (the part has
+    // little fp64 throughput); the warp's prefix in fp64
+    float ls = 0.f, lc = 0.f;
     int mylast = -1;
-#pragma unroll
-    for (int j = 0; j < 32; ++j) {
-      if (j < cnt) {
-        const float r = draw_term<T, PAIR>(rp.at(j), PAIR ? rq.at(j) : 0.f, (pw >> j) & 1u, d, Lp, fp, Lq, fq);
-        lsum += (double)r;
-        if (r > 0.f) mylast = t0 + j;
-      }
+    for (int j = 0; j < cnt; ++j) {
+      const float r = draw_term<T, PAIR>(zp_at(t0 + j), zq_at(t0 + j), (pw >> j) & 1u, d, Lp, fp, Lq, fq);
+      const float y = __fsub_rn(r, lc), tt = __fadd_rn(ls, y);
+      lc = __fsub_rn(__fsub_rn(tt, ls), y);
+      ls = tt;
+      if (r > 0.f) mylast = a + t0 + j;
     }
+    const double lsum = (double)ls;
     const double incl = warp_incl_scan_d(lsum, lane);
     const double tot = __shfl_sync(0xffffffffu, incl, 31);
     const unsigned hit = __ballot_sync(0xffffffffu, carry + incl > t);
@@ -1120,14 +1232,15 @@ __device__ int range_draw(const SegParams& P, int rp_row, int rq_row, int a, int
       const int L = __ffs(hit) - 1;
       int f = -1;
       if (lane == L) {
-        // the same terms again, in the same order
-        double acc = carry + (incl - lsum);
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          if (j < cnt && f < 0) {
-            acc += (double)draw_term<T, PAIR>(rp.at(j), PAIR ? rq.at(j) : 0.f, (pw >> j) & 1u, d, Lp, fp, Lq, fq);
-            if (acc > t) f = t0 + j;
-          }
+        // the same terms again, summed the same way, in the same order
+        const double before_lane = carry + (incl - lsum);
+        float as = 0.f, ac = 0.f;
+        for (int j = 0; j < cnt && f < 0; ++j) {
+          const float r = draw_term<T, PAIR>(zp_at(t0 + j), zq_at(t0 + j), (pw >> j) & 1u, d, Lp, fp, Lq, fq);
+          const float y = __fsub_rn(r, ac), tt = __fadd_rn(as, y);
+          ac = __fsub_rn(__fsub_rn(tt, as), y);
+          as = tt;
+          if (before_lane + (double)as > t) f = a + t0 + j;
         }
         if (f < 0) f = mylast;
       }
@@ -1139,23 +1252,29 @@ __device__ int range_draw(const SegParams& P, int rp_row, int rq_row, int a, int
     if (ml >= 0) lastpos = ml;
     carry += tot;
   }
+  __syncwarp();     // the buffer is free again once every lane is done with it
   return found >= 0 ? found : lastpos;
 }
 
 // The owning part of a draw over `nparts` (<= 512) part masses (mass(j) for
-// part j; lane l holds parts l*per .. l*per + per - 1, all loaded at once)
-// at t = u * total: returns the part, sets *before to the mass before it
-// and *total to the total mass.
+// part j) at t = u * total: returns the part, sets *before to the mass
+// before it and *total to the total mass.  The masses go to the warp's draw
+// area (as doubles, at most kDrawBytes), lane l summing parts
+// l*per .. l*per + per - 1; the lane that holds t walks its parts again.
 template <typename F>
-__device__ int owning_part(int nparts, F&& mass, double u, double* before, double* total, int lane) {
+__device__ int owning_part(int nparts, F&& mass, double u, double* before, double* total, const DrawBuf& db,
+                           int lane) {
+  double* m = reinterpret_cast<double*>(db.p);
+  for (int j = lane; j < nparts; j += 32) m[j] = mass(j);
+  __syncwarp();
   const int per = (nparts + 31) / 32;
-  const int j0 = lane * per;
-  double m[16];
-#pragma unroll
-  for (int q = 0; q < 16; ++q) m[q] = (q < per && j0 + q < nparts) ? mass(j0 + q) : 0.0;
+  const int j0 = min(lane * per, nparts), j1 = min(j0 + per, nparts);
   double ls = 0.0;
-#pragma unroll
-  for (int q = 0; q < 16; ++q) ls += m[q];
+  int lp = -1;
+  for (int j = j0; j < j1; ++j) {
+    ls += m[j];
+    if (m[j] > 0.0) lp = j;
+  }
   const double incl = warp_incl_scan_d(ls, lane);
   const double tot = __shfl_sync(0xffffffffu, incl, 31);
   *total = tot;
@@ -1163,53 +1282,57 @@ __device__ int owning_part(int nparts, F&& mass, double u, double* before, doubl
   const unsigned hit = __ballot_sync(0xffffffffu, incl > t && ls > 0.0);
   int part = -1;
   double bef = 0.0;
-  int lp = -1;
-  double lb = 0.0;
-  {
-    // this lane's first part that takes t, and its last part with mass
-    double acc = incl - ls;
-#pragma unroll
-    for (int q = 0; q < 16; ++q) {
-      if (m[q] > 0.0) {
-        if (part < 0 && acc + m[q] > t) {
-          part = j0 + q;
-          bef = acc;
-        }
-        lp = j0 + q;
-        lb = acc;
-      }
-      acc += m[q];
-    }
-  }
   if (hit) {
     const int L = __ffs(hit) - 1;
-    const int pl = __shfl_sync(0xffffffffu, part, L);
-    const double bl = __shfl_sync(0xffffffffu, bef, L);
-    const int ll = __shfl_sync(0xffffffffu, lp, L);
-    const double lbl = __shfl_sync(0xffffffffu, lb, L);
-    part = pl >= 0 ? pl : ll;       // rounding: the lane's last part with mass
-    bef = pl >= 0 ? bl : lbl;
+    if (lane == L) {
+      // this lane's first part that takes t, and its last part with mass
+      double acc = incl - ls, lb = 0.0;
+      for (int j = j0; j < j1; ++j) {
+        if (m[j] > 0.0) {
+          if (part < 0 && acc + m[j] > t) {
+            part = j;
+            bef = acc;
+          }
+          lb = acc;
+        }
+        acc += m[j];
+      }
+      if (part < 0) {       // rounding: the lane's last part with mass
+        part = lp;
+        bef = lb;
+      }
+    }
+    part = __shfl_sync(0xffffffffu, part, L);
+    bef = __shfl_sync(0xffffffffu, bef, L);
   } else {
     // t out of reach (rounding): the last part with mass
     const unsigned has = __ballot_sync(0xffffffffu, lp >= 0);
-    part = -1;
     if (has) {
       const int L = 31 - __clz(has);
+      double lb = 0.0;
+      if (lane == L) {
+        double acc = incl - ls;
+        for (int j = j0; j < lp; ++j) acc += m[j];
+        lb = acc;
+      }
       part = __shfl_sync(0xffffffffu, lp, L);
       bef = __shfl_sync(0xffffffffu, lb, L);
     }
   }
+  __syncwarp();     // the draw area is free again
   *before = bef;
   return part;
 }
 
-// The exact log2 normaliser L = M + log2 S of a row as an fp32 value and a
-// factor: 2^(y - L) = 2^(y - Lf) * f, f = 2^(Lf - L), so that rounding L to
-// fp32 scales no probability.
-__device__ __forceinline__ void split_norm(double M, double S, float* Lf, float* f) {
-  const double L = M + log2(S);
-  *Lf = (float)L;
-  *f = (float)exp2((double)*Lf - L);
+// A row's log2 normaliser M + log2 S as an fp32 value Lf and a factor f with
+// 2^(y - M) / S = 2^(y - Lf) * f: f = 2^(Lf - M) / S makes up for the
+// rounding of Lf, so that y - Lf stays small for the tokens that carry the
+// mass (their exponent keeps its precision) and no probability is scaled.
+// fp32 throughout: the part has little fp64 throughput.
+__device__ __forceinline__ void split_norm(float M, float S, float* Lf, float* f) {
+  const float L = M + log2f(S);
+  *Lf = L;
+  *f = exp2f(L - M) / S;
 }
 
 // The pass-1 partial of unit u, warp w, recomputed from global memory when
@@ -1258,33 +1381,33 @@ __device__ float2 fixup_partial(const SegParams& P, int u, int w, int lane) {
 // Draw from p of target row r (the bonus token, or a rejection whose
 // residual mass is 0) with uniform u, from the row's pass-1 masses.
 template <typename T>
-__device__ int draw_from_p(const SegParams& P, int r, float u, int lane) {
+__device__ int draw_from_p(const SegParams& P, const DrawBuf& db, int r, float u, int lane) {
   const SegRowStat rs = ld_stat(P.rowstat + r);
   const float2* pp = P.part1 + (size_t)r * P.g.nseg * kSegGroupWarps;
-  const double M = rs.M, S = rs.S;
+  const float M = rs.M, S = rs.S;
   auto mass = [&](int j) -> double {
     const float2 v = __ldcg(pp + j);
-    return v.y == 0.f ? 0.0 : (double)v.y * exp2((double)v.x - M) / S;
+    return v.y == 0.f ? 0.0 : (double)(v.y * exp2f(v.x - M) / S);
   };
   double before, total;
-  const int part = owning_part(P.g.nseg * kSegGroupWarps, mass, (double)u, &before, &total, lane);
+  const int part = owning_part(P.g.nseg * kSegGroupWarps, mass, (double)u, &before, &total, db, lane);
   if (part < 0) return -1;
   const SegRowDesc d = ld_desc(P.rowdesc + r);
   const int a = (part / kSegGroupWarps) * P.g.seg + (part % kSegGroupWarps) * P.g.wr;
   const int n = min(P.g.wr, P.V - a);
   float L, f;
   split_norm(M, S, &L, &f);
-  return range_draw<T, false>(P, d.src, -1, a, n, d, L, f, 0.f, 0.f, d.b, (double)u * total - before, lane);
+  return range_draw<T, false>(P, db, d.src, -1, a, n, d, L, f, 0.f, 0.f, d.b, (double)u * total - before, lane);
 }
 
 // Draw from the residual max(p - q, 0) of position p with uniform u, from
 // the position's pass-2 masses; -2 if the residual mass is 0.
 template <typename T>
-__device__ int draw_residual(const SegParams& P, int p, int b, float u, int lane) {
+__device__ int draw_residual(const SegParams& P, const DrawBuf& db, int p, int b, float u, int lane) {
   const float* pp = P.part2 + (size_t)p * P.g.upj * kSegGroupWarps;
   auto mass = [&](int j) -> double { return (double)__ldcg(pp + j); };
   double before, total;
-  const int part = owning_part(P.g.upj * kSegGroupWarps, mass, (double)u, &before, &total, lane);
+  const int part = owning_part(P.g.upj * kSegGroupWarps, mass, (double)u, &before, &total, db, lane);
   if (!(total > 0.0)) return -2;
   if (part < 0) return -1;
   const SegJobDesc jd = ld_job(P.jobdesc + p);
@@ -1292,7 +1415,7 @@ __device__ int draw_residual(const SegParams& P, int p, int b, float u, int lane
   const int h = part / kSegGroupWarps, w = part % kSegGroupWarps;
   const int a = (h >> 1) * P.g.seg + (h & 1) * (P.g.seg / 2) + w * P.g.wr2;
   const int n = min(P.g.wr2, P.V - a);
-  return range_draw<T, true>(P, p + b, P.NT + p, a, n, d, jd.Lp, jd.fp, jd.Lq, jd.fq, b, (double)u * total - before,
+  return range_draw<T, true>(P, db, p + b, P.NT + p, a, n, d, jd.Lp, jd.fp, jd.Lq, jd.fq, b, (double)u * total - before,
                              lane);
 }
 
@@ -1301,7 +1424,7 @@ __device__ int draw_residual(const SegParams& P, int p, int b, float u, int lane
 // residual of j (from p_j if that residual has no mass), or the bonus token
 // from the last target row when every draft is accepted.
 template <typename T>
-__device__ void finalize(const SegParams& P, int b, int lane) {
+__device__ void finalize(const SegParams& P, const DrawBuf& db, int b, int lane) {
   const int d0 = __ldg(P.cu_draft + b), K = __ldg(P.cu_draft + b + 1) - d0, off = d0 + b;
   bool acc = true;
   if (lane < K) {
@@ -1314,10 +1437,10 @@ __device__ void finalize(const SegParams& P, int b, int lane) {
   const int base = 2 * d0 + b;      // the request's first row
   int tok = -1;
   if (j < K) {
-    tok = draw_residual<T>(P, d0 + j, b, ufin, lane);
-    if (tok == -2) tok = draw_from_p<T>(P, base + 2 * j, ufin, lane);
+    tok = draw_residual<T>(P, db, d0 + j, b, ufin, lane);
+    if (tok == -2) tok = draw_from_p<T>(P, db, base + 2 * j, ufin, lane);
   } else if (!(P.flags & 1u)) {
-    tok = draw_from_p<T>(P, base + 2 * K, ufin, lane);
+    tok = draw_from_p<T>(P, db, base + 2 * K, ufin, lane);
   }
   for (int s = lane; s <= K; s += 32) {
     int o = -1;
@@ -1525,6 +1648,11 @@ __device__ void recorder(const SegParams& P, const Ring& R, int lane) {
   // the job entry of candidate cb + j; the published ones, in order, are
   // queued for the producer
   const unsigned G = gridDim.x, upj = (unsigned)P.g.upj, njob = (unsigned)P.total;
+  const int* cu = cu_of(P, R);
+  const int dealt = dealt_units(P), n_dealt = static_units(P), n_units = P.NR * P.g.nseg;
+  unsigned stail = 0;       // claimed pass-1 units queued
+  bool steal_done = dealt >= n_units;
+  if (steal_done && lane == 0) st_rel_cta(R.misc() + 15, 1u);
   unsigned cb = 0, jtail = 0;
   unsigned long long ent = 0;
   bool pend = false, jq_done = false;
@@ -1599,6 +1727,41 @@ __device__ void recorder(const SegParams& P, const Ring& R, int lane) {
         pend = true;
       }
     }
+    // 3. pass-1 units past the dealt ones: once the producer's dealt units
+    //    are nearly issued (misc[13]), claim kStealChunk at a time while the
+    //    queue holds fewer than kStealAhead; lane j works out the geometry
+    //    of the j-th
+    if (!steal_done && stail - ld_acq_cta(R.misc() + 14) + kStealChunk <= (unsigned)kStealAhead &&
+        (int)*reinterpret_cast<volatile unsigned*>(R.misc() + 13) + kStealLead >= n_dealt) {
+      int u0 = 0;
+      if (lane == 0) u0 = dealt + (int)atom_add_gpu(P.ctl + kCtlSteal, (unsigned)kStealChunk);
+      u0 = __shfl_sync(0xffffffffu, u0, 0);
+      const int n = max(0, min(kStealChunk, n_units - u0));
+      if (lane < n) {
+        const int u = u0 + lane, r = u / P.g.nseg, sg = u - r * P.g.nseg;
+        const int2 bs = row_src(P, cu, r);
+        SegSteal e;
+        e.tok0 = sg * P.g.seg;
+        e.n = min(P.g.seg, P.V - e.tok0);
+        e.u = u;
+        e.pad = 0;
+        e.logits = reinterpret_cast<unsigned long long>(row_ptr<T>(P, bs.y) + (size_t)e.tok0 * sizeof(T));
+        e.bits = reinterpret_cast<unsigned long long>(reinterpret_cast<const unsigned char*>(P.bitmap) +
+                                                      (size_t)bs.x * P.g.bm_bytes + (size_t)sg * (P.g.seg / 8));
+        e.desc = reinterpret_cast<unsigned long long>(P.rowdesc + r);
+        R.sq()[(stail + lane) % kSegSq] = e;
+      }
+      __syncwarp();
+      if (n > 0) {
+        if (lane == 0) st_rel_cta(R.misc() + 6, stail + (unsigned)n);
+        stail += (unsigned)n;
+        progress = true;
+      }
+      if (n < kStealChunk) {
+        steal_done = true;
+        if (lane == 0) st_rel_cta(R.misc() + 15, 1u);   // no more claimed pass-1 units
+      }
+    }
     if (progress) {
       t_last = clock64();
       continue;
@@ -1620,7 +1783,7 @@ __device__ void recorder(const SegParams& P, const Ring& R, int lane) {
 template <typename T>
 __device__ __forceinline__ void queue_final(const SegParams& P, const Ring& R, unsigned& tail, int b, int lane) {
   if (tail - ld_acq_cta(R.misc() + 11) >= (unsigned)kSegFq) {
-    finalize<T>(P, b, lane);
+    finalize<T>(P, draw_buf(R, 1), b, lane);
     return;
   }
   __syncwarp();
@@ -1639,7 +1802,7 @@ __device__ void finisher(const SegParams& P, const Ring& R, int lane) {
   long long t_last = clock64();
   for (;;) {
     if (head < ld_acq_cta(R.misc() + 10)) {
-      finalize<T>(P, R.fq()[head % kSegFq], lane);
+      finalize<T>(P, draw_buf(R, 0), R.fq()[head % kSegFq], lane);
       ++head;
       __syncwarp();
       if (lane == 0) st_rel_cta(R.misc() + 11, head);
@@ -1779,6 +1942,11 @@ __global__ void __launch_bounds__(kSegThreads, 1) seg_verify_kernel(const __grid
     for (int s = 0; s < kSegSlots; ++s) {
       mbar_init(R.full() + s, 1);
       mbar_init(R.empty() + s, kSegGroupWarps);
+    }
+    for (int i = 0; i < 2; ++i) {
+      const DrawBuf db = draw_buf(R, i);
+      mbar_init(db.bar, 1);
+      *db.phase = 0u;
     }
     fence_mbar_init();
   }
