@@ -1229,22 +1229,20 @@ __device__ int range_draw(const SegParams& P, const DrawBuf& db, int rp_row, int
     const double tot = __shfl_sync(0xffffffffu, incl, 31);
     const unsigned hit = __ballot_sync(0xffffffffu, carry + incl > t);
     if (hit) {
+      // lane L's run again, one token per lane: the terms' prefix in token
+      // order (a warp scan) against what is left of t after the lanes before
+      // L; rounding can leave it short, and then the run's last token with
+      // mass is the draw
       const int L = __ffs(hit) - 1;
-      int f = -1;
-      if (lane == L) {
-        // the same terms again, summed the same way, in the same order
-        const double before_lane = carry + (incl - lsum);
-        float as = 0.f, ac = 0.f;
-        for (int j = 0; j < cnt && f < 0; ++j) {
-          const float r = draw_term<T, PAIR>(zp_at(t0 + j), zq_at(t0 + j), (pw >> j) & 1u, d, Lp, fp, Lq, fq);
-          const float y = __fsub_rn(r, ac), tt = __fadd_rn(as, y);
-          ac = __fsub_rn(__fsub_rn(tt, as), y);
-          as = tt;
-          if (before_lane + (double)as > t) f = a + t0 + j;
-        }
-        if (f < 0) f = mylast;
-      }
-      found = __shfl_sync(0xffffffffu, f, L);
+      const int tL = __shfl_sync(0xffffffffu, t0, L), cL = __shfl_sync(0xffffffffu, cnt, L);
+      const uint32_t pL = __shfl_sync(0xffffffffu, pw, L);
+      const double rest = t - (carry + __shfl_sync(0xffffffffu, incl - lsum, L));
+      const float r = lane < cL ? draw_term<T, PAIR>(zp_at(tL + lane), zq_at(tL + lane), (pL >> lane) & 1u, d, Lp, fp,
+                                                     Lq, fq)
+                                : 0.f;
+      const float pre = warp_incl_scan(r, lane);
+      const unsigned over = __ballot_sync(0xffffffffu, lane < cL && (double)pre > rest);
+      found = over ? a + tL + __ffs(over) - 1 : __shfl_sync(0xffffffffu, mylast, L);
     }
     int ml = mylast;
 #pragma unroll
