@@ -418,7 +418,7 @@ def bench_gpu(args, rank, world, dist):
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": traffic, "peak_kind": peak_kind, "kernel": KERNEL,
                      "algorithmic_bytes_per_launch": alg_bytes, "launch_ms": 1000 * launch_s,
-                     "launch_timing": "CUDA events around each call on its stream (counter clear and kernel)"},
+                     "launch_timing": "CUDA events around each call on its stream (one kernel launch)"},
         "e2e": {"value": e2e_value, "unit": "requests/s", "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h), "steps": args.steps},
         "gpu_launches": args.steps * n_win,
@@ -498,7 +498,16 @@ def bench_extras(dev, peak: float, cpu_seconds: float) -> dict:
     sec = timed(lambda: sv.spec_verify_sample(a1, device=dev, workspace=ws1, stream=stream))
     out["qwen25_single_B1_K8"] = line("qwen", b1.logit_bytes() + small, sec,
                                       oracle_rate(oracle.verify_batch, b1, budget), "sample_verify_kernel (resident)")
-    out["qwen25_single_B1_K8_breakdown"] = small_batch_breakdown(dev, d1, ws1, stream)
+    a1s = d1.args(flags=8)
+    calls = [("resident (default)", lambda: sv.spec_verify_sample(a1, device=dev, workspace=ws1, stream=stream)),
+             ("split", lambda: sv.spec_verify_sample(a1s, device=dev, workspace=ws1, stream=stream))]
+    bg8 = W.greedy_single(8)
+    dg8 = to_device(bg8, dev)
+    wsg8 = sv.make_workspace(bg8.B, bg8.total_drafts, bg8.V, dev)
+    ag8 = dg8.args()
+    calls.append(("greedy K=8", lambda: sv.spec_verify_greedy(ag8, device=dev, workspace=wsg8, stream=stream)))
+    out["B1_breakdown"] = small_batch_breakdown(dev, calls, stream)
+    del dg8, wsg8
     for K in (1, 2, 4, 8):
         bg = W.greedy_single(K)
         dg = to_device(bg, dev)
@@ -524,7 +533,7 @@ def bench_extras(dev, peak: float, cpu_seconds: float) -> dict:
     ab = db.args()
     sec = timed(lambda: sv.spec_tv_budget(ab, device=dev, workspace=wsb, stream=stream))
     tvbytes = 2 * bb.total_drafts * bb.V * 2 + 4 * int(bb.hist.size) + 16 * bb.total_drafts
-    out["tv_budget_batched_B64_K8"] = line("tv", tvbytes, sec, None, "seg_verify_kernel (TV only)")
+    out["tv_budget_batched_B64_K8"] = line("tv", tvbytes, sec, None, "pipe_verify_kernel (TV only)")
     sec = timed(lambda: sv.spec_draft_confidence(ab, 0.6, device=dev, workspace=wsb, stream=stream))
     cbytes = bb.total_drafts * bb.V * 2 + 4 * int(bb.hist.size) + 8 * bb.total_drafts
     rate = oracle_rate(lambda batch, reqs: oracle.draft_confidence_batch(batch, 0.6, reqs), bb, budget)
@@ -534,21 +543,17 @@ def bench_extras(dev, peak: float, cpu_seconds: float) -> dict:
     return out
 
 
-def small_batch_breakdown(dev, db, ws, stream, iters: int = 200) -> dict:
-    """Where a B=1 call's time goes, per kernel choice: the host's time to
-    check the arguments and enqueue the work (no synchronisation), the GPU
-    span of one call (CUDA events around it, L2 warm), the GPU span of the
-    same calls issued back to back (launches overlap the host), and the
-    span of an empty device operation on the stream (the floor any launch
-    pays)."""
+def small_batch_breakdown(dev, calls, stream, iters: int = 200) -> dict:
+    """Where a B=1 call's time goes, for each (name, call) given: the host's
+    time to check the arguments and enqueue the work (no synchronisation),
+    the GPU span of one call (CUDA events around it, L2 warm), the GPU span
+    of the same calls issued back to back (launches overlap the host), and
+    the span of an empty device operation on the stream (the floor any
+    launch pays).  Every call is one kernel launch."""
     import torch
 
-    import speculative_decoding_verification_23_gb300 as sv
-
     res = {}
-    for name, flags in (("resident (default)", 0), ("split", 8)):
-        args = db.args(flags=flags)
-        call = lambda: sv.spec_verify_sample(args, device=dev, workspace=ws, stream=stream)
+    for name, call in calls:
         for _ in range(10):
             call()
         torch.cuda.synchronize()
@@ -573,7 +578,7 @@ def small_batch_breakdown(dev, db, ws, stream, iters: int = 200) -> dict:
         b.synchronize()
         res[name] = {"host_enqueue_us": round(host_us, 2), "gpu_span_us": round(float(np.median(spans)), 2),
                      "back_to_back_us": round(a.elapsed_time(b) * 1000.0 / iters, 2),
-                     "launches_per_call": 2 if flags == 0 else 1}
+                     "launches_per_call": 1}
     x = torch.empty(1, device=dev)
     spans = []
     for _ in range(50):

@@ -78,11 +78,15 @@
  * the launch.  No entry point ever traps on the device.
  *
  * Workspace: spec_workspace_bytes(B, total_drafts, V) bytes of device
- * memory, at least 256-byte aligned.  Its contents need no initialisation:
- * the split-vocabulary sampling kernel clears its counters itself at its
- * start (one launch per call); the other kernels' calls clear theirs with a
- * cudaMemsetAsync on `stream` before their launch.  Calls that share one
- * workspace must be ordered (same stream, or synchronised).
+ * memory, at least 256-byte aligned.  Its contents need no initialisation
+ * and every call is one kernel launch: the split-vocabulary sampling kernel
+ * clears its counters itself at its start; the other kernels count each
+ * request's arrivals on a 64-bit word tagged with the call (a process-wide
+ * call number in [1, 2^40)), and a word with another tag counts as zero.
+ * Under stream capture the tag would replay with the graph, so a captured
+ * call also captures a cudaMemsetAsync of its B counter words (tag 0).
+ * Calls that share one workspace must be ordered (same stream, or
+ * synchronised).
  */
 #ifndef SPEC_VERIFY_H
 #define SPEC_VERIFY_H
@@ -236,7 +240,7 @@ int spec_draft_confidence(const spec_args *args, float threshold, float *out_con
  *
  * Zeroing: as for the workspace entry point (the split-vocabulary kernel
  * clears its counters at its start; the cluster kernel's counters are
- * cleared with a cudaMemsetAsync before its launch); everything else in the
+ * call-tagged, cleared only under stream capture); everything else in the
  * buffer is written before it is read.
  *
  * Address: every call looks the buffer up with cudaGetSymbolAddress for the

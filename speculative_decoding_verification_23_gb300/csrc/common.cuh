@@ -9,6 +9,8 @@
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 
+#include "spec_internal.h"   // kTagShift
+
 namespace sv {
 
 // Per-request status bits (the same values as spec_verify.h).
@@ -107,6 +109,26 @@ struct RingFills {
       if ((filled >> s) & 1u) (void)mbar_wait(&full[s], (par >> s) & 1u);
   }
 };
+
+// ------------------------------------------- arrival counters, call-tagged
+// A request's arrival counter is one 64-bit word: the calling launch's tag
+// in the high 40 bits, that launch's arrivals in the low 24.  A word with
+// any other tag (an earlier call's, or whatever the memory held) counts as
+// no arrival yet, so the counters need no initial value and no clearing
+// launch between calls.  Returns the arrivals of this launch before this
+// one.  The loop ends: each failed exchange means another arrival landed,
+// and a launch has finitely many.
+
+__device__ __forceinline__ int tagged_arrive(unsigned long long* ctr, unsigned long long tag) {
+  unsigned long long v = *reinterpret_cast<volatile unsigned long long*>(ctr);
+  for (;;) {
+    const bool mine = (v >> kTagShift) == tag;
+    const unsigned long long nv = mine ? v + 1ull : (tag << kTagShift) | 1ull;
+    const unsigned long long got = atomicCAS(ctr, v, nv);
+    if (got == v) return mine ? (int)(v & ((1ull << kTagShift) - 1ull)) : 0;
+    v = got;
+  }
+}
 
 // Position in the ring: slot index and the parity of its current use.
 struct RingCursor {

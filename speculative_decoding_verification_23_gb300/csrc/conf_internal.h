@@ -81,7 +81,8 @@ struct ConfParams {
   float* out_conf;         // [total]
   int* out_k_eff;          // [B]
   int* out_status;         // [B] or null
-  int* counters;           // [B]
+  unsigned long long* counters;   // [B] call-tagged arrivals (tagged_arrive)
+  unsigned long long tag;         // this call's tag
   ConfPartial* partials;   // [total * nck]
   ConfLayout CL;           // pipelined variant only
 };

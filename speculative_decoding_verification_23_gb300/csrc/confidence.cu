@@ -203,7 +203,7 @@ __global__ void __launch_bounds__(kGreedyThreads) confidence_kernel(const __grid
     P.partials[(size_t)d * P.nck + ck] = cp;
     __threadfence();
     const int target = kread * P.nck;
-    const int old = atomicAdd(P.counters + b, 1);
+    const int old = tagged_arrive(P.counters + b, P.tag);
     s_last = (K == kread) && (old == target - 1);
   }
   __syncthreads();
@@ -496,7 +496,7 @@ __device__ __forceinline__ void conf_setup(const ConfParams& P, const CSmem& S, 
       cp.pad = 0;
       P.partials[d] = cp;
       __threadfence();
-      last = atomicAdd(P.counters + r.b, 1) == r.K - 1;
+      last = tagged_arrive(P.counters + r.b, P.tag) == r.K - 1;
     }
     if (__shfl_sync(0xffffffffu, last, 0)) {
       // the request's last row: status and the confidence-stopped count

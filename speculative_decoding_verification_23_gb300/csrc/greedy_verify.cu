@@ -152,7 +152,7 @@ __global__ void __launch_bounds__(kGreedyThreads) greedy_verify_kernel(const __g
     P.partials[(size_t)row * P.nck + ck] = gp;
     __threadfence();
     const int target = (K + 1) * P.nck;
-    const int old = atomicAdd(P.counters + b, 1);
+    const int old = tagged_arrive(P.counters + b, P.tag);
     s_last = K >= 0 && old == target - 1;
   }
   __syncthreads();

@@ -111,7 +111,7 @@ __device__ __forceinline__ void finish_item(const SampleParams& P, const Item& i
   if (tg == 0) {
     P.inval[(size_t)item * kMaxCluster] = flags;
     __threadfence();
-    const int old = atomicAdd(P.counters + b, 1);
+    const int old = tagged_arrive(P.counters + b, P.tag);
     *shflag = (old == K) && K >= 0 && it.rows_ok;
   }
   if (bar >= 0) named_sync(bar, nthr);

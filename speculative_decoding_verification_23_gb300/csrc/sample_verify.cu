@@ -981,7 +981,7 @@ __global__ void __launch_bounds__(((RESIDENT ? kResidentWarps : kStreamWarps) + 
           P.inval[(size_t)item * kMaxCluster + rank] = S.misc_i[kMiFlags];
           __threadfence();
           const int target = C * (K + 1);
-          const int old = atomicAdd(P.counters + b, 1);
+          const int old = tagged_arrive(P.counters + b, P.tag);
           S.misc_i[kMiFinalize] = (old == target - 1) && K >= 0 && it.rows_ok;
         }
         consumer_sync<NCT>();

@@ -9,6 +9,10 @@
 
 namespace sv {
 
+// Call-tagged arrival counters (tagged_arrive): bits of a counter word below
+// the call's tag, i.e. the most arrivals one call may count.
+constexpr int kTagShift = 24;
+
 // ----------------------------------------------------------------- sampling
 constexpr int kChunk = 256;                 // tokens per warp-chunk (8 per lane)
 // Consumer warps per CTA: the resident variant runs one 16-warp CTA per SM;
@@ -197,7 +201,8 @@ struct SampleParams {
   float* out_px;
   float* out_qx;
   // workspace
-  int* counters;         // [B]
+  unsigned long long* counters;   // [B] call-tagged arrivals (tagged_arrive)
+  unsigned long long tag;         // this call's tag
   ItemResult* results;   // [total + B]
   int* inval;            // [(total + B) * kMaxCluster]
   // geometry
@@ -232,7 +237,8 @@ struct GreedyParams {
   int* out_tokens;
   int* out_accepted;
   int* out_status;
-  int* counters;         // [B]
+  unsigned long long* counters;   // [B] call-tagged arrivals (tagged_arrive)
+  unsigned long long tag;         // this call's tag
   GreedyPartial* partials;  // [(total + B) * nck]
 };
 
@@ -248,7 +254,7 @@ inline WorkspaceLayout make_workspace_layout(int B, int total, int V) {
   size_t items = (size_t)total + (size_t)B;
   size_t nck = ((size_t)V + kGreedyChunk - 1) / kGreedyChunk;
   W.off_counters = 0;
-  size_t off = align_up_z((size_t)B * 4, 256);
+  size_t off = align_up_z((size_t)B * 8, 256);
   W.off_results = off;
   off = align_up_z(off + items * sizeof(ItemResult), 256);
   W.off_inval = off;

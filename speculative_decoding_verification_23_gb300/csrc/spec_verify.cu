@@ -115,6 +115,32 @@ struct NvtxRange {
 constexpr long long kSegWaitLimit = 4000000000ll;
 std::atomic<long long> g_seg_wait_limit{kSegWaitLimit};
 
+// Tags of the calls whose kernels count arrivals with tagged_arrive: one per
+// call, in [1, 2^40).  Outside stream capture a call takes a fresh tag and
+// enqueues nothing but its kernel.  Under capture the tag would be replayed
+// with the graph, so the call captures a clear of its B counters instead and
+// uses tag 0, which a cleared word carries.
+std::atomic<unsigned long long> g_call_tag{0};
+
+int call_tag(unsigned long long* counters, int B, cudaStream_t s, unsigned long long* tag) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(s, &cs) != cudaSuccess) {
+    cudaGetLastError();
+    return SPEC_ERR_LAUNCH;
+  }
+  if (cs != cudaStreamCaptureStatusNone) {
+    if (cudaMemsetAsync(counters, 0, (size_t)B * sizeof(unsigned long long), s) != cudaSuccess) {
+      cudaGetLastError();
+      return SPEC_ERR_LAUNCH;
+    }
+    *tag = 0;
+    return SPEC_OK;
+  }
+  const unsigned long long span = (1ull << (64 - sv::kTagShift)) - 1ull;
+  *tag = g_call_tag.fetch_add(1, std::memory_order_relaxed) % span + 1ull;
+  return SPEC_OK;
+}
+
 // The split-vocabulary kernel can serve sampling without top-p when a row
 // has at most kSegMaxSegs segments (V <= 491520 bf16, 245760 fp32).
 bool seg_fits(const spec_args* a) {
@@ -125,11 +151,14 @@ bool seg_fits(const spec_args* a) {
 // kernel would not take in one wave (`resident_pick`: the choice made
 // without hints).  SPEC_PREFER_RESIDENT and SPEC_PREFER_STREAMING keep the
 // kernels they name.
-bool use_seg(const spec_args* a, bool resident_pick) {
+// TV-only calls need the second pass over every position, which the
+// pipelined kernel serves from L2 (its two passes over a row run back to
+// back), so they take the split kernel only when asked for it.
+bool use_seg(const spec_args* a, bool resident_pick, bool tv_only) {
   if (!seg_fits(a)) return false;
   if (a->flags & SPEC_PREFER_SPLIT) return true;
   if (a->flags & (SPEC_PREFER_RESIDENT | SPEC_PREFER_STREAMING)) return false;
-  return !resident_pick;
+  return !resident_pick && !tv_only;
 }
 
 // The split-vocabulary kernel (no top-p): sampling or the TV quantities.
@@ -216,7 +245,7 @@ int run_sample(sv::SampleParams& P, const spec_args* a, void* ws, cudaStream_t s
     C_str *= 2;
   const bool str_ok = C_str <= sv::kMaxCluster;
   const bool resident_pick = res_ok && (!str_ok || (long long)P.n_items * C_res <= num_sms);
-  if (use_seg(a, resident_pick)) return run_seg(P, a, ws, num_sms, max_smem, stream);
+  if (use_seg(a, resident_pick, P.mode == sv::kModeTvOnly)) return run_seg(P, a, ws, num_sms, max_smem, stream);
   bool resident;
   if ((a->flags & SPEC_PREFER_RESIDENT) && res_ok) resident = true;
   else if ((a->flags & SPEC_PREFER_STREAMING) && str_ok) resident = false;
@@ -227,26 +256,20 @@ int run_sample(sv::SampleParams& P, const spec_args* a, void* ws, cudaStream_t s
   if (!resident && !str_ok && !pipe_ok) return SPEC_ERR_SHAPE;
   const sv::WorkspaceLayout W = sv::make_workspace_layout(a->B, a->total_drafts, a->V);
   unsigned char* w = static_cast<unsigned char*>(ws);
-  P.counters = reinterpret_cast<int*>(w + W.off_counters);
+  P.counters = reinterpret_cast<unsigned long long*>(w + W.off_counters);
   P.results = reinterpret_cast<sv::ItemResult*>(w + W.off_results);
   P.inval = reinterpret_cast<int*>(w + W.off_inval);
+  P.tag = 0;
+  if (P.mode == sv::kModeSample) {
+    rc = call_tag(P.counters, a->B, stream, &P.tag);
+    if (rc) return rc;
+  }
   if (!resident && pipe_ok) {
     P.PL = L_pipe;
-    if (P.mode == sv::kModeSample &&
-        cudaMemsetAsync(P.counters, 0, (size_t)a->B * sizeof(int), stream) != cudaSuccess) {
-      cudaGetLastError();
-      return SPEC_ERR_LAUNCH;
-    }
     return sv::launch_pipe_verify(P, a->dtype == SPEC_BF16, num_sms, stream);
   }
   P.C = resident ? C_res : C_str;
   P.L = resident ? L_res : L_str;
-  if (P.mode == sv::kModeSample) {
-    if (cudaMemsetAsync(P.counters, 0, (size_t)a->B * sizeof(int), stream) != cudaSuccess) {
-      cudaGetLastError();
-      return SPEC_ERR_LAUNCH;
-    }
-  }
   return sv::launch_sample_verify(P, a->dtype == SPEC_BF16, topp, stream);
 }
 
@@ -383,12 +406,10 @@ int spec_verify_greedy(const spec_args* a, int32_t* out_tokens, int32_t* out_acc
   P.out_tokens = out_tokens;
   P.out_accepted = out_accepted;
   P.out_status = out_status;
-  P.counters = reinterpret_cast<int*>(w + W.off_counters);
+  P.counters = reinterpret_cast<unsigned long long*>(w + W.off_counters);
   P.partials = reinterpret_cast<sv::GreedyPartial*>(w + W.off_partials);
-  if (cudaMemsetAsync(P.counters, 0, (size_t)a->B * sizeof(int), s) != cudaSuccess) {
-    cudaGetLastError();
-    return SPEC_ERR_LAUNCH;
-  }
+  rc = call_tag(P.counters, a->B, s, &P.tag);
+  if (rc) return rc;
   return sv::launch_greedy_verify(P, a->dtype == SPEC_BF16, s) == 0 ? SPEC_OK : SPEC_ERR_LAUNCH;
 }
 
@@ -435,12 +456,10 @@ int spec_draft_confidence(const spec_args* a, float threshold, float* out_conf, 
   P.out_conf = out_conf;
   P.out_k_eff = out_k_eff;
   P.out_status = out_status;
-  P.counters = reinterpret_cast<int*>(w + W.off_counters);
+  P.counters = reinterpret_cast<unsigned long long*>(w + W.off_counters);
   P.partials = reinterpret_cast<sv::ConfPartial*>(w + W.off_partials);
-  if (cudaMemsetAsync(P.counters, 0, (size_t)a->B * sizeof(int), s) != cudaSuccess) {
-    cudaGetLastError();
-    return SPEC_ERR_LAUNCH;
-  }
+  rc = call_tag(P.counters, a->B, s, &P.tag);
+  if (rc) return rc;
   // at least one draft row per SM: the pipelined kernel (whole rows per
   // CTA); smaller batches spread each row over 8192-token chunks
   if (a->total_drafts >= num_sms && sv::choose_conf_layout(a->V, es, a->B, max_smem, &P.CL) == 0)
