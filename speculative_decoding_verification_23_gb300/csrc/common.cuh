@@ -116,18 +116,20 @@ struct RingFills {
 // any other tag (an earlier call's, or whatever the memory held) counts as
 // no arrival yet, so the counters need no initial value and no clearing
 // launch between calls.  Returns the arrivals of this launch before this
-// one.  The loop ends: each failed exchange means another arrival landed,
-// and a launch has finitely many.
-
+// one.
+//
+// An arrival that reads another tag first resets the word to (tag, 0) with
+// one compare-and-swap against the value it read; then every arrival adds
+// one.  Only this launch's arrivals write the word while it runs, and each
+// writes it with this launch's tag, so a failed reset means the word already
+// carries the tag, and no add lands on a stale word.  No retry loop: under
+// many simultaneous arrivals a loop of exchanges costs quadratically many
+// atomics at one address.
 __device__ __forceinline__ int tagged_arrive(unsigned long long* ctr, unsigned long long tag) {
-  unsigned long long v = *reinterpret_cast<volatile unsigned long long*>(ctr);
-  for (;;) {
-    const bool mine = (v >> kTagShift) == tag;
-    const unsigned long long nv = mine ? v + 1ull : (tag << kTagShift) | 1ull;
-    const unsigned long long got = atomicCAS(ctr, v, nv);
-    if (got == v) return mine ? (int)(v & ((1ull << kTagShift) - 1ull)) : 0;
-    v = got;
-  }
+  const unsigned long long v = *reinterpret_cast<volatile unsigned long long*>(ctr);
+  if ((v >> kTagShift) != tag) atomicCAS(ctr, v, tag << kTagShift);
+  const unsigned long long old = atomicAdd(ctr, 1ull);
+  return (int)(old & ((1ull << kTagShift) - 1ull));
 }
 
 // Position in the ring: slot index and the parity of its current use.
