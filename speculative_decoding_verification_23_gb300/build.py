@@ -17,7 +17,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libspecverify.so")
-SOURCES = ["spec_verify.cu", "sample_verify.cu", "pipe_verify.cu", "seg_verify.cu", "greedy_verify.cu", "confidence.cu"]
+SOURCES = ["spec_verify.cu", "sample_verify.cu", "pipe_verify.cu", "seg_verify.cu", "greedy_verify.cu", "confidence.cu",
+           "topp_verify.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xptxas", "-v"]
 

@@ -12,6 +12,7 @@
 #include "spec_internal.h"
 #include "conf_internal.h"
 #include "seg_internal.h"
+#include "topp_internal.h"
 
 namespace sv {
 int choose_resident_layout(int V, int elem_bytes, bool topp, int max_smem, int* C_out, SmemLayout* L_out);
@@ -25,6 +26,8 @@ int launch_confidence(const ConfParams& P, bool bf16, cudaStream_t stream);
 int choose_conf_layout(int V, int elem_bytes, int B, int max_smem, ConfLayout* out);
 int launch_conf_pipe(const ConfParams& P, bool bf16, int num_sms, cudaStream_t stream);
 int launch_seg_verify(const SegParams& P, bool bf16, int num_sms, cudaStream_t stream);
+int launch_topp_verify(const ToppParams& P, bool bf16, int num_sms, cudaStream_t stream);
+int topp_cut_smem_bytes();
 int seg_smem_bytes();
 unsigned* seg_ctl_address();
 }  // namespace sv
@@ -223,6 +226,59 @@ int run_seg(const sv::SampleParams& S, const spec_args* a, void* ws, int num_sms
   return sv::launch_seg_verify(P, a->dtype == SPEC_BF16, num_sms, stream) == 0 ? SPEC_OK : SPEC_ERR_LAUNCH;
 }
 
+// The top-p path (row-cut and finish kernels) serves top-p batches unless a
+// cluster kernel is asked for, when its records fit the buffer the call has
+// (a workspace is always large enough; the fixed scratch may not be) and V
+// fits its penalty bitmap.
+bool use_topp(const spec_args* a, size_t ws_bytes, int max_smem) {
+  if (!a->top_p || (a->flags & (SPEC_PREFER_RESIDENT | SPEC_PREFER_STREAMING))) return false;
+  if (a->V > sv::kCutMaxV || sv::topp_cut_smem_bytes() > max_smem) return false;
+  return sv::make_topp_workspace(a->B, a->total_drafts, a->V).total <= ws_bytes;
+}
+
+int run_topp(const sv::SampleParams& S, const spec_args* a, void* ws, int num_sms, cudaStream_t stream) {
+  const sv::ToppWorkspace W = sv::make_topp_workspace(a->B, a->total_drafts, a->V);
+  unsigned char* w = static_cast<unsigned char*>(ws);
+  sv::ToppParams P;
+  std::memset(&P, 0, sizeof(P));
+  P.target = a->target_logits;
+  P.ld_t = a->ld_target;
+  P.draft = a->draft_logits;
+  P.ld_d = a->ld_draft;
+  P.cu_draft = a->cu_draft;
+  P.draft_tokens = a->draft_tokens;
+  P.cu_hist = a->cu_hist;
+  P.hist = a->hist_tokens;
+  P.temperature = a->temperature;
+  P.rep_penalty = a->rep_penalty;
+  P.top_p = a->top_p;
+  P.tv_budget = a->tv_budget;
+  P.uniforms = S.uniforms;
+  P.B = a->B;
+  P.V = a->V;
+  P.total = a->total_drafts;
+  P.max_k = a->max_k;
+  P.flags = a->flags;
+  P.mode = S.mode;
+  P.NT = a->total_drafts + a->B;
+  P.NR = 2 * a->total_drafts + a->B;
+  P.out_tokens = S.out_tokens;
+  P.out_accepted = S.out_accepted;
+  P.out_status = S.out_status;
+  P.out_tv = S.out_tv;
+  P.out_theta = S.out_theta;
+  P.out_px = S.out_px;
+  P.out_qx = S.out_qx;
+  P.rows = reinterpret_cast<sv::CutRow*>(w + W.off_rows);
+  P.pool_ctr = reinterpret_cast<unsigned long long*>(w + W.off_ctr);
+  P.broken = P.pool_ctr + 1;
+  P.pool = reinterpret_cast<int*>(w + W.off_pool);
+  P.pool_cap = W.pool_cap;
+  const int rc = call_tag(P.pool_ctr, 1, stream, &P.tag);
+  if (rc) return rc;
+  return sv::launch_topp_verify(P, a->dtype == SPEC_BF16, num_sms, stream) == 0 ? SPEC_OK : SPEC_ERR_LAUNCH;
+}
+
 // Picks the kernel variant.  Resident (each logit read once, values kept in
 // the shared memory of a C-CTA cluster) when every work item gets its own
 // cluster in one wave; otherwise the split-vocabulary kernel without top-p
@@ -230,11 +286,12 @@ int run_seg(const sv::SampleParams& S, const spec_args* a, void* ws, int num_sms
 // flags override the choice; SPEC_PREFER_STREAMING without top-p names the
 // pipelined kernel (one CTA per SM, pass 1 of the next item overlapping
 // pass 2 of the current one).
-int run_sample(sv::SampleParams& P, const spec_args* a, void* ws, cudaStream_t stream) {
+int run_sample(sv::SampleParams& P, const spec_args* a, void* ws, size_t ws_bytes, cudaStream_t stream) {
   int max_smem = 0, num_sms = 0, smem_per_sm = 0;
   int rc = device_props(&max_smem, &num_sms, &smem_per_sm);
   if (rc) return rc;
   const bool topp = a->top_p != nullptr;
+  if (topp && use_topp(a, ws_bytes, max_smem)) return run_topp(P, a, ws, num_sms, stream);
   const int es = elem_bytes(a->dtype);
   int C_res = 0;
   sv::SmemLayout L_res{}, L_str{};
@@ -313,7 +370,8 @@ size_t spec_workspace_bytes(int32_t B, int32_t total_drafts, int32_t V) {
     const size_t m = sv::make_seg_workspace(B, total_drafts, V, es).total;
     if (m > n) n = m;
   }
-  return n;
+  const size_t t = sv::make_topp_workspace(B, total_drafts, V).total;
+  return t > n ? t : n;
 }
 
 int spec_verify_sample(const spec_args* a, int32_t* out_tokens, int32_t* out_accepted, int32_t* out_status,
@@ -331,7 +389,7 @@ int spec_verify_sample(const spec_args* a, int32_t* out_tokens, int32_t* out_acc
   P.out_accepted = out_accepted;
   P.out_status = out_status;
   P.n_items = a->total_drafts + a->B;
-  return run_sample(P, a, workspace, reinterpret_cast<cudaStream_t>(stream));
+  return run_sample(P, a, workspace, ws_bytes, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int spec_verify_sample_static(const spec_args* a, int32_t* out_tokens, int32_t* out_accepted, int32_t* out_status,
@@ -351,7 +409,7 @@ int spec_verify_sample_static(const spec_args* a, int32_t* out_tokens, int32_t* 
   P.out_accepted = out_accepted;
   P.out_status = out_status;
   P.n_items = a->total_drafts + a->B;
-  return run_sample(P, a, scratch, reinterpret_cast<cudaStream_t>(stream));
+  return run_sample(P, a, scratch, SPEC_STATIC_SCRATCH_BYTES, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int spec_tv_budget(const spec_args* a, float* out_tv, float* out_theta, float* out_p_at_draft,
@@ -372,7 +430,7 @@ int spec_tv_budget(const spec_args* a, float* out_tv, float* out_theta, float* o
   P.out_px = out_p_at_draft;
   P.out_qx = out_q_at_draft;
   P.n_items = a->total_drafts;
-  return run_sample(P, a, workspace, reinterpret_cast<cudaStream_t>(stream));
+  return run_sample(P, a, workspace, ws_bytes, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int spec_verify_greedy(const spec_args* a, int32_t* out_tokens, int32_t* out_accepted, int32_t* out_status,

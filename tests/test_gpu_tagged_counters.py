@@ -1,8 +1,9 @@
 """Arrival counters without a clearing launch.
 
 The greedy, cluster, pipelined and confidence kernels count each request's
-arrivals on a 64-bit word tagged with the call: a word that carries another
-call's tag, or any bytes the memory happened to hold, counts as no arrival.
+arrivals (the top-p path, its pool's fill) on a 64-bit word tagged with the
+call: a word that carries another call's tag, or any bytes the memory
+happened to hold, counts as no arrival.
 So a workspace full of random bytes, and one that earlier calls left behind,
 give the oracle's results, and a call enqueues its kernel alone.  Under
 stream capture a call captures a clear of its counters (tag 0), so a graph
@@ -47,8 +48,9 @@ def _check_sample(batch, got, ref):
     assert near <= 1
 
 
-@pytest.mark.parametrize("flags,top_p", [(RESIDENT, 1.0), (STREAMING, 1.0), (STREAMING, [0.9, 0.5, 0.95, 0.3, 1.0, 0.7])],
-                         ids=["resident", "pipelined", "cluster-top-p"])
+@pytest.mark.parametrize("flags,top_p", [(RESIDENT, 1.0), (STREAMING, 1.0), (STREAMING, [0.9, 0.5, 0.95, 0.3, 1.0, 0.7]),
+                                         (0, [0.9, 0.5, 0.95, 0.3, 1.0, 0.7])],
+                         ids=["resident", "pipelined", "cluster-top-p", "row-cut-top-p"])
 def test_sample_on_a_random_workspace_and_repeated(flags, top_p):
     import torch
 
