@@ -34,6 +34,8 @@ constexpr int kCutPoolPerRow = 1024;                       // kept-list entries 
 constexpr int kCutPoolMax = 1 << 23;                       // pool entries at most
 constexpr int kCutListMax = 32768;                         // a longer kept set is not listed (dense)
 constexpr int kFinThreads = 256;
+constexpr int kCutViaRow = 1 << 16;                        // a record flag, not a status bit
+constexpr int kCutStatusMask = 0xffff;
 
 // Per logical row (request order: request b's rows start at 2 cu_draft[b] + b;
 // target row i at 2i, draft row i at 2i + 1, the bonus row at 2K).
@@ -44,7 +46,7 @@ struct CutRow {
   float Sk;       // kept mass, in units of 2^(z'c - M)
   int n;          // kept tokens listed in the pool; -1: not listed (dense)
   int off;        // the list's first pool entry
-  int flags;      // kStatusBadLogits
+  int flags;      // kStatusBadLogits; kCutViaRow: the cut was selected over the row in global memory
   float S;        // the row's whole mass, in units of 2^(z'c - M)
   unsigned tag;   // low 32 bits of the writing call's tag (a row the call left unwritten keeps another)
 };

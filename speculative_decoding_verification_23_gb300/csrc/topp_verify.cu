@@ -637,7 +637,10 @@ __device__ void cut_consumers(const ToppParams& P, unsigned char* smem, uint64_t
       const double target = (double)x.tp * (double)S;
       bool win = ncand <= kCutCand;
       if (win) win = select_cut<T, false>(P, x, cand, ncand, M, target, hm, hc, bits, ms, ct, cw, lane);
-      if (!win) select_cut<T, true>(P, x, cand, ncand, M, target, hm, hc, bits, ms, ct, cw, lane);
+      if (!win) {
+        select_cut<T, true>(P, x, cand, ncand, M, target, hm, hc, bits, ms, ct, cw, lane);
+        rec.flags |= kCutViaRow;
+      }
       const unsigned tk = ms->tau_key;
       rec.tau = okey_val(tk);
       rec.Sk = (float)ms->Sk;
@@ -898,7 +901,7 @@ __global__ void __launch_bounds__(kFinThreads) topp_finish_kernel(const __grid_c
     }
     for (int j = tid; j <= 2 * K; j += kFinThreads) {
       const CutRow R = P.rows[base + j];
-      s |= R.tag != tag32 ? kStatusTimeout : R.flags;
+      s |= R.tag != tag32 ? kStatusTimeout : (R.flags & kCutStatusMask);
     }
   }
   if (s) atomicOr(&fm.st, s);
