@@ -132,15 +132,6 @@ __device__ __forceinline__ int tagged_arrive(unsigned long long* ctr, unsigned l
   return (int)(old & ((1ull << kTagShift) - 1ull));
 }
 
-// The same word as a fill counter: adds n and returns this launch's count
-// before the add.
-__device__ __forceinline__ unsigned tagged_add(unsigned long long* ctr, unsigned long long tag, unsigned n) {
-  const unsigned long long v = *reinterpret_cast<volatile unsigned long long*>(ctr);
-  if ((v >> kTagShift) != tag) atomicCAS(ctr, v, tag << kTagShift);
-  const unsigned long long old = atomicAdd(ctr, (unsigned long long)n);
-  return (unsigned)(old & ((1ull << kTagShift) - 1ull));
-}
-
 // Position in the ring: slot index and the parity of its current use.
 struct RingCursor {
   uint32_t slot = 0, phase = 0;

@@ -270,11 +270,10 @@ int run_topp(const sv::SampleParams& S, const spec_args* a, void* ws, int num_sm
   P.out_px = S.out_px;
   P.out_qx = S.out_qx;
   P.rows = reinterpret_cast<sv::CutRow*>(w + W.off_rows);
-  P.pool_ctr = reinterpret_cast<unsigned long long*>(w + W.off_ctr);
-  P.broken = P.pool_ctr + 1;
+  P.broken = reinterpret_cast<unsigned long long*>(w + W.off_ctr);
   P.pool = reinterpret_cast<int*>(w + W.off_pool);
   P.pool_cap = W.pool_cap;
-  const int rc = call_tag(P.pool_ctr, 1, stream, &P.tag);
+  const int rc = call_tag(P.broken, 1, stream, &P.tag);
   if (rc) return rc;
   return sv::launch_topp_verify(P, a->dtype == SPEC_BF16, num_sms, stream) == 0 ? SPEC_OK : SPEC_ERR_LAUNCH;
 }

@@ -12,8 +12,9 @@
 //  - the finish kernel takes each request's decisions, TV distances and
 //    draws from those lists alone, gathering the other row's logits at the
 //    listed tokens (a filtered row is zero off its list).
-// A row whose list does not fit the pool (or a request with top_p = 1) is
-// marked dense, and the finish kernel scans its rows in full.
+// A row whose list does not fit its CTA's share of the pool (or a request
+// with top_p = 1) is not listed, and the finish kernel scans its rows in
+// full.
 #pragma once
 
 #include <cstddef>
@@ -78,17 +79,15 @@ struct ToppParams {
   float* out_px;
   float* out_qx;
   CutRow* rows;                  // [NR]
-  int* pool;                     // kept token lists
-  unsigned long long* pool_ctr;  // call-tagged entries taken (tagged_add)
+  int* pool;                     // kept token lists; CTA c of the row-cut grid fills
+                                 // [c, c + 1) * (pool_cap / gridDim) in row order
   unsigned long long* broken;    // (tag << 1) | (cu_draft is not a valid packing)
-  unsigned long long tag;
-  int pool_cap;                  // pool entries (<= kCutPoolMax; with the failed adds of
-                                 // one launch, at most kCutListMax per CTA, the count stays
-                                 // below the counter word's 2^24)
+  unsigned long long tag;        // the call's tag (rows carry its low 32 bits)
+  int pool_cap;                  // pool entries
 };
 
 struct ToppWorkspace {
-  size_t off_rows, off_ctr, off_pool, total;
+  size_t off_rows, off_ctr, off_pool, total;   // off_ctr: the `broken` word
   int pool_cap;
 };
 

@@ -273,210 +273,274 @@ __device__ __forceinline__ unsigned cmax_u(unsigned v, CutMisc* ms, int cw, int 
 }
 
 // Visits every token of the select's source with (index, penalised logit):
-// the candidates inside the window (from shared memory), or the whole row
-// (from global memory).
+// the candidates (from shared memory), or the whole row (from global
+// memory, eight 16-byte loads in flight per thread).
 template <typename T, bool GLOBAL, typename F>
-__device__ __forceinline__ void visit(const ToppParams& P, const RowCtx& x, const int2* cand, int ncand, float ylo,
+__device__ __forceinline__ void visit(const ToppParams& P, const RowCtx& x, const int2* cand, int ncand,
                                       const uint32_t* bits, int ct, F&& f) {
   if constexpr (!GLOBAL) {
     for (int j = ct; j < ncand; j += kCutConsumers) {
       const int2 e = cand[j];
-      const float z = __int_as_float(e.y);
-      if (__fmul_rn(z, x.c) >= ylo) f(e.x, z);
+      f(e.x, __int_as_float(e.y));
     }
   } else {
     constexpr int N = Vec<T>::N;
+    constexpr int kDepth = 8;
     const uint4* row = reinterpret_cast<const uint4*>(logits_row<T>(P, x.m.src));
     const int nv = row_bytes(P, (int)sizeof(T)) / 16;
-    for (int v = ct; v < nv; v += kCutConsumers) {
-      float z[8];
-      bool bad = false;
-      pen_vec<T>(__ldcg(row + v), v * N, x, bits, P.V, z, bad);
+    for (int v0 = ct; v0 < nv; v0 += kDepth * kCutConsumers) {
+      uint4 raw[kDepth];
 #pragma unroll
-      for (int j = 0; j < N; ++j)
-        if (v * N + j < P.V) f(v * N + j, z[j]);
+      for (int q = 0; q < kDepth; ++q) {
+        const int v = v0 + q * kCutConsumers;
+        raw[q] = v < nv ? __ldcg(row + v) : make_uint4(0u, 0u, 0u, 0u);
+      }
+#pragma unroll
+      for (int q = 0; q < kDepth; ++q) {
+        const int v = v0 + q * kCutConsumers;
+        if (v >= nv) break;
+        float z[8];
+        bool bad = false;
+        pen_vec<T>(raw[q], v * N, x, bits, P.V, z, bad);
+#pragma unroll
+        for (int j = 0; j < N; ++j)
+          if (v * N + j < P.V) f(v * N + j, z[j]);
+      }
     }
   }
 }
 
-// The exact cut of the row over a source: the largest key kappa with
-// sum over tokens of key >= kappa of 2^(z'c - M) >= target, by mass
-// histograms over shrinking key ranges.  Returns false when the source does
-// not hold the cut (only possible for the window: its mass is short of the
-// target); on success ms->tau_key, ms->Sk (the kept mass) and ms->n_upper
-// (at least the kept count) are set.  With GLOBAL the source is the whole
-// row, and when rounding leaves the target out of reach every token is kept.
-template <typename T, bool GLOBAL>
-__device__ bool select_cut(const ToppParams& P, const RowCtx& x, const int2* cand, int ncand, float M, double target,
-                           float* hm, int* hc, const uint32_t* bits, CutMisc* ms, int ct, int cw, int lane) {
-  const float ylo = M - kCutWindow;
-  // the key range of the source
+// One level of the select: a histogram of mass (2^(z'c - M)) and count
+// over the bins that `binf` assigns (-1: not in this level), then the first
+// bin from the top whose inclusive mass, with `above` before the first
+// bin, reaches the target.  Every consumer thread gets the same result.
+struct BinPick {
+  int b;          // the bin (-1: none reaches the target)
+  int lastb;      // the last bin with tokens
+  double above;   // mass before bin b (with the level's `above`)
+  int n_above;    // tokens before bin b (with the level's count)
+  int cnt;        // tokens in bin b
+};
+
+template <typename T, bool GLOBAL, typename BinF>
+__device__ BinPick pick_bin(const ToppParams& P, const RowCtx& x, const int2* cand, int ncand, float M,
+                            double target, double above, int n_above, float* hm, int* hc, const uint32_t* bits,
+                            CutMisc* ms, int ct, int cw, int lane, BinF&& binf) {
+  for (int j = ct; j < kCutBins; j += kCutConsumers) {
+    hm[j] = 0.f;
+    hc[j] = 0;
+  }
+  csync();
+  visit<T, GLOBAL>(P, x, cand, ncand, bits, ct, [&](int, float z) {
+    const int bin = binf(z);
+    if (bin < 0) return;
+    atomicAdd(hm + bin, ex2(__fmul_rn(z, x.c) - M));
+    atomicAdd(hc + bin, 1);
+  });
+  csync();
+  static_assert(kCutBins == 2 * kCutConsumers, "two bins per consumer thread");
+  const double m0 = (double)hm[2 * ct], m1 = (double)hm[2 * ct + 1];
+  const int c0 = hc[2 * ct], c1 = hc[2 * ct + 1];
+  const double incl = warp_incl_scan_d(m0 + m1, lane);
+  int cincl = c0 + c1;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int t = __shfl_up_sync(0xffffffffu, cincl, o);
+    if (lane >= o) cincl += t;
+  }
+  if (lane == 31) {
+    ms->dred[cw] = incl;
+    ms->ired[cw] = cincl;
+  }
+  csync();
+  double wbase = 0.0;
+  int cbase = 0;
+  for (int w = 0; w < cw; ++w) {
+    wbase += ms->dred[w];
+    cbase += ms->ired[w];
+  }
+  const double excl = above + wbase + incl - (m0 + m1);
+  const int cexcl = n_above + cbase + cincl - (c0 + c1);
+  int pick = 0x7fffffff;
+  if (excl + m0 >= target && c0 > 0) pick = 2 * ct;
+  else if (excl + m0 + m1 >= target && c1 > 0) pick = 2 * ct + 1;
+  int last = c1 > 0 ? 2 * ct + 1 : (c0 > 0 ? 2 * ct : -1);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    pick = min(pick, __shfl_xor_sync(0xffffffffu, pick, o));
+    last = max(last, __shfl_xor_sync(0xffffffffu, last, o));
+  }
+  if (lane == 0) {
+    ms->kred[cw] = (unsigned)pick;
+    ms->ired2[cw] = last;
+  }
+  csync();
+  BinPick r;
+  int b = 0x7fffffff;
+  r.lastb = -1;
+  for (int w = 0; w < kCutConsumerWarps; ++w) {
+    b = min(b, (int)ms->kred[w]);
+    r.lastb = max(r.lastb, ms->ired2[w]);
+  }
+  r.b = b == 0x7fffffff ? -1 : b;
+  csync();
+  // the owner of the chosen bin (or of the last one) publishes what lies above it
+  const int ob = r.b >= 0 ? r.b : r.lastb;
+  if (ob >= 0 && ob >> 1 == ct) {
+    ms->above = (ob & 1) ? excl + m0 : excl;
+    ms->n_upper = (ob & 1) ? cexcl + c0 : cexcl;
+    ms->bstar = (ob & 1) ? c1 : c0;
+  }
+  csync();
+  r.above = ms->above;
+  r.n_above = ms->n_upper;
+  r.cnt = ms->bstar;
+  csync();
+  return r;
+}
+
+// The cut among at most 32 tokens (those `inb` accepts), with `above` the
+// mass and `n_above` the count of the tokens of higher keys: the tokens
+// sorted by key, ties walked together.  Sets ms->tau_key, ms->Sk and
+// ms->n_upper (an upper bound on the kept count).
+template <typename T, bool GLOBAL, typename InB>
+__device__ void small_cut(const ToppParams& P, const RowCtx& x, const int2* cand, int ncand, float M, double target,
+                          double above, int n_above, float* hm, int* hc, const uint32_t* bits, CutMisc* ms, int ct,
+                          int cw, int lane, InB&& inb) {
+  if (ct == 0) ms->nsmall = 0;
+  csync();
+  unsigned* sk = reinterpret_cast<unsigned*>(hc);
+  float* smass = hm;
+  visit<T, GLOBAL>(P, x, cand, ncand, bits, ct, [&](int, float z) {
+    if (!inb(z)) return;
+    const int s = atomicAdd(&ms->nsmall, 1);
+    if (s < 32) {
+      sk[s] = okey(z);
+      smass[s] = ex2(__fmul_rn(z, x.c) - M);
+    }
+  });
+  csync();
+  if (cw == 0) {
+    const int n = min(ms->nsmall, 32);
+    const unsigned k = lane < n ? sk[lane] : 0u;
+    const double w = lane < n ? (double)smass[lane] : 0.0;
+    double grp = 0.0, hi_mass = 0.0;
+    for (int j = 0; j < n; ++j) {
+      const unsigned kj = __shfl_sync(0xffffffffu, k, j);
+      const double wj = __shfl_sync(0xffffffffu, w, j);
+      if (lane < n) {
+        if (kj == k) grp += wj;
+        else if (kj > k) hi_mass += wj;
+      }
+    }
+    // a key is the cut when its upper set (itself included) reaches the
+    // target and the keys above it do not; the lowest key if none does
+    const double upto = above + hi_mass + grp;
+    const bool is_cut = lane < n && upto >= target && above + hi_mass < target;
+    const unsigned cm = __ballot_sync(0xffffffffu, is_cut);
+    unsigned best;
+    double bsk;
+    if (cm) {
+      const int L = __ffs(cm) - 1;
+      best = __shfl_sync(0xffffffffu, k, L);
+      bsk = __shfl_sync(0xffffffffu, upto, L);
+    } else {
+      unsigned mk = lane < n ? k : 0xffffffffu;
+      double tot = lane < n ? w : 0.0;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        mk = min(mk, __shfl_xor_sync(0xffffffffu, mk, o));
+        tot += __shfl_xor_sync(0xffffffffu, tot, o);
+      }
+      best = mk;
+      bsk = above + tot;
+    }
+    if (lane == 0) {
+      ms->tau_key = best;
+      ms->Sk = bsk;
+      ms->n_upper = n_above + n;
+    }
+  }
+  csync();
+}
+
+// The exact cut over the tokens of a source that `inr` accepts, with the
+// mass and count of higher tokens given: levels of 1024 bins over shrinking
+// ranges of the order keys of z' (each level narrows the range 1024-fold),
+// until one key or at most 32 tokens remain.  When rounding leaves the
+// target out of reach, down to the lowest token.
+template <typename T, bool GLOBAL, typename InR>
+__device__ void key_levels(const ToppParams& P, const RowCtx& x, const int2* cand, int ncand, float M, double target,
+                           double above, int n_above, float* hm, int* hc, const uint32_t* bits, CutMisc* ms, int ct,
+                           int cw, int lane, InR&& inr) {
   unsigned klo = 0xffffffffu, khi = 0u;
-  visit<T, GLOBAL>(P, x, cand, ncand, ylo, bits, ct, [&](int, float z) {
-    if (z > -INFINITY) {
+  visit<T, GLOBAL>(P, x, cand, ncand, bits, ct, [&](int, float z) {
+    if (z > -INFINITY && inr(z)) {
       klo = min(klo, okey(z));
       khi = max(khi, okey(z));
     }
   });
   klo = cmin_u(klo, ms, cw, lane);
   khi = cmax_u(khi, ms, cw, lane);
-  if (klo > khi) return false;          // nothing with mass
-  double above = 0.0;
-  int cnt_above = 0;
-  for (int level = 0; level < 6; ++level) {
-    for (int j = ct; j < kCutBins; j += kCutConsumers) {
-      hm[j] = 0.f;
-      hc[j] = 0;
-    }
-    csync();
+  for (int level = 0; level < 6 && klo <= khi; ++level) {
     const unsigned long long range = (unsigned long long)(khi - klo) + 1ull;
-    visit<T, GLOBAL>(P, x, cand, ncand, ylo, bits, ct, [&](int, float z) {
-      const uint32_t k = okey(z);
-      if (k < klo || k > khi) return;
-      const int bin = (int)(((unsigned long long)(khi - k) * (unsigned long long)kCutBins) / range);
-      atomicAdd(hm + bin, ex2(__fmul_rn(z, x.c) - M));
-      atomicAdd(hc + bin, 1);
-    });
-    csync();
-    // first bin (from the top) whose inclusive mass reaches the target
-    static_assert(kCutBins == 2 * kCutConsumers, "two bins per consumer thread");
-    const double m0 = (double)hm[2 * ct], m1 = (double)hm[2 * ct + 1];
-    const int c0 = hc[2 * ct], c1 = hc[2 * ct + 1];
-    double incl = warp_incl_scan_d(m0 + m1, lane);
-    int cincl = c0 + c1;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int t = __shfl_up_sync(0xffffffffu, cincl, o);
-      if (lane >= o) cincl += t;
-    }
-    if (lane == 31) {
-      ms->dred[cw] = incl;
-      ms->ired[cw] = cincl;
-    }
-    csync();
-    double wbase = 0.0;
-    int cbase = 0;
-    for (int w = 0; w < cw; ++w) {
-      wbase += ms->dred[w];
-      cbase += ms->ired[w];
-    }
-    const double excl = above + wbase + incl - (m0 + m1);
-    const int cexcl = cnt_above + cbase + cincl - (c0 + c1);
-    int pick = 0x7fffffff;
-    if (excl + m0 >= target && c0 > 0) pick = 2 * ct;
-    else if (excl + m0 + m1 >= target && c1 > 0) pick = 2 * ct + 1;
-    int last = c1 > 0 ? 2 * ct + 1 : (c0 > 0 ? 2 * ct : -1);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      pick = min(pick, __shfl_xor_sync(0xffffffffu, pick, o));
-      last = max(last, __shfl_xor_sync(0xffffffffu, last, o));
-    }
-    if (lane == 0) {
-      ms->kred[cw] = (unsigned)pick;
-      ms->ired2[cw] = last;
-    }
-    csync();
-    int b = 0x7fffffff, lastb = -1;
-    for (int w = 0; w < kCutConsumerWarps; ++w) {
-      b = min(b, (int)ms->kred[w]);
-      lastb = max(lastb, ms->ired2[w]);
-    }
-    csync();
-    if (b == 0x7fffffff) {
-      if (!GLOBAL) return false;        // the window does not hold the cut
-      b = lastb;                        // out of reach by rounding: down to the lowest token
-    }
-    // the owner of bin b publishes the mass and count above it
-    if (b >> 1 == ct) {
-      ms->above = (b & 1) ? excl + m0 : excl;
-      ms->n_upper = (b & 1) ? cexcl + c0 : cexcl;
-      ms->bstar = (b & 1) ? c1 : c0;
-      ms->Sk = (b & 1) ? m1 : m0;
-    }
-    csync();
-    above = ms->above;
-    cnt_above = ms->n_upper;
-    const int cnt_b = ms->bstar;
-    const double mass_b = ms->Sk;
+    const unsigned lo = klo, hi = khi;
+    auto kbin = [&](float z) -> int {
+      const uint32_t kz = okey(z);
+      if (kz < lo || kz > hi || !inr(z)) return -1;
+      return (int)(((unsigned long long)(hi - kz) * (unsigned long long)kCutBins) / range);
+    };
+    BinPick bp = pick_bin<T, GLOBAL>(P, x, cand, ncand, M, target, above, n_above, hm, hc, bits, ms, ct, cw, lane,
+                                     kbin);
+    const int b = bp.b >= 0 ? bp.b : bp.lastb;
     const unsigned lo_off = (unsigned)(((unsigned long long)b * range + kCutBins - 1) / kCutBins);
     const unsigned hi_off = (unsigned)(((unsigned long long)(b + 1) * range + kCutBins - 1) / kCutBins) - 1u;
-    const unsigned nkhi = khi - lo_off, nklo = khi - hi_off;
-    csync();
-    if (nklo == nkhi) {
-      // one key: every token of it is kept
-      if (ct == 0) {
-        ms->tau_key = nkhi;
-        ms->Sk = above + mass_b;
-        ms->n_upper = cnt_above + cnt_b;
-      }
-      csync();
-      return true;
-    }
-    if (cnt_b <= 32) {
-      // a few tokens: sort them by key (descending) and walk the ties
-      if (ct == 0) ms->nsmall = 0;
-      csync();
-      unsigned* sk = reinterpret_cast<unsigned*>(hc);     // the histogram is read; reuse it
-      float* smass = hm;
-      visit<T, GLOBAL>(P, x, cand, ncand, ylo, bits, ct, [&](int, float z) {
-        const uint32_t k = okey(z);
-        if (k < nklo || k > nkhi) return;
-        const int s = atomicAdd(&ms->nsmall, 1);
-        if (s < 32) {
-          sk[s] = k;
-          smass[s] = ex2(__fmul_rn(z, x.c) - M);
-        }
-      });
-      csync();
-      if (cw == 0) {
-        const int n = min(ms->nsmall, 32);
-        const unsigned k = lane < n ? sk[lane] : 0u;
-        const double w = lane < n ? (double)smass[lane] : 0.0;
-        // rank by key, descending; equal keys share the tie group's mass
-        double grp = 0.0, hi_mass = 0.0;
-        for (int j = 0; j < n; ++j) {
-          const unsigned kj = __shfl_sync(0xffffffffu, k, j);
-          const double wj = __shfl_sync(0xffffffffu, w, j);
-          if (lane < n) {
-            if (kj == k) grp += wj;
-            else if (kj > k) hi_mass += wj;
-          }
-        }
-        // a key is the cut when its upper set (itself included) reaches the
-        // target and the keys above it do not; the lowest key if none does
-        const double upto = above + hi_mass + grp;
-        const bool is_cut = lane < n && upto >= target && above + hi_mass < target;
-        const unsigned cm = __ballot_sync(0xffffffffu, is_cut);
-        unsigned best;
-        double bsk;
-        if (cm) {
-          const int L = __ffs(cm) - 1;
-          best = __shfl_sync(0xffffffffu, k, L);
-          bsk = __shfl_sync(0xffffffffu, upto, L);
-        } else {
-          unsigned mk = lane < n ? k : 0xffffffffu;
-          double tot = lane < n ? w : 0.0;
-#pragma unroll
-          for (int o = 16; o > 0; o >>= 1) {
-            mk = min(mk, __shfl_xor_sync(0xffffffffu, mk, o));
-            tot += __shfl_xor_sync(0xffffffffu, tot, o);
-          }
-          best = mk;
-          bsk = above + tot;
-        }
-        if (lane == 0) {
-          ms->tau_key = best;
-          ms->Sk = bsk;
-          ms->n_upper = cnt_above + n;
-        }
-      }
-      csync();
-      return true;
+    const unsigned nkhi = hi - lo_off, nklo = hi - hi_off;
+    above = bp.above;
+    n_above = bp.n_above;
+    if (nklo == nkhi || bp.cnt <= 32) {
+      small_cut<T, GLOBAL>(P, x, cand, ncand, M, target, above, n_above, hm, hc, bits, ms, ct, cw, lane,
+                           [&](float z) {
+                             const uint32_t kz = okey(z);
+                             return kz >= nklo && kz <= nkhi && inr(z);
+                           });
+      return;
     }
     klo = nklo;
     khi = nkhi;
   }
-  // key ranges shrink 1024-fold a level: six levels always end in one key
+  // the key ranges shrink 1024-fold a level, so the loop ends in small_cut
+  if (ct == 0) {
+    ms->tau_key = klo;
+    ms->Sk = target;
+    ms->n_upper = n_above;
+  }
+  csync();
+}
+
+// The cut from the candidates: a first level of 1024 bins uniform in z'c
+// over the window [M - kCutWindow, M], then the tokens of the chosen bin.
+// False when the window's mass is short of the target (the cut lies below
+// it).
+template <typename T>
+__device__ bool select_window(const ToppParams& P, const RowCtx& x, const int2* cand, int ncand, float M,
+                              double target, float* hm, int* hc, const uint32_t* bits, CutMisc* ms, int ct, int cw,
+                              int lane) {
+  const float ylo = M - kCutWindow;
+  const float scale = (float)kCutBins / kCutWindow;
+  auto ybin = [=](float z) -> int {
+    const float y = __fmul_rn(z, x.c);
+    if (!(y >= ylo)) return -1;
+    return min(kCutBins - 1, (int)((M - y) * scale));
+  };
+  const BinPick bp = pick_bin<T, false>(P, x, cand, ncand, M, target, 0.0, 0, hm, hc, bits, ms, ct, cw, lane, ybin);
+  if (bp.b < 0) return false;
+  const int b = bp.b;
+  auto inb = [=](float z) { return ybin(z) == b; };
+  if (bp.cnt <= 32)
+    small_cut<T, false>(P, x, cand, ncand, M, target, bp.above, bp.n_above, hm, hc, bits, ms, ct, cw, lane, inb);
+  else
+    key_levels<T, false>(P, x, cand, ncand, M, target, bp.above, bp.n_above, hm, hc, bits, ms, ct, cw, lane, inb);
   return true;
 }
 
@@ -493,6 +557,11 @@ __device__ void cut_consumers(const ToppParams& P, unsigned char* smem, uint64_t
   float* hm = reinterpret_cast<float*>(smem + kOffHm);
   int* hc = reinterpret_cast<int*>(smem + kOffHc);
   const unsigned tag32 = (unsigned)P.tag;
+  const int tpc = kCutChunkBytes / (int)sizeof(T);   // tokens per chunk
+  // this CTA's share of the pool, taken row by row
+  const int pool_per = P.pool_cap / (int)gridDim.x;
+  const int pool0 = (int)blockIdx.x * pool_per;
+  int pool_used = 0;
   int k = 0;          // chunks taken from the ring
   int par = 0;        // which abort snapshot this row reads
   for (int r = blockIdx.x; r < P.NR; r += gridDim.x, par ^= 1) {
@@ -548,10 +617,20 @@ __device__ void cut_consumers(const ToppParams& P, unsigned char* smem, uint64_t
       const uint4 v1 = ct + kCutConsumers < nvec ? slot[ct + kCutConsumers] : zero4;
       __syncwarp();
       if (lane == 0) mbar_arrive(empty + s);
-      const int tok0 = ch * (kCutChunkBytes / (int)sizeof(T));
+      const int tok0 = ch * tpc;
       float z[2][8];
-      pen_vec<T>(v0, tok0 + ct * N, x, bits, P.V, z[0], bad);
-      pen_vec<T>(v1, tok0 + (ct + kCutConsumers) * N, x, bits, P.V, z[1], bad);
+      if (!x.pen && tok0 + tpc <= P.V) {
+        // the common chunk: every token real, no penalty
+        Vec<T>::cvt(v0, z[0]);
+        Vec<T>::cvt(v1, z[1]);
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+          for (int j = 0; j < N; ++j) bad |= !(z[h][j] < INFINITY);
+      } else {
+        pen_vec<T>(v0, tok0 + ct * N, x, bits, P.V, z[0], bad);
+        pen_vec<T>(v1, tok0 + (ct + kCutConsumers) * N, x, bits, P.V, z[1], bad);
+      }
       float y[2][8];
       float vm = -INFINITY;
 #pragma unroll
@@ -561,6 +640,13 @@ __device__ void cut_consumers(const ToppParams& P, unsigned char* smem, uint64_t
           y[h][j] = __fmul_rn(z[h][j], x.c);
           vm = fmaxf(vm, y[h][j]);
         }
+      if (ch == 0) {
+        // the first chunk's maximum primes the CTA's, so that the first
+        // chunk does not take most of its tokens as candidates
+        const float wmax = warp_max(vm);
+        if (lane == 0 && wmax > -INFINITY) atomicMax(&ms->cta_max, fkey_i(wmax));
+        csync();
+      }
       if (vm > rt) {
         st *= ex2(rt - vm);
         rt = vm;
@@ -570,10 +656,11 @@ __device__ void cut_consumers(const ToppParams& P, unsigned char* smem, uint64_t
         for (int h = 0; h < 2; ++h)
 #pragma unroll
           for (int j = 0; j < N; ++j) st += ex2(y[h][j] - rt);
-      // candidates: within the window of the running maximum (this warp's,
-      // or the CTA's as the warps have published it)
-      const float wm = warp_max(rt);
-      const float thr = fmaxf(wm, fval_i(*reinterpret_cast<volatile int*>(&ms->cta_max))) - kCutWindow;
+      // candidates: within the window of the running maximum (this thread's,
+      // or the CTA's as the threads have published it; neither exceeds M)
+      const float cm = fval_i(*reinterpret_cast<volatile int*>(&ms->cta_max));
+      if (rt > cm) atomicMax(&ms->cta_max, fkey_i(rt));
+      const float thr = fmaxf(rt, cm) - kCutWindow;
       int kt = 0;
 #pragma unroll
       for (int h = 0; h < 2; ++h)
@@ -600,7 +687,6 @@ __device__ void cut_consumers(const ToppParams& P, unsigned char* smem, uint64_t
               ++pos;
             }
       }
-      if (lane == 0 && wm > -INFINITY) atomicMax(&ms->cta_max, fkey_i(wm));
     }
     // ---- the row's maximum and mass
     float M = rt, S = st;
@@ -636,42 +722,34 @@ __device__ void cut_consumers(const ToppParams& P, unsigned char* smem, uint64_t
     if (x.usable && !rbad && x.tp < 1.f) {
       const double target = (double)x.tp * (double)S;
       bool win = ncand <= kCutCand;
-      if (win) win = select_cut<T, false>(P, x, cand, ncand, M, target, hm, hc, bits, ms, ct, cw, lane);
+      if (win) win = select_window<T>(P, x, cand, ncand, M, target, hm, hc, bits, ms, ct, cw, lane);
       if (!win) {
-        select_cut<T, true>(P, x, cand, ncand, M, target, hm, hc, bits, ms, ct, cw, lane);
+        key_levels<T, true>(P, x, cand, ncand, M, target, 0.0, 0, hm, hc, bits, ms, ct, cw, lane,
+                            [](float) { return true; });
         rec.flags |= kCutViaRow;
       }
       const unsigned tk = ms->tau_key;
       rec.tau = okey_val(tk);
       rec.Sk = (float)ms->Sk;
       const int nup = ms->n_upper;
-      // the kept list: room in the pool (a peek first, so that failed adds
-      // stay few), then the tokens with key >= tk
-      if (ct == 0) {
-        int off = -1;
-        const unsigned long long v = *reinterpret_cast<volatile unsigned long long*>(P.pool_ctr);
-        const unsigned have = (v >> kTagShift) == P.tag ? (unsigned)(v & ((1ull << kTagShift) - 1ull)) : 0u;
-        if (nup <= kCutListMax && (long long)have + nup <= (long long)P.pool_cap) {
-          const unsigned old = tagged_add(P.pool_ctr, P.tag, (unsigned)nup);
-          if ((long long)old + nup <= (long long)P.pool_cap) off = (int)old;
-        }
-        ms->dense = off;
-        ms->nlist = 0;
-      }
-      csync();
-      const int off = ms->dense;
-      if (off >= 0) {
+      // the kept list, in this CTA's share of the pool (every thread keeps
+      // the same count); a set that does not fit is not listed
+      if (nup <= kCutListMax && pool_used + nup <= pool_per) {
+        const int off = pool0 + pool_used;
+        if (ct == 0) ms->nlist = 0;
+        csync();
         auto put = [&](int v, float z) {
           if (okey(z) >= tk) {
             const int q = atomicAdd(&ms->nlist, 1);
             if (q < nup) P.pool[off + q] = v;
           }
         };
-        if (win) visit<T, false>(P, x, cand, ncand, M - kCutWindow, bits, ct, put);
-        else visit<T, true>(P, x, cand, ncand, M - kCutWindow, bits, ct, put);
+        if (win) visit<T, false>(P, x, cand, ncand, bits, ct, put);
+        else visit<T, true>(P, x, cand, ncand, bits, ct, put);
         csync();
         rec.n = min(ms->nlist, nup);
         rec.off = off;
+        pool_used += rec.n;
       }
     }
     if (ct == 0) P.rows[r] = rec;
