@@ -320,6 +320,7 @@ struct BinPick {
   double above;   // mass before bin b (with the level's `above`)
   int n_above;    // tokens before bin b (with the level's count)
   int cnt;        // tokens in bin b
+  double mass;    // their mass
 };
 
 template <typename T, bool GLOBAL, typename BinF>
@@ -390,11 +391,13 @@ __device__ BinPick pick_bin(const ToppParams& P, const RowCtx& x, const int2* ca
     ms->above = (ob & 1) ? excl + m0 : excl;
     ms->n_upper = (ob & 1) ? cexcl + c0 : cexcl;
     ms->bstar = (ob & 1) ? c1 : c0;
+    ms->Sk = (ob & 1) ? m1 : m0;
   }
   csync();
   r.above = ms->above;
   r.n_above = ms->n_upper;
   r.cnt = ms->bstar;
+  r.mass = ms->Sk;
   csync();
   return r;
 }
@@ -498,7 +501,17 @@ __device__ void key_levels(const ToppParams& P, const RowCtx& x, const int2* can
     const unsigned nkhi = hi - lo_off, nklo = hi - hi_off;
     above = bp.above;
     n_above = bp.n_above;
-    if (nklo == nkhi || bp.cnt <= 32) {
+    if (nklo == nkhi) {
+      // one key: every token of it is kept, however many tie
+      if (ct == 0) {
+        ms->tau_key = nkhi;
+        ms->Sk = above + bp.mass;
+        ms->n_upper = n_above + bp.cnt;
+      }
+      csync();
+      return;
+    }
+    if (bp.cnt <= 32) {
       small_cut<T, GLOBAL>(P, x, cand, ncand, M, target, above, n_above, hm, hc, bits, ms, ct, cw, lane,
                            [&](float z) {
                              const uint32_t kz = okey(z);
@@ -620,26 +633,20 @@ __device__ void cut_consumers(const ToppParams& P, unsigned char* smem, uint64_t
       const int tok0 = ch * tpc;
       float z[2][8];
       if (!x.pen && tok0 + tpc <= P.V) {
-        // the common chunk: every token real, no penalty
+        // the common chunk: every token real, no penalty (NaN and +inf show
+        // in the row's mass and maximum, checked once per row)
         Vec<T>::cvt(v0, z[0]);
         Vec<T>::cvt(v1, z[1]);
-#pragma unroll
-        for (int h = 0; h < 2; ++h)
-#pragma unroll
-          for (int j = 0; j < N; ++j) bad |= !(z[h][j] < INFINITY);
       } else {
         pen_vec<T>(v0, tok0 + ct * N, x, bits, P.V, z[0], bad);
         pen_vec<T>(v1, tok0 + (ct + kCutConsumers) * N, x, bits, P.V, z[1], bad);
       }
-      float y[2][8];
-      float vm = -INFINITY;
+      float zm = -INFINITY;
 #pragma unroll
       for (int h = 0; h < 2; ++h)
 #pragma unroll
-        for (int j = 0; j < N; ++j) {
-          y[h][j] = __fmul_rn(z[h][j], x.c);
-          vm = fmaxf(vm, y[h][j]);
-        }
+        for (int j = 0; j < N; ++j) zm = fmaxf(zm, z[h][j]);
+      const float vm = __fmul_rn(zm, x.c);      // the chunk's largest z'c (c > 0: the product keeps the order)
       if (ch == 0) {
         // the first chunk's maximum primes the CTA's, so that the first
         // chunk does not take most of its tokens as candidates
@@ -651,21 +658,33 @@ __device__ void cut_consumers(const ToppParams& P, unsigned char* smem, uint64_t
         st *= ex2(rt - vm);
         rt = vm;
       }
-      if (rt > -INFINITY)
+      if (rt > -INFINITY) {
+        const float nrt = -rt;
 #pragma unroll
         for (int h = 0; h < 2; ++h)
 #pragma unroll
-          for (int j = 0; j < N; ++j) st += ex2(y[h][j] - rt);
+          for (int j = 0; j < N; ++j) st += ex2(fmaf(z[h][j], x.c, nrt));
+      } else {
+        // nothing above -inf yet in this thread: a NaN would skip the sum
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+          for (int j = 0; j < N; ++j) bad |= z[h][j] != z[h][j];
+      }
       // candidates: within the window of the running maximum (this thread's,
-      // or the CTA's as the threads have published it; neither exceeds M)
+      // or the CTA's as the threads have published it; neither exceeds M),
+      // tested on z' against a bound a little below thr / c, so that every
+      // token with z'c >= thr (as the select computes z'c) is taken
       const float cm = fval_i(*reinterpret_cast<volatile int*>(&ms->cta_max));
       if (rt > cm) atomicMax(&ms->cta_max, fkey_i(rt));
       const float thr = fmaxf(rt, cm) - kCutWindow;
+      const float tz = thr / x.c;
+      const float zthr = tz - (fabsf(tz) * 1e-5f + 1e-30f);
       int kt = 0;
 #pragma unroll
       for (int h = 0; h < 2; ++h)
 #pragma unroll
-        for (int j = 0; j < N; ++j) kt += (y[h][j] >= thr && y[h][j] > -INFINITY) ? 1 : 0;
+        for (int j = 0; j < N; ++j) kt += (z[h][j] >= zthr && z[h][j] > -INFINITY) ? 1 : 0;
       if (__ballot_sync(0xffffffffu, kt > 0)) {
         int incl = kt;
 #pragma unroll
@@ -681,7 +700,7 @@ __device__ void cut_consumers(const ToppParams& P, unsigned char* smem, uint64_t
         for (int h = 0; h < 2; ++h)
 #pragma unroll
           for (int j = 0; j < N; ++j)
-            if (y[h][j] >= thr && y[h][j] > -INFINITY) {
+            if (z[h][j] >= zthr && z[h][j] > -INFINITY) {
               if (pos < kCutCand)
                 cand[pos] = make_int2(tok0 + (ct + h * kCutConsumers) * N + j, __float_as_int(z[h][j]));
               ++pos;
@@ -705,7 +724,7 @@ __device__ void cut_consumers(const ToppParams& P, unsigned char* smem, uint64_t
     M = -INFINITY;
     S = 0.f;
     for (int w = 0; w < kCutConsumerWarps; ++w) ref_merge(M, S, ms->wM[w], ms->wS[w]);
-    const bool rbad = ms->bad != 0 || !(M > -INFINITY);
+    const bool rbad = ms->bad != 0 || !(M > -INFINITY) || !(M < INFINITY) || !(S >= 0.f);
     const int ncand = ms->ncand;
     csync();
     if (ms->snap[par]) break;            // a wait ran out: the row is not recorded
