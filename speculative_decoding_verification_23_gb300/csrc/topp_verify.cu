@@ -162,6 +162,36 @@ __device__ __forceinline__ bool cut_wait(uint64_t* bar, uint32_t parity, CutMisc
 }
 
 // ------------------------------------------------------------ the producer
+// The ring holds kCutSlots chunks (96 KB), too few bytes in flight for an
+// SM's share of HBM bandwidth at the latency of a loaded memory system.  So
+// the producer also prefetches into L2 the chunk kCutPrefetch positions
+// ahead of the one it copies (384 KB ahead), before it waits for a free
+// slot: the copies then mostly read L2, and the prefetches keep HBM busy
+// while the consumers select a row's cut.
+constexpr int kCutPrefetch = 24;
+
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
+// A position in this CTA's chunk sequence (rows blockIdx.x + j gridDim.x,
+// chunks 0 .. nch - 1 of each).
+struct ChunkCursor {
+  int r = 0, ch = 0;
+  const unsigned char* src = nullptr;
+  template <typename T>
+  __device__ __forceinline__ void start(const ToppParams& P, int row) {
+    r = row;
+    ch = 0;
+    RowMap m;
+    src = r < P.NR ? logits_row<T>(P, map_row(P, r, m) ? m.src : 0) : nullptr;
+  }
+  template <typename T>
+  __device__ __forceinline__ void next(const ToppParams& P, int nch) {
+    if (++ch == nch) start<T>(P, r + (int)gridDim.x);
+  }
+};
+
 template <typename T>
 __device__ void cut_producer(const ToppParams& P, unsigned char* ring, uint64_t* full, uint64_t* empty, CutMisc* ms,
                              int lane) {
@@ -169,24 +199,27 @@ __device__ void cut_producer(const ToppParams& P, unsigned char* ring, uint64_t*
   const uint64_t pol = l2_policy_evict_first();
   const int rb = row_bytes(P, (int)sizeof(T));
   const int nch = (rb + kCutChunkBytes - 1) / kCutChunkBytes;
+  auto chunk_bytes = [&](int ch) { return (uint32_t)min(kCutChunkBytes, rb - ch * kCutChunkBytes); };
   RingFills fills;
-  int k = 0;
-  bool ok = true;
-  for (int r = blockIdx.x; r < P.NR && ok; r += gridDim.x) {
-    RowMap m;
-    const bool mapped = map_row(P, r, m);
-    const unsigned char* src = logits_row<T>(P, mapped ? m.src : 0);
-    for (int ch = 0; ch < nch; ++ch, ++k) {
-      const int s = k % kCutSlots;
-      if (k >= kCutSlots && !cut_wait(empty + s, (uint32_t)((k / kCutSlots - 1) & 1), ms)) {
-        ok = false;
-        break;
-      }
-      const int bytes = min(kCutChunkBytes, rb - ch * kCutChunkBytes);
-      mbar_arrive_expect_tx(full + s, (uint32_t)bytes);
-      bulk_g2s(ring + (size_t)s * kCutChunkBytes, src + (size_t)ch * kCutChunkBytes, (uint32_t)bytes, full + s, pol);
-      fills.note((uint32_t)s, (uint32_t)((k / kCutSlots) & 1));
+  ChunkCursor cur, pre;
+  cur.start<T>(P, blockIdx.x);
+  pre.start<T>(P, blockIdx.x);
+  for (int i = 0; i < kCutPrefetch && pre.r < P.NR; ++i) {
+    prefetch_l2(pre.src + (size_t)pre.ch * kCutChunkBytes, chunk_bytes(pre.ch));
+    pre.next<T>(P, nch);
+  }
+  for (int k = 0; cur.r < P.NR; ++k) {
+    if (pre.r < P.NR) {
+      prefetch_l2(pre.src + (size_t)pre.ch * kCutChunkBytes, chunk_bytes(pre.ch));
+      pre.next<T>(P, nch);
     }
+    const int s = k % kCutSlots;
+    if (k >= kCutSlots && !cut_wait(empty + s, (uint32_t)((k / kCutSlots - 1) & 1), ms)) break;
+    const uint32_t bytes = chunk_bytes(cur.ch);
+    mbar_arrive_expect_tx(full + s, bytes);
+    bulk_g2s(ring + (size_t)s * kCutChunkBytes, cur.src + (size_t)cur.ch * kCutChunkBytes, bytes, full + s, pol);
+    fills.note((uint32_t)s, (uint32_t)((k / kCutSlots) & 1));
+    cur.next<T>(P, nch);
   }
   // nothing may land in shared memory after the CTA exits
   fills.drain(full, kCutSlots);
