@@ -53,9 +53,15 @@ CLOCK_WINDOW_S = 0.2           # the K-step window repeats until this much time 
 METRIC = "spec-verify rows/s and logits HBM GB/s (% of GB300 peak) at B=64 K=8 V=152064"
 
 
-def kernel_hash() -> str:
+TOPP_SOURCES = ["speculative_decoding_verification_23_gb300/csrc/topp_verify.cu",
+                "speculative_decoding_verification_23_gb300/csrc/topp_internal.h",
+                "speculative_decoding_verification_23_gb300/csrc/common.cuh"]
+TOPP_SUMMARY = os.path.join(ROOT, "profiles", "topp_kernels_ragged.json")
+
+
+def kernel_hash(sources=None) -> str:
     h = hashlib.sha256()
-    for f in KERNEL_SOURCES:
+    for f in (sources or KERNEL_SOURCES):
         with open(os.path.join(ROOT, f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -525,7 +531,7 @@ def bench_extras(dev, peak: float, cpu_seconds: float) -> dict:
     sec = timed(lambda: sv.spec_verify_sample(ar, device=dev, workspace=wsr, stream=stream), iters=10)
     out["ragged_top_p_B256_fp32"] = line("ragged", br.logit_bytes() + 8 * (br.total_drafts + br.B) + 16 * br.B,
                                          sec, oracle_rate(oracle.verify_batch, br, budget),
-                                         "sample_verify_kernel (streaming, top-p)")
+                                         "topp_cut_kernel + topp_finish_kernel")
     del dr, wsr
     bb = make_workload(0)
     db = to_device(bb, dev)
@@ -703,6 +709,67 @@ def profile(args) -> int:
     return 0
 
 
+def topp_run() -> int:
+    """`--topp-run`: three top-p calls on the ragged workload (B=256, K 1..8,
+    V=152064, fp32), the command the top-p kernels' ncu capture runs."""
+    import torch
+
+    import speculative_decoding_verification_23_gb300 as sv
+    from speculative_decoding_verification_23_gb300 import workload as W
+    from speculative_decoding_verification_23_gb300.device_batch import to_device
+
+    b = W.ragged_top_p(0)
+    db = to_device(b)
+    ws = sv.make_workspace(b.B, b.total_drafts, b.V)
+    a = db.args()
+    for _ in range(3):
+        sv.spec_verify_sample(a, workspace=ws)
+    torch.cuda.synchronize()
+    return 0
+
+
+def profile_topp() -> int:
+    """The top-p kernels on the ragged workload: duration and DRAM bytes of
+    each kernel's last launch (three metrics, a few passes, 1.6 GB of
+    inputs on the device), against the algorithmic bytes of the workload."""
+    import csv
+
+    base = [sys.executable, os.path.abspath(__file__), "--topp-run"]
+    if subprocess.call(base, stdout=subprocess.DEVNULL) != 0:
+        print("plain top-p run failed; not profiling", file=sys.stderr)
+        return 1
+    log = os.path.join(ROOT, "gpurun_out", "topp_prof.csv")
+    rc = subprocess.call(["ncu", "--metrics", "gpu__time_duration.sum,dram__bytes_read.sum,dram__bytes_write.sum",
+                          "--clock-control", "none", "-k", "regex:topp_", "-c", "6", "--csv", "--log-file", log] + base,
+                         stdout=subprocess.DEVNULL)
+    if rc:
+        return rc
+    scale = {"byte": 1, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9, "nsecond": 1e-3, "usecond": 1.0, "msecond": 1e3,
+             "ns": 1e-3, "us": 1.0, "ms": 1e3}
+    per = {}
+    with open(log) as f:
+        lines = [l for l in f if l.startswith('"')]
+    for r in csv.DictReader(lines):
+        name = "topp_cut_kernel" if "topp_cut" in r["Kernel Name"] else "topp_finish_kernel"
+        v = float(r["Metric Value"].replace(",", "")) * scale.get(r.get("Metric Unit", ""), 1.0)
+        per.setdefault(name, {})[r["Metric Name"]] = v      # the last launch wins
+    algo = 1574182000
+    out = {"kernels": {}, "workload": "ragged top-p B=256 K 1..8 V=152064 fp32", "algorithmic_bytes": algo,
+           "kernel_hash": kernel_hash(TOPP_SOURCES), "command": "python bench.py --profile"}
+    for name, m in per.items():
+        out["kernels"][name] = {"duration_us_under_ncu": m.get("gpu__time_duration.sum"),
+                                "dram_read_bytes": int(m.get("dram__bytes_read.sum", 0)),
+                                "dram_write_bytes": int(m.get("dram__bytes_write.sum", 0))}
+    cut = out["kernels"].get("topp_cut_kernel", {})
+    if cut:
+        out["cut_traffic_over_algorithmic"] = (cut["dram_read_bytes"] + cut["dram_write_bytes"]) / algo
+    for path in (TOPP_SUMMARY, os.path.join(ROOT, "gpurun_out", os.path.basename(TOPP_SUMMARY))):
+        with open(path, "w") as f:
+            json.dump(out, f, indent=2)
+    print(json.dumps(out), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -714,12 +781,17 @@ def main():
     ap.add_argument("--extras", action="store_true",
                     help="also time the other configurations and entry points (adds about a minute)")
     ap.add_argument("--profile", action="store_true",
-                    help="ncu launch list and one capture of the sampling kernel -> profiles/")
+                    help="ncu launch list and one capture of the sampling kernel, and the top-p kernels' "
+                         "durations and DRAM bytes -> profiles/")
+    ap.add_argument("--topp-run", action="store_true", help=argparse.SUPPRESS)
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
+    if args.topp_run:
+        sys.exit(topp_run())
     if args.profile:
-        sys.exit(profile(args))
+        rc = profile(args)
+        sys.exit(rc or profile_topp())
     if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
         sys.exit(relaunch(args))
     if args.impl == "reference":

@@ -651,6 +651,7 @@ __device__ void cut_consumers(const ToppParams& P, unsigned char* smem, uint64_t
       csync();
     }
     // ---- the streaming pass
+    const float inv_c = 1.f / x.c;     // the candidate bound's margin covers its rounding
     float rt = -INFINITY, st = 0.f;
     bool bad = false;
     for (int ch = 0; ch < nch; ++ch, ++k) {
@@ -674,11 +675,17 @@ __device__ void cut_consumers(const ToppParams& P, unsigned char* smem, uint64_t
         pen_vec<T>(v0, tok0 + ct * N, x, bits, P.V, z[0], bad);
         pen_vec<T>(v1, tok0 + (ct + kCutConsumers) * N, x, bits, P.V, z[1], bad);
       }
-      float zm = -INFINITY;
+      float zm2[2];
 #pragma unroll
-      for (int h = 0; h < 2; ++h)
-#pragma unroll
-        for (int j = 0; j < N; ++j) zm = fmaxf(zm, z[h][j]);
+      for (int h = 0; h < 2; ++h) {
+        float a = fmaxf(z[h][0], z[h][1]), b2 = fmaxf(z[h][2], z[h][3]);
+        if constexpr (N == 8) {
+          a = fmaxf(a, fmaxf(z[h][4], z[h][5]));
+          b2 = fmaxf(b2, fmaxf(z[h][6], z[h][7]));
+        }
+        zm2[h] = fmaxf(a, b2);
+      }
+      const float zm = fmaxf(zm2[0], zm2[1]);
       const float vm = __fmul_rn(zm, x.c);      // the chunk's largest z'c (c > 0: the product keeps the order)
       if (ch == 0) {
         // the first chunk's maximum primes the CTA's, so that the first
@@ -693,10 +700,12 @@ __device__ void cut_consumers(const ToppParams& P, unsigned char* smem, uint64_t
       }
       if (rt > -INFINITY) {
         const float nrt = -rt;
+        float acc[2] = {0.f, 0.f};
 #pragma unroll
         for (int h = 0; h < 2; ++h)
 #pragma unroll
-          for (int j = 0; j < N; ++j) st += ex2(fmaf(z[h][j], x.c, nrt));
+          for (int j = 0; j < N; ++j) acc[j & 1] += ex2(fmaf(z[h][j], x.c, nrt));
+        st += acc[0] + acc[1];
       } else {
         // nothing above -inf yet in this thread: a NaN would skip the sum
 #pragma unroll
@@ -711,7 +720,7 @@ __device__ void cut_consumers(const ToppParams& P, unsigned char* smem, uint64_t
       const float cm = fval_i(*reinterpret_cast<volatile int*>(&ms->cta_max));
       if (rt > cm) atomicMax(&ms->cta_max, fkey_i(rt));
       const float thr = fmaxf(rt, cm) - kCutWindow;
-      const float tz = thr / x.c;
+      const float tz = thr * inv_c;
       const float zthr = tz - (fabsf(tz) * 1e-5f + 1e-30f);
       int kt = 0;
 #pragma unroll
