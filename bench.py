@@ -770,6 +770,78 @@ def profile_topp() -> int:
     return 0
 
 
+SMALL_RUNS = {
+    # name: (kernel regex, workload, algorithmic bytes, profile file)
+    "greedy": ("greedy_verify_kernel", "greedy B=1 K=8 V=151936 bf16", 9 * 151936 * 2 + 4 * 18,
+               "greedy_verify_kernel_B1_K8.json"),
+    "resident": ("sample_verify_kernel", "Qwen2.5-shaped B=1 K=8 V=152064 bf16 D=0.5", 5171292,
+                 "sample_verify_kernel_resident_B1_K8.json"),
+    "confidence": ("conf_pipe_kernel", "batched B=64 K=8 V=152064 bf16, threshold 0.6", 155848704,
+                   "conf_pipe_kernel_batched.json"),
+}
+
+
+def small_run(name: str) -> int:
+    """`--small-run NAME`: five calls of one small entry point (the command
+    the small kernels' ncu captures run)."""
+    import torch
+
+    import speculative_decoding_verification_23_gb300 as sv
+    from speculative_decoding_verification_23_gb300 import workload as W
+    from speculative_decoding_verification_23_gb300.device_batch import to_device
+
+    b = {"greedy": lambda: W.greedy_single(8), "resident": lambda: W.qwen25_single(0.5),
+         "confidence": lambda: make_workload(0)}[name]()
+    db = to_device(b)
+    ws = sv.make_workspace(b.B, b.total_drafts, b.V)
+    a = db.args()
+    for _ in range(5):
+        if name == "greedy":
+            sv.spec_verify_greedy(a, workspace=ws)
+        elif name == "resident":
+            sv.spec_verify_sample(a, workspace=ws)
+        else:
+            sv.spec_draft_confidence(a, 0.6, workspace=ws)
+    torch.cuda.synchronize()
+    return 0
+
+
+def profile_small() -> int:
+    """`--profile-small`: duration and DRAM bytes of the greedy, resident
+    cluster and confidence kernels on their own workloads (three metrics,
+    the last of three captured launches), with the algorithmic bytes."""
+    import csv
+
+    scale = {"byte": 1, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9, "nsecond": 1e-3, "usecond": 1.0, "msecond": 1e3}
+    for name, (kern, workload, algo, fname) in SMALL_RUNS.items():
+        base = [sys.executable, os.path.abspath(__file__), "--small-run", name]
+        if subprocess.call(base, stdout=subprocess.DEVNULL) != 0:
+            print(f"plain {name} run failed; not profiling", file=sys.stderr)
+            return 1
+        log = os.path.join(ROOT, "gpurun_out", f"small_{name}.csv")
+        rc = subprocess.call(["ncu", "--metrics", "gpu__time_duration.sum,dram__bytes_read.sum,dram__bytes_write.sum",
+                              "--clock-control", "none", "-k", "regex:" + kern, "-s", "2", "-c", "3", "--csv",
+                              "--log-file", log] + base, stdout=subprocess.DEVNULL)
+        if rc:
+            return rc
+        m = {}
+        with open(log) as f:
+            lines = [l for l in f if l.startswith('"')]
+        for r in csv.DictReader(lines):
+            m[r["Metric Name"]] = float(r["Metric Value"].replace(",", "")) * scale.get(r.get("Metric Unit", ""), 1.0)
+        rd, wr = int(m.get("dram__bytes_read.sum", 0)), int(m.get("dram__bytes_write.sum", 0))
+        out = {"kernel": kern, "workload": workload, "algorithmic_bytes": algo,
+               "duration_us_under_ncu": m.get("gpu__time_duration.sum"), "dram_read_bytes": rd,
+               "dram_write_bytes": wr, "traffic_over_algorithmic": (rd + wr) / algo,
+               "note": "cold-cache, serialised launch under ncu: compare bytes, not the duration",
+               "command": "python bench.py --profile-small"}
+        for path in (os.path.join(ROOT, "profiles", fname), os.path.join(ROOT, "gpurun_out", fname)):
+            with open(path, "w") as f:
+                json.dump(out, f, indent=2)
+        print(json.dumps(out), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -784,11 +856,18 @@ def main():
                     help="ncu launch list and one capture of the sampling kernel, and the top-p kernels' "
                          "durations and DRAM bytes -> profiles/")
     ap.add_argument("--topp-run", action="store_true", help=argparse.SUPPRESS)
+    ap.add_argument("--profile-small", action="store_true",
+                    help="ncu durations and DRAM bytes of the greedy, resident cluster and confidence kernels")
+    ap.add_argument("--small-run", default=None, help=argparse.SUPPRESS)
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     if args.topp_run:
         sys.exit(topp_run())
+    if args.small_run:
+        sys.exit(small_run(args.small_run))
+    if args.profile_small:
+        sys.exit(profile_small())
     if args.profile:
         rc = profile(args)
         sys.exit(rc or profile_topp())
