@@ -812,7 +812,8 @@ def profile_small() -> int:
     the last of three captured launches), with the algorithmic bytes."""
     import csv
 
-    scale = {"byte": 1, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9, "nsecond": 1e-3, "usecond": 1.0, "msecond": 1e3}
+    scale = {"byte": 1, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9, "nsecond": 1e-3, "usecond": 1.0, "msecond": 1e3,
+             "ns": 1e-3, "us": 1.0, "ms": 1e3}
     for name, (kern, workload, algo, fname) in SMALL_RUNS.items():
         base = [sys.executable, os.path.abspath(__file__), "--small-run", name]
         if subprocess.call(base, stdout=subprocess.DEVNULL) != 0:
