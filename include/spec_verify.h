@@ -144,8 +144,12 @@ enum {
    pipelined kernel (about one work item per SM in flight, each item's
    second pass re-read from L2); with top-p, the cluster kernel's streaming
    variant.  Without a hint: RESIDENT when the batch fits in one wave, else
-   SPLIT without top-p (rows of at most 32 segments: V <= 491520 bf16,
-   245760 fp32) and the streaming cluster kernel with top-p. */
+   SPLIT (rows of at most 32 segments: V <= 491520 bf16, 245760 fp32).
+   With top-p and no RESIDENT or STREAMING hint (SPLIT included), the top-p
+   path: a row-cut kernel reads every row once and keeps each row's exact
+   nucleus as a token list, and a finish kernel decides and draws from the
+   lists (V <= 262144, and the buffer large enough for its records: always
+   for a workspace). */
 #define SPEC_PREFER_RESIDENT 2u
 #define SPEC_PREFER_STREAMING 4u
 #define SPEC_PREFER_SPLIT 8u
@@ -234,7 +238,10 @@ int spec_draft_confidence(const spec_args *args, float threshold, float *out_con
  * segment (segments of 15360 bf16 or 7680 fp32 logits), V/8 bytes of
  * penalty bitmap per request and 64 bytes per vocabulary segment and draft;
  * for B = 64, K = 8, V = 152064 it is 2.4 MiB in bf16 and 3.3 MiB in fp32.
- * With top-p (the cluster kernel) it is 96 bytes per work item
+ * With top-p the top-p path needs 32 bytes per logical row and 4 KiB of
+ * kept-token lists per row (B = 256, total_drafts = 1152: 10.5 MiB, over
+ * the scratch); when that does not fit, the cluster kernel serves the
+ * batch, with 96 bytes per work item
  * (total_drafts + B).  A batch that does not fit returns
  * SPEC_ERR_STATIC_SCRATCH and enqueues nothing.
  *
