@@ -66,6 +66,17 @@ def test_workspace_size_grows_with_batch(lib):
     assert 0 < a < b and b % 256 == 0
 
 
+@pytest.mark.parametrize("B,total", [(1, 0), (3, 7), (256, 1152), (4096, 32768)])
+def test_workspace_covers_the_top_p_records(lib, B, total):
+    """The top-p path keeps a 32-byte record per logical row (2 total + B),
+    one word, and kept-token lists of 1024 int32 entries per row on average
+    (2^23 at most): spec_workspace_bytes covers them for any V."""
+    nr = 2 * total + B
+    need = nr * 32 + 4 * min(nr * 1024, 1 << 23)
+    for V in (16, 152064):
+        assert sv.spec_workspace_bytes(B, total, V) >= need
+
+
 def _args(**kw):
     a = sv.SpecArgs()
     a.B, a.V, a.total_drafts, a.max_k, a.dtype = 1, 16, 1, 1, sv.SPEC_F32
